@@ -1,0 +1,460 @@
+"""Throughput of the gated delta rule on GB300: one JSON line.
+
+Step = one pass of the whole hot path over the 27B-shape long-context workload: a
+Qwen3.6-27B-shape gated-delta-net layer (16 key / 48 value heads, d = 128, width-4 conv,
+bf16 inputs, fp32 state), B = 1, T = 131072 tokens processed as 256 prefill calls of 512
+tokens, each followed by a checkpoint SAVE of the recurrent + conv state into a slot bank.
+`value` = prefill tokens/s.  In the same run the batched decode step of the same layer
+shape (B = 128 sequences, 256 consecutive steps on HBM-resident state) is timed and
+reported as HBM GB/s under "decode".
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+
+Under torchrun (N > 1) every rank runs the same workload on its own GPU (independent
+sequences: no data-path collective); the control plane (barrier, max of the times) uses
+gloo.  `--impl reference` times the fp64 CPU oracle on a bounded sample of the same
+workload instead (rank 0 only).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+import gdn_inputs as gi  # noqa: E402
+
+METRIC = "GDN prefill tokens/s (27B layer shape) and decode state-update HBM GB/s"
+HK, HV, D, W = 16, 48, 128, 4
+T_TOTAL, BUCKET = 131072, 512
+DECODE_B, DECODE_STEPS = 128, 256
+C_CONV = (2 * HK + HV) * D
+# algorithmic work (chunked WY/UT form, d = 128, C = 64): 6 d^2 + 10 C d FLOP per token per
+# value head on the tensor cores
+FLOP_PER_TOKEN = HV * (6 * D * D + 10 * 64 * D)
+# decode bytes per sequence per step (bf16 out): state r+w, conv state r+w, x, out, gates
+DECODE_BYTES_PER_SEQ = (2 * HV * D * D * 4 + 2 * (W - 1) * C_CONV * 2 + C_CONV * 2
+                        + HV * D * 2 + 2 * HV * 2)
+CLOCK_QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return dict(hbm_gbs=float(d["hbm_gbs"]), bf16=float(d["bf16_tflops"]),
+                    bf16_sustained=float(d.get("bf16_tflops_sustained", d["bf16_tflops"])),
+                    source="measured")
+    return dict(hbm_gbs=6800.0, bf16=1900.0, bf16_sustained=1700.0, source="fallback")
+
+
+# ------------------------------------------------------------------ clocks
+
+class ClockSampler:
+    def __init__(self, gpu_index: int):
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{gpu_index}.csv")
+        self.gpu = gpu_index
+
+    def __enter__(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={CLOCK_QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=self.f, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.f.close()
+
+    def summary(self):
+        if self.proc is None or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        rows = []
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append(dict(sm=float(parts[1]), smax=float(parts[2]),
+                                 hw=parts[5], hwt=parts[6], swt=parts[7], pcap=parts[8]))
+            except ValueError:
+                continue
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        reasons = set()
+        for r in rows:
+            for k, name in (("hw", "hw_slowdown"), ("hwt", "hw_thermal_slowdown"),
+                            ("swt", "sw_thermal_slowdown"), ("pcap", "sw_power_cap")):
+                if r[k].lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(r["sm"] for r in rows),
+                "sm_max_mhz": max(r["smax"] for r in rows), "samples": len(rows),
+                "reasons": sorted(reasons)}
+
+
+# ------------------------------------------------------------------ workload
+
+def make_prefill_workload(device):
+    sh = gi.GDNShape(1, T_TOTAL, HK, HV, conv_width=W)
+    inp = gi.make_inputs_device(sh, seed=4000, device=device)
+    nbk = T_TOTAL // BUCKET
+    bank = torch.empty(nbk, HV, D, D, device=device)
+    cbank = torch.empty(nbk, W - 1, C_CONV, dtype=torch.bfloat16, device=device)
+    out = torch.empty(1, T_TOTAL, HV, D, dtype=torch.bfloat16, device=device)
+    import gated_deltanet_linear_13_gb300 as gdn
+    ws = torch.empty(gdn.gdn_prefill_workspace_size(1, BUCKET, HK, HV, W), dtype=torch.uint8,
+                     device=device)
+    rows = torch.zeros(1, dtype=torch.int32, device=device)
+    slot_ids = torch.arange(nbk, dtype=torch.int32, device=device)
+    return dict(inp=inp, bank=bank, cbank=cbank, out=out, ws=ws, rows=rows, slots=slot_ids)
+
+
+def prefill_step(gdn, wl):
+    """A fresh sequence: 256 bucket calls of 512 tokens, a checkpoint SAVE after each."""
+    inp = wl["inp"]
+    inp.state.zero_()
+    inp.conv_state.zero_()
+    for i in range(T_TOTAL // BUCKET):
+        t0 = i * BUCKET
+        gdn.gdn_chunk_prefill(inp.x[:, t0:t0 + BUCKET], None, None, inp.a[:, t0:t0 + BUCKET],
+                              inp.b[:, t0:t0 + BUCKET], inp.A_log, inp.dt_bias, inp.state,
+                              wl["out"][:, t0:t0 + BUCKET], num_k_heads=HK,
+                              conv_weight=inp.conv_weight, conv_state=inp.conv_state,
+                              workspace=wl["ws"])
+        gdn.gdn_state_checkpoint("save", inp.state, inp.conv_state, wl["bank"], wl["cbank"],
+                                 wl["rows"], wl["slots"][i:i + 1], num_k_heads=HK)
+
+
+def prefill_calls_only(gdn, wl):
+    """The 256 bucket prefill calls of a step without the checkpoints (kernel timing)."""
+    inp = wl["inp"]
+    for i in range(T_TOTAL // BUCKET):
+        t0 = i * BUCKET
+        gdn.gdn_chunk_prefill(inp.x[:, t0:t0 + BUCKET], None, None, inp.a[:, t0:t0 + BUCKET],
+                              inp.b[:, t0:t0 + BUCKET], inp.A_log, inp.dt_bias, inp.state,
+                              wl["out"][:, t0:t0 + BUCKET], num_k_heads=HK,
+                              conv_weight=inp.conv_weight, conv_state=inp.conv_state,
+                              workspace=wl["ws"])
+
+
+def make_decode_workload(device):
+    sh = gi.GDNShape(DECODE_B, 1, HK, HV, conv_width=W)
+    dec = gi.make_decode_inputs_device(sh, DECODE_STEPS, seed=3628, device=device)
+    g = torch.Generator(device=device)
+    g.manual_seed(3629)
+    state = torch.randn(DECODE_B, HV, D, D, generator=g, device=device) * 0.02
+    conv_state = torch.randn(DECODE_B, W - 1, C_CONV, generator=g, device=device).to(torch.bfloat16)
+    cw = (torch.randn(C_CONV, W, generator=g, device=device) / 2).to(torch.bfloat16)
+    A_log = torch.rand(HV, generator=g, device=device) * math.log(16.0)
+    dt_bias = torch.zeros(HV, device=device)
+    out = torch.empty(DECODE_STEPS, DECODE_B, HV, D, dtype=torch.bfloat16, device=device)
+    return dict(dec=dec, state=state, conv_state=conv_state, cw=cw, A_log=A_log,
+                dt_bias=dt_bias, out=out)
+
+
+def decode_steps(gdn, wl, events=None):
+    dec = wl["dec"]
+    for t in range(DECODE_STEPS):
+        if events is not None:
+            events[t][0].record()
+        gdn.gdn_decode_step(dec["x"][t].view(DECODE_B, 1, C_CONV), None, None,
+                            dec["a"][t].view(DECODE_B, 1, HV), dec["b"][t].view(DECODE_B, 1, HV),
+                            wl["A_log"], wl["dt_bias"], wl["state"],
+                            wl["out"][t].view(DECODE_B, 1, HV, D), num_k_heads=HK,
+                            conv_weight=wl["cw"], conv_state=wl["conv_state"])
+        if events is not None:
+            events[t][1].record()
+
+
+# ------------------------------------------------------------------ CPU oracle baseline
+
+def oracle_sample(tokens: int, heads: int = HV, seed: int = 4000):
+    """fp64 oracle over the first `tokens` tokens of `heads` value heads of the 27B-shape
+    workload (host-generated inputs, same distributions).  Returns (seconds, threads)."""
+    import oracle
+    sh = gi.GDNShape(1, tokens, HK, HV, conv_width=W)
+    inp = gi.make_inputs(sh, seed=seed, dtype="bf16")
+    nthreads = len(os.sched_getaffinity(0))
+    t = time.perf_counter()
+    oracle.layer(num_k_heads=HK, num_v_heads=HV, x=inp.x, a=inp.a, b=inp.b, A_log=inp.A_log,
+                 dt_bias=inp.dt_bias, conv_weight=inp.conv_weight, conv_state=inp.conv_state,
+                 nthreads=nthreads)
+    return time.perf_counter() - t, nthreads
+
+
+def cpu_model():
+    try:
+        for line in open("/proc/cpuinfo"):
+            if line.lower().startswith(("model name", "cpu part")):
+                return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return "unknown"
+
+
+def run_reference(args):
+    """The reference arm: the fp64 oracle on the host cores, bounded sample per step."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    tokens = args.ref_tokens
+    for _ in range(args.warmup):
+        oracle_sample(min(tokens, 64))
+    times = []
+    nthreads = 1
+    for _ in range(args.steps):
+        s, nthreads = oracle_sample(tokens)
+        times.append(s)
+    tok_s = tokens * args.steps / sum(times)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": tok_s, "unit": "tokens/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * sum(times) / len(times), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": "qwen36_27b_gdn_prefill_T131072_bucket512",
+                   "sample_tokens_per_step": tokens, "heads": HV},
+        "cpu_baseline": {"value": tok_s, "unit": "tokens/s", "cores": nthreads,
+                         "kind": "oracle", "cpu": cpu_model(),
+                         "sample": f"first {tokens} tokens x {HV} value heads of the 27B-shape "
+                                   f"workload (conv + norm + gates + recurrence, fp64)"},
+        "e2e": {"value": tok_s, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+    return 0
+
+
+# ------------------------------------------------------------------ main
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="gdn", choices=["gdn", "reference"])
+    ap.add_argument("--ref-tokens", type=int, default=2048)
+    ap.add_argument("--cpu-tokens", type=int, default=2048)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    args = ap.parse_args()
+    if args.impl == "reference":
+        return run_reference(args)
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("gloo")
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+
+    def barrier():
+        torch.cuda.synchronize()
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    def max_over_ranks(x: float) -> float:
+        if dist is None:
+            return x
+        t = torch.tensor([x], dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return float(t.item())
+
+    import gated_deltanet_linear_13_gb300 as gdn
+    from gated_deltanet_linear_13_gb300 import build_lib
+    build_lib.build()
+    gdn.load_library()
+    peaks = load_peaks()
+
+    # ---------------- prefill (the step), replayed as one CUDA graph of public-API calls
+    wl = make_prefill_workload(device)
+    prefill_step(gdn, wl)                      # eager once: attribute set-up, errors surface
+    st = gdn.gdn_get_device_error()
+    if st != 0:
+        raise RuntimeError(f"device error in the eager step: {gdn.gdn_status_string(st)}")
+    nbk = T_TOTAL // BUCKET
+    g_step = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g_step):
+        prefill_step(gdn, wl)
+    g_calls = torch.cuda.CUDAGraph()          # the prefill calls alone, for the kernel timing
+    with torch.cuda.graph(g_calls):
+        prefill_calls_only(gdn, wl)
+    for _ in range(args.warmup):
+        g_step.replay()
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    barrier()
+    with ClockSampler(local) as clk:
+        t_start.record()
+        for _ in range(args.steps):
+            g_step.replay()
+        t_end.record()
+        barrier()
+        # per-launch duration of the prefill call, inside the same sampled window
+        c0 = torch.cuda.Event(enable_timing=True)
+        c1 = torch.cuda.Event(enable_timing=True)
+        reps = max(1, args.steps)
+        g_calls.replay()
+        c0.record()
+        for _ in range(reps):
+            g_calls.replay()
+        c1.record()
+        barrier()
+    prefill_ms = t_start.elapsed_time(t_end)
+    call_ms = c0.elapsed_time(c1) / (reps * nbk)
+    clocks = clk.summary()
+    st = gdn.gdn_get_device_error()
+    if st != 0:
+        raise RuntimeError(f"device error in the timed region: {gdn.gdn_status_string(st)}")
+    prefill_ms = max_over_ranks(prefill_ms)
+    ms_per_step = prefill_ms / args.steps
+    value = world * T_TOTAL * args.steps / (prefill_ms / 1e3)
+    achieved_tflops = FLOP_PER_TOKEN * BUCKET / (call_ms / 1e3) / 1e12
+
+    # ---------------- decode (same run, HBM-resident state), 256 steps as one CUDA graph
+    dwl = make_decode_workload(device)
+    decode_steps(gdn, dwl)
+    st = gdn.gdn_get_device_error()
+    if st != 0:
+        raise RuntimeError(f"device error in decode: {gdn.gdn_status_string(st)}")
+    g_dec = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g_dec):
+        decode_steps(gdn, dwl)
+    for _ in range(3):
+        g_dec.replay()
+    d0 = torch.cuda.Event(enable_timing=True)
+    d1 = torch.cuda.Event(enable_timing=True)
+    dreps = 3
+    barrier()
+    d0.record()
+    for _ in range(dreps):
+        g_dec.replay()
+    d1.record()
+    barrier()
+    mean_ms = d0.elapsed_time(d1) / (dreps * DECODE_STEPS)
+    # eager per-step timing (launch overhead included) for reference
+    dev_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(DECODE_STEPS)]
+    decode_steps(gdn, dwl, dev_ev)
+    barrier()
+    eager_ms = statistics.median(a.elapsed_time(b) for a, b in dev_ev)
+    dec_bytes = DECODE_BYTES_PER_SEQ * DECODE_B
+    dec_gbs = dec_bytes / (mean_ms / 1e3) / 1e9
+    st = gdn.gdn_get_device_error()
+    if st != 0:
+        raise RuntimeError(f"device error in decode: {gdn.gdn_status_string(st)}")
+    del g_dec, dwl
+
+    # ---------------- end to end through the public API with host buffers
+    e2e = None
+    if not args.no_e2e:
+        inp = wl["inp"]
+        hx = torch.empty(inp.x.shape, dtype=inp.x.dtype, pin_memory=True)
+        ha = torch.empty(inp.a.shape, dtype=inp.a.dtype, pin_memory=True)
+        hb = torch.empty(inp.b.shape, dtype=inp.b.dtype, pin_memory=True)
+        hout = torch.empty(wl["out"].shape, dtype=wl["out"].dtype, pin_memory=True)
+        hx.copy_(inp.x)
+        ha.copy_(inp.a)
+        hb.copy_(inp.b)
+        e2e_steps = max(1, min(args.steps, 3))
+
+        def e2e_step():
+            inp.x.copy_(hx, non_blocking=True)
+            inp.a.copy_(ha, non_blocking=True)
+            inp.b.copy_(hb, non_blocking=True)
+            g_step.replay()
+            hout.copy_(wl["out"], non_blocking=True)
+
+        e2e_step()
+        barrier()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(e2e_steps):
+            e2e_step()
+        e1.record()
+        barrier()
+        e2e_ms = max_over_ranks(e0.elapsed_time(e1))
+        h2d = (hx.numel() * hx.element_size() + ha.numel() * ha.element_size() +
+               hb.numel() * hb.element_size())
+        d2h = hout.numel() * hout.element_size()
+        e2e = {"value": world * T_TOTAL * e2e_steps / (e2e_ms / 1e3), "unit": "tokens/s",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "ms_per_step": e2e_ms / e2e_steps}
+
+    # ---------------- CPU oracle baseline (rank 0, bounded sample)
+    cpu = None
+    if rank == 0 and not args.no_cpu:
+        secs, nthreads = oracle_sample(args.cpu_tokens)
+        cpu = {"value": args.cpu_tokens / secs, "unit": "tokens/s", "cores": nthreads,
+               "kind": "oracle", "cpu": cpu_model(), "seconds": secs,
+               "sample": f"first {args.cpu_tokens} tokens x {HV} value heads of the 27B-shape "
+                         f"workload (conv + norm + gates + recurrence, fp64)"}
+
+    if rank == 0:
+        launches_per_step = nbk * 3   # conv + recurrence + checkpoint per bucket
+        line = {
+            "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic",
+            "config": {"workload": "qwen36_27b_gdn_prefill_T131072_bucket512",
+                       "batch": 1, "seq_len": T_TOTAL, "bucket": BUCKET, "num_k_heads": HK,
+                       "num_v_heads": HV, "head_dim": D, "conv_width": W, "chunk": 64,
+                       "checkpoint_every": BUCKET, "l2": "inputs larger than L2 (2.7 GB x)",
+                       "parallelism": f"replicas x{world}"},
+            "roofline": {"bound": "tensor", "achieved": achieved_tflops,
+                         "peak": peaks["bf16_sustained"], "unit": "TFLOP/s",
+                         "frac": achieved_tflops / peaks["bf16_sustained"], "traffic": None,
+                         "kernel": "gdn_chunk_prefill (conv + chunked recurrence), 512 tokens",
+                         "flop_per_launch": FLOP_PER_TOKEN * BUCKET,
+                         "launch_ms": call_ms, "peak_source": peaks["source"] + " sustained"},
+            "decode": {"metric": "decode state-update HBM GB/s", "value": dec_gbs,
+                       "unit": "GB/s", "batch": DECODE_B, "steps": DECODE_STEPS,
+                       "step_ms_graph_mean": mean_ms, "step_ms_eager_median": eager_ms,
+                       "bytes_per_step": dec_bytes,
+                       "roofline": {"bound": "hbm", "achieved": dec_gbs,
+                                    "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                                    "frac": dec_gbs / peaks["hbm_gbs"], "traffic": None,
+                                    "peak_source": peaks["source"]},
+                       "l2": "state 805 MB > L2"},
+            "e2e": e2e,
+            "cpu_baseline": cpu,
+            "clocks": clocks,
+            "gpu_launches": launches_per_step * args.steps,
+        }
+        print(json.dumps(line))
+    if dist is not None:
+        dist.barrier()
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,304 @@
+"""gated_deltanet_linear_13_gb300 -- Python binding of libgdn.so (GB300 / sm_103a).
+
+The gated delta rule (Gated DeltaNet) behind a C ABI (``include/gdn.h``):
+``gdn_chunk_prefill``, ``gdn_decode_step``, ``causal_conv1d_update``, ``gdn_state_checkpoint``.
+This module only marshals torch tensors into pointers and sizes: every step of the path runs
+in the CUDA kernels of ``libgdn.so``.  It checks shapes, dtypes, devices and contiguity
+before handing raw pointers to the library (a wrong size would otherwise let a kernel read
+past a buffer).  If ``libgdn.so`` is missing the import fails: there is no fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libgdn.so")
+HEAD_DIM = 128
+
+GDN_OK = 0
+GDN_F32, GDN_BF16 = 0, 1
+STATUS_NAMES = {0: "GDN_OK", 1: "GDN_ERR_INVALID_ARGUMENT", 2: "GDN_ERR_UNSUPPORTED",
+                3: "GDN_ERR_WORKSPACE", 4: "GDN_ERR_CUDA", 5: "GDN_ERR_DEVICE_TIMEOUT",
+                6: "GDN_ERR_DEVICE_INDEX"}
+
+EXPORTED = ("gdn_prefill_workspace_size", "gdn_chunk_prefill", "gdn_decode_step",
+            "causal_conv1d_update", "gdn_state_checkpoint", "gdn_get_device_error",
+            "gdn_status_string", "gdn_version")
+
+
+class GDNError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {STATUS_NAMES.get(status, status)}")
+
+
+class GdnDims(ctypes.Structure):
+    _fields_ = [("batch", ctypes.c_int32), ("seqlen", ctypes.c_int32),
+                ("num_k_heads", ctypes.c_int32), ("num_v_heads", ctypes.c_int32),
+                ("head_dim", ctypes.c_int32), ("chunk_size", ctypes.c_int32),
+                ("conv_width", ctypes.c_int32), ("num_slots", ctypes.c_int32)]
+
+
+class GdnOpts(ctypes.Structure):
+    _fields_ = [("in_dtype", ctypes.c_int), ("out_dtype", ctypes.c_int),
+                ("qk_l2norm", ctypes.c_int32), ("l2_eps", ctypes.c_float),
+                ("scale", ctypes.c_float), ("conv_silu", ctypes.c_int32),
+                ("gates_precomputed", ctypes.c_int32)]
+
+
+_vp = ctypes.c_void_p
+_lib = None
+
+
+def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
+    """Load libgdn.so (raises OSError when it has not been built)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise OSError(f"libgdn.so not found at {path}: build it with "
+                      "`python -m gated_deltanet_linear_13_gb300.build_lib`")
+    L = ctypes.CDLL(path)
+    dp, op = ctypes.POINTER(GdnDims), ctypes.POINTER(GdnOpts)
+    L.gdn_prefill_workspace_size.restype = ctypes.c_size_t
+    L.gdn_prefill_workspace_size.argtypes = [dp, op]
+    L.gdn_chunk_prefill.restype = ctypes.c_int
+    L.gdn_chunk_prefill.argtypes = [dp, op] + [_vp] * 14 + [ctypes.c_size_t, _vp]
+    L.gdn_decode_step.restype = ctypes.c_int
+    L.gdn_decode_step.argtypes = [dp, op] + [_vp] * 13 + [_vp]
+    L.causal_conv1d_update.restype = ctypes.c_int
+    L.causal_conv1d_update.argtypes = ([ctypes.c_int32] * 4 + [ctypes.c_int] + [_vp] * 4 +
+                                       [ctypes.c_int32, _vp, ctypes.c_int32, _vp, _vp])
+    L.gdn_state_checkpoint.restype = ctypes.c_int
+    L.gdn_state_checkpoint.argtypes = ([ctypes.c_int32, dp, ctypes.c_int] + [_vp] * 4 +
+                                       [ctypes.c_int32, _vp, _vp, ctypes.c_int32, _vp])
+    L.gdn_get_device_error.restype = ctypes.c_int
+    L.gdn_get_device_error.argtypes = [_vp]
+    L.gdn_status_string.restype = ctypes.c_char_p
+    L.gdn_status_string.argtypes = [ctypes.c_int]
+    L.gdn_version.restype = ctypes.c_int32
+    L.gdn_version.argtypes = []
+    _lib = L
+    return L
+
+
+# ---------------------------------------------------------------- marshalling helpers
+
+def _dt(t: torch.Tensor) -> int:
+    if t.dtype == torch.bfloat16:
+        return GDN_BF16
+    if t.dtype == torch.float32:
+        return GDN_F32
+    raise TypeError(f"unsupported dtype {t.dtype}")
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else t.data_ptr()
+
+
+def _need(t: Optional[torch.Tensor], name: str, shape, dtype, device):
+    if t is None:
+        raise ValueError(f"{name} is required")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name}: shape {tuple(t.shape)}, expected {tuple(shape)}")
+    if t.dtype != dtype:
+        raise TypeError(f"{name}: dtype {t.dtype}, expected {dtype}")
+    if t.device != device:
+        raise ValueError(f"{name}: on {t.device}, expected {device}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _check(status: int, where: str):
+    if status != GDN_OK:
+        raise GDNError(status, where)
+
+
+def _layer_dims(q, k, v, a, num_k_heads, conv_weight, conv_state, state, state_slots,
+                num_slots_hint):
+    B, T, Hv = a.shape
+    W = 0 if conv_weight is None else conv_weight.shape[1]
+    if W > 0:
+        Hk = num_k_heads
+        C = (2 * Hk + Hv) * HEAD_DIM
+        if q.shape != (B, T, C):
+            raise ValueError(f"x: shape {tuple(q.shape)}, expected {(B, T, C)}")
+    else:
+        Hk = q.shape[2]
+    num_slots = state.shape[0]
+    if state_slots is None and num_slots < B:
+        raise ValueError("state has fewer rows than the batch and no state_slots given")
+    return B, T, Hk, Hv, W, num_slots
+
+
+def _check_layer(q, k, v, a, b, A_log, dt_bias, conv_weight, conv_bias, state, conv_state,
+                 state_slots, out, B, T, Hk, Hv, W, num_slots, gates_precomputed):
+    dev = q.device
+    if dev.type != "cuda":
+        raise ValueError("tensors must be on a CUDA device")
+    in_t = q.dtype
+    d = HEAD_DIM
+    C = (2 * Hk + Hv) * d
+    if W > 0:
+        if k is not None or v is not None:
+            raise ValueError("with a conv, pass the pre-conv x as q and k = v = None")
+        _need(conv_weight, "conv_weight", (C, W), in_t, dev)
+        if conv_bias is not None:
+            _need(conv_bias, "conv_bias", (C,), in_t, dev)
+        if W > 1:
+            _need(conv_state, "conv_state", (num_slots, W - 1, C), in_t, dev)
+    else:
+        _need(q, "q", (B, T, Hk, d), in_t, dev)
+        _need(k, "k", (B, T, Hk, d), in_t, dev)
+        _need(v, "v", (B, T, Hv, d), in_t, dev)
+    gt = torch.float32 if gates_precomputed else in_t
+    _need(a, "a", (B, T, Hv), gt, dev)
+    _need(b, "b", (B, T, Hv), gt, dev)
+    if not gates_precomputed:
+        _need(A_log, "A_log", (Hv,), torch.float32, dev)
+    if dt_bias is not None:
+        _need(dt_bias, "dt_bias", (Hv,), torch.float32, dev)
+    _need(state, "state", (num_slots, Hv, d, d), torch.float32, dev)
+    if state_slots is not None:
+        _need(state_slots, "state_slots", (B,), torch.int32, dev)
+    if out.device != dev or not out.is_contiguous() or tuple(out.shape) != (B, T, Hv, d):
+        raise ValueError(f"out: expected contiguous {(B, T, Hv, d)} on {dev}")
+
+
+def _opts(in_dtype, out_dtype, qk_l2norm, eps, scale, conv_silu, gates_precomputed):
+    return GdnOpts(in_dtype, out_dtype, int(qk_l2norm), float(eps), float(scale),
+                   int(conv_silu), int(gates_precomputed))
+
+
+# ---------------------------------------------------------------- public API
+
+def gdn_prefill_workspace_size(batch: int, seqlen: int, num_k_heads: int, num_v_heads: int,
+                               conv_width: int, in_dtype=torch.bfloat16) -> int:
+    L = load_library()
+    dims = GdnDims(batch, seqlen, num_k_heads, num_v_heads, HEAD_DIM, 64, conv_width, 0)
+    dt = GDN_BF16 if in_dtype == torch.bfloat16 else GDN_F32
+    opts = _opts(dt, dt, 1, 1e-6, 1.0, 1, 0)
+    return int(L.gdn_prefill_workspace_size(ctypes.byref(dims), ctypes.byref(opts)))
+
+
+def gdn_chunk_prefill(q, k, v, a, b, A_log, dt_bias, state, out, *, num_k_heads=None,
+                      conv_weight=None, conv_bias=None, conv_state=None, state_slots=None,
+                      scale: float = 1.0, eps: float = 1e-6, qk_l2norm: bool = True,
+                      conv_silu: bool = True, gates_precomputed: bool = False,
+                      workspace: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """Chunked prefill (see gdn_chunk_prefill in include/gdn.h).  With a conv, ``q`` is the
+    pre-conv x [B,T,C_conv] and ``k = v = None``.  ``state`` (and ``conv_state``) are updated
+    in place; ``out`` [B,T,Hv,128] is written.  Returns ``out``."""
+    L = load_library()
+    B, T, Hk, Hv, W, num_slots = _layer_dims(q, k, v, a, num_k_heads, conv_weight, conv_state,
+                                             state, state_slots, None)
+    _check_layer(q, k, v, a, b, A_log, dt_bias, conv_weight, conv_bias, state, conv_state,
+                 state_slots, out, B, T, Hk, Hv, W, num_slots, gates_precomputed)
+    dims = GdnDims(B, T, Hk, Hv, HEAD_DIM, 64, W, num_slots)
+    opts = _opts(_dt(q), _dt(out), qk_l2norm, eps, scale, conv_silu, gates_precomputed)
+    need = int(L.gdn_prefill_workspace_size(ctypes.byref(dims), ctypes.byref(opts)))
+    if need and workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    st = L.gdn_chunk_prefill(ctypes.byref(dims), ctypes.byref(opts), _ptr(q), _ptr(k), _ptr(v),
+                             _ptr(a), _ptr(b), _ptr(A_log), _ptr(dt_bias), _ptr(conv_weight),
+                             _ptr(conv_bias), _ptr(state), _ptr(conv_state), _ptr(state_slots),
+                             _ptr(out), _ptr(workspace), ws_bytes, _stream(stream))
+    _check(st, "gdn_chunk_prefill")
+    return out
+
+
+def gdn_decode_step(q, k, v, a, b, A_log, dt_bias, state, out, *, num_k_heads=None,
+                    conv_weight=None, conv_bias=None, conv_state=None, state_slots=None,
+                    scale: float = 1.0, eps: float = 1e-6, qk_l2norm: bool = True,
+                    conv_silu: bool = True, gates_precomputed: bool = False,
+                    stream=None) -> torch.Tensor:
+    """One decode step for B sequences (T = 1), fused into one kernel launch."""
+    L = load_library()
+    B, T, Hk, Hv, W, num_slots = _layer_dims(q, k, v, a, num_k_heads, conv_weight, conv_state,
+                                             state, state_slots, None)
+    if T != 1:
+        raise ValueError("gdn_decode_step takes exactly one token per sequence")
+    _check_layer(q, k, v, a, b, A_log, dt_bias, conv_weight, conv_bias, state, conv_state,
+                 state_slots, out, B, T, Hk, Hv, W, num_slots, gates_precomputed)
+    dims = GdnDims(B, 1, Hk, Hv, HEAD_DIM, 64, W, num_slots)
+    opts = _opts(_dt(q), _dt(out), qk_l2norm, eps, scale, conv_silu, gates_precomputed)
+    st = L.gdn_decode_step(ctypes.byref(dims), ctypes.byref(opts), _ptr(q), _ptr(k), _ptr(v),
+                           _ptr(a), _ptr(b), _ptr(A_log), _ptr(dt_bias), _ptr(conv_weight),
+                           _ptr(conv_bias), _ptr(state), _ptr(conv_state), _ptr(state_slots),
+                           _ptr(out), _stream(stream))
+    _check(st, "gdn_decode_step")
+    return out
+
+
+def causal_conv1d_update(x, weight, conv_state, y, *, bias=None, state_slots=None,
+                         silu: bool = True, stream=None) -> torch.Tensor:
+    """Standalone causal depthwise conv with carried state: x, y [B,T,C]; weight [C,W];
+    conv_state [num_slots, W-1, C] updated in place."""
+    L = load_library()
+    B, T, C = x.shape
+    W = weight.shape[1]
+    dev, dt = x.device, x.dtype
+    _need(x, "x", (B, T, C), dt, dev)
+    _need(y, "y", (B, T, C), dt, dev)
+    _need(weight, "weight", (C, W), dt, dev)
+    if bias is not None:
+        _need(bias, "bias", (C,), dt, dev)
+    ns = conv_state.shape[0]
+    _need(conv_state, "conv_state", (ns, W - 1, C), dt, dev)
+    if state_slots is not None:
+        _need(state_slots, "state_slots", (B,), torch.int32, dev)
+    st = L.causal_conv1d_update(B, T, C, W, _dt(x), _ptr(x), _ptr(weight), _ptr(bias),
+                                _ptr(conv_state), ns, _ptr(state_slots), int(silu), _ptr(y),
+                                _stream(stream))
+    _check(st, "causal_conv1d_update")
+    return y
+
+
+def gdn_state_checkpoint(op: str, state, conv_state, slot_state, slot_conv_state, rows, slots,
+                         *, num_k_heads: int, stream=None) -> None:
+    """op 'save' (live rows -> bank slots) or 'restore' (bank slots -> live rows)."""
+    L = load_library()
+    opc = {"save": 0, "restore": 1}[op]
+    ns, Hv, d, _ = state.shape
+    nb = slot_state.shape[0]
+    dev = state.device
+    _need(state, "state", (ns, Hv, d, d), torch.float32, dev)
+    _need(slot_state, "slot_state", (nb, Hv, d, d), torch.float32, dev)
+    W = 0
+    cdt = GDN_BF16
+    if conv_state is not None:
+        W = conv_state.shape[1] + 1
+        C = conv_state.shape[2]
+        if C != (2 * num_k_heads + Hv) * d:
+            raise ValueError("conv_state channels do not match the head geometry")
+        _need(conv_state, "conv_state", (ns, W - 1, C), conv_state.dtype, dev)
+        _need(slot_conv_state, "slot_conv_state", (nb, W - 1, C), conv_state.dtype, dev)
+        cdt = _dt(conv_state)
+    n = rows.shape[0]
+    _need(rows, "rows", (n,), torch.int32, dev)
+    _need(slots, "slots", (n,), torch.int32, dev)
+    dims = GdnDims(ns, 1, num_k_heads, Hv, d, 64, W, ns)
+    st = L.gdn_state_checkpoint(opc, ctypes.byref(dims), cdt, _ptr(state), _ptr(conv_state),
+                                _ptr(slot_state), _ptr(slot_conv_state), nb, _ptr(rows),
+                                _ptr(slots), n, _stream(stream))
+    _check(st, "gdn_state_checkpoint")
+
+
+def gdn_get_device_error(stream=None) -> int:
+    """Synchronise the stream and return (and clear) the device error status code."""
+    return int(load_library().gdn_get_device_error(_stream(stream)))
+
+
+def gdn_status_string(status: int) -> str:
+    return load_library().gdn_status_string(int(status)).decode()

@@ -1,0 +1,63 @@
+// Indexed save / restore of the recurrent state and conv state between live rows and a
+// checkpoint-slot bank (PR #164 "Hybrid APC Runtime": checkpoint slots with restore and
+// commit masks).  A plain bit copy with 128-bit loads and stores; a negative row or slot
+// masks the pair out.
+#include "common.cuh"
+
+using namespace gdn;
+
+static __device__ unsigned int g_err_ckpt;
+
+unsigned gdn_take_error_checkpoint() {
+  unsigned v = 0, z = 0;
+  cudaMemcpyFromSymbol(&v, g_err_ckpt, sizeof(v));
+  cudaMemcpyToSymbol(g_err_ckpt, &z, sizeof(z));
+  return v;
+}
+
+__global__ void __launch_bounds__(256) gdn_checkpoint_kernel(
+    int op, long long state_v4, long long conv_v4, float4* state, uint4* conv_state,
+    int num_rows, float4* slot_state, uint4* slot_conv, int num_bank, const int32_t* rows,
+    const int32_t* slots, int n) {
+  const int i = blockIdx.y;
+  const int row = rows[i], slot = slots[i];
+  if (row < 0 || slot < 0) return;                       // masked pair
+  if (row >= num_rows || slot >= num_bank) {
+    if (threadIdx.x == 0 && blockIdx.x == 0) atomicOr(&g_err_ckpt, kErrIndex);
+    return;
+  }
+  float4* s_live = state + (size_t)row * state_v4;
+  float4* s_bank = slot_state + (size_t)slot * state_v4;
+  const float4* src = op == 0 ? s_live : s_bank;
+  float4* dst = op == 0 ? s_bank : s_live;
+  const long long stride = (long long)gridDim.x * blockDim.x;
+  for (long long e = (long long)blockIdx.x * blockDim.x + threadIdx.x; e < state_v4; e += stride)
+    dst[e] = src[e];
+  if (conv_v4 > 0) {
+    uint4* c_live = conv_state + (size_t)row * conv_v4;
+    uint4* c_bank = slot_conv + (size_t)slot * conv_v4;
+    const uint4* csrc = op == 0 ? c_live : c_bank;
+    uint4* cdst = op == 0 ? c_bank : c_live;
+    for (long long e = (long long)blockIdx.x * blockDim.x + threadIdx.x; e < conv_v4; e += stride)
+      cdst[e] = csrc[e];
+  }
+}
+
+cudaError_t gdn_launch_checkpoint(int op, int Hv, int d, int conv_elems, int conv_elem_bytes,
+                                  float* state, void* conv_state, int num_rows,
+                                  float* slot_state, void* slot_conv_state, int num_bank,
+                                  const int32_t* rows, const int32_t* slots, int n,
+                                  cudaStream_t stream) {
+  if (n == 0) return cudaSuccess;
+  const long long state_v4 = (long long)Hv * d * d / 4;
+  const long long conv_v4 = (long long)conv_elems * conv_elem_bytes / 16;
+  // ~64 KB per block: enough blocks per pair to keep HBM busy even for one pair
+  int bx = (int)((state_v4 * 16 + 65535) / 65536);
+  if (bx < 1) bx = 1;
+  dim3 grid((unsigned)bx, (unsigned)n, 1);
+  gdn_checkpoint_kernel<<<grid, 256, 0, stream>>>(op, state_v4, conv_v4, (float4*)state,
+                                                  (uint4*)conv_state, num_rows,
+                                                  (float4*)slot_state, (uint4*)slot_conv_state,
+                                                  num_bank, rows, slots, n);
+  return cudaGetLastError();
+}

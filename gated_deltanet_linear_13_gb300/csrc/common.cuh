@@ -1,0 +1,108 @@
+// Internal helpers shared by the kernels of libgdn.so (not part of the C ABI).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "gdn.h"
+
+namespace gdn {
+
+constexpr int kHeadDim = 128;
+constexpr int kChunk = 64;
+
+// Bits of a translation unit's device error word.
+enum : unsigned { kErrIndex = 1u, kErrTimeout = 2u };
+
+// ----------------------------------------------------------------- element access
+
+__device__ __forceinline__ float ld_elem(const float* p) { return *p; }
+__device__ __forceinline__ float ld_elem(const __nv_bfloat16* p) { return __bfloat162float(*p); }
+__device__ __forceinline__ void st_elem(float* p, float x) { *p = x; }
+__device__ __forceinline__ void st_elem(__nv_bfloat16* p, float x) { *p = __float2bfloat16_rn(x); }
+
+template <typename T> __device__ __forceinline__ T from_float(float x);
+template <> __device__ __forceinline__ float from_float<float>(float x) { return x; }
+template <> __device__ __forceinline__ __nv_bfloat16 from_float<__nv_bfloat16>(float x) {
+  return __float2bfloat16_rn(x);
+}
+
+// ----------------------------------------------------------------- gates
+
+// softplus(x) = max(x, 0) + log(1 + exp(-|x|)), written with the library's log1pf / expf.
+__device__ __forceinline__ float softplus_f(float x) {
+  return fmaxf(x, 0.0f) + log1pf(expf(-fabsf(x)));
+}
+__device__ __forceinline__ float sigmoid_f(float x) { return 1.0f / (1.0f + expf(-x)); }
+__device__ __forceinline__ float silu_f(float x) { return x * sigmoid_f(x); }
+
+// Gate of the model card's correctness contract: g = -exp(A_log) * softplus(a + dt_bias).
+__device__ __forceinline__ float gate_g(float a, float A_log, float dt_bias) {
+  return -expf(A_log) * softplus_f(a + dt_bias);
+}
+
+// Sets a kernel's dynamic shared-memory limit once per device (so that launches issued later,
+// e.g. under CUDA-graph capture, make no attribute calls).
+template <typename K>
+inline cudaError_t set_smem_once(K kernel, int bytes, unsigned* done_mask) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const unsigned bit = 1u << (dev & 31);
+  if (*done_mask & bit) return cudaSuccess;
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess) *done_mask |= bit;
+  return e;
+}
+
+// ----------------------------------------------------------------- warp reductions
+
+__device__ __forceinline__ float warp_sum(float x) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+  return x;
+}
+
+}  // namespace gdn
+
+// ----------------------------------------------------------------- launchers (gdn_api.cu)
+
+struct GdnLayerArgs {
+  // geometry
+  int B, T, Hk, Hv, W, C_conv, num_slots;
+  // options
+  int in_bf16, out_bf16, l2norm, silu, gates_pre;
+  float eps, scale;
+  // post-conv operands for the recurrence kernels: element pointers + token strides
+  const void* q; const void* k; const void* v;
+  long long q_tok_stride, k_tok_stride, v_tok_stride;   // elements between tokens
+  // raw pre-conv activation (decode / conv)
+  const void* x;
+  const void* a; const void* b;
+  const float* A_log; const float* dt_bias;
+  const void* conv_w; const void* conv_b;
+  float* state; void* conv_state;
+  const int32_t* slots;
+  void* out;
+};
+
+cudaError_t gdn_launch_decode(const GdnLayerArgs& args, cudaStream_t stream);
+cudaError_t gdn_launch_prefill_simt(const GdnLayerArgs& args, cudaStream_t stream);
+cudaError_t gdn_launch_prefill_tc(const GdnLayerArgs& args, cudaStream_t stream);
+cudaError_t gdn_launch_conv(int B, int T, int C, int W, int bf16, const void* x,
+                            long long x_tok_stride, const void* w, const void* bias,
+                            void* conv_state, int num_slots, const int32_t* slots, int silu,
+                            void* y, long long y_tok_stride, cudaStream_t stream);
+cudaError_t gdn_launch_checkpoint(int op, int Hv, int d, int conv_elems, int conv_elem_bytes,
+                                  float* state, void* conv_state, int num_rows,
+                                  float* slot_state, void* slot_conv_state, int num_bank,
+                                  const int32_t* rows, const int32_t* slots, int n,
+                                  cudaStream_t stream);
+
+// Per-translation-unit device error words: read and clear (host side, synchronous copy).
+unsigned gdn_take_error_decode();
+unsigned gdn_take_error_conv();
+unsigned gdn_take_error_checkpoint();
+unsigned gdn_take_error_prefill_simt();
+unsigned gdn_take_error_prefill_tc();

@@ -1,0 +1,246 @@
+// The C ABI of libgdn.so: host-side validation, workspace sizing, kernel dispatch, status.
+// Every argument is checked before any CUDA call; see include/gdn.h for the contract.
+#include <math.h>
+#include <string.h>
+
+#include "common.cuh"
+
+namespace {
+
+constexpr int32_t kVersion = 100;
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
+size_t elem_bytes(gdn_dtype t) { return t == GDN_BF16 ? 2 : 4; }
+
+struct Checked {
+  int B, T, Hk, Hv, W, Cc, num_slots;
+  size_t in_elem;
+};
+
+gdn_status check_dims(const gdn_dims* d, const gdn_opts* o, bool decode, Checked* out) {
+  if (!d || !o) return GDN_ERR_INVALID_ARGUMENT;
+  if (d->batch < 0 || d->seqlen < 0 || d->num_k_heads < 1 || d->num_v_heads < 1 ||
+      d->num_slots < 0 || d->conv_width < 0 || d->chunk_size < 0)
+    return GDN_ERR_INVALID_ARGUMENT;
+  if (d->num_v_heads % d->num_k_heads != 0) return GDN_ERR_INVALID_ARGUMENT;
+  if (d->head_dim != gdn::kHeadDim) return GDN_ERR_UNSUPPORTED;
+  if (d->chunk_size != 0 && d->chunk_size != gdn::kChunk) return GDN_ERR_UNSUPPORTED;
+  if (d->conv_width > 4) return GDN_ERR_UNSUPPORTED;
+  if ((o->in_dtype != GDN_F32 && o->in_dtype != GDN_BF16) ||
+      (o->out_dtype != GDN_F32 && o->out_dtype != GDN_BF16))
+    return GDN_ERR_INVALID_ARGUMENT;
+  if (o->in_dtype == GDN_F32 && o->out_dtype != GDN_F32) return GDN_ERR_UNSUPPORTED;
+  if (!(o->l2_eps >= 0.0f) || !isfinite(o->l2_eps) || !isfinite(o->scale))
+    return GDN_ERR_INVALID_ARGUMENT;
+  if (decode) {
+    if (d->seqlen != 1) return GDN_ERR_INVALID_ARGUMENT;
+    if (d->num_v_heads / d->num_k_heads > 8) return GDN_ERR_UNSUPPORTED;
+  }
+  // grid limits: batch rides on gridDim.z / gridDim.x
+  if (d->batch > 65535) return GDN_ERR_UNSUPPORTED;
+  if ((long long)d->num_v_heads * d->head_dim > (1 << 20)) return GDN_ERR_UNSUPPORTED;
+  out->B = d->batch;
+  out->T = d->seqlen;
+  out->Hk = d->num_k_heads;
+  out->Hv = d->num_v_heads;
+  out->W = d->conv_width;
+  out->Cc = (2 * d->num_k_heads + d->num_v_heads) * d->head_dim;
+  out->num_slots = d->num_slots ? d->num_slots : d->batch;
+  out->in_elem = elem_bytes(o->in_dtype);
+  return GDN_OK;
+}
+
+// Pointer checks shared by prefill and decode.  Fills the kernel argument block.
+gdn_status check_layer_ptrs(const Checked& c, const gdn_opts* o, const void* q, const void* k,
+                            const void* v, const void* a, const void* b, const float* A_log,
+                            const float* dt_bias, const void* conv_weight,
+                            const void* conv_bias, float* state, void* conv_state,
+                            const int32_t* slots, void* out, GdnLayerArgs* L) {
+  if (!q || !a || !b || !state || !out) return GDN_ERR_INVALID_ARGUMENT;
+  if (!aligned16(q) || !aligned16(state) || !aligned16(out)) return GDN_ERR_INVALID_ARGUMENT;
+  if (!aligned4(a) || !aligned4(b)) return GDN_ERR_INVALID_ARGUMENT;
+  if (!o->gates_precomputed && (!A_log || !aligned4(A_log))) return GDN_ERR_INVALID_ARGUMENT;
+  if (dt_bias && !aligned4(dt_bias)) return GDN_ERR_INVALID_ARGUMENT;
+  if (slots && !aligned4(slots)) return GDN_ERR_INVALID_ARGUMENT;
+  if (!slots && c.num_slots < c.B) return GDN_ERR_INVALID_ARGUMENT;
+  if (c.W > 0) {
+    if (k || v) return GDN_ERR_INVALID_ARGUMENT;       // x arrives in q
+    if (!conv_weight || !aligned4(conv_weight)) return GDN_ERR_INVALID_ARGUMENT;
+    if (conv_bias && !aligned4(conv_bias)) return GDN_ERR_INVALID_ARGUMENT;
+    if (c.W > 1 && (!conv_state || !aligned16(conv_state))) return GDN_ERR_INVALID_ARGUMENT;
+  } else {
+    if (!k || !v || !aligned16(k) || !aligned16(v)) return GDN_ERR_INVALID_ARGUMENT;
+  }
+  memset(L, 0, sizeof(*L));
+  L->B = c.B; L->T = c.T; L->Hk = c.Hk; L->Hv = c.Hv; L->W = c.W; L->C_conv = c.Cc;
+  L->num_slots = c.num_slots;
+  L->in_bf16 = o->in_dtype == GDN_BF16;
+  L->out_bf16 = o->out_dtype == GDN_BF16;
+  L->l2norm = o->qk_l2norm != 0;
+  L->silu = o->conv_silu != 0;
+  L->gates_pre = o->gates_precomputed != 0;
+  L->eps = o->l2_eps;
+  L->scale = o->scale;
+  L->a = a; L->b = b; L->A_log = A_log; L->dt_bias = dt_bias;
+  L->conv_w = conv_weight; L->conv_b = conv_bias;
+  L->state = state; L->conv_state = conv_state; L->slots = slots; L->out = out;
+  if (c.W > 0) {
+    L->x = q;
+  } else {
+    L->q = q; L->k = k; L->v = v;
+    L->q_tok_stride = (long long)c.Hk * gdn::kHeadDim;
+    L->k_tok_stride = (long long)c.Hk * gdn::kHeadDim;
+    L->v_tok_stride = (long long)c.Hv * gdn::kHeadDim;
+  }
+  return GDN_OK;
+}
+
+size_t workspace_bytes_for(const Checked& c) {
+  if (c.W == 0) return 0;
+  return (size_t)c.B * (size_t)c.T * (size_t)c.Cc * c.in_elem;
+}
+
+}  // namespace
+
+extern "C" {
+
+int32_t gdn_version(void) { return kVersion; }
+
+const char* gdn_status_string(gdn_status s) {
+  switch (s) {
+    case GDN_OK: return "GDN_OK";
+    case GDN_ERR_INVALID_ARGUMENT: return "GDN_ERR_INVALID_ARGUMENT";
+    case GDN_ERR_UNSUPPORTED: return "GDN_ERR_UNSUPPORTED";
+    case GDN_ERR_WORKSPACE: return "GDN_ERR_WORKSPACE";
+    case GDN_ERR_CUDA: return "GDN_ERR_CUDA";
+    case GDN_ERR_DEVICE_TIMEOUT: return "GDN_ERR_DEVICE_TIMEOUT";
+    case GDN_ERR_DEVICE_INDEX: return "GDN_ERR_DEVICE_INDEX";
+  }
+  return "GDN_UNKNOWN_STATUS";
+}
+
+size_t gdn_prefill_workspace_size(const gdn_dims* dims, const gdn_opts* opts) {
+  Checked c;
+  if (check_dims(dims, opts, false, &c) != GDN_OK) return 0;
+  return workspace_bytes_for(c);
+}
+
+gdn_status gdn_chunk_prefill(const gdn_dims* dims, const gdn_opts* opts, const void* q,
+                             const void* k, const void* v, const void* a, const void* b,
+                             const float* A_log, const float* dt_bias, const void* conv_weight,
+                             const void* conv_bias, float* state, void* conv_state,
+                             const int32_t* state_slots, void* out, void* workspace,
+                             size_t workspace_bytes, void* stream) {
+  Checked c;
+  gdn_status st = check_dims(dims, opts, false, &c);
+  if (st != GDN_OK) return st;
+  if (c.B == 0 || c.T == 0) return GDN_OK;
+  GdnLayerArgs L;
+  st = check_layer_ptrs(c, opts, q, k, v, a, b, A_log, dt_bias, conv_weight, conv_bias, state,
+                        conv_state, state_slots, out, &L);
+  if (st != GDN_OK) return st;
+  const size_t need = workspace_bytes_for(c);
+  if (need > 0 && (!workspace || workspace_bytes < need || !aligned16(workspace)))
+    return GDN_ERR_WORKSPACE;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (c.W > 0) {
+    // conv (+SiLU) of all channels into the workspace, conv state updated in place
+    cudaError_t e = gdn_launch_conv(c.B, c.T, c.Cc, c.W, L.in_bf16, q, c.Cc, conv_weight,
+                                    conv_bias, conv_state, c.num_slots, state_slots,
+                                    L.silu, workspace, c.Cc, s);
+    if (e != cudaSuccess) return GDN_ERR_CUDA;
+    const char* y = static_cast<const char*>(workspace);
+    L.q = y;
+    L.k = y + (size_t)c.Hk * gdn::kHeadDim * c.in_elem;
+    L.v = y + (size_t)2 * c.Hk * gdn::kHeadDim * c.in_elem;
+    L.q_tok_stride = L.k_tok_stride = L.v_tok_stride = c.Cc;
+  }
+  cudaError_t e = L.in_bf16 ? gdn_launch_prefill_tc(L, s) : gdn_launch_prefill_simt(L, s);
+  return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+}
+
+gdn_status gdn_decode_step(const gdn_dims* dims, const gdn_opts* opts, const void* q,
+                           const void* k, const void* v, const void* a, const void* b,
+                           const float* A_log, const float* dt_bias, const void* conv_weight,
+                           const void* conv_bias, float* state, void* conv_state,
+                           const int32_t* state_slots, void* out, void* stream) {
+  Checked c;
+  gdn_status st = check_dims(dims, opts, true, &c);
+  if (st != GDN_OK) return st;
+  if (c.B == 0) return GDN_OK;
+  GdnLayerArgs L;
+  st = check_layer_ptrs(c, opts, q, k, v, a, b, A_log, dt_bias, conv_weight, conv_bias, state,
+                        conv_state, state_slots, out, &L);
+  if (st != GDN_OK) return st;
+  cudaError_t e = gdn_launch_decode(L, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+}
+
+gdn_status causal_conv1d_update(int32_t batch, int32_t seqlen, int32_t channels, int32_t width,
+                                gdn_dtype dtype, const void* x, const void* weight,
+                                const void* bias, void* conv_state, int32_t num_slots,
+                                const int32_t* state_slots, int32_t silu, void* y,
+                                void* stream) {
+  if (batch < 0 || seqlen < 0 || channels < 0 || num_slots < 0) return GDN_ERR_INVALID_ARGUMENT;
+  if (dtype != GDN_F32 && dtype != GDN_BF16) return GDN_ERR_INVALID_ARGUMENT;
+  if (width < 2 || width > 4) return GDN_ERR_UNSUPPORTED;
+  if (channels % 8 != 0) return GDN_ERR_UNSUPPORTED;
+  if (batch > 65535) return GDN_ERR_UNSUPPORTED;
+  if (batch == 0 || seqlen == 0 || channels == 0) return GDN_OK;
+  const int ns = num_slots ? num_slots : batch;
+  if (!state_slots && ns < batch) return GDN_ERR_INVALID_ARGUMENT;
+  if (!x || !weight || !conv_state || !y) return GDN_ERR_INVALID_ARGUMENT;
+  if (!aligned16(x) || !aligned16(y) || !aligned16(conv_state) || !aligned4(weight))
+    return GDN_ERR_INVALID_ARGUMENT;
+  if ((bias && !aligned4(bias)) || (state_slots && !aligned4(state_slots)))
+    return GDN_ERR_INVALID_ARGUMENT;
+  if (x == y) return GDN_ERR_INVALID_ARGUMENT;
+  cudaError_t e = gdn_launch_conv(batch, seqlen, channels, width, dtype == GDN_BF16, x, channels,
+                                  weight, bias, conv_state, ns, state_slots, silu != 0, y,
+                                  channels, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+}
+
+gdn_status gdn_state_checkpoint(int32_t op, const gdn_dims* dims, gdn_dtype conv_dtype,
+                                float* state, void* conv_state, float* slot_state,
+                                void* slot_conv_state, int32_t num_bank_slots,
+                                const int32_t* rows, const int32_t* slots, int32_t n,
+                                void* stream) {
+  if (op != 0 && op != 1) return GDN_ERR_INVALID_ARGUMENT;
+  if (!dims || n < 0 || num_bank_slots < 0) return GDN_ERR_INVALID_ARGUMENT;
+  if (dims->num_k_heads < 1 || dims->num_v_heads < 1 || dims->conv_width < 0 ||
+      dims->num_slots < 0 || dims->batch < 0)
+    return GDN_ERR_INVALID_ARGUMENT;
+  if (dims->head_dim != gdn::kHeadDim) return GDN_ERR_UNSUPPORTED;
+  if (dims->conv_width > 4) return GDN_ERR_UNSUPPORTED;
+  if (conv_dtype != GDN_F32 && conv_dtype != GDN_BF16) return GDN_ERR_INVALID_ARGUMENT;
+  if (n > 65535) return GDN_ERR_UNSUPPORTED;
+  if (n == 0) return GDN_OK;
+  const int num_rows = dims->num_slots ? dims->num_slots : dims->batch;
+  if (!state || !slot_state || !rows || !slots) return GDN_ERR_INVALID_ARGUMENT;
+  if (!aligned16(state) || !aligned16(slot_state) || !aligned4(rows) || !aligned4(slots))
+    return GDN_ERR_INVALID_ARGUMENT;
+  const int Cc = (2 * dims->num_k_heads + dims->num_v_heads) * dims->head_dim;
+  const int conv_elems = dims->conv_width > 1 ? (dims->conv_width - 1) * Cc : 0;
+  if (conv_elems > 0 && (!conv_state || !slot_conv_state || !aligned16(conv_state) ||
+                         !aligned16(slot_conv_state)))
+    return GDN_ERR_INVALID_ARGUMENT;
+  cudaError_t e = gdn_launch_checkpoint(op, dims->num_v_heads, dims->head_dim, conv_elems,
+                                        (int)elem_bytes(conv_dtype), state, conv_state,
+                                        num_rows, slot_state, slot_conv_state, num_bank_slots,
+                                        rows, slots, n, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+}
+
+gdn_status gdn_get_device_error(void* stream) {
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return GDN_ERR_CUDA;
+  unsigned bits = gdn_take_error_decode() | gdn_take_error_conv() | gdn_take_error_checkpoint() |
+                  gdn_take_error_prefill_simt() | gdn_take_error_prefill_tc();
+  if (cudaGetLastError() != cudaSuccess) return GDN_ERR_CUDA;
+  if (bits & gdn::kErrTimeout) return GDN_ERR_DEVICE_TIMEOUT;
+  if (bits & gdn::kErrIndex) return GDN_ERR_DEVICE_INDEX;
+  return GDN_OK;
+}
+
+}  // extern "C"

@@ -163,3 +163,25 @@ def make_inputs_device(shape: GDNShape, seed: int, device, dtype: str = "bf16",
     dt_bias = torch.zeros(Hv, device=device)
     S = torch.zeros(B, Hv, d, d, device=device)
     return GDNInputs(shape, dtype, q, k, v, x, a, b, A_log, dt_bias, cw, S, cs)
+
+
+def make_decode_inputs_device(shape: GDNShape, steps: int, seed: int, device,
+                              dtype: str = "bf16"):
+    """Per-step decode inputs on the device: x [steps, B, C_conv] (or q/k/v [steps, B, H, d]
+    without a conv), a, b [steps, B, Hv]; step t's slices are contiguous."""
+    B, Hk, Hv, d = shape.batch, shape.num_k_heads, shape.num_v_heads, shape.head_dim
+    tdt = torch.bfloat16 if dtype == "bf16" else torch.float32
+    g = torch.Generator(device=device)
+    g.manual_seed(seed)
+
+    def randn(*s):
+        return torch.randn(*s, generator=g, device=device, dtype=torch.float32).to(tdt)
+
+    out = {}
+    if shape.conv_width > 0:
+        out["x"] = randn(steps, B, shape.conv_channels)
+    else:
+        out["q"], out["k"], out["v"] = (randn(steps, B, Hk, d), randn(steps, B, Hk, d),
+                                        randn(steps, B, Hv, d))
+    out["a"], out["b"] = randn(steps, B, Hv), randn(steps, B, Hv)
+    return out

@@ -1,0 +1,204 @@
+/*
+ * gdn.h -- C ABI of the GB300 (sm_103a) gated delta rule library, libgdn.so.
+ *
+ * The operation (Gated DeltaNet linear attention), per value head, token by token:
+ *     S_t = exp(g_t) S_{t-1} (I - beta_t k_t k_t^T) + beta_t v_t k_t^T,   o_t = S_t q_t
+ * with a 128 x 128 fp32 state S[v][k], L2-normalised q and k, and a short causal depthwise
+ * conv in front.  Defined by the model card "Qwen3.5 Gated Delta Net NKI Kernel for AWS
+ * Neuron", section "How It Works" (the five per-token steps: decay, read, delta, write,
+ * output; the card stores state[k][v] = S^T) and section "Correctness Contract" (the gate
+ * g = -exp(A_log) * softplus(a + dt_bias) <= 0, d_k = d_v = 128, each (batch, head)
+ * independent).  The chunked prefill form with a direct triangular solve of (I + A) follows
+ * PR #164 "Fused DeltaNet Direct-Solve Follow-Up" ("Why This Exists", "Implementation
+ * Details"); decode with conv state + recurrent state caching follows the model card's
+ * "Notice"; checkpoint slots with restore/commit masks follow PR #164 "Hybrid APC Runtime".
+ *
+ * Conventions shared by every entry point
+ *   - Memory: every tensor pointer is a DEVICE pointer owned by the caller.  The library
+ *     allocates nothing; the only global state is the device error word (see
+ *     gdn_get_device_error).  Arrays are dense, row-major, in the layouts stated below.
+ *     q/k/v (or x), state, conv state, out, y, workspace and the checkpoint bank must be
+ *     16-byte aligned; a, b, A_log, dt_bias, conv weight / bias and the int32 index arrays
+ *     4-byte aligned.
+ *   - Validation: arguments are checked on the host before any CUDA call; a bad argument
+ *     returns GDN_ERR_INVALID_ARGUMENT or GDN_ERR_UNSUPPORTED and launches nothing.
+ *   - Asynchrony: work is enqueued on `stream` (a cudaStream_t; NULL = legacy default
+ *     stream) and returns immediately.  A failed launch returns GDN_ERR_CUDA.  Conditions
+ *     found on the device (an out-of-range slot index, a bounded wait that gave up) are
+ *     recorded in the error word and reported by gdn_get_device_error.
+ *   - The library never aborts, exits, prints or traps.  Calls on different streams with
+ *     disjoint buffers may run concurrently.
+ *   - Slots: state arrays hold `num_slots` rows.  `state_slots[b]` (device int32, may be
+ *     NULL = identity) names the row that batch entry b reads and updates in place; a
+ *     negative entry skips batch entry b entirely (its outputs are left untouched), as for
+ *     padded rows of a prefix-cache bucket.  An entry >= num_slots is skipped and recorded
+ *     as GDN_ERR_DEVICE_INDEX.
+ */
+#ifndef GDN_H_
+#define GDN_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  GDN_OK = 0,
+  GDN_ERR_INVALID_ARGUMENT = 1,  /* null / misaligned pointer, bad size, bad enum */
+  GDN_ERR_UNSUPPORTED = 2,       /* valid but not implemented (head_dim != 128, ...) */
+  GDN_ERR_WORKSPACE = 3,         /* workspace missing or smaller than required */
+  GDN_ERR_CUDA = 4,              /* a CUDA runtime call or launch failed */
+  GDN_ERR_DEVICE_TIMEOUT = 5,    /* a bounded device-side wait gave up */
+  GDN_ERR_DEVICE_INDEX = 6       /* a device-side slot/row index was out of range (skipped) */
+} gdn_status;
+
+typedef enum { GDN_F32 = 0, GDN_BF16 = 1 } gdn_dtype;
+
+/* Problem geometry. */
+typedef struct {
+  int32_t batch;        /* B >= 0: sequences in this call */
+  int32_t seqlen;       /* T >= 0: tokens per sequence (gdn_decode_step: must be 1) */
+  int32_t num_k_heads;  /* Hk >= 1 */
+  int32_t num_v_heads;  /* Hv, a multiple of Hk with Hv / Hk <= 8; value head h reads key
+                           head h / (Hv / Hk) */
+  int32_t head_dim;     /* d = d_k = d_v; must be 128 */
+  int32_t chunk_size;   /* prefill chunk length C; 0 or 64 (64 is the only one built) */
+  int32_t conv_width;   /* W: 0 = q, k, v arrive post-conv; 2..4 = causal depthwise conv of
+                           width W over the concatenated q|k|v channels first */
+  int32_t num_slots;    /* rows of the state / conv-state arrays; 0 means `batch` */
+} gdn_dims;
+
+/* Numerical options. */
+typedef struct {
+  gdn_dtype in_dtype;         /* q/k/v (or x), a, b, conv weight / bias, conv state */
+  gdn_dtype out_dtype;        /* out */
+  int32_t qk_l2norm;          /* 1: q, k <- x / sqrt(sum x^2 + l2_eps) per head vector */
+  float l2_eps;               /* epsilon inside the square root (1e-6 typical) */
+  float scale;                /* factor applied to q after normalisation (1.0 typical) */
+  int32_t conv_silu;          /* 1: SiLU after the conv (ignored when conv_width == 0) */
+  int32_t gates_precomputed;  /* 0: a, b are raw gate inputs in in_dtype and
+                                    g = -exp(A_log[h]) softplus(a + dt_bias[h]),
+                                    beta = sigmoid(b);
+                                 1: a holds g and b holds beta, both fp32 */
+} gdn_opts;
+
+/*
+ * Precision modes.  in_dtype = GDN_BF16: bf16 operands on the tensor cores (tcgen05) with
+ * fp32 accumulation and an fp32 state; out_dtype GDN_BF16 or GDN_F32.  in_dtype = GDN_F32
+ * with out_dtype = GDN_F32 is the all-fp32 mode (fp32 FMA throughout).  Other combinations
+ * return GDN_ERR_UNSUPPORTED.
+ */
+
+/*
+ * Bytes of device workspace gdn_chunk_prefill needs for these dims/opts (0 when none):
+ * the post-conv activations when conv_width > 0.  Returns 0 for invalid dims.
+ */
+size_t gdn_prefill_workspace_size(const gdn_dims* dims, const gdn_opts* opts);
+
+/*
+ * gdn_chunk_prefill -- chunked context encoding of B sequences of T tokens.
+ * Definition: the recurrence above, computed per chunk of C = 64 tokens in WY/UT form with a
+ * direct (forward-substitution) solve of (I + A), A strictly lower triangular, carrying the
+ * fp32 state across chunks (PR #164 "Fused DeltaNet Direct-Solve Follow-Up").  A last chunk
+ * shorter than C is handled as a shorter chunk.  Results equal the token-by-token recurrence
+ * up to rounding.
+ *
+ *   q, k, v      conv_width == 0: q [B,T,Hk,d], k [B,T,Hk,d], v [B,T,Hv,d] in in_dtype.
+ *                conv_width  > 0: q points to the pre-conv activation x [B,T,C_conv] in
+ *                in_dtype with channels ordered q | k | v, C_conv = (2 Hk + Hv) d; k and v
+ *                must be NULL.
+ *   a, b         [B,T,Hv] gate inputs (in_dtype), or g and beta (fp32) when
+ *                gates_precomputed.
+ *   A_log        [Hv] fp32 (ignored when gates_precomputed).
+ *   dt_bias      [Hv] fp32 or NULL (= 0).
+ *   conv_weight  [C_conv, W] in in_dtype (required when conv_width > 0, else ignored).
+ *   conv_bias    [C_conv] in in_dtype or NULL (= 0).
+ *   state        [num_slots, Hv, d, d] fp32, S[v][k]; read and written in place.
+ *   conv_state   [num_slots, W-1, C_conv] in in_dtype: the last W-1 pre-conv inputs, oldest
+ *                first; read and written in place (ignored when conv_width == 0).
+ *   state_slots  [B] device int32 or NULL; see "Slots" above.
+ *   out          [B,T,Hv,d] in out_dtype.
+ *   workspace    device scratch of at least gdn_prefill_workspace_size() bytes (may be NULL
+ *                when that is 0); contents are not preserved between calls.
+ * T == 0 or B == 0 is a no-op returning GDN_OK.
+ */
+gdn_status gdn_chunk_prefill(const gdn_dims* dims, const gdn_opts* opts, const void* q,
+                             const void* k, const void* v, const void* a, const void* b,
+                             const float* A_log, const float* dt_bias, const void* conv_weight,
+                             const void* conv_bias, float* state, void* conv_state,
+                             const int32_t* state_slots, void* out, void* workspace,
+                             size_t workspace_bytes, void* stream);
+
+/*
+ * gdn_decode_step -- one new token for each of B sequences (batched token generation).
+ * Definition: one step of the recurrence (model card "How It Works") on the state already
+ * resident in HBM, with the conv update, SiLU, L2 norm and gates fused, as in the model
+ * card's "Notice" on conv-state + recurrent-state caching.  One kernel launch.
+ * Arguments as gdn_chunk_prefill with T = 1 (dims->seqlen must be 1); no workspace.
+ * Requires Hv / Hk <= 8.
+ */
+gdn_status gdn_decode_step(const gdn_dims* dims, const gdn_opts* opts, const void* q,
+                           const void* k, const void* v, const void* a, const void* b,
+                           const float* A_log, const float* dt_bias, const void* conv_weight,
+                           const void* conv_bias, float* state, void* conv_state,
+                           const int32_t* state_slots, void* out, void* stream);
+
+/*
+ * causal_conv1d_update -- the short causal depthwise conv with a carried state, standalone
+ * (model card "How It Works": the causal conv1d around the recurrence; "Notice": conv state
+ * caching).  y[b,t,c] = bias[c] + sum_{j<W} w[c][j] * x[b, t-W+1+j, c], where positions
+ * before the sequence start read conv_state[slot, W-1+(t-W+1+j), c]; then SiLU when `silu`.
+ * conv_state[slot] becomes the last W-1 inputs (oldest first).
+ *   x, y         [B,T,channels] in `dtype` (y may not alias x).
+ *   weight       [channels, W]; bias [channels] or NULL.
+ *   conv_state   [num_slots, W-1, channels] in place; state_slots as above (num_slots 0 = B).
+ * 2 <= W <= 4.  channels must be a multiple of 8.
+ */
+gdn_status causal_conv1d_update(int32_t batch, int32_t seqlen, int32_t channels, int32_t width,
+                                gdn_dtype dtype, const void* x, const void* weight,
+                                const void* bias, void* conv_state, int32_t num_slots,
+                                const int32_t* state_slots, int32_t silu, void* y,
+                                void* stream);
+
+/*
+ * gdn_state_checkpoint -- copy recurrent + conv state between live rows and a slot bank
+ * (PR #164 "Hybrid APC Runtime": checkpoint-slot lifecycle, restore and commit masks; the
+ * reusable prefix of "Why this is larger than a normal contrib model").  A bit copy, so a
+ * run resumed from a checkpoint continues exactly as the uninterrupted run.
+ *   op           0 = SAVE (live row rows[i] -> bank slot slots[i]),
+ *                1 = RESTORE (bank slot slots[i] -> live row rows[i]).
+ *   dims         uses num_v_heads, head_dim, conv_width, num_k_heads, num_slots (live rows).
+ *   state        [num_slots, Hv, d, d] fp32; conv_state [num_slots, W-1, C_conv] in conv_dtype
+ *                (may be NULL when conv_width == 0).
+ *   slot_state   [num_bank_slots, Hv, d, d] fp32; slot_conv_state [num_bank_slots, W-1,
+ *                C_conv] (NULL when conv_width == 0).
+ *   rows, slots  [n] device int32.  A negative entry in either masks pair i out (no copy);
+ *                an entry past its array is skipped and recorded as GDN_ERR_DEVICE_INDEX.
+ * Pairs must not write the same destination twice in one call.
+ */
+gdn_status gdn_state_checkpoint(int32_t op, const gdn_dims* dims, gdn_dtype conv_dtype,
+                                float* state, void* conv_state, float* slot_state,
+                                void* slot_conv_state, int32_t num_bank_slots,
+                                const int32_t* rows, const int32_t* slots, int32_t n,
+                                void* stream);
+
+/*
+ * Synchronises `stream`, then returns and clears the device error word: GDN_OK, or the
+ * first condition recorded by a kernel since the last call (GDN_ERR_DEVICE_INDEX,
+ * GDN_ERR_DEVICE_TIMEOUT), or GDN_ERR_CUDA if the synchronisation itself failed.
+ */
+gdn_status gdn_get_device_error(void* stream);
+
+/* Static text for a status code (never NULL). */
+const char* gdn_status_string(gdn_status status);
+
+/* Library ABI version (major * 100 + minor). */
+int32_t gdn_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GDN_H_ */

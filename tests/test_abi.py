@@ -1,0 +1,160 @@
+"""The C ABI without a GPU: the library loads, exports every symbol that include/gdn.h
+declares, and rejects bad arguments on the host before any CUDA call.
+
+Every call below is built to FAIL validation (or to be a documented no-op): none of them
+ever reaches a kernel launch, so they are safe on any machine, with or without a GPU.
+"""
+import ctypes
+import os
+import re
+
+import pytest
+
+import gated_deltanet_linear_13_gb300 as gdn
+from gated_deltanet_linear_13_gb300 import GdnDims, GdnOpts, build_lib
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    build_lib.build()
+    return gdn.load_library()
+
+
+def _declared_functions():
+    src = open(os.path.join(ROOT, "include", "gdn.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b([a-z_0-9]+)\s*\(", src)) - {"sizeof"})
+
+
+def test_exports_every_declared_symbol(L):
+    declared = _declared_functions()
+    assert set(declared) == set(gdn.EXPORTED), declared
+    for name in declared:
+        assert hasattr(L, name), f"libgdn.so does not export {name}"
+
+
+def test_status_strings_and_version(L):
+    for code, name in gdn.STATUS_NAMES.items():
+        assert gdn.gdn_status_string(code) == name
+    assert gdn.gdn_status_string(99) == "GDN_UNKNOWN_STATUS"
+    assert L.gdn_version() == 100
+
+
+def _dims(**kw):
+    base = dict(batch=1, seqlen=16, num_k_heads=16, num_v_heads=16, head_dim=128,
+                chunk_size=64, conv_width=0, num_slots=0)
+    base.update(kw)
+    return GdnDims(*[base[f] for f, _ in GdnDims._fields_])
+
+
+def _opts(**kw):
+    base = dict(in_dtype=gdn.GDN_BF16, out_dtype=gdn.GDN_BF16, qk_l2norm=1, l2_eps=1e-6,
+                scale=1.0, conv_silu=1, gates_precomputed=0)
+    base.update(kw)
+    return GdnOpts(*[base[f] for f, _ in GdnOpts._fields_])
+
+
+A = 0x10000   # fake, 16-byte aligned addresses: only ever used in calls that fail validation
+
+
+def _prefill(L, dims, opts, q=A, k=A, v=A, a=A, b=A, A_log=A, state=A, out=A, ws=None, wsb=0,
+             conv_w=None, conv_state=None):
+    return L.gdn_chunk_prefill(ctypes.byref(dims), ctypes.byref(opts), q, k, v, a, b, A_log,
+                               None, conv_w, None, state, conv_state, None, out, ws, wsb, None)
+
+
+@pytest.mark.parametrize("field,value,status", [
+    ("head_dim", 64, 2), ("chunk_size", 32, 2), ("conv_width", 5, 2),
+    ("num_v_heads", 24 + 1, 1), ("batch", -1, 1), ("seqlen", -3, 1), ("num_k_heads", 0, 1),
+    ("batch", 70000, 2),
+])
+def test_prefill_rejects_bad_dims(L, field, value, status):
+    assert _prefill(L, _dims(**{field: value}), _opts()) == status
+
+
+def test_prefill_rejects_bad_opts(L):
+    assert _prefill(L, _dims(), _opts(in_dtype=7)) == 1
+    assert _prefill(L, _dims(), _opts(in_dtype=gdn.GDN_F32, out_dtype=gdn.GDN_BF16)) == 2
+    assert _prefill(L, _dims(), _opts(l2_eps=-1.0)) == 1
+    assert _prefill(L, _dims(), _opts(scale=float("nan"))) == 1
+
+
+def test_prefill_rejects_bad_pointers(L):
+    d, o = _dims(), _opts()
+    assert _prefill(L, d, o, q=None) == 1
+    assert _prefill(L, d, o, state=None) == 1
+    assert _prefill(L, d, o, out=None) == 1
+    assert _prefill(L, d, o, q=A + 8) == 1          # misaligned tensor
+    assert _prefill(L, d, o, a=A + 2) == 1          # misaligned gate input
+    assert _prefill(L, d, o, A_log=None) == 1        # needed unless gates are precomputed
+    assert _prefill(L, d, o, k=None) == 1            # no conv: k and v are required
+    # with a conv, x arrives in q and k / v must be NULL; weight and conv state required
+    dc = _dims(conv_width=4)
+    assert _prefill(L, dc, o, conv_w=A, conv_state=A) == 1                  # k, v given
+    assert _prefill(L, dc, o, k=None, v=None, conv_w=None, conv_state=A) == 1
+    assert _prefill(L, dc, o, k=None, v=None, conv_w=A, conv_state=None) == 1
+    # state with fewer rows than the batch and no slot map
+    assert _prefill(L, _dims(batch=4, num_slots=2), o) == 1
+
+
+def test_prefill_workspace_checked(L):
+    dc, o = _dims(conv_width=4), _opts()
+    need = L.gdn_prefill_workspace_size(ctypes.byref(dc), ctypes.byref(o))
+    assert need == 1 * 16 * (2 * 16 + 16) * 128 * 2
+    assert L.gdn_prefill_workspace_size(ctypes.byref(_dims()), ctypes.byref(o)) == 0
+    assert L.gdn_prefill_workspace_size(ctypes.byref(_dims(head_dim=7)), ctypes.byref(o)) == 0
+    assert _prefill(L, dc, o, k=None, v=None, conv_w=A, conv_state=A, ws=None) == 3
+    assert _prefill(L, dc, o, k=None, v=None, conv_w=A, conv_state=A, ws=A, wsb=need - 1) == 3
+    assert _prefill(L, dc, o, k=None, v=None, conv_w=A, conv_state=A, ws=A + 4, wsb=need) == 3
+
+
+def test_empty_calls_are_noops(L):
+    # B == 0 or T == 0: GDN_OK without touching any pointer or CUDA
+    assert _prefill(L, _dims(batch=0), _opts(), q=None, state=None, out=None) == 0
+    assert _prefill(L, _dims(seqlen=0), _opts(), q=None, state=None, out=None) == 0
+
+
+def test_decode_rejects_bad_arguments(L):
+    def dec(dims, opts, **kw):
+        p = dict(q=A, k=A, v=A, a=A, b=A, A_log=A, state=A, out=A)
+        p.update(kw)
+        return L.gdn_decode_step(ctypes.byref(dims), ctypes.byref(opts), p["q"], p["k"], p["v"],
+                                 p["a"], p["b"], p["A_log"], None, None, None, p["state"], None,
+                                 None, p["out"], None)
+    assert dec(_dims(seqlen=2), _opts()) == 1                     # one token per sequence
+    assert dec(_dims(seqlen=1, num_k_heads=1, num_v_heads=16), _opts()) == 2   # Hv/Hk > 8
+    assert dec(_dims(seqlen=1, head_dim=256), _opts()) == 2
+    assert dec(_dims(seqlen=1), _opts(), state=A + 4) == 1
+    assert dec(_dims(seqlen=1, batch=0), _opts(), q=None) == 0
+
+
+def test_conv_rejects_bad_arguments(L):
+    def conv(B=1, T=4, C=64, W=4, dt=gdn.GDN_BF16, x=A, w=A, cs=A, ns=0, y=A + 4096):
+        return L.causal_conv1d_update(B, T, C, W, dt, x, w, None, cs, ns, None, 1, y, None)
+    assert conv(W=5) == 2
+    assert conv(W=1) == 2
+    assert conv(C=12) == 2
+    assert conv(dt=3) == 1
+    assert conv(x=None) == 1
+    assert conv(x=A + 8) == 1
+    assert conv(y=A) == 1                      # y aliases x
+    assert conv(B=2, ns=1) == 1                # fewer state rows than sequences, no slot map
+    assert conv(T=0, x=None) == 0              # empty
+
+
+def test_checkpoint_rejects_bad_arguments(L):
+    d = _dims(conv_width=4, num_slots=2)
+    def ck(op=0, dims=d, dt=gdn.GDN_BF16, st=A, cs=A, ss=A, scs=A, nb=4, rows=A, slots=A, n=1):
+        return L.gdn_state_checkpoint(op, ctypes.byref(dims), dt, st, cs, ss, scs, nb, rows,
+                                      slots, n, None)
+    assert ck(op=2) == 1
+    assert ck(n=-1) == 1
+    assert ck(dims=_dims(head_dim=64)) == 2
+    assert ck(st=None) == 1
+    assert ck(rows=None) == 1
+    assert ck(cs=None) == 1
+    assert ck(ss=A + 8) == 1
+    assert ck(n=70000) == 2
+    assert ck(n=0, st=None) == 0
