@@ -12,6 +12,9 @@
 // scalings of the raw tiles, so the tensor cores always see raw bf16 q/k/v:
 //   G = [K;Q] K^T (one M=128 MMA)  ->  A, P (with 1/||k||, scale/||q||, decays)
 //   T' = T diag(beta e^G / ||k||),  T'' = T diag(beta)      (the solve, fp32 FMA)
+// T', T'', P and U^T enter the tensor cores as bf16 pairs hi + lo (hi = rn(x), lo = rn(x-hi)),
+// which keeps ~16 mantissa bits in the small intra-chunk products; the state snapshot S0,
+// W, Q~ and K~ are single bf16 (their rounding costs far less at the output).
 //   W^T = K^T T'^T,  U'^T = V^T T''^T                          (M = d = 128)
 //   Q~ = diag(scale e^G / ||q||) Q,  K~ = diag(e^{G_C-G} / ||k||) K
 //   U^T = U'^T - S0 W^T,  O^T = S0 Q~^T + U^T P^T,  S = e^{G_C} S0 + U^T K~
@@ -54,12 +57,14 @@ constexpr uint32_t IN_V = 32 * KB;                // V tile: [2][64 rows][128 B]
 constexpr uint32_t OFF_KT = 96 * KB;              // K~  [2][64][128 B]
 constexpr uint32_t OFF_NW = 112 * KB;             // -W^T [128 rows d_k][128 B]
 constexpr uint32_t OFF_S0 = 128 * KB;             // S0 bf16 [2][128][128 B] | solve A, T fp32
-constexpr uint32_t OFF_UT = 160 * KB;             // U^T bf16 [128][128 B]
-constexpr uint32_t OFF_P = 176 * KB;              // P bf16 [64][128 B]
-constexpr uint32_t OFF_T1 = 184 * KB;             // T' bf16 [64][128 B]
-constexpr uint32_t OFF_T2 = 192 * KB;             // T'' bf16 [64][128 B]
-constexpr uint32_t OFF_OUT = OFF_UT;              // output staging (aliases UT, P, T1)
-constexpr uint32_t OFF_MISC = 200 * KB;
+// T', T'' (hi, lo) [64][128 B] each; later U^T (hi, lo) [128][128 B]; later output staging
+constexpr uint32_t OFF_TU = 160 * KB;
+constexpr uint32_t OFF_T1H = OFF_TU, OFF_T1L = OFF_TU + 8 * KB;
+constexpr uint32_t OFF_T2H = OFF_TU + 16 * KB, OFF_T2L = OFF_TU + 24 * KB;
+constexpr uint32_t OFF_UTH = OFF_TU, OFF_UTL = OFF_TU + 16 * KB;
+constexpr uint32_t OFF_OUT = OFF_TU;
+constexpr uint32_t OFF_PH = 192 * KB, OFF_PL = 200 * KB;   // P (hi, lo) [64][128 B]
+constexpr uint32_t OFF_MISC = 208 * KB;
 constexpr uint32_t MISC_X = 2048;                 // solve scratch, 3 x 16 x 16 fp32
 constexpr uint32_t MISC_BAR = 5120;
 constexpr uint32_t SMEM_BYTES = OFF_MISC + 6 * KB + KB;   // + alignment slack
@@ -112,6 +117,27 @@ __device__ __forceinline__ void store_row_bf16(uint32_t tile, int r, int c0, con
     st_shared_v4(sw128(tile, r, c0 + c), pack_bf16(w[0] * mul, w[1] * mul),
                  pack_bf16(w[2] * mul, w[3] * mul), pack_bf16(w[4] * mul, w[5] * mul),
                  pack_bf16(w[6] * mul, w[7] * mul));
+  }
+}
+
+// 32 fp32 values -> bf16 hi = rn(v) and lo = rn(v - hi) rows of two tiles (v = hi + lo to
+// about 2^-16 relative): the small intra-chunk matrices keep ~16 mantissa bits this way.
+__device__ __forceinline__ void store_row_hilo(uint32_t tile_hi, uint32_t tile_lo, int r, int c0,
+                                               const float* v) {
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    uint32_t hw[4], lw[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float x0 = v[8 * c + 2 * e], x1 = v[8 * c + 2 * e + 1];
+      const __nv_bfloat162 h = __floats2bfloat162_rn(x0, x1);
+      const float2 hf = __bfloat1622float2(h);
+      const __nv_bfloat162 l = __floats2bfloat162_rn(x0 - hf.x, x1 - hf.y);
+      hw[e] = *reinterpret_cast<const uint32_t*>(&h);
+      lw[e] = *reinterpret_cast<const uint32_t*>(&l);
+    }
+    st_shared_v4(sw128(tile_hi, r, c0 + c), hw[0], hw[1], hw[2], hw[3]);
+    st_shared_v4(sw128(tile_lo, r, c0 + c), lw[0], lw[1], lw[2], lw[3]);
   }
 }
 
@@ -386,7 +412,7 @@ __global__ void __launch_bounds__(THREADS, 1)
           const int s = 32 * hc + j;
           v[j] = (s <= r) ? expf(Gr - sG[s]) * v[j] * mr * sNk[s] : 0.f;
         }
-        store_row_bf16(sb + OFF_P, r, 4 * hc, v, 1.0f);
+        store_row_hilo(sb + OFF_PH, sb + OFF_PL, r, 4 * hc, v);
       }
     }
     // ---- Q~ = diag(scale e^G / ||q||) Q in place;  K~ = diag(e^{G_C-G} / ||k||) K -> KT
@@ -407,35 +433,44 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
     __syncthreads();
 
-    // ---- the direct solve T = (I + A)^{-1}, then T' and T'' as bf16 B operands
+    // ---- the direct solve T = (I + A)^{-1}, then T' and T'' as bf16 (hi, lo) B operands
     solve_unit_lower(As, Ts, sX, tid);
     for (int idx = tid; idx < 1024; idx += THREADS) {
       const int which = idx >> 9, r = (idx >> 3) & 63, c = idx & 7;
       const float* trow = Ts + r * LA + 8 * c;
-      float w[8];
+      uint32_t hw[4], lw[4];
 #pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        const int s = 8 * c + e;
-        const float f = which ? sBeta[s] : sBeta[s] * sEG[s] * sNk[s];
-        w[e] = trow[e] * f;
+      for (int e = 0; e < 4; ++e) {
+        const int s = 8 * c + 2 * e;
+        const float f0 = which ? sBeta[s] : sBeta[s] * sEG[s] * sNk[s];
+        const float f1 = which ? sBeta[s + 1] : sBeta[s + 1] * sEG[s + 1] * sNk[s + 1];
+        const float x0 = trow[2 * e] * f0, x1 = trow[2 * e + 1] * f1;
+        const __nv_bfloat162 h = __floats2bfloat162_rn(x0, x1);
+        const float2 hf = __bfloat1622float2(h);
+        const __nv_bfloat162 l = __floats2bfloat162_rn(x0 - hf.x, x1 - hf.y);
+        hw[e] = *reinterpret_cast<const uint32_t*>(&h);
+        lw[e] = *reinterpret_cast<const uint32_t*>(&l);
       }
-      st_shared_v4(sw128(sb + (which ? OFF_T2 : OFF_T1), r, c), pack_bf16(w[0], w[1]),
-                   pack_bf16(w[2], w[3]), pack_bf16(w[4], w[5]), pack_bf16(w[6], w[7]));
+      st_shared_v4(sw128(sb + (which ? OFF_T2H : OFF_T1H), r, c), hw[0], hw[1], hw[2], hw[3]);
+      st_shared_v4(sw128(sb + (which ? OFF_T2L : OFF_T1L), r, c), lw[0], lw[1], lw[2], lw[3]);
     }
     fence_proxy_async_smem();
     __syncthreads();
 
-    // ---- MMA 3/4: W^T = K^T T'^T (M = d_k), U'^T = V^T T''^T (M = d_v)  (K = 64 tokens)
+    // ---- MMA 3/4: W^T = K^T T'^T (M = d_k), U'^T = V^T T''^T (M = d_v)  (K = 64 tokens),
+    //      T' and T'' each as hi + lo
     if (tid == 0) {
       tc_fence_after();
 #pragma unroll
-      for (int k = 0; k < 4; ++k)
-        mma_bf16(tmem + TM_W, sdesc_sw128(buf + k * 2048, IN_KQ_KB, 1024),
-                 sdesc_sw128(sb + OFF_T1 + k * 32, 16, 1024), ID_KT, k > 0);
+      for (int k = 0; k < 8; ++k)
+        mma_bf16(tmem + TM_W, sdesc_sw128(buf + (k & 3) * 2048, IN_KQ_KB, 1024),
+                 sdesc_sw128(sb + (k < 4 ? OFF_T1H : OFF_T1L) + (k & 3) * 32, 16, 1024), ID_KT,
+                 k > 0);
 #pragma unroll
-      for (int k = 0; k < 4; ++k)
-        mma_bf16(tmem + TM_U, sdesc_sw128(buf + IN_V + k * 2048, 8 * KB, 1024),
-                 sdesc_sw128(sb + OFF_T2 + k * 32, 16, 1024), ID_KT, k > 0);
+      for (int k = 0; k < 8; ++k)
+        mma_bf16(tmem + TM_U, sdesc_sw128(buf + IN_V + (k & 3) * 2048, 8 * KB, 1024),
+                 sdesc_sw128(sb + (k < 4 ? OFF_T2H : OFF_T2L) + (k & 3) * 32, 16, 1024), ID_KT,
+                 k > 0);
       mma_commit(bar_mma);
     }
     // ---- C0 (overlaps MMA 3/4): S -> S0 (bf16 A operand [i][j], K-major); S <- e^{G_C} S
@@ -486,29 +521,32 @@ __global__ void __launch_bounds__(THREADS, 1)
     if (!mbar_wait_bounded(bar_mma, mma_phase)) atomicExch(sAbort, 1);
     mma_phase ^= 1;
     tc_fence_after();
-    // ---- C2: U^T -> bf16 A operand [i][s], K-major
+    // ---- C2: U^T -> bf16 (hi, lo) A operands [i][s], K-major
     {
       float v[32];
       tmem_ld32(tmem + lane_off + TM_U + 32 * hc, v);
       tmem_wait_ld();
-      store_row_bf16(sb + OFF_UT, row, 4 * hc, v, 1.0f);
+      store_row_hilo(sb + OFF_UTH, sb + OFF_UTL, row, 4 * hc, v);
     }
     fence_proxy_async_smem();
     tc_fence_before();
     __syncthreads();
     if (*sAbort) { aborted = true; break; }
 
-    // ---- C3: O^T += U^T P^T ;  S += U^T K~   (K = 64 tokens)
+    // ---- C3: O^T += U^T P^T (as Uh Ph + Ul Ph + Uh Pl) ;  S += U^T K~ (as Uh K~ + Ul K~)
     if (tid == 0) {
       tc_fence_after();
 #pragma unroll
-      for (int k = 0; k < 4; ++k)
-        mma_bf16(tmem + TM_O, sdesc_sw128(sb + OFF_UT + k * 32, 16, 1024),
-                 sdesc_sw128(sb + OFF_P + k * 32, 16, 1024), ID_SQ, true);
+      for (int k = 0; k < 12; ++k) {
+        const uint32_t ua = (k < 4 || k >= 8) ? OFF_UTH : OFF_UTL;
+        const uint32_t pb = (k < 8) ? OFF_PH : OFF_PL;
+        mma_bf16(tmem + TM_O, sdesc_sw128(sb + ua + (k & 3) * 32, 16, 1024),
+                 sdesc_sw128(sb + pb + (k & 3) * 32, 16, 1024), ID_SQ, true);
+      }
 #pragma unroll
-      for (int k = 0; k < 4; ++k)
-        mma_bf16(tmem + TM_S, sdesc_sw128(sb + OFF_UT + k * 32, 16, 1024),
-                 sdesc_sw128(sb + OFF_KT + k * 2048, 8 * KB, 1024), ID_UK, true);
+      for (int k = 0; k < 8; ++k)
+        mma_bf16(tmem + TM_S, sdesc_sw128(sb + (k < 4 ? OFF_UTH : OFF_UTL) + (k & 3) * 32, 16, 1024),
+                 sdesc_sw128(sb + OFF_KT + (k & 3) * 2048, 8 * KB, 1024), ID_UK, true);
       mma_commit(bar_mma);
     }
     if (!mbar_wait_bounded(bar_mma, mma_phase)) atomicExch(sAbort, 1);
