@@ -36,7 +36,7 @@ import gdn_inputs as gi  # noqa: E402
 METRIC = "GDN prefill tokens/s (27B layer shape) and decode state-update HBM GB/s"
 HK, HV, D, W = 16, 48, 128, 4
 T_TOTAL, BUCKET = 131072, 512
-DECODE_B, DECODE_STEPS = 128, 256
+DECODE_B, DECODE_STEPS = 128, 256   # --prefill-tokens / --decode-batch shrink these for ncu
 C_CONV = (2 * HK + HV) * D
 # algorithmic work (chunked WY/UT form, d = 128, C = 64): 6 d^2 + 10 C d FLOP per token per
 # value head on the tensor cores
@@ -259,7 +259,13 @@ def main():
     ap.add_argument("--cpu-tokens", type=int, default=2048)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--prefill-tokens", type=int, default=T_TOTAL,
+                    help="tokens of the prefill workload (a multiple of 512; smaller only for "
+                         "profiling captures, the reported workload is 131072)")
+    ap.add_argument("--decode-batch", type=int, default=DECODE_B)
     args = ap.parse_args()
+    globals()["T_TOTAL"] = args.prefill_tokens
+    globals()["DECODE_B"] = args.decode_batch
     if args.impl == "reference":
         return run_reference(args)
 

@@ -51,8 +51,8 @@ cudaError_t gdn_launch_checkpoint(int op, int Hv, int d, int conv_elems, int con
   if (n == 0) return cudaSuccess;
   const long long state_v4 = (long long)Hv * d * d / 4;
   const long long conv_v4 = (long long)conv_elems * conv_elem_bytes / 16;
-  // ~64 KB per block: enough blocks per pair to keep HBM busy even for one pair
-  int bx = (int)((state_v4 * 16 + 65535) / 65536);
+  // ~8 KB per block: enough blocks per pair to keep HBM busy even for one pair
+  int bx = (int)((state_v4 * 16 + 8191) / 8192);
   if (bx < 1) bx = 1;
   dim3 grid((unsigned)bx, (unsigned)n, 1);
   gdn_checkpoint_kernel<<<grid, 256, 0, stream>>>(op, state_v4, conv_v4, (float4*)state,

@@ -24,7 +24,7 @@ unsigned gdn_take_error_conv() {
   return v;
 }
 
-constexpr int TCH = 32;   // tokens per thread
+constexpr int TCH = 8;    // tokens per thread (>= W - 1)
 
 __device__ __forceinline__ void load8(const __nv_bfloat16* p, float (&v)[8]) {
   uint4 u = *reinterpret_cast<const uint4*>(p);
@@ -58,8 +58,8 @@ __global__ void __launch_bounds__(128) gdn_conv_kernel(int B, int T_, int C, int
                                                        T* cs, int num_slots,
                                                        const int32_t* slots, int silu, T* y,
                                                        long long ys) {
-  const int c0 = (blockIdx.x * blockDim.x + threadIdx.x) * 8;
-  const int t0 = blockIdx.y * TCH;
+  const int c0 = (blockIdx.y * blockDim.x + threadIdx.x) * 8;
+  const int t0 = blockIdx.x * TCH;
   const int b = blockIdx.z;
   if (c0 >= C) return;
   const int slot = slots ? slots[b] : b;
@@ -94,7 +94,7 @@ __global__ void __launch_bounds__(128) gdn_conv_kernel(int B, int T_, int C, int
   }
   // new conv state (first token run only): last W-1 inputs, read before anything is written
   float nst[3][8];
-  const bool owner = (blockIdx.y == 0);
+  const bool owner = (blockIdx.x == 0);
   if (owner) {
 #pragma unroll
     for (int i = 0; i < 3; ++i) {
@@ -106,9 +106,17 @@ __global__ void __launch_bounds__(128) gdn_conv_kernel(int B, int T_, int C, int
     }
   }
   const int t1 = min(T_, t0 + TCH);
-  for (int t = t0; t < t1; ++t) {
-    float xn[8], out[8];
-    load8(xb + (size_t)t * xs, xn);
+  // all of this run's inputs are independent loads: issue them together
+  float xr[TCH][8];
+#pragma unroll
+  for (int i = 0; i < TCH; ++i)
+    if (t0 + i < t1) load8(xb + (size_t)(t0 + i) * xs, xr[i]);
+#pragma unroll
+  for (int i = 0; i < TCH; ++i) {
+    if (t0 + i >= t1) break;
+    const int t = t0 + i;
+    float out[8];
+    const float (&xn)[8] = xr[i];
 #pragma unroll
     for (int c = 0; c < 8; ++c) {
       float acc = bi[c];
@@ -143,7 +151,7 @@ cudaError_t gdn_launch_conv(int B, int T, int C, int W, int bf16, const void* x,
                             void* y, long long y_tok_stride, cudaStream_t stream) {
   if (B == 0 || T == 0) return cudaSuccess;
   const int threads = 128;
-  dim3 grid((unsigned)((C / 8 + threads - 1) / threads), (unsigned)((T + TCH - 1) / TCH),
+  dim3 grid((unsigned)((T + TCH - 1) / TCH), (unsigned)((C / 8 + threads - 1) / threads),
             (unsigned)B);
   if (bf16)
     gdn_conv_kernel<__nv_bfloat16><<<grid, threads, 0, stream>>>(

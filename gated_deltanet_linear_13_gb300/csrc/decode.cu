@@ -28,8 +28,12 @@ unsigned gdn_take_error_decode() {
   return v;
 }
 
-__device__ __forceinline__ void cluster_arrive_release() {
-  asm volatile("barrier.cluster.arrive.release.aligned;\n" ::: "memory");
+// Relaxed arrive: the only ordering needed is "every CTA's loads of the old conv state have
+// returned before the writer stores the new one", and those loaded values are consumed (a
+// data dependence) before the arrive.  A release arrive would also wait for the state-row
+// loads already in flight, which stalls the stream.
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;\n" ::: "memory");
 }
 __device__ __forceinline__ void cluster_wait_acquire() {
   asm volatile("barrier.cluster.wait.acquire.aligned;\n" ::: "memory");
@@ -94,6 +98,13 @@ __global__ void __launch_bounds__(256) gdn_decode_kernel(GdnLayerArgs p, int nsp
     return;
   }
 
+  // The state rows do not depend on the conv / norm / gates: issue their loads first so that
+  // their latency overlaps the prologue.
+  float* Sg = p.state + (((size_t)slot * p.Hv + h) * D + r0 + (threadIdx.x >> 5) * RPW) * D;
+  float4 s[RPW];
+#pragma unroll
+  for (int i = 0; i < RPW; ++i) s[i] = reinterpret_cast<const float4*>(Sg + i * D)[lane];
+
   __shared__ __align__(16) float sq[D];
   __shared__ __align__(16) float sk[D];
   __shared__ float sv[R];
@@ -146,7 +157,7 @@ __global__ void __launch_bounds__(256) gdn_decode_kernel(GdnLayerArgs p, int nsp
   if (lane == 0) red[warp] = ss;
   __syncthreads();
   // every CTA of the cluster has now read the old conv state it needs
-  cluster_arrive_release();
+  cluster_arrive_relaxed();
   {
     const float n2 = isk ? (red[4] + red[5] + red[6] + red[7]) : (red[0] + red[1] + red[2] + red[3]);
     const float inv = p.l2norm ? 1.0f / sqrtf(n2 + p.eps) : 1.0f;
@@ -166,10 +177,6 @@ __global__ void __launch_bounds__(256) gdn_decode_kernel(GdnLayerArgs p, int nsp
   // ---- 3. stream this CTA's R rows of S: each warp owns RPW consecutive rows
   const float4 k4 = reinterpret_cast<const float4*>(sk)[lane];
   const float4 q4 = reinterpret_cast<const float4*>(sq)[lane];
-  float* Sg = p.state + (((size_t)slot * p.Hv + h) * D + r0 + warp * RPW) * D;
-  float4 s[RPW];
-#pragma unroll
-  for (int i = 0; i < RPW; ++i) s[i] = reinterpret_cast<const float4*>(Sg + i * D)[lane];
 #pragma unroll
   for (int i = 0; i < RPW; ++i) {
     const float al = warp_sum(dot4(s[i], k4));

@@ -212,8 +212,9 @@ __global__ void __launch_bounds__(THREADS, 1)
                           const __grid_constant__ CUtensorMap tm_v,
                           const __grid_constant__ CUtensorMap tm_o, const TcParams p) {
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                           ~static_cast<uintptr_t>(1023));
+  // 1024-byte aligned base, formed by offsetting the shared array itself so that every
+  // pointer derived from it stays in the shared state space (no generic accesses)
+  uint8_t* sm = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
   const uint32_t sb = smem_addr(sm);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int q4 = warp & 3, hc = warp >> 2;
@@ -298,6 +299,27 @@ __global__ void __launch_bounds__(THREADS, 1)
   uint32_t mma_phase = 0;
   bool aborted = false;
 
+  // raw gate inputs of the next chunk, loaded one chunk ahead by warp 0 (2 tokens per lane)
+  float ra[2] = {0.f, 0.f}, rb[2] = {0.f, 0.f};
+  auto load_gates = [&](int n) {
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      const int t = n * C + 2 * lane + e;
+      ra[e] = rb[e] = 0.f;
+      if (t < p.T) {
+        const size_t gi = ((size_t)b * p.T + t) * p.Hv + h;
+        if (p.gates_pre) {
+          ra[e] = reinterpret_cast<const float*>(p.a)[gi];
+          rb[e] = reinterpret_cast<const float*>(p.b)[gi];
+        } else {
+          ra[e] = ld_gate<Tin>(p.a, gi);
+          rb[e] = ld_gate<Tin>(p.b, gi);
+        }
+      }
+    }
+  };
+  if (warp == 0) load_gates(0);
+
   for (int n = 0; n < nchunks; ++n) {
     const int t0 = n * C;
     const uint32_t buf = sb + ((n & 1) ? OFF_IN1 : OFF_IN0);
@@ -309,18 +331,12 @@ __global__ void __launch_bounds__(THREADS, 1)
       float g2[2] = {0.f, 0.f}, b2[2] = {0.f, 0.f};
 #pragma unroll
       for (int e = 0; e < 2; ++e) {
-        const int t = t0 + 2 * lane + e;
-        if (t < p.T) {
-          const size_t gi = ((size_t)b * p.T + t) * p.Hv + h;
-          if (p.gates_pre) {
-            g2[e] = reinterpret_cast<const float*>(p.a)[gi];
-            b2[e] = reinterpret_cast<const float*>(p.b)[gi];
-          } else {
-            g2[e] = gate_g(ld_gate<Tin>(p.a, gi), A_log_h, dtb_h);
-            b2[e] = sigmoid_f(ld_gate<Tin>(p.b, gi));
-          }
+        if (t0 + 2 * lane + e < p.T) {
+          g2[e] = p.gates_pre ? ra[e] : gate_g(ra[e], A_log_h, dtb_h);
+          b2[e] = p.gates_pre ? rb[e] : sigmoid_f(rb[e]);
         }
       }
+      if (n + 1 < nchunks) load_gates(n + 1);
       float s = g2[0] + g2[1];
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
