@@ -26,8 +26,9 @@ STATUS_NAMES = {0: "GDN_OK", 1: "GDN_ERR_INVALID_ARGUMENT", 2: "GDN_ERR_UNSUPPOR
                 6: "GDN_ERR_DEVICE_INDEX"}
 
 EXPORTED = ("gdn_prefill_workspace_size", "gdn_chunk_prefill", "gdn_decode_step",
-            "causal_conv1d_update", "gdn_state_checkpoint", "gdn_get_device_error",
-            "gdn_status_string", "gdn_version")
+            "causal_conv1d_update", "gdn_state_checkpoint", "gdn_chunk_prefill_noalloc",
+            "gdn_get_device_error", "gdn_status_string", "gdn_version")
+NOALLOC_SCRATCH_BYTES = 32 << 20   # GDN_NOALLOC_SCRATCH_BYTES in include/gdn.h
 
 
 class GDNError(RuntimeError):
@@ -68,6 +69,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     L.gdn_prefill_workspace_size.argtypes = [dp, op]
     L.gdn_chunk_prefill.restype = ctypes.c_int
     L.gdn_chunk_prefill.argtypes = [dp, op] + [_vp] * 14 + [ctypes.c_size_t, _vp]
+    L.gdn_chunk_prefill_noalloc.restype = ctypes.c_int
+    L.gdn_chunk_prefill_noalloc.argtypes = [dp, op] + [_vp] * 13 + [_vp]
     L.gdn_decode_step.restype = ctypes.c_int
     L.gdn_decode_step.argtypes = [dp, op] + [_vp] * 13 + [_vp]
     L.causal_conv1d_update.restype = ctypes.c_int
@@ -215,6 +218,31 @@ def gdn_chunk_prefill(q, k, v, a, b, A_log, dt_bias, state, out, *, num_k_heads=
                              _ptr(conv_bias), _ptr(state), _ptr(conv_state), _ptr(state_slots),
                              _ptr(out), _ptr(workspace), ws_bytes, _stream(stream))
     _check(st, "gdn_chunk_prefill")
+    return out
+
+
+def gdn_chunk_prefill_noalloc(q, k, v, a, b, A_log, dt_bias, state, out, *, num_k_heads=None,
+                              conv_weight=None, conv_bias=None, conv_state=None,
+                              state_slots=None, scale: float = 1.0, eps: float = 1e-6,
+                              qk_l2norm: bool = True, conv_silu: bool = True,
+                              gates_precomputed: bool = False, stream=None) -> torch.Tensor:
+    """gdn_chunk_prefill without a workspace, for callers that cannot allocate: the library's
+    fixed device scratch array (NOALLOC_SCRATCH_BYTES per GPU) holds the post-conv
+    activations.  Raises GDNError(GDN_ERR_WORKSPACE) when the call needs more than that.
+    Calls that overlap on the GPU share that array and must be serialised."""
+    L = load_library()
+    B, T, Hk, Hv, W, num_slots = _layer_dims(q, k, v, a, num_k_heads, conv_weight, conv_state,
+                                             state, state_slots, None)
+    _check_layer(q, k, v, a, b, A_log, dt_bias, conv_weight, conv_bias, state, conv_state,
+                 state_slots, out, B, T, Hk, Hv, W, num_slots, gates_precomputed)
+    dims = GdnDims(B, T, Hk, Hv, HEAD_DIM, 64, W, num_slots)
+    opts = _opts(_dt(q), _dt(out), qk_l2norm, eps, scale, conv_silu, gates_precomputed)
+    st = L.gdn_chunk_prefill_noalloc(ctypes.byref(dims), ctypes.byref(opts), _ptr(q), _ptr(k),
+                                     _ptr(v), _ptr(a), _ptr(b), _ptr(A_log), _ptr(dt_bias),
+                                     _ptr(conv_weight), _ptr(conv_bias), _ptr(state),
+                                     _ptr(conv_state), _ptr(state_slots), _ptr(out),
+                                     _stream(stream))
+    _check(st, "gdn_chunk_prefill_noalloc")
     return out
 
 

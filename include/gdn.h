@@ -185,6 +185,35 @@ gdn_status gdn_state_checkpoint(int32_t op, const gdn_dims* dims, gdn_dtype conv
                                 void* stream);
 
 /*
+ * gdn_chunk_prefill_noalloc -- gdn_chunk_prefill for callers that cannot allocate device
+ * memory.  The pages have no counterpart of this call; it is a convenience of this library.
+ *
+ * With a conv in front (conv_width > 0) the prefill needs scratch memory for the post-conv
+ * activations, which gdn_chunk_prefill takes from a caller-provided workspace.  Some callers
+ * cannot provide one: code recorded into a CUDA graph that must not call cudaMalloc, plug-ins
+ * that a host framework hands only input and output pointers, services whose allocator
+ * forbids allocations after start-up.  This variant takes the same arguments minus the
+ * workspace and uses a file-scope device array of GDN_NOALLOC_SCRATCH_BYTES bytes instead;
+ * every GPU that loads the library holds that array until the process exits.  It calls no
+ * cudaMalloc, cudaFree or other allocating routine.
+ *   - Limit: if gdn_prefill_workspace_size() of the call exceeds GDN_NOALLOC_SCRATCH_BYTES
+ *     (for bf16, B * T * C_conv * 2 bytes; e.g. 1536 tokens at C_conv = 10240), it returns
+ *     GDN_ERR_WORKSPACE and launches nothing.  Calls without a conv use no scratch.
+ *   - Set-up: the first call on a device looks up the array's device address (with that
+ *     device current) and caches it; make that first call before any stream capture.
+ *   - Sharing: all calls share the one array and it keeps the last call's contents (nothing
+ *     in it has to start at zero: each call writes every byte it reads).  Calls that overlap
+ *     on the GPU (different streams, concurrent graph replays) race on it: serialise them.
+ */
+#define GDN_NOALLOC_SCRATCH_BYTES (32u << 20)
+gdn_status gdn_chunk_prefill_noalloc(const gdn_dims* dims, const gdn_opts* opts, const void* q,
+                                     const void* k, const void* v, const void* a, const void* b,
+                                     const float* A_log, const float* dt_bias,
+                                     const void* conv_weight, const void* conv_bias,
+                                     float* state, void* conv_state,
+                                     const int32_t* state_slots, void* out, void* stream);
+
+/*
  * Synchronises `stream`, then returns and clears the device error word: GDN_OK, or the
  * first condition recorded by a kernel since the last call (GDN_ERR_DEVICE_INDEX,
  * GDN_ERR_DEVICE_TIMEOUT), or GDN_ERR_CUDA if the synchronisation itself failed.
