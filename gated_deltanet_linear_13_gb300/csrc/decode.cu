@@ -7,8 +7,11 @@
 // Row independence: row i of S only needs v_i, and the output o_i only needs row i:
 //     alpha = s_i . k,  gamma = s_i . q,  delta_i = beta (v_i - e^g alpha),
 //     s_i <- e^g s_i + delta_i k,        o_i = e^g gamma + delta_i (k . q)
-// (o = S_new q = e^g S q + delta (k . q)), so each row is streamed through once: one warp
-// reads the 512-byte row with 128-bit loads, reduces two dot products, writes the row back.
+// (o = S_new q = e^g S q + delta (k . q)), so each row is streamed through once.  A CTA's
+// R contiguous state rows (R * 512 bytes) move HBM -> shared memory with one TMA bulk copy
+// issued before the conv / norm / gates prologue, and back with one bulk store: the bytes in
+// flight do not depend on registers or occupancy.  In shared memory one warp handles a
+// 512-byte row with 128-bit accesses and two warp-wide dot products.
 //
 // Work split: a thread-block cluster per (b, key head); its CTAs are the r = Hv/Hk value
 // heads of that key head times `nsplit` row blocks of R = 128/nsplit rows.  Every CTA
@@ -16,8 +19,10 @@
 // reads of the old q/k conv state before the one CTA that writes the new one.  The v
 // channels of rows [r0, r0+R) belong to one CTA only.
 #include "common.cuh"
+#include "sm100_ptx.cuh"
 
 using namespace gdn;
+using namespace gdn::ptx;
 
 static __device__ unsigned int g_err_decode;
 
@@ -98,12 +103,21 @@ __global__ void __launch_bounds__(256) gdn_decode_kernel(GdnLayerArgs p, int nsp
     return;
   }
 
-  // The state rows do not depend on the conv / norm / gates: issue their loads first so that
-  // their latency overlaps the prologue.
-  float* Sg = p.state + (((size_t)slot * p.Hv + h) * D + r0 + (threadIdx.x >> 5) * RPW) * D;
-  float4 s[RPW];
-#pragma unroll
-  for (int i = 0; i < RPW; ++i) s[i] = reinterpret_cast<const float4*>(Sg + i * D)[lane];
+  // The state rows do not depend on the conv / norm / gates: one bulk copy brings this CTA's
+  // R rows into shared memory while the prologue runs.
+  extern __shared__ __align__(128) float sS[];   // [R][D]
+  __shared__ __align__(8) uint64_t sbar;
+  float* Sg = p.state + (((size_t)slot * p.Hv + h) * D + r0) * D;
+  const uint32_t bar = smem_addr(&sbar);
+  if (tid == 0) {
+    mbar_init(bar, 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (tid == 0) {
+    mbar_arrive_expect_tx(bar, R * D * 4);
+    bulk_load(smem_addr(sS), Sg, R * D * 4, bar);
+  }
 
   __shared__ __align__(16) float sq[D];
   __shared__ __align__(16) float sk[D];
@@ -174,9 +188,15 @@ __global__ void __launch_bounds__(256) gdn_decode_kernel(GdnLayerArgs p, int nsp
   const float g = sgate[0], beta = sgate[1];
   const float eg = expf(g);
 
-  // ---- 3. stream this CTA's R rows of S: each warp owns RPW consecutive rows
+  // ---- 3. update this CTA's R rows of S in shared memory: each warp owns RPW rows
   const float4 k4 = reinterpret_cast<const float4*>(sk)[lane];
   const float4 q4 = reinterpret_cast<const float4*>(sq)[lane];
+  const bool landed = mbar_wait_bounded(bar, 0);
+  if (!landed && tid == 0) atomicOr(&g_err_decode, kErrTimeout);
+  float* Sw = sS + warp * RPW * D;
+  float4 s[RPW];
+#pragma unroll
+  for (int i = 0; i < RPW; ++i) s[i] = reinterpret_cast<const float4*>(Sw + i * D)[lane];
 #pragma unroll
   for (int i = 0; i < RPW; ++i) {
     const float al = warp_sum(dot4(s[i], k4));
@@ -188,10 +208,15 @@ __global__ void __launch_bounds__(256) gdn_decode_kernel(GdnLayerArgs p, int nsp
     t.y = fmaf(eg, s[i].y, delta * k4.y);
     t.z = fmaf(eg, s[i].z, delta * k4.z);
     t.w = fmaf(eg, s[i].w, delta * k4.w);
-    reinterpret_cast<float4*>(Sg + i * D)[lane] = t;
+    reinterpret_cast<float4*>(Sw + i * D)[lane] = t;
     if (lane == 0) so[row] = fmaf(eg, ga, delta * kq);
   }
+  fence_proxy_async_smem();
   __syncthreads();
+  if (tid == 0 && landed) {
+    bulk_store(Sg, smem_addr(sS), R * D * 4);
+    tma_store_commit();
+  }
   // ---- 4. outputs and conv state
   if (tid < R) {
     Tout* o = (Tout*)p.out + ((size_t)b * p.Hv + h) * D + r0 + tid;
@@ -200,15 +225,19 @@ __global__ void __launch_bounds__(256) gdn_decode_kernel(GdnLayerArgs p, int nsp
   }
   cluster_wait_acquire();
   if (p.W > 1 && hh == 0 && sp == 0) conv_store_state<Tin>(p, slot, ch, win);
+  if (tid == 0) tma_store_wait_all();     // the bulk store has read shared memory and landed
 }
 
 template <typename Tin, typename Tout, int R>
 static cudaError_t launch_decode_t(const GdnLayerArgs& p, int nsplit, cudaStream_t stream) {
+  static unsigned done = 0;
+  cudaError_t e = set_smem_once(gdn_decode_kernel<Tin, Tout, R>, R * kHeadDim * 4, &done);
+  if (e != cudaSuccess) return e;
   const int r = p.Hv / p.Hk;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)(p.B * p.Hk * r * nsplit), 1, 1);
   cfg.blockDim = dim3(256, 1, 1);
-  cfg.dynamicSmemBytes = 0;
+  cfg.dynamicSmemBytes = (size_t)R * kHeadDim * 4;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
