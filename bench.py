@@ -49,6 +49,24 @@ CLOCK_QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.ac
                "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
 
+def measured_traffic(key: str):
+    """DRAM bytes per launch recorded from an ncu capture (profiles/traffic.json), or None
+    when the kernel sources changed since that capture."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        rec = json.load(open(path))[key]
+    except (OSError, KeyError, ValueError):
+        return None
+    for src, digest in rec.get("sources", {}).items():
+        try:
+            if hashlib.sha256(open(os.path.join(ROOT, src), "rb").read()).hexdigest() != digest:
+                return None
+        except OSError:
+            return None
+    return rec["bytes"]
+
+
 def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -437,7 +455,8 @@ def main():
                        "parallelism": f"replicas x{world}"},
             "roofline": {"bound": "tensor", "achieved": achieved_tflops,
                          "peak": peaks["bf16_sustained"], "unit": "TFLOP/s",
-                         "frac": achieved_tflops / peaks["bf16_sustained"], "traffic": None,
+                         "frac": achieved_tflops / peaks["bf16_sustained"],
+                         "traffic": measured_traffic("prefill_call"),
                          "kernel": "gdn_chunk_prefill (conv + chunked recurrence), 512 tokens",
                          "flop_per_launch": FLOP_PER_TOKEN * BUCKET,
                          "launch_ms": call_ms, "peak_source": peaks["source"] + " sustained"},
@@ -447,7 +466,8 @@ def main():
                        "bytes_per_step": dec_bytes,
                        "roofline": {"bound": "hbm", "achieved": dec_gbs,
                                     "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                                    "frac": dec_gbs / peaks["hbm_gbs"], "traffic": None,
+                                    "frac": dec_gbs / peaks["hbm_gbs"],
+                                    "traffic": measured_traffic("decode_step"),
                                     "peak_source": peaks["source"]},
                        "l2": "state 805 MB > L2"},
             "e2e": e2e,
