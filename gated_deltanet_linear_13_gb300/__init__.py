@@ -28,7 +28,7 @@ STATUS_NAMES = {0: "GDN_OK", 1: "GDN_ERR_INVALID_ARGUMENT", 2: "GDN_ERR_UNSUPPOR
 EXPORTED = ("gdn_prefill_workspace_size", "gdn_chunk_prefill", "gdn_decode_step",
             "causal_conv1d_update", "gdn_state_checkpoint", "gdn_chunk_prefill_noalloc",
             "gdn_get_device_error", "gdn_status_string", "gdn_version")
-NOALLOC_SCRATCH_BYTES = 32 << 20   # GDN_NOALLOC_SCRATCH_BYTES in include/gdn.h
+NOALLOC_SCRATCH_BYTES = 64 << 20   # GDN_NOALLOC_SCRATCH_BYTES in include/gdn.h
 
 
 class GDNError(RuntimeError):

@@ -85,7 +85,13 @@ struct GdnLayerArgs {
   float* state; void* conv_state;
   const int32_t* slots;
   void* out;
+  // workspace of the tensor-core prefill (chunk tiles between its two kernels)
+  void* scratch;
+  size_t scratch_bytes;
 };
+
+// Workspace bytes the tensor-core prefill needs for B sequences of T tokens, Hv value heads.
+size_t gdn_prefill_tc_scratch_bytes(int B, int T, int Hv);
 
 cudaError_t gdn_launch_decode(const GdnLayerArgs& args, cudaStream_t stream);
 cudaError_t gdn_launch_prefill_simt(const GdnLayerArgs& args, cudaStream_t stream);

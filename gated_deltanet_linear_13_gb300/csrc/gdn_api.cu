@@ -96,9 +96,17 @@ gdn_status check_layer_ptrs(const Checked& c, const gdn_opts* o, const void* q, 
   return GDN_OK;
 }
 
-size_t workspace_bytes_for(const Checked& c) {
+// Workspace: [post-conv activations, when conv_width > 0][tensor-core prefill tiles, bf16].
+size_t conv_bytes_for(const Checked& c) {
   if (c.W == 0) return 0;
-  return (size_t)c.B * (size_t)c.T * (size_t)c.Cc * c.in_elem;
+  const size_t n = (size_t)c.B * (size_t)c.T * (size_t)c.Cc * c.in_elem;
+  return (n + 1023) & ~(size_t)1023;
+}
+
+size_t workspace_bytes_for(const Checked& c, const gdn_opts* o) {
+  size_t n = conv_bytes_for(c);
+  if (o->in_dtype == GDN_BF16) n += gdn_prefill_tc_scratch_bytes(c.B, c.T, c.Hv);
+  return n;
 }
 
 }  // namespace
@@ -123,7 +131,7 @@ const char* gdn_status_string(gdn_status s) {
 size_t gdn_prefill_workspace_size(const gdn_dims* dims, const gdn_opts* opts) {
   Checked c;
   if (check_dims(dims, opts, false, &c) != GDN_OK) return 0;
-  return workspace_bytes_for(c);
+  return workspace_bytes_for(c, opts);
 }
 
 gdn_status gdn_chunk_prefill(const gdn_dims* dims, const gdn_opts* opts, const void* q,
@@ -140,10 +148,13 @@ gdn_status gdn_chunk_prefill(const gdn_dims* dims, const gdn_opts* opts, const v
   st = check_layer_ptrs(c, opts, q, k, v, a, b, A_log, dt_bias, conv_weight, conv_bias, state,
                         conv_state, state_slots, out, &L);
   if (st != GDN_OK) return st;
-  const size_t need = workspace_bytes_for(c);
+  const size_t need = workspace_bytes_for(c, opts);
   if (need > 0 && (!workspace || workspace_bytes < need || !aligned16(workspace)))
     return GDN_ERR_WORKSPACE;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const size_t conv_bytes = conv_bytes_for(c);
+  L.scratch = need > conv_bytes ? static_cast<char*>(workspace) + conv_bytes : nullptr;
+  L.scratch_bytes = need - conv_bytes;
   if (c.W > 0) {
     // conv (+SiLU) of all channels into the workspace, conv state updated in place
     cudaError_t e = gdn_launch_conv(c.B, c.T, c.Cc, c.W, L.in_bf16, q, c.Cc, conv_weight,

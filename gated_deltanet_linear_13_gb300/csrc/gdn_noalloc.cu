@@ -1,7 +1,7 @@
 // gdn_chunk_prefill_noalloc: chunked prefill for callers that cannot allocate device memory.
 //
-// With a conv in front (conv_width > 0) the prefill needs scratch memory for the post-conv
-// activations, which gdn_chunk_prefill takes from a caller-provided workspace.  Some callers
+// The prefill needs scratch memory (post-conv activations, the tensor-core path's chunk
+// tiles), which gdn_chunk_prefill takes from a caller-provided workspace.  Some callers
 // cannot provide one: code running inside a CUDA-graph capture that must not call
 // cudaMalloc, plug-ins handed only input and output pointers by a host framework, or
 // allocators that forbid allocations outside start-up.  This entry point uses instead a

@@ -92,8 +92,11 @@ typedef struct {
  */
 
 /*
- * Bytes of device workspace gdn_chunk_prefill needs for these dims/opts (0 when none):
- * the post-conv activations when conv_width > 0.  Returns 0 for invalid dims.
+ * Bytes of device workspace gdn_chunk_prefill needs for these dims/opts (0 when none): the
+ * post-conv activations when conv_width > 0, plus, for bf16 inputs, the per-chunk operand
+ * tiles the tensor-core prefill passes from its chunk-local kernel to its state-chain kernel
+ * (80 KB per chunk and value head for a slice of at most ~48 MB).  Returns 0 for invalid
+ * dims.
  */
 size_t gdn_prefill_workspace_size(const gdn_dims* dims, const gdn_opts* opts);
 
@@ -188,8 +191,8 @@ gdn_status gdn_state_checkpoint(int32_t op, const gdn_dims* dims, gdn_dtype conv
  * gdn_chunk_prefill_noalloc -- gdn_chunk_prefill for callers that cannot allocate device
  * memory.  The pages have no counterpart of this call; it is a convenience of this library.
  *
- * With a conv in front (conv_width > 0) the prefill needs scratch memory for the post-conv
- * activations, which gdn_chunk_prefill takes from a caller-provided workspace.  Some callers
+ * The prefill needs scratch memory (post-conv activations, the tensor-core path's chunk
+ * tiles), which gdn_chunk_prefill takes from a caller-provided workspace.  Some callers
  * cannot provide one: code recorded into a CUDA graph that must not call cudaMalloc, plug-ins
  * that a host framework hands only input and output pointers, services whose allocator
  * forbids allocations after start-up.  This variant takes the same arguments minus the
@@ -197,15 +200,15 @@ gdn_status gdn_state_checkpoint(int32_t op, const gdn_dims* dims, gdn_dtype conv
  * every GPU that loads the library holds that array until the process exits.  It calls no
  * cudaMalloc, cudaFree or other allocating routine.
  *   - Limit: if gdn_prefill_workspace_size() of the call exceeds GDN_NOALLOC_SCRATCH_BYTES
- *     (for bf16, B * T * C_conv * 2 bytes; e.g. 1536 tokens at C_conv = 10240), it returns
- *     GDN_ERR_WORKSPACE and launches nothing.  Calls without a conv use no scratch.
+ *     (64 MiB: e.g. one 512-token call of the 27B shape, 16/48 heads with the conv), it
+ *     returns GDN_ERR_WORKSPACE and launches nothing.
  *   - Set-up: the first call on a device looks up the array's device address (with that
  *     device current) and caches it; make that first call before any stream capture.
  *   - Sharing: all calls share the one array and it keeps the last call's contents (nothing
  *     in it has to start at zero: each call writes every byte it reads).  Calls that overlap
  *     on the GPU (different streams, concurrent graph replays) race on it: serialise them.
  */
-#define GDN_NOALLOC_SCRATCH_BYTES (32u << 20)
+#define GDN_NOALLOC_SCRATCH_BYTES (64u << 20)
 gdn_status gdn_chunk_prefill_noalloc(const gdn_dims* dims, const gdn_opts* opts, const void* q,
                                      const void* k, const void* v, const void* a, const void* b,
                                      const float* A_log, const float* dt_bias,

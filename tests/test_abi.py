@@ -102,8 +102,14 @@ def test_prefill_rejects_bad_pointers(L):
 def test_prefill_workspace_checked(L):
     dc, o = _dims(conv_width=4), _opts()
     need = L.gdn_prefill_workspace_size(ctypes.byref(dc), ctypes.byref(o))
-    assert need == 1 * 16 * (2 * 16 + 16) * 128 * 2
-    assert L.gdn_prefill_workspace_size(ctypes.byref(_dims()), ctypes.byref(o)) == 0
+    # bf16: one chunk x 16 value heads of 80 KB tiles + their e^{G_C} (256-byte rounded)
+    tiles = 1 * 16 * 80 * 1024 + 256
+    assert need == 1 * 16 * (2 * 16 + 16) * 128 * 2 + tiles
+    assert L.gdn_prefill_workspace_size(ctypes.byref(_dims()), ctypes.byref(o)) == tiles
+    # the all-fp32 path needs only the conv activations
+    of = _opts(in_dtype=gdn.GDN_F32, out_dtype=gdn.GDN_F32)
+    assert L.gdn_prefill_workspace_size(ctypes.byref(_dims()), ctypes.byref(of)) == 0
+    assert L.gdn_prefill_workspace_size(ctypes.byref(dc), ctypes.byref(of)) == 1 * 16 * 6144 * 4
     assert L.gdn_prefill_workspace_size(ctypes.byref(_dims(head_dim=7)), ctypes.byref(o)) == 0
     assert _prefill(L, dc, o, k=None, v=None, conv_w=A, conv_state=A, ws=None) == 3
     assert _prefill(L, dc, o, k=None, v=None, conv_w=A, conv_state=A, ws=A, wsb=need - 1) == 3
