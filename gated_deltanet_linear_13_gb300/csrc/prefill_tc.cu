@@ -86,6 +86,7 @@ struct TcParams {
   const int32_t* slots;
   uint8_t* units;         // workspace: ns * B * Hv units of UNIT_BYTES
   float* egc;             // workspace: e^{G_C} per unit
+  void* out;              // [B][T][Hv][D] output, Tout
 };
 
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
@@ -519,22 +520,33 @@ __global__ void __launch_bounds__(LGT, 2)
 }
 
 // ======================================================================= chain kernel
-// One CTA per (value head h, sequence b), 256 threads (warp w: TMEM lane quarter w % 4,
-// column half w / 4).  Per chunk: the five tiles of the local kernel plus V, double-buffered.
+// One CTA per (value head h, sequence b): eight epilogue warps (warp w: TMEM lane quarter
+// w % 4, column half w / 4) and one issuer warp whose lane 0 issues every copy and MMA, so
+// that no epilogue thread ever stalls behind the tensor-core queue.  The two sides meet only
+// at mbarriers.  Per chunk: the five tiles of the local kernel plus V, double-buffered.
+//
+// The chain S -> S0 -> U -> S is the critical path; per chunk it runs
+//   C0 (S0 = bf16(S), S *= e^{G_C})  ->  U^T += S0 (-W)^T  ->  C2 (U^T -> bf16 hi / lo)
+//   ->  S += U^T K~
+// with one commit barrier after each of its two MMA groups.  The output MMAs (O^T = S0 Q~^T,
+// O^T += U^T P^T) and the state-independent U'^T = V^T T''^T of the next chunk are issued
+// behind them and run while the epilogue warps work on the next step; the finished output
+// tile of a chunk goes from TMEM straight to HBM while the next chunk's MMAs run.  A buffer's
+// tiles other than P are free once S of its chunk is final; P once the output MMAs are done.
 constexpr uint32_t CH_BUF = 96 * KB;            // unit tiles (80 KB) + V [2][64][128 B] (16 KB)
 constexpr uint32_t CH_V = 80 * KB;
-constexpr uint32_t CH_OUT = 2 * CH_BUF;         // output staging, 16 KB
-constexpr uint32_t CH_MISC = CH_OUT + 16 * KB;  // e^{G_C} of the slice (2 KB), barriers
+constexpr uint32_t CH_MISC = 2 * CH_BUF;        // e^{G_C} of the slice (2 KB), barriers
 constexpr uint32_t CH_SMEM = CH_MISC + 3 * KB + KB;
-constexpr int CH_THREADS = 256;
+constexpr int CH_EPI = 256;                     // epilogue threads
+constexpr int CH_THREADS = CH_EPI + 32;         // + the issuer warp
 constexpr int MAX_SLICE = 512;
-// TMEM columns
-constexpr uint32_t TM_S = 0, TM_U = 128, TM_O = 192, TM_SU = 320, CH_TMEM = 512;
+// TMEM columns: S fp32 | U^T fp32 | O^T fp32 x 2 | S0 bf16 packed | U^T bf16 hi | lo
+constexpr uint32_t TM_S = 0, TM_U = 128, TM_O = 192, TM_S0 = 320, TM_UH = 384, TM_UL = 416;
+constexpr uint32_t CH_TMEM = 512;
 
 template <typename Tout>
 __global__ void __launch_bounds__(CH_THREADS, 1)
-    gdn_chunk_chain_kernel(const __grid_constant__ CUtensorMap tm_v,
-                           const __grid_constant__ CUtensorMap tm_o, const TcParams p) {
+    gdn_chunk_chain_kernel(const __grid_constant__ CUtensorMap tm_v, const TcParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
   const uint32_t sb = smem_addr(sm);
@@ -548,205 +560,251 @@ __global__ void __launch_bounds__(CH_THREADS, 1)
   }
   float* sEgc = reinterpret_cast<float*>(sm + CH_MISC);
   uint64_t* barmem = reinterpret_cast<uint64_t*>(sm + CH_MISC + 2048);
-  uint32_t* sTmem = reinterpret_cast<uint32_t*>(sm + CH_MISC + 2048 + 32);
-  volatile int* sAbort = reinterpret_cast<volatile int*>(sm + CH_MISC + 2048 + 36);
+  uint32_t* sTmem = reinterpret_cast<uint32_t*>(sm + CH_MISC + 2048 + 128);
+  volatile int* sAbort = reinterpret_cast<volatile int*>(sm + CH_MISC + 2048 + 132);
   const uint32_t bar_ld0 = smem_addr(&barmem[0]), bar_ld1 = smem_addr(&barmem[1]);
-  const uint32_t bar_mma = smem_addr(&barmem[2]);
-  const size_t u0 = ((size_t)b * p.Hv + h) * p.ns;       // first unit of this head's slice
+  const uint32_t bar_u = smem_addr(&barmem[2]);     // MMA: U^T += S0 (-W)^T done (and all before)
+  const uint32_t bar_s = smem_addr(&barmem[3]);     // MMA: S += U^T K~ done (and all before)
+  const uint32_t bar_o = smem_addr(&barmem[4]);     // MMA: output MMAs done (and all before)
+  const uint32_t bar_fin = smem_addr(&barmem[5]);   // MMA: teardown, everything issued done
+  const uint32_t bar_c0 = smem_addr(&barmem[6]);    // epilogue: S0 packed, S rescaled
+  const uint32_t bar_c2 = smem_addr(&barmem[7]);    // epilogue: U^T hi / lo packed (and the
+                                                    // previous output tile read out of TMEM)
+  const size_t u0 = ((size_t)b * p.Hv + h) * p.ns;  // first unit of this head's slice
+  const bool issuer = (tid == CH_EPI);
 
-  auto load_chunk = [&](int nl) {
+  // copies of chunk nl into buffer nl & 1: everything but P, then P (16 KB) on its own
+  auto load_main = [&](int nl) {
     const uint32_t buf = sb + (nl & 1) * CH_BUF;
     const uint32_t bar = (nl & 1) ? bar_ld1 : bar_ld0;
     const uint8_t* unit = p.units + (u0 + nl) * UNIT_BYTES;
     mbar_arrive_expect_tx(bar, 96 * KB);
-#pragma unroll
-    for (int t = 0; t < 5; ++t) bulk_load(buf + t * 16 * KB, unit + t * 16 * KB, 16 * KB, bar);
+    bulk_load(buf + U_NW, unit + U_NW, 32 * KB, bar);     // -W^T, Q~
+    bulk_load(buf + U_KT, unit + U_KT, 32 * KB, bar);     // K~, T''
     tma_load_3d(buf + CH_V, &tm_v, h * D, (p.n0 + nl) * C, b, bar);
     tma_load_3d(buf + CH_V + 8 * KB, &tm_v, h * D + 64, (p.n0 + nl) * C, b, bar);
   };
-  if (tid == 0) {
-    mbar_init(bar_ld0, 1);
-    mbar_init(bar_ld1, 1);
-    mbar_init(bar_mma, 1);
+  auto load_p = [&](int nl) {
+    const uint32_t bar = (nl & 1) ? bar_ld1 : bar_ld0;
+    bulk_load(sb + (nl & 1) * CH_BUF + U_P, p.units + (u0 + nl) * UNIT_BYTES + U_P, 16 * KB, bar);
+  };
+  // per buffer (issuer only): chunk of the copy issued and not yet waited for, or -1, and
+  // whether its P part has been issued too
+  int ld_chunk[2] = {-1, -1};
+  bool ld_has_p[2] = {false, false};
+  if (issuer) {
+    for (int i = 0; i < 6; ++i) mbar_init(smem_addr(&barmem[i]), 1);
+    for (int i = 6; i < 8; ++i) mbar_init(smem_addr(&barmem[i]), CH_EPI / 32);
     *sAbort = 0;
     fence_mbar_init();
-    load_chunk(0);
-    if (p.ns > 1) load_chunk(1);
+    for (int i = 0; i < 2 && i < p.ns; ++i) {
+      load_main(i);
+      load_p(i);
+      ld_chunk[i] = i;
+      ld_has_p[i] = true;
+    }
   }
   if (warp == 0) {
     tmem_alloc(smem_addr(sTmem), CH_TMEM);
     tmem_relinquish();
   }
   for (int i = tid; i < p.ns; i += CH_THREADS) sEgc[i] = p.egc[u0 + i];
+  const int gw = warp & 3, hc = (warp >> 2) & 1;
+  const uint32_t lane_off = static_cast<uint32_t>(gw * 32) << 16;
+  const int row = 32 * gw + lane;                       // state row / d_v index of this thread
+  float* Sg = p.state + ((size_t)slot * p.Hv + h) * D * D + (size_t)row * D + 64 * hc;
+  // the entering state (fp32, row i -> TMEM lane i; this thread: 64 columns), loaded while
+  // TMEM is being allocated
+  float sv[64];
+  if (tid < CH_EPI) {
+#pragma unroll
+    for (int q = 0; q < 16; ++q) {
+      const float4 f = reinterpret_cast<const float4*>(Sg)[q];
+      sv[4 * q] = f.x; sv[4 * q + 1] = f.y; sv[4 * q + 2] = f.z; sv[4 * q + 3] = f.w;
+    }
+  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *sTmem;
-  const int gw = warp & 3, hc = warp >> 2;
-  const uint32_t lane_off = static_cast<uint32_t>(gw * 32) << 16;
-  const int row = 32 * gw + lane;                       // state row / d_v index of this thread
 
-  // ---- the entering state -> TMEM (fp32, row i in lane i; this thread: 64 columns)
-  float* Sg = p.state + ((size_t)slot * p.Hv + h) * D * D + (size_t)row * D + 64 * hc;
-  {
-    float v[32];
-#pragma unroll
-    for (int g = 0; g < 2; ++g) {
-#pragma unroll
-      for (int q = 0; q < 8; ++q) {
-        const float4 f = reinterpret_cast<const float4*>(Sg + 32 * g)[q];
-        v[4 * q] = f.x; v[4 * q + 1] = f.y; v[4 * q + 2] = f.z; v[4 * q + 3] = f.w;
+  if (issuer) {
+    // ======================= issuer: copies and MMAs, in chain order
+    for (int nl = 0; nl < p.ns; ++nl) {
+      const uint32_t buf = sb + (nl & 1) * CH_BUF;
+      const uint32_t tmO = tmem + TM_O + 64 * (nl & 1);
+      // U'^T = V^T T''^T of this chunk (T'' as hi + lo; M = d_v, N = K = 64 tokens).  TM_U
+      // was last read by C2 of the previous chunk, which the previous C3 waited for.
+      // (a wait that gives up makes every other wait of the CTA give up too)
+      if (!mbar_wait_or_abort((nl & 1) ? bar_ld1 : bar_ld0, (nl >> 1) & 1, sAbort)) {
+        *sAbort = 1;
+        break;
       }
-      tmem_st32(tmem + lane_off + TM_S + 64 * hc + 32 * g, v);
-    }
-    tmem_wait_st();
-  }
-
-  constexpr int OUT_ROWS = (int)(16 * KB / (D * sizeof(Tout)));   // tokens per staging pass
-  // output tile of slice chunk nl (O^T in TMEM: lane = d_v index, column = token) -> HBM
-  auto store_out = [&](int nl) {
-    const uint32_t tmO = tmem + lane_off + TM_O + 64 * (nl & 1);
-    Tout* stg = reinterpret_cast<Tout*>(sm + CH_OUT);
-#pragma unroll
-    for (int pass = 0; pass < 64 / OUT_ROWS; ++pass) {
-      if (tid == 0) tma_store_wait_read();       // the staging buffer is free again
-      __syncthreads();
-      if (OUT_ROWS == 64 || hc == pass) {
-        float v[32];
-        tmem_ld32(tmO + 32 * hc, v);
-        tmem_wait_ld();
-        const int rbase = 32 * hc - pass * OUT_ROWS;
-#pragma unroll
-        for (int jj = 0; jj < 32; ++jj) stg[(rbase + jj) * D + row] = from_float<Tout>(v[jj]);
-      }
-      fence_proxy_async_smem();
-      __syncthreads();
-      if (tid == 0) {
-        tma_store_3d(&tm_o, sb + CH_OUT, h * D, (p.n0 + nl) * C + pass * OUT_ROWS, b);
-        tma_store_commit();
-      }
-    }
-  };
-
-  bool pend_mma = false, aborted = false;
-  uint32_t mma_phase = 0;
-  for (int nl = 0; nl < p.ns; ++nl) {
-    const uint32_t buf = sb + (nl & 1) * CH_BUF;
-    const uint32_t tmO = tmem + TM_O + 64 * (nl & 1);
-    if (!mbar_wait_or_abort((nl & 1) ? bar_ld1 : bar_ld0, (nl >> 1) & 1, sAbort)) *sAbort = 1;
-    __syncthreads();
-    if (*sAbort) { aborted = true; break; }
-    // ---- U'^T = V^T T''^T (T'' as hi + lo; M = d_v, N = 64 tokens, K = 64 tokens)
-    if (tid == 0) {
+      ld_chunk[nl & 1] = -1;
       tc_fence_after();
 #pragma unroll
       for (int k = 0; k < 8; ++k)
         mma_bf16(tmem + TM_U, sdesc_sw128(buf + CH_V + (k & 3) * 2048, 8 * KB, 1024),
                  sdesc_sw128(buf + U_T2 + (k < 4 ? 0 : 8 * KB) + (k & 3) * 32, 16, 1024), ID_KT,
                  k > 0);
-    }
-    // ---- C0: S -> S0 (bf16, packed into TMEM as the A operand);  S <- e^{G_C} S
-    {
-      const float egc = sEgc[nl];
-#pragma unroll
-      for (int g = 0; g < 2; ++g) {
-        const uint32_t ta = tmem + lane_off + TM_S + 64 * hc + 32 * g;
-        float v[32];
-        uint32_t pk[16];
-        tmem_ld32(ta, v);
-        tmem_wait_ld();
-#pragma unroll
-        for (int jj = 0; jj < 16; ++jj) pk[jj] = pack_bf16(v[2 * jj], v[2 * jj + 1]);
-        tmem_st16(tmem + lane_off + TM_SU + 32 * hc + 16 * g, pk);
-#pragma unroll
-        for (int jj = 0; jj < 32; ++jj) v[jj] *= egc;
-        tmem_st32(ta, v);
+      // C1 once C0 is done: U^T += S0 (-W)^T (critical), then O^T = S0 Q~^T
+      if (!mbar_wait_or_abort(bar_c0, nl & 1, sAbort)) {
+        *sAbort = 1;
+        break;
       }
-      tmem_wait_st();
-    }
-    tc_fence_before();
-    __syncthreads();
-    // ---- C1: U^T += S0 (-W)^T ;  O^T = S0 Q~^T   (M = d_v, N = 64 tokens, K = d_k)
-    if (tid == 0) {
       tc_fence_after();
 #pragma unroll
       for (int k = 0; k < 8; ++k)
-        mma_bf16_ta(tmem + TM_U, tmem + TM_SU + 8 * k,
+        mma_bf16_ta(tmem + TM_U, tmem + TM_S0 + 8 * k,
                     sdesc_sw128(buf + U_NW + k * 2048, 8 * KB, 1024), ID_SW, true);
+      mma_commit(bar_u);
+      // C0 waited for S of the previous chunk: the other buffer's tiles but P are free
+      if (nl >= 1 && nl + 1 < p.ns) {
+        load_main(nl + 1);
+        ld_chunk[(nl + 1) & 1] = nl + 1;
+        ld_has_p[(nl + 1) & 1] = false;
+      }
+      // this O buffer was last read out for chunk nl - 2, before C2 of chunk nl - 1
 #pragma unroll
       for (int k = 0; k < 8; ++k)
-        mma_bf16_ta(tmO, tmem + TM_SU + 8 * k,
+        mma_bf16_ta(tmO, tmem + TM_S0 + 8 * k,
                     sdesc_sw128(buf + U_QT + (k >> 2) * 8 * KB + (k & 3) * 32, 16, 1024), ID_SQ,
                     k > 0);
-      mma_commit(bar_mma);
-    }
-    pend_mma = true;
-    // while C1 runs: the output of the previous chunk
-    if (nl > 0) store_out(nl - 1);
-    if (!mbar_wait_or_abort(bar_mma, mma_phase, sAbort)) *sAbort = 1;
-    mma_phase ^= 1;
-    pend_mma = false;
-    tc_fence_after();
-    // ---- C2: U^T (fp32) -> bf16 hi / lo, packed into TMEM as A operands
-    {
-      float v[32];
-      uint32_t hu[16], lu[16];
-      tmem_ld32(tmem + lane_off + TM_U + 32 * hc, v);
-      tmem_wait_ld();
-#pragma unroll
-      for (int jj = 0; jj < 16; ++jj) pack_hilo(v[2 * jj], v[2 * jj + 1], hu[jj], lu[jj]);
-      tmem_st16(tmem + lane_off + TM_SU + 16 * hc, hu);
-      tmem_st16(tmem + lane_off + TM_SU + 32 + 16 * hc, lu);
-      tmem_wait_st();
-    }
-    tc_fence_before();
-    __syncthreads();
-    if (*sAbort) { aborted = true; break; }
-    // ---- C3: O^T += U^T P^T (Uh Ph + Ul Ph + Uh Pl) ;  S += U^T K~ (Uh K~ + Ul K~)
-    if (tid == 0) {
+      // C3 once C2 is done: S += U^T K~ (Uh K~ + Ul K~; critical), then
+      // O^T += U^T P^T (Uh Ph + Ul Ph + Uh Pl)
+      if (!mbar_wait_or_abort(bar_c2, nl & 1, sAbort)) {
+        *sAbort = 1;
+        break;
+      }
       tc_fence_after();
 #pragma unroll
+      for (int k = 0; k < 8; ++k)
+        mma_bf16_ta(tmem + TM_S, tmem + (k < 4 ? TM_UH : TM_UL) + 8 * (k & 3),
+                    sdesc_sw128(buf + U_KT + (k & 3) * 2048, 8 * KB, 1024), ID_UK, true);
+      mma_commit(bar_s);
+#pragma unroll
       for (int k = 0; k < 12; ++k) {
-        const uint32_t ua = (k < 4 || k >= 8) ? 0u : 32u;
+        const uint32_t ua = (k < 4 || k >= 8) ? TM_UH : TM_UL;
         const uint32_t pb = (k < 8) ? 0u : 8 * KB;
-        mma_bf16_ta(tmO, tmem + TM_SU + ua + 8 * (k & 3),
+        mma_bf16_ta(tmO, tmem + ua + 8 * (k & 3),
                     sdesc_sw128(buf + U_P + pb + (k & 3) * 32, 16, 1024), ID_SQ, true);
       }
-#pragma unroll
-      for (int k = 0; k < 8; ++k)
-        mma_bf16_ta(tmem + TM_S, tmem + TM_SU + (k < 4 ? 0u : 32u) + 8 * (k & 3),
-                    sdesc_sw128(buf + U_KT + (k & 3) * 2048, 8 * KB, 1024), ID_UK, true);
-      mma_commit(bar_mma);
+      mma_commit(bar_o);
+      // C2 waited for U^T, i.e. for every MMA before it, the previous output MMAs included:
+      // the other buffer's P is free
+      if (nl >= 1 && ld_chunk[(nl + 1) & 1] == nl + 1) {
+        load_p(nl + 1);
+        ld_has_p[(nl + 1) & 1] = true;
+      }
     }
-    pend_mma = true;
-    if (!mbar_wait_or_abort(bar_mma, mma_phase, sAbort)) *sAbort = 1;
-    mma_phase ^= 1;
-    pend_mma = false;
-    tc_fence_after();
-    // this buffer has been fully read: load chunk nl + 2 into it
-    if (tid == 0 && nl + 2 < p.ns && !*sAbort) load_chunk(nl + 2);
-  }
-  if (!aborted && !*sAbort && p.ns > 0) {
-    store_out(p.ns - 1);
-    // the leaving state: TMEM -> HBM (fp32)
-    float v[32];
-#pragma unroll
-    for (int g = 0; g < 2; ++g) {
-      tmem_ld32(tmem + lane_off + TM_S + 64 * hc + 32 * g, v);
+  } else if (tid < CH_EPI) {
+    // ======================= epilogue warps
+    tmem_st32(tmem + lane_off + TM_S + 64 * hc, *reinterpret_cast<float(*)[32]>(&sv[0]));
+    tmem_st32(tmem + lane_off + TM_S + 64 * hc + 32, *reinterpret_cast<float(*)[32]>(&sv[32]));
+    tmem_wait_st();
+    Tout* outp = static_cast<Tout*>(p.out) + (size_t)b * p.T * p.Hv * D + (size_t)h * D + row;
+    const size_t ots = (size_t)p.Hv * D;                // output token stride (elements)
+    // output tile of slice chunk nl (O^T in TMEM: lane = d_v index, column = token) -> HBM;
+    // a warp writes 32 consecutive d_v of one token per store
+    auto store_out = [&](int nl) {
+      float v[32];
+      tmem_ld32(tmem + lane_off + TM_O + 64 * (nl & 1) + 32 * hc, v);
       tmem_wait_ld();
+      const int t0 = (p.n0 + nl) * C + 32 * hc;
+      const int nt = min(32, p.T - t0);
+      Tout* o = outp + (size_t)t0 * ots;
 #pragma unroll
-      for (int q = 0; q < 8; ++q)
-        reinterpret_cast<float4*>(Sg + 32 * g)[q] =
-            make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+      for (int jj = 0; jj < 32; ++jj)
+        if (jj < nt) o[(size_t)jj * ots] = from_float<Tout>(v[jj]);
+    };
+    bool ok = true;
+    for (int nl = 0; nl < p.ns && ok; ++nl) {
+      // ---- C0: S -> S0 (bf16, packed into TMEM as the A operand);  S <- e^{G_C} S
+      if (nl > 0 && !mbar_wait_or_abort(bar_s, (nl - 1) & 1, sAbort)) { ok = false; break; }
+      tc_fence_after();
+      {
+        const float egc = sEgc[nl];
+        const uint32_t ta = tmem + lane_off + TM_S + 64 * hc;
+        float v[64];
+        tmem_ld32(ta, *reinterpret_cast<float(*)[32]>(&v[0]));
+        tmem_ld32(ta + 32, *reinterpret_cast<float(*)[32]>(&v[32]));
+        tmem_wait_ld();
+#pragma unroll
+        for (int g = 0; g < 2; ++g) {
+          uint32_t pk[16];
+#pragma unroll
+          for (int jj = 0; jj < 16; ++jj)
+            pk[jj] = pack_bf16(v[32 * g + 2 * jj], v[32 * g + 2 * jj + 1]);
+          tmem_st16(tmem + lane_off + TM_S0 + 32 * hc + 16 * g, pk);
+        }
+#pragma unroll
+        for (int jj = 0; jj < 64; ++jj) v[jj] *= egc;
+        tmem_st32(ta, *reinterpret_cast<float(*)[32]>(&v[0]));
+        tmem_st32(ta + 32, *reinterpret_cast<float(*)[32]>(&v[32]));
+        tmem_wait_st();
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_c0);
+      // ---- while U^T is being finished: the output of the previous chunk
+      if (nl > 0) {
+        if (!mbar_wait_or_abort(bar_o, (nl - 1) & 1, sAbort)) { ok = false; break; }
+        tc_fence_after();
+        store_out(nl - 1);
+      }
+      // ---- C2: U^T (fp32) -> bf16 hi / lo, packed into TMEM as A operands
+      if (!mbar_wait_or_abort(bar_u, nl & 1, sAbort)) { ok = false; break; }
+      tc_fence_after();
+      {
+        float v[32];
+        uint32_t hu[16], lu[16];
+        tmem_ld32(tmem + lane_off + TM_U + 32 * hc, v);
+        tmem_wait_ld();
+#pragma unroll
+        for (int jj = 0; jj < 16; ++jj) pack_hilo(v[2 * jj], v[2 * jj + 1], hu[jj], lu[jj]);
+        tmem_st16(tmem + lane_off + TM_UH + 16 * hc, hu);
+        tmem_st16(tmem + lane_off + TM_UL + 16 * hc, lu);
+        tmem_wait_st();
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_c2);
     }
+    if (ok && p.ns > 0) {
+      if (mbar_wait_or_abort(bar_o, (p.ns - 1) & 1, sAbort)) {
+        tc_fence_after();
+        store_out(p.ns - 1);
+        // the leaving state: TMEM -> HBM (fp32)
+        float v[32];
+#pragma unroll
+        for (int g = 0; g < 2; ++g) {
+          tmem_ld32(tmem + lane_off + TM_S + 64 * hc + 32 * g, v);
+          tmem_wait_ld();
+#pragma unroll
+          for (int q = 0; q < 8; ++q)
+            reinterpret_cast<float4*>(Sg + 32 * g)[q] =
+                make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+        }
+      } else {
+        ok = false;
+      }
+    }
+    if (!ok) *sAbort = 1;
   }
-  if (tid == 0) {
-    tma_store_wait_all();
-    if (pend_mma) mbar_wait_bounded(bar_mma, mma_phase, 1u << 16);
-    if (*sAbort) atomicOr(&g_err_tc, kErrTimeout);
+  if (issuer) {
+    // nothing may still write this CTA's shared memory or TMEM when it exits: first every
+    // MMA issued (after which every tile is free), then every copy issued
+    mma_commit(bar_fin);
+    mbar_wait_bounded(bar_fin, 0, 1u << 16);
+    for (int i = 0; i < 2; ++i) {
+      if (ld_chunk[i] < 0) continue;
+      if (!ld_has_p[i]) load_p(ld_chunk[i]);        // completes the phase the copy counts on
+      mbar_wait_bounded(i ? bar_ld1 : bar_ld0, (ld_chunk[i] >> 1) & 1, 1u << 16);
+    }
   }
   tc_fence_before();
   __syncthreads();
+  if (tid == 0 && *sAbort) atomicOr(&g_err_tc, kErrTimeout);
   if (warp == 0) {
     tc_fence_after();
     tmem_dealloc(tmem, CH_TMEM);
@@ -804,18 +862,14 @@ int slice_chunks(int B, int Hv, int nch) {
 
 template <typename Tout>
 cudaError_t launch_tc_t(const GdnLayerArgs& L, cudaStream_t stream) {
-  CUtensorMap mq, mk, mv, mo;
-  constexpr int out_rows = (int)(16 * KB / (D * sizeof(Tout)));
+  CUtensorMap mq, mk, mv;
   const bool ok =
       make_map(&mq, L.q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, L.Hk * D, L.T, L.B, L.q_tok_stride,
                64, 64, true) &&
       make_map(&mk, L.k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, L.Hk * D, L.T, L.B, L.k_tok_stride,
                64, 64, true) &&
       make_map(&mv, L.v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, L.Hv * D, L.T, L.B, L.v_tok_stride,
-               64, 64, true) &&
-      make_map(&mo, L.out,
-               sizeof(Tout) == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
-               (int)sizeof(Tout), L.Hv * D, L.T, L.B, (long long)L.Hv * D, 128, out_rows, false);
+               64, 64, true);
   if (!ok) return cudaErrorInvalidValue;
   static unsigned done_l = 0, done_c = 0;
   cudaError_t e = set_smem_once(gdn_chunk_local_kernel<__nv_bfloat16>, (int)L_SMEM, &done_l);
@@ -833,13 +887,14 @@ cudaError_t launch_tc_t(const GdnLayerArgs& L, cudaStream_t stream) {
   p.A_log = L.A_log; p.dt_bias = L.dt_bias; p.state = L.state; p.slots = L.slots;
   p.units = static_cast<uint8_t*>(L.scratch);
   p.egc = reinterpret_cast<float*>(p.units + units * UNIT_BYTES);
+  p.out = L.out;
   for (int n0 = 0; n0 < nch; n0 += ns_max) {
     p.n0 = n0;
     p.ns = nch - n0 < ns_max ? nch - n0 : ns_max;
     gdn_chunk_local_kernel<__nv_bfloat16>
         <<<dim3((unsigned)p.ns, (unsigned)L.Hv, (unsigned)L.B), LGT, L_SMEM, stream>>>(mq, mk, p);
     gdn_chunk_chain_kernel<Tout>
-        <<<dim3((unsigned)(L.B * L.Hv)), CH_THREADS, CH_SMEM, stream>>>(mv, mo, p);
+        <<<dim3((unsigned)(L.B * L.Hv)), CH_THREADS, CH_SMEM, stream>>>(mv, p);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
