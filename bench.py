@@ -49,14 +49,16 @@ CLOCK_QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.ac
                "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
 
-def measured_traffic(key: str):
+def measured_traffic(key: str, workload: str):
     """DRAM bytes per launch recorded from an ncu capture (profiles/traffic.json), or None
-    when the kernel sources changed since that capture."""
+    when the kernel sources changed since that capture or it was of another workload."""
     import hashlib
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         rec = json.load(open(path))[key]
     except (OSError, KeyError, ValueError):
+        return None
+    if rec.get("workload") != workload:
         return None
     for src, digest in rec.get("sources", {}).items():
         try:
@@ -442,7 +444,12 @@ def main():
                          f"workload (conv + norm + gates + recurrence, fp64)"}
 
     if rank == 0:
-        launches_per_step = nbk * 3   # conv + recurrence + checkpoint per bucket
+        # per bucket: conv, then (chunk-local kernel + state-chain kernel) per slice of
+        # chunks whose tiles fit the 48 MB slice budget (80 KB per chunk and value head),
+        # then the checkpoint
+        nch = BUCKET // 64
+        per_slice = max(1, min(512, nch, (48 << 20) // (HV * 80 * 1024)))
+        launches_per_step = nbk * (1 + 2 * (-(-nch // per_slice)) + 1)
         line = {
             "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
@@ -456,7 +463,7 @@ def main():
             "roofline": {"bound": "tensor", "achieved": achieved_tflops,
                          "peak": peaks["bf16_sustained"], "unit": "TFLOP/s",
                          "frac": achieved_tflops / peaks["bf16_sustained"],
-                         "traffic": measured_traffic("prefill_call"),
+                         "traffic": measured_traffic("prefill_call", f"qwen36_27b_prefill_bucket{BUCKET}"),
                          "kernel": "gdn_chunk_prefill (conv + chunked recurrence), 512 tokens",
                          "flop_per_launch": FLOP_PER_TOKEN * BUCKET,
                          "launch_ms": call_ms, "peak_source": peaks["source"] + " sustained"},
@@ -467,7 +474,7 @@ def main():
                        "roofline": {"bound": "hbm", "achieved": dec_gbs,
                                     "peak": peaks["hbm_gbs"], "unit": "GB/s",
                                     "frac": dec_gbs / peaks["hbm_gbs"],
-                                    "traffic": measured_traffic("decode_step"),
+                                    "traffic": measured_traffic("decode_step", f"qwen36_27b_decode_B{DECODE_B}"),
                                     "peak_source": peaks["source"]},
                        "l2": "state 805 MB > L2"},
             "e2e": e2e,

@@ -328,7 +328,7 @@ __global__ void __launch_bounds__(LGT, 2)
     __syncthreads();
     if (*sAbort) break;
     // ---- MMA 1: G = [K; Q] K^T  (M = 128: k_0..k_63, q_0..q_63; N = 64; K = 128)
-    if (tid == 0) {
+    if (warp == 0 && elect_one()) {
       tc_fence_after();
 #pragma unroll
       for (int k = 0; k < 8; ++k) {
@@ -470,9 +470,11 @@ __global__ void __launch_bounds__(LGT, 2)
     fence_proxy_async_smem();
     __syncthreads();
     // ---- T'' to the chain; MMA 3: W^T = K^T T'^T (M = d_k, N = 64 tokens, K = 64 tokens)
-    if (tid == 0) {
+    if (tid == 0) {                   // (bulk-copy groups are per thread: thread 0 waits)
       bulk_store(unit + U_T2, sb + L_SOLVE + 16 * KB, 16 * KB);
       tma_store_commit();
+    }
+    if (warp == 0 && elect_one()) {
       tc_fence_after();
 #pragma unroll
       for (int k = 0; k < 8; ++k)
@@ -521,9 +523,9 @@ __global__ void __launch_bounds__(LGT, 2)
 
 // ======================================================================= chain kernel
 // One CTA per (value head h, sequence b): eight epilogue warps (warp w: TMEM lane quarter
-// w % 4, column half w / 4) and one issuer warp whose lane 0 issues every copy and MMA, so
-// that no epilogue thread ever stalls behind the tensor-core queue.  The two sides meet only
-// at mbarriers.  Per chunk: the five tiles of the local kernel plus V, double-buffered.
+// w % 4, column half w / 4) and one issuer warp, one elected lane of which issues every copy
+// and MMA, so that no epilogue thread ever stalls behind the tensor-core queue.  The two
+// sides meet only at mbarriers.  Per chunk: the five tiles of the local kernel plus V, double-buffered.
 //
 // The chain S -> S0 -> U -> S is the critical path; per chunk it runs
 //   C0 (S0 = bf16(S), S *= e^{G_C})  ->  U^T += S0 (-W)^T  ->  C2 (U^T -> bf16 hi / lo)
@@ -570,40 +572,40 @@ __global__ void __launch_bounds__(CH_THREADS, 1)
   const uint32_t bar_c0 = smem_addr(&barmem[6]);    // epilogue: S0 packed, S rescaled
   const uint32_t bar_c2 = smem_addr(&barmem[7]);    // epilogue: U^T hi / lo packed (and the
                                                     // previous output tile read out of TMEM)
+  const uint32_t bar_p0 = smem_addr(&barmem[8]), bar_p1 = smem_addr(&barmem[9]);   // P copies
   const size_t u0 = ((size_t)b * p.Hv + h) * p.ns;  // first unit of this head's slice
-  const bool issuer = (tid == CH_EPI);
+  const bool issuer_warp = (warp == CH_EPI / 32);
 
-  // copies of chunk nl into buffer nl & 1: everything but P, then P (16 KB) on its own
+  // copies of chunk nl into buffer nl & 1: everything but P, and P (16 KB, needed only by the
+  // last MMA group) on a barrier of its own
   auto load_main = [&](int nl) {
     const uint32_t buf = sb + (nl & 1) * CH_BUF;
     const uint32_t bar = (nl & 1) ? bar_ld1 : bar_ld0;
     const uint8_t* unit = p.units + (u0 + nl) * UNIT_BYTES;
-    mbar_arrive_expect_tx(bar, 96 * KB);
+    mbar_arrive_expect_tx(bar, 80 * KB);
     bulk_load(buf + U_NW, unit + U_NW, 32 * KB, bar);     // -W^T, Q~
     bulk_load(buf + U_KT, unit + U_KT, 32 * KB, bar);     // K~, T''
     tma_load_3d(buf + CH_V, &tm_v, h * D, (p.n0 + nl) * C, b, bar);
     tma_load_3d(buf + CH_V + 8 * KB, &tm_v, h * D + 64, (p.n0 + nl) * C, b, bar);
   };
   auto load_p = [&](int nl) {
-    const uint32_t bar = (nl & 1) ? bar_ld1 : bar_ld0;
+    const uint32_t bar = (nl & 1) ? bar_p1 : bar_p0;
+    mbar_arrive_expect_tx(bar, 16 * KB);
     bulk_load(sb + (nl & 1) * CH_BUF + U_P, p.units + (u0 + nl) * UNIT_BYTES + U_P, 16 * KB, bar);
   };
-  // per buffer (issuer only): chunk of the copy issued and not yet waited for, or -1, and
-  // whether its P part has been issued too
-  int ld_chunk[2] = {-1, -1};
-  bool ld_has_p[2] = {false, false};
-  if (issuer) {
-    for (int i = 0; i < 6; ++i) mbar_init(smem_addr(&barmem[i]), 1);
-    for (int i = 6; i < 8; ++i) mbar_init(smem_addr(&barmem[i]), CH_EPI / 32);
+  // per buffer (issuer warp): chunk of the main / P copy issued and not yet waited for, or -1
+  int ld_chunk[2] = {-1, -1}, lp_chunk[2] = {-1, -1};
+  if (tid == CH_EPI) {
+    for (int i = 0; i < 10; ++i) mbar_init(smem_addr(&barmem[i]), (i == 6 || i == 7) ? CH_EPI / 32 : 1);
     *sAbort = 0;
     fence_mbar_init();
     for (int i = 0; i < 2 && i < p.ns; ++i) {
       load_main(i);
       load_p(i);
-      ld_chunk[i] = i;
-      ld_has_p[i] = true;
     }
   }
+  if (warp == CH_EPI / 32)
+    for (int i = 0; i < 2 && i < p.ns; ++i) ld_chunk[i] = lp_chunk[i] = i;
   if (warp == 0) {
     tmem_alloc(smem_addr(sTmem), CH_TMEM);
     tmem_relinquish();
@@ -628,74 +630,91 @@ __global__ void __launch_bounds__(CH_THREADS, 1)
   tc_fence_after();
   const uint32_t tmem = *sTmem;
 
-  if (issuer) {
-    // ======================= issuer: copies and MMAs, in chain order
+  if (issuer_warp) {
+    // ======================= issuer warp: the whole warp runs the loop and waits, one
+    // elected lane issues the copies and MMAs (in chain order)
+    const bool leader = elect_one();
     for (int nl = 0; nl < p.ns; ++nl) {
       const uint32_t buf = sb + (nl & 1) * CH_BUF;
       const uint32_t tmO = tmem + TM_O + 64 * (nl & 1);
       // U'^T = V^T T''^T of this chunk (T'' as hi + lo; M = d_v, N = K = 64 tokens).  TM_U
       // was last read by C2 of the previous chunk, which the previous C3 waited for.
       // (a wait that gives up makes every other wait of the CTA give up too)
-      if (!mbar_wait_or_abort((nl & 1) ? bar_ld1 : bar_ld0, (nl >> 1) & 1, sAbort)) {
+      if (!__all_sync(0xffffffffu,
+                      mbar_wait_or_abort((nl & 1) ? bar_ld1 : bar_ld0, (nl >> 1) & 1, sAbort))) {
         *sAbort = 1;
         break;
       }
       ld_chunk[nl & 1] = -1;
       tc_fence_after();
+      if (leader) {
 #pragma unroll
-      for (int k = 0; k < 8; ++k)
-        mma_bf16(tmem + TM_U, sdesc_sw128(buf + CH_V + (k & 3) * 2048, 8 * KB, 1024),
-                 sdesc_sw128(buf + U_T2 + (k < 4 ? 0 : 8 * KB) + (k & 3) * 32, 16, 1024), ID_KT,
-                 k > 0);
+        for (int k = 0; k < 8; ++k)
+          mma_bf16(tmem + TM_U, sdesc_sw128(buf + CH_V + (k & 3) * 2048, 8 * KB, 1024),
+                   sdesc_sw128(buf + U_T2 + (k < 4 ? 0 : 8 * KB) + (k & 3) * 32, 16, 1024),
+                   ID_KT, k > 0);
+      }
+      __syncwarp();
       // C1 once C0 is done: U^T += S0 (-W)^T (critical), then O^T = S0 Q~^T
-      if (!mbar_wait_or_abort(bar_c0, nl & 1, sAbort)) {
+      if (!__all_sync(0xffffffffu, mbar_wait_or_abort(bar_c0, nl & 1, sAbort))) {
         *sAbort = 1;
         break;
       }
       tc_fence_after();
+      if (leader) {
 #pragma unroll
-      for (int k = 0; k < 8; ++k)
-        mma_bf16_ta(tmem + TM_U, tmem + TM_S0 + 8 * k,
-                    sdesc_sw128(buf + U_NW + k * 2048, 8 * KB, 1024), ID_SW, true);
-      mma_commit(bar_u);
-      // C0 waited for S of the previous chunk: the other buffer's tiles but P are free
-      if (nl >= 1 && nl + 1 < p.ns) {
-        load_main(nl + 1);
-        ld_chunk[(nl + 1) & 1] = nl + 1;
-        ld_has_p[(nl + 1) & 1] = false;
+        for (int k = 0; k < 8; ++k)
+          mma_bf16_ta(tmem + TM_U, tmem + TM_S0 + 8 * k,
+                      sdesc_sw128(buf + U_NW + k * 2048, 8 * KB, 1024), ID_SW, true);
+        mma_commit(bar_u);
+        // C0 waited for S of the previous chunk: the other buffer's tiles but P are free
+        if (nl >= 1 && nl + 1 < p.ns) load_main(nl + 1);
+        // this O buffer was last read out for chunk nl - 2, before C2 of chunk nl - 1
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+          mma_bf16_ta(tmO, tmem + TM_S0 + 8 * k,
+                      sdesc_sw128(buf + U_QT + (k >> 2) * 8 * KB + (k & 3) * 32, 16, 1024),
+                      ID_SQ, k > 0);
       }
-      // this O buffer was last read out for chunk nl - 2, before C2 of chunk nl - 1
-#pragma unroll
-      for (int k = 0; k < 8; ++k)
-        mma_bf16_ta(tmO, tmem + TM_S0 + 8 * k,
-                    sdesc_sw128(buf + U_QT + (k >> 2) * 8 * KB + (k & 3) * 32, 16, 1024), ID_SQ,
-                    k > 0);
+      __syncwarp();
+      if (nl >= 1 && nl + 1 < p.ns) ld_chunk[(nl + 1) & 1] = nl + 1;
       // C3 once C2 is done: S += U^T K~ (Uh K~ + Ul K~; critical), then
       // O^T += U^T P^T (Uh Ph + Ul Ph + Uh Pl)
-      if (!mbar_wait_or_abort(bar_c2, nl & 1, sAbort)) {
+      if (!__all_sync(0xffffffffu, mbar_wait_or_abort(bar_c2, nl & 1, sAbort))) {
         *sAbort = 1;
         break;
       }
       tc_fence_after();
+      if (leader) {
 #pragma unroll
-      for (int k = 0; k < 8; ++k)
-        mma_bf16_ta(tmem + TM_S, tmem + (k < 4 ? TM_UH : TM_UL) + 8 * (k & 3),
-                    sdesc_sw128(buf + U_KT + (k & 3) * 2048, 8 * KB, 1024), ID_UK, true);
-      mma_commit(bar_s);
-#pragma unroll
-      for (int k = 0; k < 12; ++k) {
-        const uint32_t ua = (k < 4 || k >= 8) ? TM_UH : TM_UL;
-        const uint32_t pb = (k < 8) ? 0u : 8 * KB;
-        mma_bf16_ta(tmO, tmem + ua + 8 * (k & 3),
-                    sdesc_sw128(buf + U_P + pb + (k & 3) * 32, 16, 1024), ID_SQ, true);
+        for (int k = 0; k < 8; ++k)
+          mma_bf16_ta(tmem + TM_S, tmem + (k < 4 ? TM_UH : TM_UL) + 8 * (k & 3),
+                      sdesc_sw128(buf + U_KT + (k & 3) * 2048, 8 * KB, 1024), ID_UK, true);
+        mma_commit(bar_s);
       }
-      mma_commit(bar_o);
+      __syncwarp();
+      if (!__all_sync(0xffffffffu,
+                      mbar_wait_or_abort((nl & 1) ? bar_p1 : bar_p0, (nl >> 1) & 1, sAbort))) {
+        *sAbort = 1;
+        break;
+      }
+      lp_chunk[nl & 1] = -1;
       // C2 waited for U^T, i.e. for every MMA before it, the previous output MMAs included:
       // the other buffer's P is free
-      if (nl >= 1 && ld_chunk[(nl + 1) & 1] == nl + 1) {
-        load_p(nl + 1);
-        ld_has_p[(nl + 1) & 1] = true;
+      const bool refill_p = nl >= 1 && nl + 1 < p.ns;
+      if (leader) {
+#pragma unroll
+        for (int k = 0; k < 12; ++k) {
+          const uint32_t ua = (k < 4 || k >= 8) ? TM_UH : TM_UL;
+          const uint32_t pb = (k < 8) ? 0u : 8 * KB;
+          mma_bf16_ta(tmO, tmem + ua + 8 * (k & 3),
+                      sdesc_sw128(buf + U_P + pb + (k & 3) * 32, 16, 1024), ID_SQ, true);
+        }
+        mma_commit(bar_o);
+        if (refill_p) load_p(nl + 1);
       }
+      __syncwarp();
+      if (refill_p) lp_chunk[(nl + 1) & 1] = nl + 1;
     }
   } else if (tid < CH_EPI) {
     // ======================= epilogue warps
@@ -791,15 +810,14 @@ __global__ void __launch_bounds__(CH_THREADS, 1)
     }
     if (!ok) *sAbort = 1;
   }
-  if (issuer) {
+  if (tid == CH_EPI) {
     // nothing may still write this CTA's shared memory or TMEM when it exits: first every
     // MMA issued (after which every tile is free), then every copy issued
     mma_commit(bar_fin);
     mbar_wait_bounded(bar_fin, 0, 1u << 16);
     for (int i = 0; i < 2; ++i) {
-      if (ld_chunk[i] < 0) continue;
-      if (!ld_has_p[i]) load_p(ld_chunk[i]);        // completes the phase the copy counts on
-      mbar_wait_bounded(i ? bar_ld1 : bar_ld0, (ld_chunk[i] >> 1) & 1, 1u << 16);
+      if (ld_chunk[i] >= 0) mbar_wait_bounded(i ? bar_ld1 : bar_ld0, (ld_chunk[i] >> 1) & 1, 1u << 16);
+      if (lp_chunk[i] >= 0) mbar_wait_bounded(i ? bar_p1 : bar_p0, (lp_chunk[i] >> 1) & 1, 1u << 16);
     }
   }
   tc_fence_before();
