@@ -86,7 +86,6 @@ struct TcParams {
   const int32_t* slots;
   uint8_t* units;         // workspace: ns * B * Hv units of UNIT_BYTES
   float* egc;             // workspace: e^{G_C} per unit
-  void* out;              // [B][T][Hv][D] output, Tout
 };
 
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
@@ -533,11 +532,13 @@ __global__ void __launch_bounds__(LGT, 2)
 // with one commit barrier after each of its two MMA groups.  The output MMAs (O^T = S0 Q~^T,
 // O^T += U^T P^T) and the state-independent U'^T = V^T T''^T of the next chunk are issued
 // behind them and run while the epilogue warps work on the next step; the finished output
-// tile of a chunk goes from TMEM straight to HBM while the next chunk's MMAs run.  A buffer's
+// tile of a chunk is transposed through shared memory (each warp its own 32 x 32 block)
+// and leaves with TMA stores while the next chunk's MMAs run.  A buffer's
 // tiles other than P are free once S of its chunk is final; P once the output MMAs are done.
 constexpr uint32_t CH_BUF = 96 * KB;            // unit tiles (80 KB) + V [2][64][128 B] (16 KB)
 constexpr uint32_t CH_V = 80 * KB;
-constexpr uint32_t CH_MISC = 2 * CH_BUF;        // e^{G_C} of the slice (2 KB), barriers
+constexpr uint32_t CH_OUT = 2 * CH_BUF;         // output staging, 2 KB per epilogue warp
+constexpr uint32_t CH_MISC = CH_OUT + 16 * KB;  // e^{G_C} of the slice (2 KB), barriers
 constexpr uint32_t CH_SMEM = CH_MISC + 3 * KB + KB;
 constexpr int CH_EPI = 256;                     // epilogue threads
 constexpr int CH_THREADS = CH_EPI + 32;         // + the issuer warp
@@ -548,7 +549,8 @@ constexpr uint32_t CH_TMEM = 512;
 
 template <typename Tout>
 __global__ void __launch_bounds__(CH_THREADS, 1)
-    gdn_chunk_chain_kernel(const __grid_constant__ CUtensorMap tm_v, const TcParams p) {
+    gdn_chunk_chain_kernel(const __grid_constant__ CUtensorMap tm_v,
+                           const __grid_constant__ CUtensorMap tm_o, const TcParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
   const uint32_t sb = smem_addr(sm);
@@ -721,25 +723,40 @@ __global__ void __launch_bounds__(CH_THREADS, 1)
     tmem_st32(tmem + lane_off + TM_S + 64 * hc, *reinterpret_cast<float(*)[32]>(&sv[0]));
     tmem_st32(tmem + lane_off + TM_S + 64 * hc + 32, *reinterpret_cast<float(*)[32]>(&sv[32]));
     tmem_wait_st();
-    Tout* outp = static_cast<Tout*>(p.out) + (size_t)b * p.T * p.Hv * D + (size_t)h * D + row;
-    const size_t ots = (size_t)p.Hv * D;                // output token stride (elements)
-    // output tile of slice chunk nl (O^T in TMEM: lane = d_v index, column = token) -> HBM;
-    // a warp writes 32 consecutive d_v of one token per store
+    constexpr int OUT_ROWS = (int)(2 * KB / (32 * sizeof(Tout)));   // tokens per staging pass
+    Tout* stg = reinterpret_cast<Tout*>(sm + CH_OUT + warp * 2 * KB);
+    // output tile of slice chunk nl (O^T in TMEM: lane = d_v index, column = token): this
+    // warp's 32 d_v x 32 tokens -> its staging block [token][32 d_v] -> HBM with a TMA store
+    // per pass (the store clips the rows past the sequence end).  Everything stays within
+    // the warp; lane 0 issues the stores and is the one that waits for their reads.
     auto store_out = [&](int nl) {
       float v[32];
       tmem_ld32(tmem + lane_off + TM_O + 64 * (nl & 1) + 32 * hc, v);
       tmem_wait_ld();
-      const int t0 = (p.n0 + nl) * C + 32 * hc;
-      const int nt = min(32, p.T - t0);
-      Tout* o = outp + (size_t)t0 * ots;
 #pragma unroll
-      for (int jj = 0; jj < 32; ++jj)
-        if (jj < nt) o[(size_t)jj * ots] = from_float<Tout>(v[jj]);
+      for (int pass = 0; pass < 32 / OUT_ROWS; ++pass) {
+        if (lane == 0) tma_store_wait_read();
+        __syncwarp();
+#pragma unroll
+        for (int jj = 0; jj < OUT_ROWS; ++jj)
+          stg[jj * 32 + lane] = from_float<Tout>(v[pass * OUT_ROWS + jj]);
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          tma_store_3d(&tm_o, smem_addr(stg), h * D + 32 * gw,
+                       (p.n0 + nl) * C + 32 * hc + pass * OUT_ROWS, b);
+          tma_store_commit();
+        }
+      }
     };
     bool ok = true;
     for (int nl = 0; nl < p.ns && ok; ++nl) {
       // ---- C0: S -> S0 (bf16, packed into TMEM as the A operand);  S <- e^{G_C} S
-      if (nl > 0 && !mbar_wait_or_abort(bar_s, (nl - 1) & 1, sAbort)) { ok = false; break; }
+      // (every wait is decided warp-uniformly: the warp syncs below must not split)
+      if (nl > 0 && !__all_sync(0xffffffffu, mbar_wait_or_abort(bar_s, (nl - 1) & 1, sAbort))) {
+        ok = false;
+        break;
+      }
       tc_fence_after();
       {
         const float egc = sEgc[nl];
@@ -767,12 +784,18 @@ __global__ void __launch_bounds__(CH_THREADS, 1)
       if (lane == 0) mbar_arrive(bar_c0);
       // ---- while U^T is being finished: the output of the previous chunk
       if (nl > 0) {
-        if (!mbar_wait_or_abort(bar_o, (nl - 1) & 1, sAbort)) { ok = false; break; }
+        if (!__all_sync(0xffffffffu, mbar_wait_or_abort(bar_o, (nl - 1) & 1, sAbort))) {
+          ok = false;
+          break;
+        }
         tc_fence_after();
         store_out(nl - 1);
       }
       // ---- C2: U^T (fp32) -> bf16 hi / lo, packed into TMEM as A operands
-      if (!mbar_wait_or_abort(bar_u, nl & 1, sAbort)) { ok = false; break; }
+      if (!__all_sync(0xffffffffu, mbar_wait_or_abort(bar_u, nl & 1, sAbort))) {
+        ok = false;
+        break;
+      }
       tc_fence_after();
       {
         float v[32];
@@ -790,7 +813,7 @@ __global__ void __launch_bounds__(CH_THREADS, 1)
       if (lane == 0) mbar_arrive(bar_c2);
     }
     if (ok && p.ns > 0) {
-      if (mbar_wait_or_abort(bar_o, (p.ns - 1) & 1, sAbort)) {
+      if (__all_sync(0xffffffffu, mbar_wait_or_abort(bar_o, (p.ns - 1) & 1, sAbort))) {
         tc_fence_after();
         store_out(p.ns - 1);
         // the leaving state: TMEM -> HBM (fp32)
@@ -808,6 +831,7 @@ __global__ void __launch_bounds__(CH_THREADS, 1)
         ok = false;
       }
     }
+    if (lane == 0) tma_store_wait_all();
     if (!ok) *sAbort = 1;
   }
   if (tid == CH_EPI) {
@@ -880,14 +904,18 @@ int slice_chunks(int B, int Hv, int nch) {
 
 template <typename Tout>
 cudaError_t launch_tc_t(const GdnLayerArgs& L, cudaStream_t stream) {
-  CUtensorMap mq, mk, mv;
+  CUtensorMap mq, mk, mv, mo;
+  constexpr int out_rows = (int)(2 * KB / (32 * sizeof(Tout)));
   const bool ok =
       make_map(&mq, L.q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, L.Hk * D, L.T, L.B, L.q_tok_stride,
                64, 64, true) &&
       make_map(&mk, L.k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, L.Hk * D, L.T, L.B, L.k_tok_stride,
                64, 64, true) &&
       make_map(&mv, L.v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, L.Hv * D, L.T, L.B, L.v_tok_stride,
-               64, 64, true);
+               64, 64, true) &&
+      make_map(&mo, L.out,
+               sizeof(Tout) == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
+               (int)sizeof(Tout), L.Hv * D, L.T, L.B, (long long)L.Hv * D, 32, out_rows, false);
   if (!ok) return cudaErrorInvalidValue;
   static unsigned done_l = 0, done_c = 0;
   cudaError_t e = set_smem_once(gdn_chunk_local_kernel<__nv_bfloat16>, (int)L_SMEM, &done_l);
@@ -905,14 +933,13 @@ cudaError_t launch_tc_t(const GdnLayerArgs& L, cudaStream_t stream) {
   p.A_log = L.A_log; p.dt_bias = L.dt_bias; p.state = L.state; p.slots = L.slots;
   p.units = static_cast<uint8_t*>(L.scratch);
   p.egc = reinterpret_cast<float*>(p.units + units * UNIT_BYTES);
-  p.out = L.out;
   for (int n0 = 0; n0 < nch; n0 += ns_max) {
     p.n0 = n0;
     p.ns = nch - n0 < ns_max ? nch - n0 : ns_max;
     gdn_chunk_local_kernel<__nv_bfloat16>
         <<<dim3((unsigned)p.ns, (unsigned)L.Hv, (unsigned)L.B), LGT, L_SMEM, stream>>>(mq, mk, p);
     gdn_chunk_chain_kernel<Tout>
-        <<<dim3((unsigned)(L.B * L.Hv)), CH_THREADS, CH_SMEM, stream>>>(mv, p);
+        <<<dim3((unsigned)(L.B * L.Hv)), CH_THREADS, CH_SMEM, stream>>>(mv, mo, p);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
