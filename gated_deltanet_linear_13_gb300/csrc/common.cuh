@@ -1,9 +1,12 @@
 // Internal helpers shared by the kernels of libgdn.so (not part of the C ABI).
 #pragma once
 
+#include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
+
+#include <utility>
 
 #include "gdn.h"
 
@@ -56,6 +59,46 @@ inline cudaError_t set_smem_once(K kernel, int bytes, unsigned* done_mask) {
   return e;
 }
 
+// Same, for the preferred shared-memory carveout (percent of the unified L1 / shared array).
+template <typename K>
+inline cudaError_t set_carveout_once(K kernel, int percent, unsigned* done_mask) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const unsigned bit = 1u << (dev & 31);
+  if (*done_mask & bit) return cudaSuccess;
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout, percent);
+  if (e == cudaSuccess) *done_mask |= bit;
+  return e;
+}
+
+// ----------------------------------------------------------------- programmatic dependent launch
+// A kernel launched with launch_pdl may start while the kernel before it in the stream is
+// still running: it does its set-up, then pdl_wait() (every thread) blocks until that kernel
+// has completed and its memory writes are visible; nothing it produced, and nothing it may
+// still read, is touched before.  pdl_trigger() in the earlier kernel lets the later one be
+// scheduled as soon as every CTA of the earlier one has issued it (else at its exit).
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;\n" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
+}
+
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                              cudaStream_t stream, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
 // ----------------------------------------------------------------- warp reductions
 
 __device__ __forceinline__ float warp_sum(float x) {
@@ -96,6 +139,12 @@ size_t gdn_prefill_tc_scratch_bytes(int B, int T, int Hv);
 cudaError_t gdn_launch_decode(const GdnLayerArgs& args, cudaStream_t stream);
 cudaError_t gdn_launch_prefill_simt(const GdnLayerArgs& args, cudaStream_t stream);
 cudaError_t gdn_launch_prefill_tc(const GdnLayerArgs& args, cudaStream_t stream);
+// 3-D tensor map over [B][T][width] elements starting at `base`, token stride `tok_stride`
+// elements; box = {box0, box1 tokens, 1 sequence}; 128-byte swizzle or none.
+bool gdn_make_map(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int elem_bytes,
+                  int width, int T, int B, long long tok_stride, int box0, int box1,
+                  bool swizzle128);
+
 cudaError_t gdn_launch_conv(int B, int T, int C, int W, int bf16, const void* x,
                             long long x_tok_stride, const void* w, const void* bias,
                             void* conv_state, int num_slots, const int32_t* slots, int silu,

@@ -270,12 +270,6 @@ __global__ void __launch_bounds__(LGT, 2)
     mbar_init(bar_mma, 1);
     *sAbort = 0;
     fence_mbar_init();
-    mbar_arrive_expect_tx(bar_in, 32 * KB);
-#pragma unroll
-    for (int kb = 0; kb < 2; ++kb) {
-      tma_load_3d(sb + L_KQ + kb * 16 * KB, &tm_k, kh * D + 64 * kb, n * C, b, bar_in);
-      tma_load_3d(sb + L_KQ + kb * 16 * KB + 8 * KB, &tm_q, kh * D + 64 * kb, n * C, b, bar_in);
-    }
   }
   if (warp == 0) {
     tmem_alloc(smem_addr(sTmem), L_TMEM);
@@ -310,6 +304,19 @@ __global__ void __launch_bounds__(LGT, 2)
     gl2[2 * lane + 1] = s * LOG2E;
     beta[2 * lane] = b2[0];
     beta[2 * lane + 1] = b2[1];
+  }
+  // the conv output (K, Q) and this slice's workspace belong to the kernels before until
+  // here.  Only then may the state-chain kernel start its set-up, which reads the state: the
+  // chain that last wrote it is then complete and visible.
+  pdl_wait();
+  pdl_trigger();
+  if (tid == 0) {
+    mbar_arrive_expect_tx(bar_in, 32 * KB);
+#pragma unroll
+    for (int kb = 0; kb < 2; ++kb) {
+      tma_load_3d(sb + L_KQ + kb * 16 * KB, &tm_k, kh * D + 64 * kb, n * C, b, bar_in);
+      tma_load_3d(sb + L_KQ + kb * 16 * KB + 8 * KB, &tm_q, kh * D + 64 * kb, n * C, b, bar_in);
+    }
   }
   tc_fence_before();
   __syncthreads();
@@ -601,10 +608,6 @@ __global__ void __launch_bounds__(CH_THREADS, 1)
     for (int i = 0; i < 10; ++i) mbar_init(smem_addr(&barmem[i]), (i == 6 || i == 7) ? CH_EPI / 32 : 1);
     *sAbort = 0;
     fence_mbar_init();
-    for (int i = 0; i < 2 && i < p.ns; ++i) {
-      load_main(i);
-      load_p(i);
-    }
   }
   if (warp == CH_EPI / 32)
     for (int i = 0; i < 2 && i < p.ns; ++i) ld_chunk[i] = lp_chunk[i] = i;
@@ -612,13 +615,14 @@ __global__ void __launch_bounds__(CH_THREADS, 1)
     tmem_alloc(smem_addr(sTmem), CH_TMEM);
     tmem_relinquish();
   }
-  for (int i = tid; i < p.ns; i += CH_THREADS) sEgc[i] = p.egc[u0 + i];
   const int gw = warp & 3, hc = (warp >> 2) & 1;
   const uint32_t lane_off = static_cast<uint32_t>(gw * 32) << 16;
   const int row = 32 * gw + lane;                       // state row / d_v index of this thread
   float* Sg = p.state + ((size_t)slot * p.Hv + h) * D * D + (size_t)row * D + 64 * hc;
   // the entering state (fp32, row i -> TMEM lane i; this thread: 64 columns), loaded while
   // TMEM is being allocated
+  // (the state was last written by the chain of the previous slice or call, whose completion
+  // the local kernel before this one waited for before letting this one start)
   float sv[64];
   if (tid < CH_EPI) {
 #pragma unroll
@@ -627,6 +631,14 @@ __global__ void __launch_bounds__(CH_THREADS, 1)
       sv[4 * q] = f.x; sv[4 * q + 1] = f.y; sv[4 * q + 2] = f.z; sv[4 * q + 3] = f.w;
     }
   }
+  // the local kernel's tiles and e^{G_C} (and the conv output V) from here on
+  pdl_wait();
+  if (tid == CH_EPI)
+    for (int i = 0; i < 2 && i < p.ns; ++i) {
+      load_main(i);
+      load_p(i);
+    }
+  for (int i = tid; i < p.ns; i += CH_THREADS) sEgc[i] = p.egc[u0 + i];
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -855,43 +867,6 @@ __global__ void __launch_bounds__(CH_THREADS, 1)
 
 // ======================================================================= host side
 
-typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
-                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
-                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
-                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn encode_fn() {
-  static EncodeTiledFn fn = nullptr;
-  if (!fn) {
-    void* ptr = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
-                                         &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<EncodeTiledFn>(ptr);
-  }
-  return fn;
-}
-
-// 3-D map over [B][T][width] elements starting at `base`, token stride `tok_stride`
-// elements; box = {box0, box1 tokens, 1 sequence}.
-bool make_map(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int elem_bytes,
-              int width, int T, int B, long long tok_stride, int box0, int box1,
-              bool swizzle128) {
-  EncodeTiledFn fn = encode_fn();
-  if (!fn) return false;
-  cuuint64_t dims[3] = {(cuuint64_t)width, (cuuint64_t)T, (cuuint64_t)B};
-  cuuint64_t strides[2] = {(cuuint64_t)(tok_stride * elem_bytes),
-                           (cuuint64_t)(tok_stride * elem_bytes) * (cuuint64_t)T};
-  cuuint32_t box[3] = {(cuuint32_t)box0, (cuuint32_t)box1, 1u};
-  cuuint32_t estr[3] = {1u, 1u, 1u};
-  CUresult r = fn(m, dt, 3, const_cast<void*>(base), dims, strides, box, estr,
-                  CU_TENSOR_MAP_INTERLEAVE_NONE,
-                  swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
-                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS;
-}
-
 // Chunks per slice: as many as keep one slice's tiles within SLICE_BUDGET bytes.
 int slice_chunks(int B, int Hv, int nch) {
   const size_t per_chunk = (size_t)B * Hv * UNIT_BYTES;
@@ -907,13 +882,13 @@ cudaError_t launch_tc_t(const GdnLayerArgs& L, cudaStream_t stream) {
   CUtensorMap mq, mk, mv, mo;
   constexpr int out_rows = (int)(2 * KB / (32 * sizeof(Tout)));
   const bool ok =
-      make_map(&mq, L.q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, L.Hk * D, L.T, L.B, L.q_tok_stride,
+      gdn_make_map(&mq, L.q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, L.Hk * D, L.T, L.B, L.q_tok_stride,
                64, 64, true) &&
-      make_map(&mk, L.k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, L.Hk * D, L.T, L.B, L.k_tok_stride,
+      gdn_make_map(&mk, L.k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, L.Hk * D, L.T, L.B, L.k_tok_stride,
                64, 64, true) &&
-      make_map(&mv, L.v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, L.Hv * D, L.T, L.B, L.v_tok_stride,
+      gdn_make_map(&mv, L.v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, L.Hv * D, L.T, L.B, L.v_tok_stride,
                64, 64, true) &&
-      make_map(&mo, L.out,
+      gdn_make_map(&mo, L.out,
                sizeof(Tout) == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
                (int)sizeof(Tout), L.Hv * D, L.T, L.B, (long long)L.Hv * D, 32, out_rows, false);
   if (!ok) return cudaErrorInvalidValue;
@@ -936,11 +911,12 @@ cudaError_t launch_tc_t(const GdnLayerArgs& L, cudaStream_t stream) {
   for (int n0 = 0; n0 < nch; n0 += ns_max) {
     p.n0 = n0;
     p.ns = nch - n0 < ns_max ? nch - n0 : ns_max;
-    gdn_chunk_local_kernel<__nv_bfloat16>
-        <<<dim3((unsigned)p.ns, (unsigned)L.Hv, (unsigned)L.B), LGT, L_SMEM, stream>>>(mq, mk, p);
-    gdn_chunk_chain_kernel<Tout>
-        <<<dim3((unsigned)(L.B * L.Hv)), CH_THREADS, CH_SMEM, stream>>>(mv, mo, p);
-    e = cudaGetLastError();
+    e = launch_pdl(gdn_chunk_local_kernel<__nv_bfloat16>,
+                   dim3((unsigned)p.ns, (unsigned)L.Hv, (unsigned)L.B), dim3(LGT), L_SMEM, stream,
+                   mq, mk, p);
+    if (e != cudaSuccess) return e;
+    e = launch_pdl(gdn_chunk_chain_kernel<Tout>, dim3((unsigned)(L.B * L.Hv)), dim3(CH_THREADS),
+                   CH_SMEM, stream, mv, mo, p);
     if (e != cudaSuccess) return e;
   }
   return cudaSuccess;
