@@ -27,14 +27,15 @@
 //     T', T'', W, Q~, K~).  Its results for the chain are five 16 KB tiles per chunk, already
 //     in the swizzled layouts the chain's MMAs read, written with bulk copies to a workspace
 //     slice small enough to stay in L2, plus e^{G_C}.
-//   * gdn_chunk_chain_kernel, one CTA per (value head, sequence): the state chain only.  It
-//     streams the tiles of chunk n+1 and n+2 with bulk copies while chunk n runs:
-//     U'^T (MMA), S0 = bf16(S) into TMEM, S <- e^{G_C} S, U^T += S0 (-W)^T, O^T = S0 Q~^T,
-//     U^T -> bf16 hi/lo in TMEM, O^T += U^T P^T, S += U^T K~; the output tile of chunk n-1
-//     leaves through a TMA store while chunk n's first MMAs run.
-// The fp32 state stays in TMEM for a whole slice.  Every mbarrier wait is bounded: on timeout
-// the CTA records GDN_ERR_DEVICE_TIMEOUT, waits (bounded) for its own copies and MMAs, frees
-// TMEM and returns.
+//   * gdn_chunk_chain_kernel, one CTA per (value head, sequence): the state chain only, with
+//     eight epilogue warps and one MMA / copy issuer warp.  Per chunk: U'^T (MMA), S0 =
+//     bf16(S) into TMEM, S <- e^{G_C} S, U^T += S0 (-W)^T, O^T = S0 Q~^T, U^T -> bf16 hi/lo in
+//     TMEM, S += U^T K~, O^T += U^T P^T; the next chunk's tiles stream in meanwhile and the
+//     previous chunk's output leaves through TMA stores.
+// Both kernels are launched with programmatic dependent launch (set-up overlaps the tail of
+// the kernel before).  The fp32 state stays in TMEM for a whole slice.  Every mbarrier wait
+// is bounded: on timeout the CTA records GDN_ERR_DEVICE_TIMEOUT, waits (bounded) for its own
+// copies and MMAs, frees TMEM and returns.
 #include "common.cuh"
 #include "sm100_ptx.cuh"
 
