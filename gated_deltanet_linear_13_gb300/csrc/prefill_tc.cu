@@ -55,7 +55,10 @@ namespace {
 
 constexpr int C = kChunk, D = kHeadDim;
 constexpr uint32_t KB = 1024;
-constexpr int LA = 64;                                // row stride (floats) of the solve matrices
+// Row stride (floats) of the fp32 solve matrices: 64 + 4 pad, so that the rows a warp's lanes
+// own start 16 bytes apart in the bank space (no conflicts when each lane writes its row).
+constexpr int LA = 68;
+constexpr uint32_t SOLVE_MAT = 64 * LA * 4;           // bytes of one solve matrix
 constexpr int LGT = 256;                              // threads of the local kernel (barrier 1)
 
 // ---- one chunk's tiles for the chain (bytes within a 80 KB unit of the workspace)
@@ -229,10 +232,11 @@ __device__ __forceinline__ void solve_unit_lower(const float* As, float* Ts, flo
 // ======================================================================= local kernel
 // One CTA per (chunk j of the slice, value head h, sequence b), 256 threads, two CTAs per SM.
 constexpr uint32_t L_KQ = 0;            // [kb][K 64 rows | Q 64 rows][128 B]; later -W^T
-constexpr uint32_t L_SOLVE = 32 * KB;   // A | T fp32 [64][64]; then T'h T'l T''h T''l
-constexpr uint32_t L_P = 64 * KB;       // P hi | P lo
-constexpr uint32_t L_KT = 80 * KB;      // K~
-constexpr uint32_t L_MISC = 96 * KB;    // factors, solve scratch, barriers
+constexpr uint32_t L_SOLVE = 32 * KB;   // A | T fp32 [64][LA]; then T'h T'l T''h T''l
+constexpr uint32_t L_P = 66 * KB;       // P hi | P lo
+constexpr uint32_t L_KT = 82 * KB;      // K~
+constexpr uint32_t L_MISC = 98 * KB;    // factors, solve scratch, barriers
+static_assert(L_SOLVE + 2 * SOLVE_MAT <= L_P, "solve matrices overlap P");
 constexpr uint32_t L_SMEM = L_MISC + 6 * KB + KB;
 constexpr uint32_t L_TMEM = 128;        // G | W^T
 
@@ -351,8 +355,9 @@ __global__ void __launch_bounds__(LGT, 2)
       const int nr = tid >> 1, kb = tid & 1;
       const uint8_t* rp = sm + L_KQ + kb * 16 * KB + (nr < 64 ? 0 : 8 * KB) + (nr & 63) * 128;
       uint4 q4[8];
+      // (chunks visited in swizzled order: lanes of different rows hit different banks)
 #pragma unroll
-      for (int c = 0; c < 8; ++c) q4[c] = reinterpret_cast<const uint4*>(rp)[c];
+      for (int c = 0; c < 8; ++c) q4[c] = reinterpret_cast<const uint4*>(rp)[c ^ (nr & 7)];
       float s4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int c = 0; c < 8; ++c) {
@@ -443,7 +448,7 @@ __global__ void __launch_bounds__(LGT, 2)
     // ---- the direct solve T = (I + A)^{-1}, then T' and T'' as bf16 hi/lo B operands
     {
       float* As = reinterpret_cast<float*>(sm + L_SOLVE);
-      float* Ts = reinterpret_cast<float*>(sm + L_SOLVE + 16 * KB);
+      float* Ts = reinterpret_cast<float*>(sm + L_SOLVE + SOLVE_MAT);
       solve_unit_lower(As, Ts, sX, tid);
       // the T'/T'' tiles reuse the A/T region: read this thread's T entries first
       float tv[2][8];
