@@ -10,7 +10,8 @@
 //   O  = diag(e^G) Q^ S0^T + P U,     S = e^{G_C} S0 + U^T diag(e^{G_C-G}) K^
 // Normalisation and every diagonal factor are folded into small matrices or into row
 // scalings of the raw tiles, so the tensor cores see raw bf16 q/k/v:
-//   G = [K;Q] K^T (one M=128 MMA)  ->  A, P (with 1/||k||, scale/||q||, decays)
+//   G = [K;Q][K;Q]^T (one M=N=128 MMA)  ->  A, P (with 1/||k||, scale/||q||, decays); the
+//   squared norms are G's diagonal
 //   T' = T diag(beta e^G / ||k||),  T'' = T diag(beta)      (the solve, fp32 FMA)
 //   W^T = K^T T'^T,  U'^T = V^T T''^T                          (M = d = 128)
 //   Q~ = diag(scale e^G / ||q||) Q,  K~ = diag(e^{G_C-G} / ||k||) K
@@ -70,7 +71,7 @@ constexpr uint32_t U_T2 = 64 * KB;    // T'' hi | T'' lo [64 rows r][128 B = 64 
 constexpr uint32_t UNIT_BYTES = 80 * KB;
 constexpr size_t SLICE_BUDGET = (size_t)48 << 20;   // workspace bytes for one slice of units
 
-constexpr uint32_t ID_G = idesc_bf16(128, 64, false, false);   // [K;Q] K^T
+constexpr uint32_t ID_G = idesc_bf16(128, 128, false, false);  // [K;Q] [K;Q]^T
 constexpr uint32_t ID_KT = idesc_bf16(128, 64, true, false);   // K^T T'^T, V^T T''^T
 constexpr uint32_t ID_SW = idesc_bf16(128, 64, false, true);   // S0 (-W)^T
 constexpr uint32_t ID_SQ = idesc_bf16(128, 64, false, false);  // S0 Q~^T, U^T P^T
@@ -150,7 +151,8 @@ __device__ __forceinline__ void store_row_hilo(uint32_t tile_hi, uint32_t tile_l
 // t_s is final, every later row r subtracts A_rs t_s) while the other threads zero the
 // strictly upper blocks; then the off-diagonal blocks by distance from the diagonal,
 //   X_ij = sum_{k=j}^{i-1} A_ik T_kj,   T_ij = -T_ii X_ij,
-// one block entry per thread, with every operand loaded before the multiply-adds.
+// 64 threads per block, each one row and four consecutive columns of it (so that every row
+// of A and every 4-wide row piece of T it loads feeds four multiply-adds).
 __device__ __forceinline__ void solve_unit_lower(const float* As, float* Ts, float* X, int lt) {
   const int w = lt >> 5, lane = lt & 31;
   if (w < 4 && lane < 16) {
@@ -185,49 +187,55 @@ __device__ __forceinline__ void solve_unit_lower(const float* As, float* Ts, flo
     }
   }
   named_bar_sync(1, LGT);
-  const int rr = lt >> 4, cc = lt & 15;
+  const int q = lt >> 6, rr = (lt >> 2) & 15, c4 = 4 * (lt & 3);
 #pragma unroll
   for (int dist = 1; dist <= 3; ++dist) {
-#pragma unroll
-    for (int q = 0; q < 4 - dist; ++q) {
-      const int i = dist + q, j = q;
+    const int i = dist + q, j = q;
+    const bool active = q < 4 - dist;
+    if (active) {
       float acc[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
       for (int k = j; k < i; ++k) {
-        float av[16], tv[16];
+        float av[16];
 #pragma unroll
         for (int m4 = 0; m4 < 4; ++m4) {
           const float4 x = *reinterpret_cast<const float4*>(As + (16 * i + rr) * LA + 16 * k + 4 * m4);
           av[4 * m4] = x.x; av[4 * m4 + 1] = x.y; av[4 * m4 + 2] = x.z; av[4 * m4 + 3] = x.w;
         }
 #pragma unroll
-        for (int m = 0; m < 16; ++m) tv[m] = Ts[(16 * k + m) * LA + 16 * j + cc];
-#pragma unroll
-        for (int m = 0; m < 16; ++m) acc[m & 3] = fmaf(av[m], tv[m], acc[m & 3]);
+        for (int m = 0; m < 16; ++m) {
+          const float4 t = *reinterpret_cast<const float4*>(Ts + (16 * k + m) * LA + 16 * j + c4);
+          acc[0] = fmaf(av[m], t.x, acc[0]);
+          acc[1] = fmaf(av[m], t.y, acc[1]);
+          acc[2] = fmaf(av[m], t.z, acc[2]);
+          acc[3] = fmaf(av[m], t.w, acc[3]);
+        }
       }
-      X[q * 256 + lt] = (acc[0] + acc[1]) + (acc[2] + acc[3]);
+      *reinterpret_cast<float4*>(X + q * 256 + rr * 16 + c4) =
+          make_float4(acc[0], acc[1], acc[2], acc[3]);
     }
     named_bar_sync(1, LGT);
-#pragma unroll
-    for (int q = 0; q < 4 - dist; ++q) {
-      const int i = dist + q, j = q;
-      float tv[16], xv[16];
+    if (active) {
+      float tv[16];
 #pragma unroll
       for (int m4 = 0; m4 < 4; ++m4) {
         const float4 x = *reinterpret_cast<const float4*>(Ts + (16 * i + rr) * LA + 16 * i + 4 * m4);
         tv[4 * m4] = x.x; tv[4 * m4 + 1] = x.y; tv[4 * m4 + 2] = x.z; tv[4 * m4 + 3] = x.w;
       }
-#pragma unroll
-      for (int m = 0; m < 16; ++m) xv[m] = X[q * 256 + m * 16 + cc];
       float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int m = 0; m < 16; ++m) acc[m & 3] = fmaf(tv[m], xv[m], acc[m & 3]);
-      Ts[(16 * i + rr) * LA + 16 * j + cc] = -((acc[0] + acc[1]) + (acc[2] + acc[3]));
+      for (int m = 0; m < 16; ++m) {
+        const float4 x = *reinterpret_cast<const float4*>(X + q * 256 + m * 16 + c4);
+        acc[0] = fmaf(tv[m], x.x, acc[0]);
+        acc[1] = fmaf(tv[m], x.y, acc[1]);
+        acc[2] = fmaf(tv[m], x.z, acc[2]);
+        acc[3] = fmaf(tv[m], x.w, acc[3]);
+      }
+      *reinterpret_cast<float4*>(Ts + (16 * i + rr) * LA + 16 * j + c4) =
+          make_float4(-acc[0], -acc[1], -acc[2], -acc[3]);
     }
     named_bar_sync(1, LGT);
   }
 }
-
 
 // ======================================================================= local kernel
 // One CTA per (chunk j of the slice, value head h, sequence b), 256 threads, two CTAs per SM.
@@ -238,7 +246,7 @@ constexpr uint32_t L_KT = 82 * KB;      // K~
 constexpr uint32_t L_MISC = 98 * KB;    // factors, solve scratch, barriers
 static_assert(L_SOLVE + 2 * SOLVE_MAT <= L_P, "solve matrices overlap P");
 constexpr uint32_t L_SMEM = L_MISC + 6 * KB + KB;
-constexpr uint32_t L_TMEM = 128;        // G | W^T
+constexpr uint32_t L_TMEM = 256;        // G (128) | W^T (64)
 
 template <typename Tin>
 __global__ void __launch_bounds__(LGT, 2)
@@ -264,6 +272,7 @@ __global__ void __launch_bounds__(LGT, 2)
   float* nq = gl2 + 192;                                 // scale / ||q_r||
   float* eG = gl2 + 256;                                 // e^{G_r}
   float* dK = gl2 + 320;                                 // e^{G_C - G_r}
+  float* fT1 = gl2 + 384;                                // beta_s e^{G_s} / ||k_s||
   float* sX = reinterpret_cast<float*>(sm + L_MISC + 2048);
   uint64_t* barmem = reinterpret_cast<uint64_t*>(sm + L_MISC + 5120);
   uint32_t* sTmem = reinterpret_cast<uint32_t*>(sm + L_MISC + 5120 + 32);
@@ -327,7 +336,7 @@ __global__ void __launch_bounds__(LGT, 2)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *sTmem;
-  const uint32_t TM_G = tmem, TM_W = tmem + 64;
+  const uint32_t TM_G = tmem, TM_W = tmem + 128;
   const int gw = warp & 3, half = warp >> 2;
   const uint32_t lane_off = static_cast<uint32_t>(gw * 32) << 16;
   const int row = 32 * gw + lane;
@@ -338,44 +347,18 @@ __global__ void __launch_bounds__(LGT, 2)
     if (!mbar_wait_or_abort(bar_in, 0, sAbort)) *sAbort = 1;
     __syncthreads();
     if (*sAbort) break;
-    // ---- MMA 1: G = [K; Q] K^T  (M = 128: k_0..k_63, q_0..q_63; N = 64; K = 128)
+    // ---- MMA 1: G = [K; Q] [K; Q]^T  (M = N = 128: k_0..k_63, q_0..q_63; K = 128).  Its
+    //      k.k and q.k blocks feed A and P, its diagonal gives the squared row norms.
     if (warp == 0 && elect_one()) {
       tc_fence_after();
 #pragma unroll
       for (int k = 0; k < 8; ++k) {
-        const uint32_t off = L_KQ + (k >> 2) * 16 * KB + (k & 3) * 32;
-        mma_bf16(TM_G, sdesc_sw128(sb + off, 16, 1024), sdesc_sw128(sb + off, 16, 1024), ID_G,
-                 k > 0);
+        const uint64_t dkq = sdesc_sw128(sb + L_KQ + (k >> 2) * 16 * KB + (k & 3) * 32, 16, 1024);
+        mma_bf16(TM_G, dkq, dkq, ID_G, k > 0);
       }
       mma_commit(bar_mma);
     }
     pend_mma = true;
-    // ---- row norms of k (rows 0..63) and q (rows 64..127) from the raw tiles
-    {
-      const int nr = tid >> 1, kb = tid & 1;
-      const uint8_t* rp = sm + L_KQ + kb * 16 * KB + (nr < 64 ? 0 : 8 * KB) + (nr & 63) * 128;
-      uint4 q4[8];
-      // (chunks visited in swizzled order: lanes of different rows hit different banks)
-#pragma unroll
-      for (int c = 0; c < 8; ++c) q4[c] = reinterpret_cast<const uint4*>(rp)[c ^ (nr & 7)];
-      float s4[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-      for (int c = 0; c < 8; ++c) {
-        const __nv_bfloat162* hv = reinterpret_cast<const __nv_bfloat162*>(&q4[c]);
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const float2 f = __bfloat1622float2(hv[e]);
-          s4[e] = fmaf(f.x, f.x, fmaf(f.y, f.y, s4[e]));
-        }
-      }
-      float ss = (s4[0] + s4[1]) + (s4[2] + s4[3]);
-      ss += __shfl_xor_sync(0xffffffffu, ss, 1);
-      if (kb == 0) {
-        const float inv = p.l2norm ? 1.0f / sqrtf(ss + p.eps) : 1.0f;
-        if (nr < 64) nk[nr] = inv; else nq[nr - 64] = inv * p.scale;
-      }
-    }
-    __syncthreads();
     if (tid < 64) {
       eG[tid] = ex2_approx(gl2[tid]);
       dK[tid] = ex2_approx(gl2[63] - gl2[tid]);
@@ -385,17 +368,31 @@ __global__ void __launch_bounds__(LGT, 2)
     mma_phase ^= 1;
     pend_mma = false;
     tc_fence_after();
-    __syncthreads();
-    if (*sAbort) break;
+    if (__syncthreads_or(*sAbort)) break;
 
     // ---- E1: G -> A (fp32 [r][s], strictly lower) and P (bf16 hi/lo [r][s], K-major)
     {
       float* As = reinterpret_cast<float*>(sm + L_SOLVE);
-      const bool isq = row >= 64;
+      const bool isq = row >= 64;                        // (warp-uniform)
       const int r = row & 63;
-      const float Gr = gl2[r], sr = (isq ? 1.0f : beta[r]) * (isq ? nq[r] : nk[r]);
-      float v[32], gs[32], ns[32];
+      float v[32], dg[32];
       tmem_ld32(TM_G + lane_off + 32 * half, v);
+      // the diagonal entry of this row: k row r in column r (warps 0 and 5 hold it), q row r in
+      // column 64 + r (read by the q warps of column half 0)
+      if (isq && half == 0) tmem_ld32(TM_G + lane_off + 64 + 32 * (gw - 2), dg);
+      tmem_wait_ld();
+      if (isq ? (half == 0) : (half == gw)) {
+        float d = 0.f;
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+          if (j == lane) d = isq ? dg[j] : v[j];
+        const float inv = p.l2norm ? 1.0f / sqrtf(d + p.eps) : 1.0f;
+        if (isq) nq[r] = inv * p.scale; else nk[r] = inv;
+      }
+      __syncthreads();
+      if (tid < 64) fT1[tid] = beta[tid] * eG[tid] * nk[tid];
+      const float Gr = gl2[r], sr = (isq ? 1.0f : beta[r]) * (isq ? nq[r] : nk[r]);
+      float gs[32], ns[32];
 #pragma unroll
       for (int j4 = 0; j4 < 8; ++j4) {
         const float4 g4 = *reinterpret_cast<const float4*>(gl2 + 32 * half + 4 * j4);
@@ -403,7 +400,6 @@ __global__ void __launch_bounds__(LGT, 2)
         gs[4 * j4] = g4.x; gs[4 * j4 + 1] = g4.y; gs[4 * j4 + 2] = g4.z; gs[4 * j4 + 3] = g4.w;
         ns[4 * j4] = n4.x; ns[4 * j4 + 1] = n4.y; ns[4 * j4 + 2] = n4.z; ns[4 * j4 + 3] = n4.w;
       }
-      tmem_wait_ld();
 #pragma unroll
       for (int j = 0; j < 32; ++j) {
         const int s = 32 * half + j;
@@ -419,21 +415,28 @@ __global__ void __launch_bounds__(LGT, 2)
               make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
       }
     }
-    // ---- Q~ = diag(scale e^G / ||q||) Q in place;  K~ = diag(e^{G_C-G} / ||k||) K -> KT
-    for (int idx = tid; idx < 2048; idx += LGT) {
-      const int isk = idx >> 10, c = idx & 1023;
-      const int kb = c >> 9, off = (c & 511) * 16, r = (c & 511) >> 3;
-      uint8_t* src = sm + L_KQ + kb * 16 * KB + (isk ? 0 : 8 * KB) + off;
-      uint8_t* dst = isk ? sm + L_KT + kb * 8 * KB + off : src;
+    // ---- Q~ = diag(scale e^G / ||q||) Q in place;  K~ = diag(e^{G_C-G} / ||k||) K -> KT.
+    //      Thread: one row of one 64-column block of K or Q (8 chunks, visited in swizzled
+    //      order so that the lanes' rows hit different banks).
+    {
+      const int blk = tid >> 6, r = tid & 63;            // blk: K kb0, K kb1, Q kb0, Q kb1
+      const bool isk = blk < 2;
+      const int kb = blk & 1;
+      const uint8_t* src = sm + L_KQ + kb * 16 * KB + (isk ? 0 : 8 * KB) + r * 128;
+      uint8_t* dst = (isk ? sm + L_KT + kb * 8 * KB : sm + L_KQ + kb * 16 * KB + 8 * KB) + r * 128;
       const float f = isk ? dK[r] * nk[r] : eG[r] * nq[r];
-      uint4 w4 = *reinterpret_cast<const uint4*>(src);
-      __nv_bfloat162* hv = reinterpret_cast<__nv_bfloat162*>(&w4);
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const float2 x = __bfloat1622float2(hv[e]);
-        hv[e] = __floats2bfloat162_rn(x.x * f, x.y * f);
+      for (int c = 0; c < 8; ++c) {
+        const int pc = (c ^ r) & 7;
+        uint4 w4 = reinterpret_cast<const uint4*>(src)[pc];
+        __nv_bfloat162* hv = reinterpret_cast<__nv_bfloat162*>(&w4);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float2 x = __bfloat1622float2(hv[e]);
+          hv[e] = __floats2bfloat162_rn(x.x * f, x.y * f);
+        }
+        reinterpret_cast<uint4*>(dst)[pc] = w4;
       }
-      *reinterpret_cast<uint4*>(dst) = w4;
     }
     fence_proxy_async_smem();
     __syncthreads();
@@ -468,10 +471,10 @@ __global__ void __launch_bounds__(LGT, 2)
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           const int s = 8 * c + 2 * e;
-          const float f10 = beta[s] * eG[s] * nk[s];
-          const float f11 = beta[s + 1] * eG[s + 1] * nk[s + 1];
-          pack_hilo(tv[jj][2 * e] * f10, tv[jj][2 * e + 1] * f11, h1[e], l1[e]);
-          pack_hilo(tv[jj][2 * e] * beta[s], tv[jj][2 * e + 1] * beta[s + 1], h2[e], l2[e]);
+          const float2 f1 = *reinterpret_cast<const float2*>(fT1 + s);
+          const float2 f2 = *reinterpret_cast<const float2*>(beta + s);
+          pack_hilo(tv[jj][2 * e] * f1.x, tv[jj][2 * e + 1] * f1.y, h1[e], l1[e]);
+          pack_hilo(tv[jj][2 * e] * f2.x, tv[jj][2 * e + 1] * f2.y, h2[e], l2[e]);
         }
         st_shared_v4(sw128(sb + L_SOLVE, r, c), h1[0], h1[1], h1[2], h1[3]);
         st_shared_v4(sw128(sb + L_SOLVE + 8 * KB, r, c), l1[0], l1[1], l1[2], l1[3]);
