@@ -120,28 +120,41 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t
                : "memory");
 }
 
-// 32 fp32 values (times mul) -> bf16 -> 4 swizzled 16-byte chunks c0..c0+3 of row r.
-__device__ __forceinline__ void store_row_bf16(uint32_t tile, int r, int c0, const float* v,
-                                               float mul) {
+// Byte offset of 16-byte chunk `c` of row `r` in a 128-byte-swizzled tile image (the layout a
+// 1024-byte aligned shared-memory copy of it has for the tensor cores).
+__device__ __forceinline__ uint32_t sw128_off(int r, int c) {
+  return (uint32_t)r * 128u + (uint32_t)((c ^ (r & 7)) << 4);
+}
+
+__device__ __forceinline__ void st_global_v4(uint8_t* p, uint32_t a, uint32_t b, uint32_t c,
+                                             uint32_t d) {
+  *reinterpret_cast<uint4*>(p) = make_uint4(a, b, c, d);
+}
+
+// 32 fp32 values (times mul) -> bf16 -> 4 swizzled 16-byte chunks c0..c0+3 of row r of a tile
+// image in global memory.
+__device__ __forceinline__ void store_row_bf16_g(uint8_t* tile, int r, int c0, const float* v,
+                                                 float mul) {
 #pragma unroll
   for (int c = 0; c < 4; ++c) {
     const float* w = v + 8 * c;
-    st_shared_v4(sw128(tile, r, c0 + c), pack_bf16(w[0] * mul, w[1] * mul),
+    st_global_v4(tile + sw128_off(r, c0 + c), pack_bf16(w[0] * mul, w[1] * mul),
                  pack_bf16(w[2] * mul, w[3] * mul), pack_bf16(w[4] * mul, w[5] * mul),
                  pack_bf16(w[6] * mul, w[7] * mul));
   }
 }
 
-// 32 fp32 values -> bf16 hi and lo rows (chunks c0..c0+3 of row r) of two tiles.
-__device__ __forceinline__ void store_row_hilo(uint32_t tile_hi, uint32_t tile_lo, int r, int c0,
-                                               const float* v) {
+// 32 fp32 values -> bf16 hi and lo rows (chunks c0..c0+3 of row r) of two tile images in
+// global memory.
+__device__ __forceinline__ void store_row_hilo_g(uint8_t* tile_hi, uint8_t* tile_lo, int r,
+                                                 int c0, const float* v) {
 #pragma unroll
   for (int c = 0; c < 4; ++c) {
     uint32_t h[4], l[4];
 #pragma unroll
     for (int e = 0; e < 4; ++e) pack_hilo(v[8 * c + 2 * e], v[8 * c + 2 * e + 1], h[e], l[e]);
-    st_shared_v4(sw128(tile_hi, r, c0 + c), h[0], h[1], h[2], h[3]);
-    st_shared_v4(sw128(tile_lo, r, c0 + c), l[0], l[1], l[2], l[3]);
+    st_global_v4(tile_hi + sw128_off(r, c0 + c), h[0], h[1], h[2], h[3]);
+    st_global_v4(tile_lo + sw128_off(r, c0 + c), l[0], l[1], l[2], l[3]);
   }
 }
 
@@ -238,18 +251,18 @@ __device__ __forceinline__ void solve_unit_lower(const float* As, float* Ts, flo
 }
 
 // ======================================================================= local kernel
-// One CTA per (chunk j of the slice, value head h, sequence b), 256 threads, two CTAs per SM.
-constexpr uint32_t L_KQ = 0;            // [kb][K 64 rows | Q 64 rows][128 B]; later -W^T
-constexpr uint32_t L_SOLVE = 32 * KB;   // A | T fp32 [64][LA]; then T'h T'l T''h T''l
-constexpr uint32_t L_P = 66 * KB;       // P hi | P lo
-constexpr uint32_t L_KT = 82 * KB;      // K~
-constexpr uint32_t L_MISC = 98 * KB;    // factors, solve scratch, barriers
-static_assert(L_SOLVE + 2 * SOLVE_MAT <= L_P, "solve matrices overlap P");
+// One CTA per (chunk j of the slice, value head h, sequence b), 256 threads, three CTAs per
+// SM.  The tiles for the chain go from registers straight to the workspace (already in the
+// swizzled layout of their shared-memory copies there), so shared memory holds only K / Q,
+// the solve and small factors.
+constexpr uint32_t L_KQ = 0;            // [kb][K 64 rows | Q 64 rows][128 B]
+constexpr uint32_t L_SOLVE = 32 * KB;   // A | T fp32 [64][LA]; then T'h T'l
+constexpr uint32_t L_MISC = L_SOLVE + 2 * SOLVE_MAT;   // factors, solve scratch, barriers
 constexpr uint32_t L_SMEM = L_MISC + 6 * KB + KB;
-constexpr uint32_t L_TMEM = 256;        // G (128) | W^T (64)
+constexpr uint32_t L_TMEM = 128;        // G (128 columns); later W^T in its first 64
 
 template <typename Tin>
-__global__ void __launch_bounds__(LGT, 2)
+__global__ void __launch_bounds__(LGT, 3)
     gdn_chunk_local_kernel(const __grid_constant__ CUtensorMap tm_q,
                            const __grid_constant__ CUtensorMap tm_k, const TcParams p) {
   extern __shared__ uint8_t smem_raw[];
@@ -336,7 +349,7 @@ __global__ void __launch_bounds__(LGT, 2)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *sTmem;
-  const uint32_t TM_G = tmem, TM_W = tmem + 128;
+  const uint32_t TM_G = tmem, TM_W = tmem;
   const int gw = warp & 3, half = warp >> 2;
   const uint32_t lane_off = static_cast<uint32_t>(gw * 32) << 16;
   const int row = 32 * gw + lane;
@@ -381,6 +394,7 @@ __global__ void __launch_bounds__(LGT, 2)
       // column 64 + r (read by the q warps of column half 0)
       if (isq && half == 0) tmem_ld32(TM_G + lane_off + 64 + 32 * (gw - 2), dg);
       tmem_wait_ld();
+      tc_fence_before();                                 // (W^T later reuses these columns)
       if (isq ? (half == 0) : (half == gw)) {
         float d = 0.f;
 #pragma unroll
@@ -407,7 +421,7 @@ __global__ void __launch_bounds__(LGT, 2)
         v[j] = keep ? ex2_approx(Gr - gs[j]) * v[j] * (sr * ns[j]) : 0.f;
       }
       if (isq) {
-        store_row_hilo(sb + L_P, sb + L_P + 8 * KB, r, 4 * half, v);
+        store_row_hilo_g(unit + U_P, unit + U_P + 8 * KB, r, 4 * half, v);
       } else {
 #pragma unroll
         for (int j = 0; j < 32; j += 4)
@@ -423,7 +437,7 @@ __global__ void __launch_bounds__(LGT, 2)
       const bool isk = blk < 2;
       const int kb = blk & 1;
       const uint8_t* src = sm + L_KQ + kb * 16 * KB + (isk ? 0 : 8 * KB) + r * 128;
-      uint8_t* dst = (isk ? sm + L_KT + kb * 8 * KB : sm + L_KQ + kb * 16 * KB + 8 * KB) + r * 128;
+      uint8_t* dst = unit + (isk ? U_KT : U_QT) + kb * 8 * KB + r * 128;
       const float f = isk ? dK[r] * nk[r] : eG[r] * nq[r];
 #pragma unroll
       for (int c = 0; c < 8; ++c) {
@@ -438,15 +452,7 @@ __global__ void __launch_bounds__(LGT, 2)
         reinterpret_cast<uint4*>(dst)[pc] = w4;
       }
     }
-    fence_proxy_async_smem();
     __syncthreads();
-    if (tid == 0) {
-      bulk_store(unit + U_P, sb + L_P, 16 * KB);
-      bulk_store(unit + U_QT, sb + L_KQ + 8 * KB, 8 * KB);
-      bulk_store(unit + U_QT + 8 * KB, sb + L_KQ + 24 * KB, 8 * KB);
-      bulk_store(unit + U_KT, sb + L_KT, 16 * KB);
-      tma_store_commit();
-    }
 
     // ---- the direct solve T = (I + A)^{-1}, then T' and T'' as bf16 hi/lo B operands
     {
@@ -478,17 +484,13 @@ __global__ void __launch_bounds__(LGT, 2)
         }
         st_shared_v4(sw128(sb + L_SOLVE, r, c), h1[0], h1[1], h1[2], h1[3]);
         st_shared_v4(sw128(sb + L_SOLVE + 8 * KB, r, c), l1[0], l1[1], l1[2], l1[3]);
-        st_shared_v4(sw128(sb + L_SOLVE + 16 * KB, r, c), h2[0], h2[1], h2[2], h2[3]);
-        st_shared_v4(sw128(sb + L_SOLVE + 24 * KB, r, c), l2[0], l2[1], l2[2], l2[3]);
+        st_global_v4(unit + U_T2 + sw128_off(r, c), h2[0], h2[1], h2[2], h2[3]);
+        st_global_v4(unit + U_T2 + 8 * KB + sw128_off(r, c), l2[0], l2[1], l2[2], l2[3]);
       }
     }
     fence_proxy_async_smem();
     __syncthreads();
-    // ---- T'' to the chain; MMA 3: W^T = K^T T'^T (M = d_k, N = 64 tokens, K = 64 tokens)
-    if (tid == 0) {                   // (bulk-copy groups are per thread: thread 0 waits)
-      bulk_store(unit + U_T2, sb + L_SOLVE + 16 * KB, 16 * KB);
-      tma_store_commit();
-    }
+    // ---- MMA 3: W^T = K^T T'^T (M = d_k, N = 64 tokens, K = 64 tokens)
     if (warp == 0 && elect_one()) {
       tc_fence_after();
 #pragma unroll
@@ -503,28 +505,18 @@ __global__ void __launch_bounds__(LGT, 2)
     mma_phase ^= 1;
     pend_mma = false;
     tc_fence_after();
-    // -W^T overwrites the K|Q region: the Q~ copies out of it must have been read
-    if (tid == 0) tma_store_wait_read();
-    __syncthreads();
-    if (*sAbort) break;
+    if (__syncthreads_or(*sAbort)) break;
     // ---- E3: W^T -> -W^T bf16 (MN-major: row = d_k index, 64 token columns)
     {
       float v[32];
       tmem_ld32(TM_W + lane_off + 32 * half, v);
       tmem_wait_ld();
-      store_row_bf16(sb + L_KQ, row, 4 * half, v, -1.0f);
-    }
-    fence_proxy_async_smem();
-    __syncthreads();
-    if (tid == 0) {
-      bulk_store(unit + U_NW, sb + L_KQ, 16 * KB);
-      tma_store_commit();
+      store_row_bf16_g(unit + U_NW, row, 4 * half, v, -1.0f);
     }
   } while (0);
 
-  // ---- teardown: copies out and (abort path only) pending MMAs, then TMEM is freed
+  // ---- teardown: (abort path only) pending MMAs, then TMEM is freed
   if (tid == 0) {
-    tma_store_wait_all();
     if (pend_mma) mbar_wait_bounded(bar_mma, mma_phase, 1u << 16);
     if (*sAbort) atomicOr(&g_err_tc, kErrTimeout);
   }
@@ -901,8 +893,10 @@ cudaError_t launch_tc_t(const GdnLayerArgs& L, cudaStream_t stream) {
                sizeof(Tout) == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
                (int)sizeof(Tout), L.Hv * D, L.T, L.B, (long long)L.Hv * D, 32, out_rows, false);
   if (!ok) return cudaErrorInvalidValue;
-  static unsigned done_l = 0, done_c = 0;
+  static unsigned done_l = 0, done_c = 0, done_lc = 0;
   cudaError_t e = set_smem_once(gdn_chunk_local_kernel<__nv_bfloat16>, (int)L_SMEM, &done_l);
+  if (e != cudaSuccess) return e;
+  e = set_carveout_once(gdn_chunk_local_kernel<__nv_bfloat16>, 100, &done_lc);   // 3 CTAs per SM
   if (e != cudaSuccess) return e;
   e = set_smem_once(gdn_chunk_chain_kernel<Tout>, (int)CH_SMEM, &done_c);
   if (e != cudaSuccess) return e;
@@ -920,11 +914,13 @@ cudaError_t launch_tc_t(const GdnLayerArgs& L, cudaStream_t stream) {
   for (int n0 = 0; n0 < nch; n0 += ns_max) {
     p.n0 = n0;
     p.ns = nch - n0 < ns_max ? nch - n0 : ns_max;
-    e = launch_pdl(gdn_chunk_local_kernel<__nv_bfloat16>,
+    // (the first slice's local kernel reads the caller's gate inputs before its grid wait: it
+    // may start early only behind this call's own conv kernel)
+    e = launch_pdl(n0 > 0 || L.W > 0, gdn_chunk_local_kernel<__nv_bfloat16>,
                    dim3((unsigned)p.ns, (unsigned)L.Hv, (unsigned)L.B), dim3(LGT), L_SMEM, stream,
                    mq, mk, p);
     if (e != cudaSuccess) return e;
-    e = launch_pdl(gdn_chunk_chain_kernel<Tout>, dim3((unsigned)(L.B * L.Hv)), dim3(CH_THREADS),
+    e = launch_pdl(true, gdn_chunk_chain_kernel<Tout>, dim3((unsigned)(L.B * L.Hv)), dim3(CH_THREADS),
                    CH_SMEM, stream, mv, mo, p);
     if (e != cudaSuccess) return e;
   }
