@@ -141,6 +141,10 @@ __device__ __forceinline__ void tma_store_commit() {
 __device__ __forceinline__ void tma_store_wait_read() {
   asm volatile("cp.async.bulk.wait_group.read 0;\n" ::: "memory");
 }
+// All but the most recently committed bulk-store group have finished reading shared memory.
+__device__ __forceinline__ void tma_store_wait_read_1() {
+  asm volatile("cp.async.bulk.wait_group.read 1;\n" ::: "memory");
+}
 
 // Wait until every committed bulk store has completed (writes visible).
 __device__ __forceinline__ void tma_store_wait_all() {
