@@ -9,12 +9,12 @@
 //     s_i <- e^g s_i + delta_i k,        o_i = e^g gamma + delta_i (k . q)
 // (o = S_new q = e^g S q + delta (k . q)), so each row is streamed through once.
 //
-// Work split: a persistent grid of two CTAs per SM; a CTA takes whole (sequence, key head)
+// Work split: a persistent grid of four CTAs per SM; a CTA takes whole (sequence, key head)
 // items in turn.  Per item it runs the conv (+SiLU) of the key head's q/k channels and of its
 // r = Hv/Hk value heads' v channels once, writes their new conv state itself (no other CTA
 // touches those channels, so no ordering across CTAs is needed), forms the L2 norms and the
-// gates, and then streams the item's r x 128 state rows through shared memory in 64-row
-// blocks of 32 KB: a three-stage ring of TMA bulk copies (loads run two blocks ahead, across
+// gates, and then streams the item's r x 128 state rows through shared memory in 32-row
+// blocks of 16 KB: a three-stage ring of TMA bulk copies (loads run two blocks ahead, across
 // item boundaries, while the updated blocks leave with bulk stores).  In shared memory one
 // warp handles a 512-byte row with 128-bit accesses and two warp-wide dot products.
 #include "common.cuh"
@@ -71,10 +71,11 @@ __device__ __forceinline__ float dot4(float4 a, float4 b) {
 }
 
 constexpr int DEC_THREADS = 256;
-constexpr int DEC_RB = 64;                           // state rows per streamed block
+constexpr int DEC_RB = 32;                           // state rows per streamed block
 constexpr int DEC_NS = 3;                            // ring stages
-constexpr int DEC_CPS = 2;                           // CTAs per SM
+constexpr int DEC_CPS = 4;                           // CTAs per SM
 constexpr int DEC_MAXR = 8;                          // value heads per key head (at most)
+constexpr int DEC_BPH = kHeadDim / DEC_RB;          // blocks per value head
 constexpr uint32_t DEC_BLOCK_BYTES = DEC_RB * kHeadDim * 4;
 // shared memory: ring | q^ | k^ | v (r heads) | e^g, beta per head | outputs x 2 | reduce | bars
 constexpr uint32_t DEC_OFF_Q = DEC_NS * DEC_BLOCK_BYTES;
@@ -87,7 +88,7 @@ constexpr uint32_t DEC_OFF_BAR = DEC_OFF_RED + 32 * 4;
 constexpr uint32_t DEC_SMEM = DEC_OFF_BAR + DEC_NS * 8 + 128;   // + alignment slack
 
 // The sequence of (item, block) pairs a CTA processes: items blockIdx.x, +gridDim.x, ...
-// whose sequence has a valid state slot, 2r blocks each.
+// whose sequence has a valid state slot, r * DEC_BPH blocks each.
 struct DecCursor {
   int item, blk;
 };
@@ -133,14 +134,15 @@ __global__ void __launch_bounds__(DEC_THREADS, DEC_CPS) gdn_decode_kernel(GdnLay
   float* red = reinterpret_cast<float*>(dsm + DEC_OFF_RED);
   uint64_t* full = reinterpret_cast<uint64_t*>(dsm + DEC_OFF_BAR);
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int r = p.Hv / p.Hk, nblk = 2 * r, nitems = p.B * p.Hk;
+  const int r = p.Hv / p.Hk, nblk = DEC_BPH * r, nitems = p.B * p.Hk;
 
-  // state rows of block (item, blk): value head kh * r + blk / 2, rows (blk % 2) * 64 ...
+  // state rows of block (item, blk): value head kh * r + blk / DEC_BPH, rows from
+  // (blk % DEC_BPH) * DEC_RB
   auto block_src = [&](const DecCursor& c) -> float* {
     const int b = c.item / p.Hk, kh = c.item % p.Hk;
     const int slot = p.slots ? p.slots[b] : b;
-    const int h = kh * r + (c.blk >> 1);
-    return p.state + (((size_t)slot * p.Hv + h) * D + (size_t)(c.blk & 1) * DEC_RB) * D;
+    const int h = kh * r + c.blk / DEC_BPH;
+    return p.state + (((size_t)slot * p.Hv + h) * D + (size_t)(c.blk % DEC_BPH) * DEC_RB) * D;
   };
   // ---- producer state (thread 0): loads run DEC_NS - 1 blocks ahead of the consumers
   DecCursor pc;
@@ -225,8 +227,8 @@ __global__ void __launch_bounds__(DEC_THREADS, DEC_CPS) gdn_decode_kernel(GdnLay
       __syncthreads();
       kq = red[8] + red[9] + red[10] + red[11];
     }
-    // ---- the block: rows r0 .. r0 + 63 of value head hh
-    const int hh = c.blk >> 1, r0 = (c.blk & 1) * DEC_RB;
+    // ---- the block: rows r0 .. r0 + DEC_RB - 1 of value head hh
+    const int hh = c.blk / DEC_BPH, r0 = (c.blk % DEC_BPH) * DEC_RB;
     const int h = kh * r + hh;
     const float eg = sg[2 * hh], beta = sg[2 * hh + 1];
     const float4 k4 = reinterpret_cast<const float4*>(sk)[lane];
