@@ -284,6 +284,7 @@ def main():
     ap.add_argument("--cpu-tokens", type=int, default=8192)
     ap.add_argument("--cpu-reps", type=int, default=12)
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-decode-sweep", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--prefill-tokens", type=int, default=T_TOTAL,
                     help="tokens of the prefill workload (a multiple of 512; smaller only for "
@@ -402,6 +403,34 @@ def main():
     if st != 0:
         raise RuntimeError(f"device error in decode: {gdn.gdn_status_string(st)}")
     del g_dec, dwl
+    # the other batch sizes of the 27B decode workload (64-step graphs), for latency
+    dec_batches = []
+    if not args.no_decode_sweep:
+        main_b, main_steps = DECODE_B, DECODE_STEPS
+        for bsz in (1, 8, 32):
+            globals()["DECODE_B"], globals()["DECODE_STEPS"] = bsz, 64
+            swl = make_decode_workload(device)
+            decode_steps(gdn, swl)
+            g_sw = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g_sw):
+                decode_steps(gdn, swl)
+            for _ in range(3):
+                g_sw.replay()
+            s0 = torch.cuda.Event(enable_timing=True)
+            s1 = torch.cuda.Event(enable_timing=True)
+            s0.record()
+            for _ in range(3):
+                g_sw.replay()
+            s1.record()
+            torch.cuda.synchronize()
+            step_ms = s0.elapsed_time(s1) / (3 * 64)
+            dec_batches.append({"batch": bsz, "step_us": 1e3 * step_ms,
+                                "gbs": DECODE_BYTES_PER_SEQ * bsz / (step_ms / 1e3) / 1e9})
+            del g_sw, swl
+        globals()["DECODE_B"], globals()["DECODE_STEPS"] = main_b, main_steps
+        st = gdn.gdn_get_device_error()
+        if st != 0:
+            raise RuntimeError(f"device error in decode: {gdn.gdn_status_string(st)}")
 
     # ---------------- end to end through the public API with host buffers
     e2e = None
@@ -524,7 +553,7 @@ def main():
                                     "frac": dec_gbs / peaks["hbm_gbs"],
                                     "traffic": measured_traffic("decode_step", f"qwen36_27b_decode_B{DECODE_B}"),
                                     "peak_source": peaks["source"]},
-                       "l2": "state 805 MB > L2"},
+                       "l2": "state 805 MB > L2", "other_batches": dec_batches},
             "e2e": e2e,
             "cpu_baseline": cpu,
             "clocks": clocks,
