@@ -285,6 +285,7 @@ def main():
     ap.add_argument("--cpu-reps", type=int, default=12)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-decode-sweep", action="store_true")
+    ap.add_argument("--e2e-streams", type=int, default=1, help="upload streams of the e2e pipeline")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--prefill-tokens", type=int, default=T_TOTAL,
                     help="tokens of the prefill workload (a multiple of 512; smaller only for "
@@ -448,19 +449,23 @@ def main():
         # stream while bucket i-1 computes and bucket i-2's output comes down on a third;
         # every byte of every step's inputs and result crosses the host link inside the
         # timed region.  The whole step is captured once as a CUDA graph.
-        s_up, s_down = torch.cuda.Stream(), torch.cuda.Stream()
+        n_up = args.e2e_streams
+        s_ups = [torch.cuda.Stream() for _ in range(n_up)]
+        s_down = torch.cuda.Stream()
         nbk = T_TOTAL // BUCKET
         ev_in = [torch.cuda.Event() for _ in range(nbk)]
         ev_out = [torch.cuda.Event() for _ in range(nbk)]
 
         def e2e_body():
             comp = torch.cuda.current_stream()
-            s_up.wait_stream(comp)
+            for su in s_ups:
+                su.wait_stream(comp)
             s_down.wait_stream(comp)
             inp.state.zero_()
             inp.conv_state.zero_()
             for i in range(nbk):
                 sl = slice(i * BUCKET, (i + 1) * BUCKET)
+                s_up = s_ups[i % n_up]
                 with torch.cuda.stream(s_up):
                     inp.x[:, sl].copy_(hx[:, sl], non_blocking=True)
                     inp.a[:, sl].copy_(ha[:, sl], non_blocking=True)
@@ -478,7 +483,8 @@ def main():
                 with torch.cuda.stream(s_down):
                     s_down.wait_event(ev_out[i])
                     hout[:, sl].copy_(wl["out"][:, sl], non_blocking=True)
-            comp.wait_stream(s_up)
+            for su in s_ups:
+                comp.wait_stream(su)
             comp.wait_stream(s_down)
 
         e2e_body()                      # eager warm-up of the pipeline
@@ -508,7 +514,7 @@ def main():
         e2e = {"value": world * T_TOTAL * e2e_steps / (e2e_ms / 1e3), "unit": "tokens/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                "ms_per_step": e2e_ms / e2e_steps,
-               "pipeline": "per 512-token bucket: upload, compute and download on three streams"}
+               "pipeline": f"per 512-token bucket: uploads on {args.e2e_streams} streams, compute, download"}
 
     # ---------------- CPU oracle baseline (rank 0, bounded sample)
     cpu = None
