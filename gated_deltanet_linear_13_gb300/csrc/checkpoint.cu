@@ -28,18 +28,25 @@ __global__ void __launch_bounds__(256) gdn_checkpoint_kernel(
   }
   float4* s_live = state + (size_t)row * state_v4;
   float4* s_bank = slot_state + (size_t)slot * state_v4;
-  const float4* src = op == 0 ? s_live : s_bank;
-  float4* dst = op == 0 ? s_bank : s_live;
+  const float4* __restrict__ src = op == 0 ? s_live : s_bank;
+  float4* __restrict__ dst = op == 0 ? s_bank : s_live;
+  // one 16-byte element per thread and pass (the grid covers the state in one pass for the
+  // usual sizes), every load of a thread issued before its stores
   const long long stride = (long long)gridDim.x * blockDim.x;
-  for (long long e = (long long)blockIdx.x * blockDim.x + threadIdx.x; e < state_v4; e += stride)
-    dst[e] = src[e];
+  const long long e0 = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  for (long long e = e0; e < state_v4; e += 2 * stride) {
+    const float4 a = src[e];
+    const bool two = e + stride < state_v4;
+    const float4 b = two ? src[e + stride] : a;
+    dst[e] = a;
+    if (two) dst[e + stride] = b;
+  }
   if (conv_v4 > 0) {
     uint4* c_live = conv_state + (size_t)row * conv_v4;
     uint4* c_bank = slot_conv + (size_t)slot * conv_v4;
-    const uint4* csrc = op == 0 ? c_live : c_bank;
-    uint4* cdst = op == 0 ? c_bank : c_live;
-    for (long long e = (long long)blockIdx.x * blockDim.x + threadIdx.x; e < conv_v4; e += stride)
-      cdst[e] = csrc[e];
+    const uint4* __restrict__ csrc = op == 0 ? c_live : c_bank;
+    uint4* __restrict__ cdst = op == 0 ? c_bank : c_live;
+    for (long long e = e0; e < conv_v4; e += stride) cdst[e] = csrc[e];
   }
 }
 
@@ -51,8 +58,11 @@ cudaError_t gdn_launch_checkpoint(int op, int Hv, int d, int conv_elems, int con
   if (n == 0) return cudaSuccess;
   const long long state_v4 = (long long)Hv * d * d / 4;
   const long long conv_v4 = (long long)conv_elems * conv_elem_bytes / 16;
-  // ~8 KB per block: enough blocks per pair to keep HBM busy even for one pair
-  int bx = (int)((state_v4 * 16 + 8191) / 8192);
+  // one 16-byte element per thread: 4 KB per block (several pairs share the 65535-block limit
+  // of grid.x only when a state is above 256 MB)
+  long long bxl = (state_v4 + 255) / 256;
+  if (bxl > 65535) bxl = 65535;
+  int bx = (int)bxl;
   if (bx < 1) bx = 1;
   dim3 grid((unsigned)bx, (unsigned)n, 1);
   gdn_checkpoint_kernel<<<grid, 256, 0, stream>>>(op, state_v4, conv_v4, (float4*)state,

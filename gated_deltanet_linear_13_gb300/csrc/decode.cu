@@ -452,7 +452,7 @@ __global__ void __launch_bounds__(256) gdn_decode_cluster_kernel(GdnLayerArgs p,
   }
   cluster_wait_acquire();
   if (p.W > 1 && hh == 0 && sp == 0) conv_store_state<Tin>(p, slot, ch, win);
-  if (tid == 0) tma_store_wait_all();     // the bulk store has read shared memory and landed
+  if (tid == 0) tma_store_wait_read();    // the bulk store has read shared memory
 }
 
 template <typename Tin, typename Tout, int R>

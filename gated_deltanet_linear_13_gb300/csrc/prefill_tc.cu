@@ -844,7 +844,9 @@ __global__ void __launch_bounds__(CH_THREADS, 1)
         ok = false;
       }
     }
-    if (lane == 0) tma_store_wait_all();
+    // the output stores must have read this warp's staging block before the CTA exits (their
+    // writes complete with the grid)
+    if (lane == 0) tma_store_wait_read();
     if (!ok) *sAbort = 1;
   }
   if (tid == CH_EPI) {
