@@ -191,3 +191,92 @@ def test_prefill_of_one_token_equals_decode(gdn):
     assert_bf16_parity(o1.cpu(), o2.cpu())
     assert_state_parity(d1.state.cpu(), d2.state.cpu())
     assert torch.equal(d1.conv_state, d2.conv_state)
+
+
+def _streaming_batch(Hk):
+    """A batch with at least two (sequence, key head) items per SM, so that gdn_decode_step
+    takes its streaming kernel rather than the per-item cluster kernel."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    return (2 * sms + Hk - 1) // Hk + 1
+
+
+@pytest.mark.parametrize("dtype,conv,Hk,Hv", [("bf16", True, 4, 12), ("f32", True, 4, 8),
+                                                ("bf16", False, 2, 16), ("bf16", False, 8, 8)])
+def test_decode_streaming_kernel(gdn, dtype, conv, Hk, Hv):
+    """Batches large enough for the streaming decode kernel: bf16 / fp32, with and without the
+    conv, GQA 1:3 / 1:2 / 1:8 / 1:1; two steps, every unit against the oracle."""
+    B = _streaming_batch(Hk)
+    sh = gi.GDNShape(B, 1, Hk, Hv, conv_width=4 if conv else 0)
+    inp = gi.make_inputs(sh, seed=4100 + Hv + (7 if conv else 0), dtype=dtype, state="normal",
+                         state_std=0.2)
+    if conv:
+        inp.conv_state = torch.randn(inp.conv_state.shape,
+                                     generator=torch.Generator().manual_seed(41))
+        if dtype == "bf16":
+            inp.conv_state = inp.conv_state.to(torch.bfloat16)
+    ref1 = oracle_full(inp)
+    dev = to_device(inp)
+    odt = torch.bfloat16 if dtype == "bf16" else torch.float32
+    out = torch.empty(B, 1, Hv, 128, dtype=odt, device="cuda")
+    if conv:
+        gdn.gdn_decode_step(dev.x, None, None, dev.a, dev.b, dev.A_log, dev.dt_bias, dev.state,
+                            out, num_k_heads=Hk, conv_weight=dev.conv_weight,
+                            conv_state=dev.conv_state)
+    else:
+        gdn.gdn_decode_step(dev.q, dev.k, dev.v, dev.a, dev.b, dev.A_log, dev.dt_bias,
+                            dev.state, out)
+    assert gdn.gdn_get_device_error() == 0
+    if dtype == "bf16":
+        assert_bf16_parity(out.cpu(), ref1.out)
+        assert_state_parity(dev.state.cpu(), ref1.state)
+    else:
+        assert_f32_parity(out.cpu(), ref1.out)
+        assert_state_parity(dev.state.cpu(), ref1.state, fp32=True)
+    if conv:
+        np.testing.assert_array_equal(dev.conv_state.float().cpu().numpy(), ref1.conv_state)
+
+
+def test_decode_streaming_slots(gdn):
+    """Streaming-size batch addressed through state_slots: padded rows (-1) untouched, the
+    rest equal to the oracle, and an out-of-range slot reported."""
+    Hk, Hv = 4, 12
+    B = _streaming_batch(Hk)
+    sh = gi.GDNShape(B, 1, Hk, Hv, conv_width=4)
+    inp = gi.make_inputs(sh, seed=4200, dtype="bf16", state="normal", state_std=0.2)
+    ref = oracle_full(inp)
+    dev = to_device(inp)
+    nbank = B + 3
+    perm = torch.randperm(nbank, generator=torch.Generator().manual_seed(42))[:B]
+    slots = perm.clone().to(torch.int32)
+    slots[::7] = -1                                   # padded rows
+    bank = torch.zeros(nbank, Hv, 128, 128, device="cuda")
+    cbank = torch.zeros(nbank, 3, sh.conv_channels, dtype=torch.bfloat16, device="cuda")
+    for b in range(B):
+        if slots[b] >= 0:
+            bank[slots[b]] = dev.state[b]
+            cbank[slots[b]] = dev.conv_state[b]
+    before = bank.clone()
+    out = torch.zeros(B, 1, Hv, 128, dtype=torch.bfloat16, device="cuda")
+    gdn.gdn_decode_step(dev.x, None, None, dev.a, dev.b, dev.A_log, dev.dt_bias, bank, out,
+                        num_k_heads=Hk, conv_weight=dev.conv_weight, conv_state=cbank,
+                        state_slots=slots.cuda())
+    assert gdn.gdn_get_device_error() == 0
+    o = out.cpu()
+    for b in range(B):
+        s = int(slots[b])
+        if s < 0:
+            assert torch.count_nonzero(o[b]) == 0
+            continue
+        assert_bf16_parity(o[b], ref.out[b], what=f"out row {b}")
+        assert_state_parity(bank[s].cpu(), ref.state[b], what=f"state row {b}")
+        np.testing.assert_array_equal(cbank[s].float().cpu().numpy(), ref.conv_state[b])
+    used = set(int(s) for s in slots if s >= 0)
+    for s in range(nbank):
+        if s not in used:
+            assert torch.equal(bank[s], before[s])
+    bad = slots.clone()
+    bad[3] = nbank + 5
+    gdn.gdn_decode_step(dev.x, None, None, dev.a, dev.b, dev.A_log, dev.dt_bias, bank, out,
+                        num_k_heads=Hk, conv_weight=dev.conv_weight, conv_state=cbank,
+                        state_slots=bad.cuda())
+    assert gdn.gdn_get_device_error() == 6
