@@ -558,7 +558,8 @@ constexpr uint32_t CH_TMEM = 512;
 template <typename Tout>
 __global__ void __launch_bounds__(CH_THREADS, 1)
     gdn_chunk_chain_kernel(const __grid_constant__ CUtensorMap tm_v,
-                           const __grid_constant__ CUtensorMap tm_o, const TcParams p) {
+                           const __grid_constant__ CUtensorMap tm_o,
+                           const __grid_constant__ CUtensorMap tm_s, const TcParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
   const uint32_t sb = smem_addr(sm);
@@ -829,16 +830,28 @@ __global__ void __launch_bounds__(CH_THREADS, 1)
       if (__all_sync(0xffffffffu, mbar_wait_or_abort(bar_o, (p.ns - 1) & 1, sAbort))) {
         tc_fence_after();
         store_out(p.ns - 1);
-        // the leaving state: TMEM -> HBM (fp32)
-        float v[32];
+        // the leaving state: TMEM -> this warp's 32 rows x 64 columns, staged in the (now idle)
+        // first tile buffer as two 128-byte-swizzled 32 x 32 blocks -> two TMA tensor stores
+        // (whole rows per request instead of one 16-byte piece of 32 rows per instruction)
+        const uint32_t stg = sb + warp * 8 * KB;
 #pragma unroll
         for (int g = 0; g < 2; ++g) {
+          float v[32];
           tmem_ld32(tmem + lane_off + TM_S + 64 * hc + 32 * g, v);
           tmem_wait_ld();
 #pragma unroll
-          for (int q = 0; q < 8; ++q)
-            reinterpret_cast<float4*>(Sg + 32 * g)[q] =
-                make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+          for (int c = 0; c < 8; ++c)
+            st_shared_v4(sw128(stg + g * 4 * KB, lane, c), __float_as_uint(v[4 * c]),
+                         __float_as_uint(v[4 * c + 1]), __float_as_uint(v[4 * c + 2]),
+                         __float_as_uint(v[4 * c + 3]));
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          const int srow = ((slot * p.Hv + h) * D) + 32 * gw;
+#pragma unroll
+          for (int g = 0; g < 2; ++g) tma_store_3d(&tm_s, stg + g * 4 * KB, 64 * hc + 32 * g, srow, 0);
+          tma_store_commit();
         }
       } else {
         ok = false;
@@ -882,7 +895,7 @@ int slice_chunks(int B, int Hv, int nch) {
 
 template <typename Tout>
 cudaError_t launch_tc_t(const GdnLayerArgs& L, cudaStream_t stream) {
-  CUtensorMap mq, mk, mv, mo;
+  CUtensorMap mq, mk, mv, mo, ms;
   constexpr int out_rows = (int)(2 * KB / (32 * sizeof(Tout)));
   const bool ok =
       gdn_make_map(&mq, L.q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, L.Hk * D, L.T, L.B, L.q_tok_stride,
@@ -893,7 +906,10 @@ cudaError_t launch_tc_t(const GdnLayerArgs& L, cudaStream_t stream) {
                64, 64, true) &&
       gdn_make_map(&mo, L.out,
                sizeof(Tout) == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
-               (int)sizeof(Tout), L.Hv * D, L.T, L.B, (long long)L.Hv * D, 32, out_rows, false);
+               (int)sizeof(Tout), L.Hv * D, L.T, L.B, (long long)L.Hv * D, 32, out_rows, false) &&
+      // the state as rows of 128 fp32: box = 32 columns x 32 rows, 128-byte swizzle
+      gdn_make_map(&ms, L.state, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, D,
+                   L.num_slots * L.Hv * D, 1, D, 32, 32, true);
   if (!ok) return cudaErrorInvalidValue;
   static unsigned done_l = 0, done_c = 0, done_lc = 0;
   cudaError_t e = set_smem_once(gdn_chunk_local_kernel<__nv_bfloat16>, (int)L_SMEM, &done_l);
@@ -923,7 +939,7 @@ cudaError_t launch_tc_t(const GdnLayerArgs& L, cudaStream_t stream) {
                    mq, mk, p);
     if (e != cudaSuccess) return e;
     e = launch_pdl(true, gdn_chunk_chain_kernel<Tout>, dim3((unsigned)(L.B * L.Hv)), dim3(CH_THREADS),
-                   CH_SMEM, stream, mv, mo, p);
+                   CH_SMEM, stream, mv, mo, ms, p);
     if (e != cudaSuccess) return e;
   }
   return cudaSuccess;
