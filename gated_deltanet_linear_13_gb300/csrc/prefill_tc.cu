@@ -120,41 +120,28 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t
                : "memory");
 }
 
-// Byte offset of 16-byte chunk `c` of row `r` in a 128-byte-swizzled tile image (the layout a
-// 1024-byte aligned shared-memory copy of it has for the tensor cores).
-__device__ __forceinline__ uint32_t sw128_off(int r, int c) {
-  return (uint32_t)r * 128u + (uint32_t)((c ^ (r & 7)) << 4);
-}
-
-__device__ __forceinline__ void st_global_v4(uint8_t* p, uint32_t a, uint32_t b, uint32_t c,
-                                             uint32_t d) {
-  *reinterpret_cast<uint4*>(p) = make_uint4(a, b, c, d);
-}
-
-// 32 fp32 values (times mul) -> bf16 -> 4 swizzled 16-byte chunks c0..c0+3 of row r of a tile
-// image in global memory.
-__device__ __forceinline__ void store_row_bf16_g(uint8_t* tile, int r, int c0, const float* v,
-                                                 float mul) {
+// 32 fp32 values (times mul) -> bf16 -> 4 swizzled 16-byte chunks c0..c0+3 of row r.
+__device__ __forceinline__ void store_row_bf16(uint32_t tile, int r, int c0, const float* v,
+                                               float mul) {
 #pragma unroll
   for (int c = 0; c < 4; ++c) {
     const float* w = v + 8 * c;
-    st_global_v4(tile + sw128_off(r, c0 + c), pack_bf16(w[0] * mul, w[1] * mul),
+    st_shared_v4(sw128(tile, r, c0 + c), pack_bf16(w[0] * mul, w[1] * mul),
                  pack_bf16(w[2] * mul, w[3] * mul), pack_bf16(w[4] * mul, w[5] * mul),
                  pack_bf16(w[6] * mul, w[7] * mul));
   }
 }
 
-// 32 fp32 values -> bf16 hi and lo rows (chunks c0..c0+3 of row r) of two tile images in
-// global memory.
-__device__ __forceinline__ void store_row_hilo_g(uint8_t* tile_hi, uint8_t* tile_lo, int r,
-                                                 int c0, const float* v) {
+// 32 fp32 values -> bf16 hi and lo rows (chunks c0..c0+3 of row r) of two tiles.
+__device__ __forceinline__ void store_row_hilo(uint32_t tile_hi, uint32_t tile_lo, int r, int c0,
+                                               const float* v) {
 #pragma unroll
   for (int c = 0; c < 4; ++c) {
     uint32_t h[4], l[4];
 #pragma unroll
     for (int e = 0; e < 4; ++e) pack_hilo(v[8 * c + 2 * e], v[8 * c + 2 * e + 1], h[e], l[e]);
-    st_global_v4(tile_hi + sw128_off(r, c0 + c), h[0], h[1], h[2], h[3]);
-    st_global_v4(tile_lo + sw128_off(r, c0 + c), l[0], l[1], l[2], l[3]);
+    st_shared_v4(sw128(tile_hi, r, c0 + c), h[0], h[1], h[2], h[3]);
+    st_shared_v4(sw128(tile_lo, r, c0 + c), l[0], l[1], l[2], l[3]);
   }
 }
 
@@ -250,11 +237,34 @@ __device__ __forceinline__ void solve_unit_lower(const float* As, float* Ts, flo
   }
 }
 
+// Row scaling in place of the two 64-row blocks (kb = 0, 1; 16 KB apart) of a K or Q tile:
+// row r of both blocks times f0[r] * f1[r].  Thread lt: block lt >> 7, row (lt >> 1) & 63,
+// chunks 4 (lt & 1) .. + 3 visited in swizzled order (the lanes' rows hit different banks).
+__device__ __forceinline__ void scale_rows_in_place(uint8_t* tile, const float* f0,
+                                                    const float* f1, int lt) {
+  const int kb = lt >> 7, r = (lt >> 1) & 63, c0 = 4 * (lt & 1);
+  uint8_t* row = tile + kb * 16 * KB + r * 128;
+  const float f = f0[r] * f1[r];
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    const int pc = ((c0 + c) ^ r) & 7;
+    uint4 w4 = reinterpret_cast<const uint4*>(row)[pc];
+    __nv_bfloat162* hv = reinterpret_cast<__nv_bfloat162*>(&w4);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float2 x = __bfloat1622float2(hv[e]);
+      hv[e] = __floats2bfloat162_rn(x.x * f, x.y * f);
+    }
+    reinterpret_cast<uint4*>(row)[pc] = w4;
+  }
+}
+
 // ======================================================================= local kernel
 // One CTA per (chunk j of the slice, value head h, sequence b), 256 threads, three CTAs per
-// SM.  The tiles for the chain go from registers straight to the workspace (already in the
-// swizzled layout of their shared-memory copies there), so shared memory holds only K / Q,
-// the solve and small factors.
+// SM.  Each tile for the chain is staged, in the swizzled layout the chain's MMAs read, in
+// shared memory that is free at that point (P in the T region before the solve, Q~ in place,
+// T'' beside T', K~ in place and -W^T over Q~ once K is read no more) and leaves with bulk
+// copies of whole rows.
 constexpr uint32_t L_KQ = 0;            // [kb][K 64 rows | Q 64 rows][128 B]
 constexpr uint32_t L_SOLVE = 32 * KB;   // A | T fp32 [64][LA]; then T'h T'l
 constexpr uint32_t L_MISC = L_SOLVE + 2 * SOLVE_MAT;   // factors, solve scratch, barriers
@@ -421,7 +431,8 @@ __global__ void __launch_bounds__(LGT, 3)
         v[j] = keep ? ex2_approx(Gr - gs[j]) * v[j] * (sr * ns[j]) : 0.f;
       }
       if (isq) {
-        store_row_hilo_g(unit + U_P, unit + U_P + 8 * KB, r, 4 * half, v);
+        // P staged in the T region of the solve (not written before the solve starts)
+        store_row_hilo(sb + L_SOLVE + SOLVE_MAT, sb + L_SOLVE + SOLVE_MAT + 8 * KB, r, 4 * half, v);
       } else {
 #pragma unroll
         for (int j = 0; j < 32; j += 4)
@@ -429,28 +440,19 @@ __global__ void __launch_bounds__(LGT, 3)
               make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
       }
     }
-    // ---- Q~ = diag(scale e^G / ||q||) Q in place;  K~ = diag(e^{G_C-G} / ||k||) K -> KT.
-    //      Thread: one row of one 64-column block of K or Q (8 chunks, visited in swizzled
-    //      order so that the lanes' rows hit different banks).
-    {
-      const int blk = tid >> 6, r = tid & 63;            // blk: K kb0, K kb1, Q kb0, Q kb1
-      const bool isk = blk < 2;
-      const int kb = blk & 1;
-      const uint8_t* src = sm + L_KQ + kb * 16 * KB + (isk ? 0 : 8 * KB) + r * 128;
-      uint8_t* dst = unit + (isk ? U_KT : U_QT) + kb * 8 * KB + r * 128;
-      const float f = isk ? dK[r] * nk[r] : eG[r] * nq[r];
-#pragma unroll
-      for (int c = 0; c < 8; ++c) {
-        const int pc = (c ^ r) & 7;
-        uint4 w4 = reinterpret_cast<const uint4*>(src)[pc];
-        __nv_bfloat162* hv = reinterpret_cast<__nv_bfloat162*>(&w4);
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const float2 x = __bfloat1622float2(hv[e]);
-          hv[e] = __floats2bfloat162_rn(x.x * f, x.y * f);
-        }
-        reinterpret_cast<uint4*>(dst)[pc] = w4;
-      }
+    // ---- Q~ = diag(scale e^G / ||q||) Q in place (Q is not read again).  Thread: half a row
+    //      of one 64-column block (4 chunks, visited in swizzled order so that the lanes' rows
+    //      hit different banks).
+    scale_rows_in_place(sm + L_KQ + 8 * KB, eG, nq, tid);
+    fence_proxy_async_smem();
+    __syncthreads();
+    if (tid == 0) {                  // (bulk-copy groups are per thread: thread 0 waits on them)
+      bulk_store(unit + U_P, sb + L_SOLVE + SOLVE_MAT, 16 * KB);
+      tma_store_commit();
+      bulk_store(unit + U_QT, sb + L_KQ + 8 * KB, 8 * KB);
+      bulk_store(unit + U_QT + 8 * KB, sb + L_KQ + 24 * KB, 8 * KB);
+      tma_store_commit();
+      tma_store_wait_read_1();       // P has been read: the solve may write T over it
     }
     __syncthreads();
 
@@ -484,12 +486,16 @@ __global__ void __launch_bounds__(LGT, 3)
         }
         st_shared_v4(sw128(sb + L_SOLVE, r, c), h1[0], h1[1], h1[2], h1[3]);
         st_shared_v4(sw128(sb + L_SOLVE + 8 * KB, r, c), l1[0], l1[1], l1[2], l1[3]);
-        st_global_v4(unit + U_T2 + sw128_off(r, c), h2[0], h2[1], h2[2], h2[3]);
-        st_global_v4(unit + U_T2 + 8 * KB + sw128_off(r, c), l2[0], l2[1], l2[2], l2[3]);
+        st_shared_v4(sw128(sb + L_SOLVE + 16 * KB, r, c), h2[0], h2[1], h2[2], h2[3]);
+        st_shared_v4(sw128(sb + L_SOLVE + 24 * KB, r, c), l2[0], l2[1], l2[2], l2[3]);
       }
     }
     fence_proxy_async_smem();
     __syncthreads();
+    if (tid == 0) {
+      bulk_store(unit + U_T2, sb + L_SOLVE + 16 * KB, 16 * KB);
+      tma_store_commit();
+    }
     // ---- MMA 3: W^T = K^T T'^T (M = d_k, N = 64 tokens, K = 64 tokens)
     if (warp == 0 && elect_one()) {
       tc_fence_after();
@@ -505,18 +511,32 @@ __global__ void __launch_bounds__(LGT, 3)
     mma_phase ^= 1;
     pend_mma = false;
     tc_fence_after();
+    if (tid == 0) tma_store_wait_read_1();   // Q~ has been read out of the Q half
     if (__syncthreads_or(*sAbort)) break;
-    // ---- E3: W^T -> -W^T bf16 (MN-major: row = d_k index, 64 token columns)
+    // ---- K is read no more: K~ = diag(e^{G_C-G} / ||k||) K in place; E3: W^T -> -W^T bf16
+    //      (MN-major: row = d_k index, 64 token columns) into the Q half
+    scale_rows_in_place(sm + L_KQ, dK, nk, tid);
     {
       float v[32];
       tmem_ld32(TM_W + lane_off + 32 * half, v);
       tmem_wait_ld();
-      store_row_bf16_g(unit + U_NW, row, 4 * half, v, -1.0f);
+      store_row_bf16(sb + L_KQ + (row < 64 ? 8 * KB : 24 * KB), row & 63, 4 * half, v, -1.0f);
+    }
+    fence_proxy_async_smem();
+    __syncthreads();
+    if (tid == 0) {
+      bulk_store(unit + U_KT, sb + L_KQ, 8 * KB);
+      bulk_store(unit + U_KT + 8 * KB, sb + L_KQ + 16 * KB, 8 * KB);
+      bulk_store(unit + U_NW, sb + L_KQ + 8 * KB, 8 * KB);
+      bulk_store(unit + U_NW + 8 * KB, sb + L_KQ + 24 * KB, 8 * KB);
+      tma_store_commit();
     }
   } while (0);
 
-  // ---- teardown: (abort path only) pending MMAs, then TMEM is freed
+  // ---- teardown: the bulk copies out have read shared memory, (abort path only) pending
+  //      MMAs are done, then TMEM is freed
   if (tid == 0) {
+    tma_store_wait_read();
     if (pend_mma) mbar_wait_bounded(bar_mma, mma_phase, 1u << 16);
     if (*sAbort) atomicOr(&g_err_tc, kErrTimeout);
   }
