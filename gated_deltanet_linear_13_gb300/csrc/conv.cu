@@ -9,7 +9,8 @@
 // A CTA owns a tile of 64 tokens x 512 bytes of channels of one sequence: one TMA copy
 // brings the tile plus the W-1 rows before it into shared memory (rows before the sequence
 // start are then taken from the conv state), and each thread slides the window down 16
-// tokens of one 8-byte column.  The thread holding a sequence's first tokens of a column is
+// tokens of one 8-byte column (256 threads, three CTAs per SM, so that a 512-token call's
+// tiles run in one wave).  The thread holding a sequence's first tokens of a column is
 // the only one that reads the old state of its channels, and it also writes the new state
 // (taken from x, which nobody modifies), so no two threads race on it.
 #include "common.cuh"
@@ -28,7 +29,7 @@ unsigned gdn_take_error_conv() {
 }
 
 constexpr int TT = 64;             // tokens per CTA tile
-constexpr int TG = 8;              // tokens per thread (a CTA has TT / TG token groups)
+constexpr int TG = 16;             // tokens per thread (a CTA has TT / TG token groups)
 constexpr int TILE_BYTES = 512;    // bytes of one token row of the tile (256 bf16 / 128 fp32)
 constexpr int WORDS = TILE_BYTES / 8;                 // 8-byte words per row
 constexpr int CONV_THREADS = WORDS * (TT / TG);       // a thread: one word x TG tokens
@@ -65,7 +66,7 @@ __device__ __forceinline__ float silu_fast(float x) {
 }
 
 template <typename T, int W>
-__global__ void __launch_bounds__(CONV_THREADS, 2) gdn_conv_kernel(
+__global__ void __launch_bounds__(CONV_THREADS, 3) gdn_conv_kernel(
     const __grid_constant__ CUtensorMap tm_x, int B, int T_, int C, const T* x, long long xs,
     const T* w, const T* bias, T* cs, int num_slots, const int32_t* slots, int silu, T* y,
     long long ys) {
