@@ -285,6 +285,7 @@ def main():
     ap.add_argument("--cpu-reps", type=int, default=12)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-decode-sweep", action="store_true")
+    ap.add_argument("--no-prefill-4b", action="store_true")
     ap.add_argument("--e2e-streams", type=int, default=1, help="upload streams of the e2e pipeline")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--prefill-tokens", type=int, default=T_TOTAL,
@@ -370,6 +371,42 @@ def main():
     ms_per_step = prefill_ms / args.steps
     value = world * T_TOTAL * args.steps / (prefill_ms / 1e3)
     achieved_tflops = FLOP_PER_TOKEN * BUCKET / (call_ms / 1e3) / 1e12
+
+    # ---------------- the 4B-shape prefill (16 / 32 heads, B = 4, T = 4096, conv, half the heads
+    #                  strongly decayed) as one call: the same kernels with four sequences
+    other_prefill = []
+    if not args.no_prefill_4b:
+        sh4 = gi.GDNShape(4, 4096, 16, 32, conv_width=W)
+        in4 = gi.make_inputs_device(sh4, seed=4400, device=device, strong_decay_half=True)
+        out4 = torch.empty(4, 4096, 32, D, dtype=torch.bfloat16, device=device)
+
+        def call4():
+            gdn.gdn_chunk_prefill(in4.x, None, None, in4.a, in4.b, in4.A_log, in4.dt_bias,
+                                  in4.state, out4, num_k_heads=16, conv_weight=in4.conv_weight,
+                                  conv_state=in4.conv_state)
+        call4()
+        g4 = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g4):
+            call4()
+        for _ in range(3):
+            g4.replay()
+        q0 = torch.cuda.Event(enable_timing=True)
+        q1 = torch.cuda.Event(enable_timing=True)
+        q0.record()
+        for _ in range(5):
+            g4.replay()
+        q1.record()
+        torch.cuda.synchronize()
+        ms4 = q0.elapsed_time(q1) / 5
+        st = gdn.gdn_get_device_error()
+        if st != 0:
+            raise RuntimeError(f"device error in the 4B prefill: {gdn.gdn_status_string(st)}")
+        tok4 = 4 * 4096 / (ms4 / 1e3)
+        tf4 = tok4 * 32 * (6 * D * D + 10 * 64 * D) / 1e12
+        other_prefill.append({"workload": "qwen35_4b_gdn_prefill_B4_T4096", "tokens_per_s": tok4,
+                              "ms_per_call": ms4, "tflops": tf4,
+                              "frac_of_bf16_sustained": tf4 / peaks["bf16_sustained"]})
+        del g4, in4, out4
 
     # ---------------- decode (same run, HBM-resident state), 256 steps as one CUDA graph
     dwl = make_decode_workload(device)
@@ -550,6 +587,7 @@ def main():
                          "kernel": "gdn_chunk_prefill (conv + chunked recurrence), 512 tokens",
                          "flop_per_launch": FLOP_PER_TOKEN * BUCKET,
                          "launch_ms": call_ms, "peak_source": peaks["source"] + " sustained"},
+            "other_prefill": other_prefill,
             "decode": {"metric": "decode state-update HBM GB/s", "value": dec_gbs,
                        "unit": "GB/s", "batch": DECODE_B, "steps": DECODE_STEPS,
                        "step_ms_graph_mean": mean_ms, "step_ms_eager_median": eager_ms,
