@@ -69,7 +69,7 @@ constexpr uint32_t U_P = 32 * KB;     // P hi | P lo  [64 rows r][128 B = 64 s],
 constexpr uint32_t U_KT = 48 * KB;    // K~     [2 blocks of 64 d_k][64 rows s][128 B], MN-major B
 constexpr uint32_t U_T2 = 64 * KB;    // T'' hi | T'' lo [64 rows r][128 B = 64 s], K-major B
 constexpr uint32_t UNIT_BYTES = 80 * KB;
-constexpr size_t SLICE_BUDGET = (size_t)48 << 20;   // workspace bytes for one slice of units
+constexpr size_t SLICE_BUDGET = (size_t)96 << 20;   // workspace bytes for one slice of units
 
 constexpr uint32_t ID_G = idesc_bf16(128, 128, false, false);  // [K;Q] [K;Q]^T
 constexpr uint32_t ID_KT = idesc_bf16(128, 64, true, false);   // K^T T'^T, V^T T''^T
