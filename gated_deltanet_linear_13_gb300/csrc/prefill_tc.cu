@@ -23,7 +23,7 @@
 // head dimension: state row i lives in TMEM lane i for the whole sequence.
 //
 // Two kernels per slice of chunks:
-//   * gdn_chunk_local_kernel, one CTA per (chunk, value head, sequence), two CTAs per SM:
+//   * gdn_chunk_local_kernel, one CTA per (chunk, value head, sequence), three CTAs per SM:
 //     everything that does not depend on the state (gates, norms, G, A, P, the direct solve,
 //     T', T'', W, Q~, K~).  Its results for the chain are five 16 KB tiles per chunk, already
 //     in the swizzled layouts the chain's MMAs read, written with bulk copies to a workspace
@@ -32,7 +32,7 @@
 //     eight epilogue warps and one MMA / copy issuer warp.  Per chunk: U'^T (MMA), S0 =
 //     bf16(S) into TMEM, S <- e^{G_C} S, U^T += S0 (-W)^T, O^T = S0 Q~^T, U^T -> bf16 hi/lo in
 //     TMEM, S += U^T K~, O^T += U^T P^T; the next chunk's tiles stream in meanwhile and the
-//     previous chunk's output leaves through TMA stores.
+//     previous chunk's output leaves through TMA stores, as does the leaving state.
 // Both kernels are launched with programmatic dependent launch (set-up overlaps the tail of
 // the kernel before).  The fp32 state stays in TMEM for a whole slice.  Every mbarrier wait
 // is bounded: on timeout the CTA records GDN_ERR_DEVICE_TIMEOUT, waits (bounded) for its own

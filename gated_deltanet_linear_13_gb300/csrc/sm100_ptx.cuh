@@ -146,11 +146,6 @@ __device__ __forceinline__ void tma_store_wait_read_1() {
   asm volatile("cp.async.bulk.wait_group.read 1;\n" ::: "memory");
 }
 
-// Wait until every committed bulk store has completed (writes visible).
-__device__ __forceinline__ void tma_store_wait_all() {
-  asm volatile("cp.async.bulk.wait_group 0;\n" ::: "memory");
-}
-
 // ---------------------------------------------------------------- tcgen05: TMEM
 
 // One full warp: allocate `ncols` TMEM columns, base address written to smem at dst.
