@@ -19,6 +19,9 @@ __global__ void __launch_bounds__(256) gdn_checkpoint_kernel(
     int op, long long state_v4, long long conv_v4, float4* state, uint4* conv_state,
     int num_rows, float4* slot_state, uint4* slot_conv, int num_bank, const int32_t* rows,
     const int32_t* slots, int n) {
+  // launched with programmatic dependent launch: everything it reads may come from the
+  // kernel before it, which has completed once this wait returns
+  pdl_wait();
   const int i = blockIdx.y;
   const int row = rows[i], slot = slots[i];
   if (row < 0 || slot < 0) return;                       // masked pair
@@ -65,9 +68,7 @@ cudaError_t gdn_launch_checkpoint(int op, int Hv, int d, int conv_elems, int con
   int bx = (int)bxl;
   if (bx < 1) bx = 1;
   dim3 grid((unsigned)bx, (unsigned)n, 1);
-  gdn_checkpoint_kernel<<<grid, 256, 0, stream>>>(op, state_v4, conv_v4, (float4*)state,
-                                                  (uint4*)conv_state, num_rows,
-                                                  (float4*)slot_state, (uint4*)slot_conv_state,
-                                                  num_bank, rows, slots, n);
-  return cudaGetLastError();
+  return launch_pdl(true, gdn_checkpoint_kernel, grid, dim3(256), 0, stream, op, state_v4,
+                    conv_v4, (float4*)state, (uint4*)conv_state, num_rows,
+                    (float4*)slot_state, (uint4*)slot_conv_state, num_bank, rows, slots, n);
 }

@@ -847,13 +847,13 @@ __global__ void __launch_bounds__(CH_THREADS, 1)
       if (lane == 0) mbar_arrive(bar_c2);
     }
     if (ok && p.ns > 0) {
-      if (__all_sync(0xffffffffu, mbar_wait_or_abort(bar_o, (p.ns - 1) & 1, sAbort))) {
+      // the leaving state, as soon as the last S update is done (the last output update may
+      // still run): TMEM -> this warp's 32 rows x 64 columns, staged as two 128-byte-swizzled
+      // 32 x 32 blocks in the tile buffer the last chunk does not use (its readers are done)
+      // -> two TMA tensor stores (whole rows per request)
+      if (__all_sync(0xffffffffu, mbar_wait_or_abort(bar_s, (p.ns - 1) & 1, sAbort))) {
         tc_fence_after();
-        store_out(p.ns - 1);
-        // the leaving state: TMEM -> this warp's 32 rows x 64 columns, staged in the (now idle)
-        // first tile buffer as two 128-byte-swizzled 32 x 32 blocks -> two TMA tensor stores
-        // (whole rows per request instead of one 16-byte piece of 32 rows per instruction)
-        const uint32_t stg = sb + warp * 8 * KB;
+        const uint32_t stg = sb + ((((p.ns - 1) & 1) ^ 1) * CH_BUF) + warp * 8 * KB;
 #pragma unroll
         for (int g = 0; g < 2; ++g) {
           float v[32];
@@ -873,10 +873,19 @@ __global__ void __launch_bounds__(CH_THREADS, 1)
           for (int g = 0; g < 2; ++g) tma_store_3d(&tm_s, stg + g * 4 * KB, 64 * hc + 32 * g, srow, 0);
           tma_store_commit();
         }
+        // then the last output tile
+        if (__all_sync(0xffffffffu, mbar_wait_or_abort(bar_o, (p.ns - 1) & 1, sAbort))) {
+          tc_fence_after();
+          store_out(p.ns - 1);
+        } else {
+          ok = false;
+        }
       } else {
         ok = false;
       }
     }
+    // everything this kernel writes has been issued: a kernel after it may start its set-up
+    pdl_trigger();
     // the output stores must have read this warp's staging block before the CTA exits (their
     // writes complete with the grid)
     if (lane == 0) tma_store_wait_read();
