@@ -286,6 +286,8 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-decode-sweep", action="store_true")
     ap.add_argument("--no-prefill-4b", action="store_true")
+    ap.add_argument("--no-single-call", action="store_true",
+                    help="skip the one-call 27B prefill with in-kernel snapshots")
     ap.add_argument("--e2e-streams", type=int, default=1, help="upload streams of the e2e pipeline")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--prefill-tokens", type=int, default=T_TOTAL,
@@ -407,6 +409,46 @@ def main():
                               "ms_per_call": ms4, "tflops": tf4,
                               "frac_of_bf16_sustained": tf4 / peaks["bf16_sustained"]})
         del g4, in4, out4
+
+    # ---------------- the same 27B-shape long-context workload as ONE call that records the
+    #                  state every 512 tokens in-kernel (into the same 256-slot bank)
+    if not args.no_single_call:
+        inp = wl["inp"]
+        ws1 = torch.empty(gdn.gdn_prefill_workspace_size(1, T_TOTAL, HK, HV, W),
+                          dtype=torch.uint8, device=device)
+        snap_rows = wl["slots"].view(1, nbk)
+
+        def call1():
+            inp.state.zero_()
+            inp.conv_state.zero_()
+            gdn.gdn_chunk_prefill_snapshots(
+                inp.x, None, None, inp.a, inp.b, inp.A_log, inp.dt_bias, inp.state, wl["out"],
+                snap_every=BUCKET, snap_state=wl["bank"], snap_conv_state=wl["cbank"],
+                snap_slots=snap_rows, num_k_heads=HK, conv_weight=inp.conv_weight,
+                conv_state=inp.conv_state, workspace=ws1)
+        call1()
+        g1 = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g1):
+            call1()
+        for _ in range(2):
+            g1.replay()
+        q0 = torch.cuda.Event(enable_timing=True)
+        q1 = torch.cuda.Event(enable_timing=True)
+        q0.record()
+        for _ in range(3):
+            g1.replay()
+        q1.record()
+        torch.cuda.synchronize()
+        ms1 = q0.elapsed_time(q1) / 3
+        st = gdn.gdn_get_device_error()
+        if st != 0:
+            raise RuntimeError(f"device error in the single-call prefill: {gdn.gdn_status_string(st)}")
+        tok1 = T_TOTAL / (ms1 / 1e3)
+        tf1 = tok1 * FLOP_PER_TOKEN / 1e12
+        other_prefill.append({"workload": "qwen36_27b_prefill_T131072_one_call_snapshot_every512",
+                              "tokens_per_s": tok1, "ms_per_call": ms1, "tflops": tf1,
+                              "frac_of_bf16_sustained": tf1 / peaks["bf16_sustained"]})
+        del g1, ws1
 
     # ---------------- decode (same run, HBM-resident state), 256 steps as one CUDA graph
     dwl = make_decode_workload(device)

@@ -27,7 +27,8 @@ STATUS_NAMES = {0: "GDN_OK", 1: "GDN_ERR_INVALID_ARGUMENT", 2: "GDN_ERR_UNSUPPOR
 
 EXPORTED = ("gdn_prefill_workspace_size", "gdn_chunk_prefill", "gdn_decode_step",
             "causal_conv1d_update", "gdn_state_checkpoint", "gdn_chunk_prefill_noalloc",
-            "gdn_get_device_error", "gdn_status_string", "gdn_version")
+            "gdn_chunk_prefill_snapshots", "gdn_get_device_error", "gdn_status_string",
+            "gdn_version")
 NOALLOC_SCRATCH_BYTES = 64 << 20   # GDN_NOALLOC_SCRATCH_BYTES in include/gdn.h
 
 
@@ -69,6 +70,10 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     L.gdn_prefill_workspace_size.argtypes = [dp, op]
     L.gdn_chunk_prefill.restype = ctypes.c_int
     L.gdn_chunk_prefill.argtypes = [dp, op] + [_vp] * 14 + [ctypes.c_size_t, _vp]
+    L.gdn_chunk_prefill_snapshots.restype = ctypes.c_int
+    L.gdn_chunk_prefill_snapshots.argtypes = ([dp, op] + [_vp] * 13 +
+                                              [ctypes.c_int32, _vp, _vp, ctypes.c_int32, _vp,
+                                               _vp, ctypes.c_size_t, _vp])
     L.gdn_chunk_prefill_noalloc.restype = ctypes.c_int
     L.gdn_chunk_prefill_noalloc.argtypes = [dp, op] + [_vp] * 13 + [_vp]
     L.gdn_decode_step.restype = ctypes.c_int
@@ -218,6 +223,47 @@ def gdn_chunk_prefill(q, k, v, a, b, A_log, dt_bias, state, out, *, num_k_heads=
                              _ptr(conv_bias), _ptr(state), _ptr(conv_state), _ptr(state_slots),
                              _ptr(out), _ptr(workspace), ws_bytes, _stream(stream))
     _check(st, "gdn_chunk_prefill")
+    return out
+
+
+def gdn_chunk_prefill_snapshots(q, k, v, a, b, A_log, dt_bias, state, out, *, snap_every: int,
+                                snap_state, snap_slots, snap_conv_state=None, num_k_heads=None,
+                                conv_weight=None, conv_bias=None, conv_state=None,
+                                state_slots=None, scale: float = 1.0, eps: float = 1e-6,
+                                qk_l2norm: bool = True, conv_silu: bool = True,
+                                gates_precomputed: bool = False,
+                                workspace: Optional[torch.Tensor] = None,
+                                stream=None) -> torch.Tensor:
+    """gdn_chunk_prefill over the whole prompt in one call, recording the state after every
+    ``snap_every`` tokens (see gdn_chunk_prefill_snapshots in include/gdn.h): snapshot j of
+    row b goes to bank row ``snap_slots[b, j]`` of ``snap_state`` [n, Hv, 128, 128] (and of
+    ``snap_conv_state`` [n, W-1, C_conv] with a conv), j < T // snap_every.  Returns ``out``."""
+    L = load_library()
+    B, T, Hk, Hv, W, num_slots = _layer_dims(q, k, v, a, num_k_heads, conv_weight, conv_state,
+                                             state, state_slots, None)
+    _check_layer(q, k, v, a, b, A_log, dt_bias, conv_weight, conv_bias, state, conv_state,
+                 state_slots, out, B, T, Hk, Hv, W, num_slots, gates_precomputed)
+    dev = q.device
+    n_snap = T // snap_every if snap_every > 0 else 0
+    nb = snap_state.shape[0]
+    _need(snap_state, "snap_state", (nb, Hv, HEAD_DIM, HEAD_DIM), torch.float32, dev)
+    _need(snap_slots, "snap_slots", (B, n_snap), torch.int32, dev)
+    if W > 1:
+        _need(snap_conv_state, "snap_conv_state", (nb, W - 1, (2 * Hk + Hv) * HEAD_DIM),
+              q.dtype, dev)
+    dims = GdnDims(B, T, Hk, Hv, HEAD_DIM, 64, W, num_slots)
+    opts = _opts(_dt(q), _dt(out), qk_l2norm, eps, scale, conv_silu, gates_precomputed)
+    need = int(L.gdn_prefill_workspace_size(ctypes.byref(dims), ctypes.byref(opts)))
+    if need and workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    st = L.gdn_chunk_prefill_snapshots(
+        ctypes.byref(dims), ctypes.byref(opts), _ptr(q), _ptr(k), _ptr(v), _ptr(a), _ptr(b),
+        _ptr(A_log), _ptr(dt_bias), _ptr(conv_weight), _ptr(conv_bias), _ptr(state),
+        _ptr(conv_state), _ptr(state_slots), _ptr(out), int(snap_every), _ptr(snap_state),
+        _ptr(snap_conv_state), nb, _ptr(snap_slots), _ptr(workspace), ws_bytes,
+        _stream(stream))
+    _check(st, "gdn_chunk_prefill_snapshots")
     return out
 
 

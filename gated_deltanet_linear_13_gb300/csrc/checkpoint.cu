@@ -72,3 +72,48 @@ cudaError_t gdn_launch_checkpoint(int op, int Hv, int d, int conv_elems, int con
                     conv_v4, (float4*)state, (uint4*)conv_state, num_rows,
                     (float4*)slot_state, (uint4*)slot_conv_state, num_bank, rows, slots, n);
 }
+
+// Conv-state snapshots of a prefill that records its state every `every` tokens: the conv
+// state after token t is the W-1 pre-conv inputs t-W+2 .. t, which are rows of the call's own
+// input x (every >= 64 > W-1), so each snapshot is a copy of `rows` rows of x.  One CTA per
+// (sequence, snapshot); 16-byte elements.
+__global__ void __launch_bounds__(256) gdn_conv_snapshot_kernel(
+    const uint8_t* x, long long x_tok_bytes, long long x_seq_bytes, int row_v4, int rows,
+    int every, int n_snap, uint4* bank, int num_bank, const int32_t* slots,
+    const int32_t* row_slots) {
+  // launched behind the prefill's kernels with programmatic dependent launch (x is an input
+  // of the call and nothing else in the call touches the bank, so the wait only keeps the
+  // copy in the call's order)
+  pdl_wait();
+  const long long i = blockIdx.x;                // b * n_snap + j
+  const long long bb = i / n_snap, j = i % n_snap;
+  const int slot = slots[i];
+  if (slot < 0 || (row_slots && row_slots[bb] < 0)) return;   // masked pair, skipped row
+  if (slot >= num_bank) {
+    if (threadIdx.x == 0) atomicOr(&g_err_ckpt, kErrIndex);
+    return;
+  }
+  const long long t0 = (j + 1) * every - rows;   // first copied token
+  const uint8_t* src = x + bb * x_seq_bytes + t0 * x_tok_bytes;
+  uint4* dst = bank + (size_t)slot * rows * row_v4;
+  const int total = rows * row_v4;
+  for (int e = threadIdx.x; e < total; e += blockDim.x) {
+    const int r = e / row_v4, c = e % row_v4;
+    dst[e] = reinterpret_cast<const uint4*>(src + r * x_tok_bytes)[c];
+  }
+}
+
+cudaError_t gdn_launch_conv_snapshots(int B, int T, int row_bytes, long long x_tok_bytes,
+                                      int rows, const void* x, int every, int n_snap,
+                                      void* bank, int num_bank, const int32_t* slots,
+                                      const int32_t* row_slots, cudaStream_t stream) {
+  if (B == 0 || n_snap == 0 || rows <= 0) return cudaSuccess;
+  if (row_bytes % 16 != 0 || x_tok_bytes % 16 != 0) return cudaErrorInvalidValue;
+  const int row_v4 = row_bytes / 16;
+  const long long pairs = (long long)B * n_snap;
+  if (pairs > 0x7fffffffLL) return cudaErrorInvalidValue;
+  dim3 grid((unsigned)pairs, 1, 1);
+  return launch_pdl(true, gdn_conv_snapshot_kernel, grid, dim3(256), 0, stream,
+                    static_cast<const uint8_t*>(x), x_tok_bytes, x_tok_bytes * T, row_v4, rows,
+                    every, n_snap, static_cast<uint4*>(bank), num_bank, slots, row_slots);
+}

@@ -135,6 +135,11 @@ struct GdnLayerArgs {
   // workspace of the tensor-core prefill (chunk tiles between its two kernels)
   void* scratch;
   size_t scratch_bytes;
+  // in-call snapshots (prefill): the state after every snap_every tokens of the call goes to
+  // bank row snap_slots[b * n_snap + j]; snap_every == 0 records none
+  int snap_every, n_snap, num_snap_slots;
+  float* snap_state;
+  const int32_t* snap_slots;
 };
 
 // Workspace bytes the tensor-core prefill needs for B sequences of T tokens, Hv value heads.
@@ -153,6 +158,13 @@ cudaError_t gdn_launch_conv(int B, int T, int C, int W, int bf16, const void* x,
                             long long x_tok_stride, const void* w, const void* bias,
                             void* conv_state, int num_slots, const int32_t* slots, int silu,
                             void* y, long long y_tok_stride, cudaStream_t stream);
+// Conv-state snapshots of an in-call snapshot prefill: snapshot j of row b is the W-1
+// pre-conv rows of x ending at token (j + 1) * every, copied to bank row slots[b * n_snap + j]
+// (nothing for a row whose row_slots entry is negative; row_slots may be NULL).
+cudaError_t gdn_launch_conv_snapshots(int B, int T, int row_bytes, long long x_tok_bytes,
+                                      int rows, const void* x, int every, int n_snap,
+                                      void* bank, int num_bank, const int32_t* slots,
+                                      const int32_t* row_slots, cudaStream_t stream);
 cudaError_t gdn_launch_checkpoint(int op, int Hv, int d, int conv_elems, int conv_elem_bytes,
                                   float* state, void* conv_state, int num_rows,
                                   float* slot_state, void* slot_conv_state, int num_bank,

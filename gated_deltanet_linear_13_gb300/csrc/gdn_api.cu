@@ -7,7 +7,7 @@
 
 namespace {
 
-constexpr int32_t kVersion = 100;
+constexpr int32_t kVersion = 101;
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
@@ -134,20 +134,38 @@ size_t gdn_prefill_workspace_size(const gdn_dims* dims, const gdn_opts* opts) {
   return workspace_bytes_for(c, opts);
 }
 
-gdn_status gdn_chunk_prefill(const gdn_dims* dims, const gdn_opts* opts, const void* q,
-                             const void* k, const void* v, const void* a, const void* b,
-                             const float* A_log, const float* dt_bias, const void* conv_weight,
-                             const void* conv_bias, float* state, void* conv_state,
-                             const int32_t* state_slots, void* out, void* workspace,
-                             size_t workspace_bytes, void* stream) {
+// gdn_chunk_prefill, with in-call snapshots when snap_every > 0
+static gdn_status prefill_impl(const gdn_dims* dims, const gdn_opts* opts, const void* q,
+                               const void* k, const void* v, const void* a, const void* b,
+                               const float* A_log, const float* dt_bias,
+                               const void* conv_weight, const void* conv_bias, float* state,
+                               void* conv_state, const int32_t* state_slots, void* out,
+                               int32_t snap_every, float* snap_state, void* snap_conv_state,
+                               int32_t num_snap_slots, const int32_t* snap_slots,
+                               void* workspace, size_t workspace_bytes, void* stream) {
   Checked c;
   gdn_status st = check_dims(dims, opts, false, &c);
   if (st != GDN_OK) return st;
+  if (snap_every < 0 || snap_every % gdn::kChunk != 0) return GDN_ERR_INVALID_ARGUMENT;
   if (c.B == 0 || c.T == 0) return GDN_OK;
   GdnLayerArgs L;
   st = check_layer_ptrs(c, opts, q, k, v, a, b, A_log, dt_bias, conv_weight, conv_bias, state,
                         conv_state, state_slots, out, &L);
   if (st != GDN_OK) return st;
+  const int n_snap = snap_every > 0 ? c.T / snap_every : 0;
+  if (n_snap > 0) {
+    if (num_snap_slots <= 0 || !snap_state || !aligned16(snap_state) || !snap_slots ||
+        !aligned4(snap_slots))
+      return GDN_ERR_INVALID_ARGUMENT;
+    if (c.W > 1 && (!snap_conv_state || !aligned16(snap_conv_state)))
+      return GDN_ERR_INVALID_ARGUMENT;
+    if ((long long)c.B * n_snap > 0x7fffffffLL) return GDN_ERR_INVALID_ARGUMENT;
+    L.snap_every = snap_every;
+    L.n_snap = n_snap;
+    L.num_snap_slots = num_snap_slots;
+    L.snap_state = snap_state;
+    L.snap_slots = snap_slots;
+  }
   const size_t need = workspace_bytes_for(c, opts);
   if (need > 0 && (!workspace || workspace_bytes < need || !aligned16(workspace)))
     return GDN_ERR_WORKSPACE;
@@ -168,7 +186,42 @@ gdn_status gdn_chunk_prefill(const gdn_dims* dims, const gdn_opts* opts, const v
     L.q_tok_stride = L.k_tok_stride = L.v_tok_stride = c.Cc;
   }
   cudaError_t e = L.in_bf16 ? gdn_launch_prefill_tc(L, s) : gdn_launch_prefill_simt(L, s);
-  return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+  if (e != cudaSuccess) return GDN_ERR_CUDA;
+  if (n_snap > 0 && c.W > 1) {
+    // the conv state at each boundary: W-1 rows of the call's pre-conv input
+    e = gdn_launch_conv_snapshots(c.B, c.T, c.Cc * c.in_elem, (long long)c.Cc * c.in_elem,
+                                  c.W - 1, q, snap_every, n_snap, snap_conv_state,
+                                  num_snap_slots, snap_slots, state_slots, s);
+    if (e != cudaSuccess) return GDN_ERR_CUDA;
+  }
+  return GDN_OK;
+}
+
+gdn_status gdn_chunk_prefill(const gdn_dims* dims, const gdn_opts* opts, const void* q,
+                             const void* k, const void* v, const void* a, const void* b,
+                             const float* A_log, const float* dt_bias, const void* conv_weight,
+                             const void* conv_bias, float* state, void* conv_state,
+                             const int32_t* state_slots, void* out, void* workspace,
+                             size_t workspace_bytes, void* stream) {
+  return prefill_impl(dims, opts, q, k, v, a, b, A_log, dt_bias, conv_weight, conv_bias, state,
+                      conv_state, state_slots, out, 0, nullptr, nullptr, 0, nullptr, workspace,
+                      workspace_bytes, stream);
+}
+
+gdn_status gdn_chunk_prefill_snapshots(const gdn_dims* dims, const gdn_opts* opts, const void* q,
+                                       const void* k, const void* v, const void* a,
+                                       const void* b, const float* A_log, const float* dt_bias,
+                                       const void* conv_weight, const void* conv_bias,
+                                       float* state, void* conv_state,
+                                       const int32_t* state_slots, void* out,
+                                       int32_t snap_every, float* snap_state,
+                                       void* snap_conv_state, int32_t num_snap_slots,
+                                       const int32_t* snap_slots, void* workspace,
+                                       size_t workspace_bytes, void* stream) {
+  if (snap_every <= 0) return GDN_ERR_INVALID_ARGUMENT;
+  return prefill_impl(dims, opts, q, k, v, a, b, A_log, dt_bias, conv_weight, conv_bias, state,
+                      conv_state, state_slots, out, snap_every, snap_state, snap_conv_state,
+                      num_snap_slots, snap_slots, workspace, workspace_bytes, stream);
 }
 
 gdn_status gdn_decode_step(const gdn_dims* dims, const gdn_opts* opts, const void* q,

@@ -75,8 +75,21 @@ __global__ void __launch_bounds__(THREADS) gdn_prefill_simt_kernel(GdnLayerArgs 
 
   for (int idx = tid; idx < R * D; idx += THREADS) Ss[(idx / D) * LD + idx % D] = Sg[idx];
 
+  // in-call snapshot j (the state after token (j + 1) snap_every) of this block's rows
+  auto snapshot = [&](int j) {
+    const int sl = p.snap_slots[(size_t)b * p.n_snap + j];
+    if (sl < 0) return;
+    if (sl >= p.num_snap_slots) {
+      if (tid == 0) atomicOr(&g_err_simt, kErrIndex);
+      return;
+    }
+    float* dst = p.snap_state + (((size_t)sl * p.Hv + h) * D + r0) * D;
+    for (int idx = tid; idx < R * D; idx += THREADS) dst[idx] = Ss[(idx / D) * LD + idx % D];
+  };
+
   for (int t0 = 0; t0 < p.T; t0 += C) {
     const int n = min(C, p.T - t0);
+    if (p.snap_every > 0 && t0 > 0 && t0 % p.snap_every == 0) snapshot(t0 / p.snap_every - 1);
     // ---- load the chunk (zero padded)
     for (int idx = tid; idx < C * D; idx += THREADS) {
       const int rr = idx / D, j = idx % D;
@@ -235,6 +248,7 @@ __global__ void __launch_bounds__(THREADS) gdn_prefill_simt_kernel(GdnLayerArgs 
     __syncthreads();
   }
   for (int idx = tid; idx < R * D; idx += THREADS) Sg[idx] = Ss[(idx / D) * LD + idx % D];
+  if (p.snap_every > 0 && p.T % p.snap_every == 0) snapshot(p.T / p.snap_every - 1);
 }
 
 template <typename Tin, typename Tout>

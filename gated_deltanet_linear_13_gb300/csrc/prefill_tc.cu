@@ -91,6 +91,10 @@ struct TcParams {
   const int32_t* slots;
   uint8_t* units;         // workspace: ns * B * Hv units of UNIT_BYTES
   float* egc;             // workspace: e^{G_C} per unit
+  // in-call snapshots: the state entering chunk n (n > 0, n a multiple of se_c, n C <= T) goes
+  // to bank row snap_slots[b * n_snap + n / se_c - 1]; se_c == 0: none
+  int se_c, n_snap, n_snap_slots;
+  const int32_t* snap_slots;
 };
 
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
@@ -579,7 +583,8 @@ template <typename Tout>
 __global__ void __launch_bounds__(CH_THREADS, 1)
     gdn_chunk_chain_kernel(const __grid_constant__ CUtensorMap tm_v,
                            const __grid_constant__ CUtensorMap tm_o,
-                           const __grid_constant__ CUtensorMap tm_s, const TcParams p) {
+                           const __grid_constant__ CUtensorMap tm_s,
+                           const __grid_constant__ CUtensorMap tm_snap, const TcParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
   const uint32_t sb = smem_addr(sm);
@@ -783,6 +788,16 @@ __global__ void __launch_bounds__(CH_THREADS, 1)
         }
       }
     };
+    // in-call snapshots: bank rows of the next boundary inside this slice (loaded a step or
+    // more ahead of its use) and of the boundary at the slice end, -1 for none
+    const int32_t* snap_row = p.se_c > 0 ? p.snap_slots + (size_t)b * p.n_snap - 1 : nullptr;
+    int snap_nb = p.se_c > 0 ? (p.n0 / p.se_c + 1) * p.se_c : 0x7fffffff;   // chunk index
+    int snap_next = snap_nb < p.n0 + p.ns ? snap_row[snap_nb / p.se_c] : -1;
+    const int n_end = p.n0 + p.ns;
+    const int snap_end =
+        (p.se_c > 0 && n_end % p.se_c == 0 && n_end * C <= p.T) ? snap_row[n_end / p.se_c] : -1;
+    if (tid == 0 && (snap_next >= p.n_snap_slots || snap_end >= p.n_snap_slots))
+      atomicOr(&g_err_tc, kErrIndex);
     bool ok = true;
     for (int nl = 0; nl < p.ns && ok; ++nl) {
       // ---- C0: S -> S0 (bf16, packed into TMEM as the A operand);  S <- e^{G_C} S
@@ -799,6 +814,37 @@ __global__ void __launch_bounds__(CH_THREADS, 1)
         tmem_ld32(ta, *reinterpret_cast<float(*)[32]>(&v[0]));
         tmem_ld32(ta + 32, *reinterpret_cast<float(*)[32]>(&v[32]));
         tmem_wait_ld();
+        // a snapshot boundary: this warp's 32 rows x 64 columns of the entering state, staged
+        // as two 128-byte-swizzled 32 x 32 blocks in the other tile buffer outside its P
+        // (every other tile of it was read by MMAs that S's completion covers; the next copy
+        // into it waits for C0) -> two TMA stores, whose reads end before C0 is signalled
+        const bool snap_here = p.n0 + nl == snap_nb;
+        if (snap_here) {
+          if (snap_next >= 0 && snap_next < p.n_snap_slots) {
+            const uint32_t stg = sb + (((nl & 1) ^ 1) * CH_BUF) +
+                                 (warp < 4 ? warp * 8 * KB : U_KT + (warp - 4) * 8 * KB);
+#pragma unroll
+            for (int g = 0; g < 2; ++g)
+#pragma unroll
+              for (int c = 0; c < 8; ++c)
+                st_shared_v4(sw128(stg + g * 4 * KB, lane, c), __float_as_uint(v[32 * g + 4 * c]),
+                             __float_as_uint(v[32 * g + 4 * c + 1]),
+                             __float_as_uint(v[32 * g + 4 * c + 2]),
+                             __float_as_uint(v[32 * g + 4 * c + 3]));
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              const int srow = ((snap_next * p.Hv + h) * D) + 32 * gw;
+#pragma unroll
+              for (int g = 0; g < 2; ++g)
+                tma_store_3d(&tm_snap, stg + g * 4 * KB, 64 * hc + 32 * g, srow, 0);
+              tma_store_commit();
+            }
+          }
+          snap_nb += p.se_c;
+          snap_next = snap_nb < n_end ? snap_row[snap_nb / p.se_c] : -1;
+          if (tid == 0 && snap_next >= p.n_snap_slots) atomicOr(&g_err_tc, kErrIndex);
+        }
 #pragma unroll
         for (int g = 0; g < 2; ++g) {
           uint32_t pk[16];
@@ -812,6 +858,7 @@ __global__ void __launch_bounds__(CH_THREADS, 1)
         tmem_st32(ta, *reinterpret_cast<float(*)[32]>(&v[0]));
         tmem_st32(ta + 32, *reinterpret_cast<float(*)[32]>(&v[32]));
         tmem_wait_st();
+        if (snap_here && lane == 0) tma_store_wait_read();
       }
       tc_fence_before();
       __syncwarp();
@@ -871,6 +918,13 @@ __global__ void __launch_bounds__(CH_THREADS, 1)
           const int srow = ((slot * p.Hv + h) * D) + 32 * gw;
 #pragma unroll
           for (int g = 0; g < 2; ++g) tma_store_3d(&tm_s, stg + g * 4 * KB, 64 * hc + 32 * g, srow, 0);
+          // the slice ends on a snapshot boundary: the same rows to the bank
+          if (snap_end >= 0 && snap_end < p.n_snap_slots) {
+            const int brow = ((snap_end * p.Hv + h) * D) + 32 * gw;
+#pragma unroll
+            for (int g = 0; g < 2; ++g)
+              tma_store_3d(&tm_snap, stg + g * 4 * KB, 64 * hc + 32 * g, brow, 0);
+          }
           tma_store_commit();
         }
         // then the last output tile
@@ -940,6 +994,15 @@ cudaError_t launch_tc_t(const GdnLayerArgs& L, cudaStream_t stream) {
       gdn_make_map(&ms, L.state, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, D,
                    L.num_slots * L.Hv * D, 1, D, 32, 32, true);
   if (!ok) return cudaErrorInvalidValue;
+  // the snapshot bank, the same way (the state map stands in when nothing is recorded)
+  CUtensorMap msn = ms;
+  const bool snaps = L.snap_every > 0 && L.n_snap > 0;
+  if (snaps) {
+    if ((long long)L.num_snap_slots * L.Hv * D > 0x7fffffffLL ||
+        !gdn_make_map(&msn, L.snap_state, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, D,
+                      L.num_snap_slots * L.Hv * D, 1, D, 32, 32, true))
+      return cudaErrorInvalidValue;
+  }
   static unsigned done_l = 0, done_c = 0, done_lc = 0;
   cudaError_t e = set_smem_once(gdn_chunk_local_kernel<__nv_bfloat16>, (int)L_SMEM, &done_l);
   if (e != cudaSuccess) return e;
@@ -958,6 +1021,10 @@ cudaError_t launch_tc_t(const GdnLayerArgs& L, cudaStream_t stream) {
   p.A_log = L.A_log; p.dt_bias = L.dt_bias; p.state = L.state; p.slots = L.slots;
   p.units = static_cast<uint8_t*>(L.scratch);
   p.egc = reinterpret_cast<float*>(p.units + units * UNIT_BYTES);
+  p.se_c = snaps ? L.snap_every / C : 0;
+  p.n_snap = snaps ? L.n_snap : 0;
+  p.n_snap_slots = snaps ? L.num_snap_slots : 0;
+  p.snap_slots = snaps ? L.snap_slots : nullptr;
   for (int n0 = 0; n0 < nch; n0 += ns_max) {
     p.n0 = n0;
     p.ns = nch - n0 < ns_max ? nch - n0 : ns_max;
@@ -968,7 +1035,7 @@ cudaError_t launch_tc_t(const GdnLayerArgs& L, cudaStream_t stream) {
                    mq, mk, p);
     if (e != cudaSuccess) return e;
     e = launch_pdl(true, gdn_chunk_chain_kernel<Tout>, dim3((unsigned)(L.B * L.Hv)), dim3(CH_THREADS),
-                   CH_SMEM, stream, mv, mo, ms, p);
+                   CH_SMEM, stream, mv, mo, ms, msn, p);
     if (e != cudaSuccess) return e;
   }
   return cudaSuccess;

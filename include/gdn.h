@@ -188,6 +188,44 @@ gdn_status gdn_state_checkpoint(int32_t op, const gdn_dims* dims, gdn_dtype conv
                                 void* stream);
 
 /*
+ * gdn_chunk_prefill_snapshots -- gdn_chunk_prefill over a whole prompt in one call that also
+ * records the recurrent and conv state every `snap_every` tokens, in-kernel.
+ * Definition: the prefix checkpoints of hybrid automatic prefix caching (PR #164 "Hybrid APC
+ * Runtime": the state at fixed token boundaries is kept in checkpoint slots so that a later
+ * request sharing the prefix resumes from it).  Snapshot j of row b (j = 0 .. n_snap-1,
+ * n_snap = T / snap_every rounded down) is the state after token (j + 1) * snap_every of this
+ * call: exactly what gdn_state_checkpoint(SAVE) would copy after gdn_chunk_prefill calls
+ * over tokens [0, (j + 1) * snap_every) in buckets of snap_every tokens, bit for bit (the
+ * chunk grid starts at the call start, so chunk boundaries and results are the same).
+ *   all arguments but the ones below: as gdn_chunk_prefill, with the same workspace size
+ *                (gdn_prefill_workspace_size); the live state and conv state end as after
+ *                gdn_chunk_prefill.
+ *   snap_every       tokens between snapshots: a positive multiple of the chunk (64), else
+ *                    GDN_ERR_INVALID_ARGUMENT.
+ *   snap_state       [num_snap_slots, Hv, d, d] fp32 bank, the layout of `state`.
+ *   snap_conv_state  [num_snap_slots, W-1, C_conv] in in_dtype, the layout of `conv_state`
+ *                    (the W-1 pre-conv inputs ending at the boundary, oldest first); ignored
+ *                    (may be NULL) when conv_width <= 1.
+ *   num_snap_slots   rows of the banks.
+ *   snap_slots       [B, n_snap] device int32: the bank row receiving snapshot j of row b; a
+ *                    negative entry records nothing; an entry >= num_snap_slots records
+ *                    nothing and sets GDN_ERR_DEVICE_INDEX.  Rows that state_slots skips
+ *                    record nothing.  No two entries may name the same bank row.
+ * The banks are written only at the recorded rows.  With n_snap == 0 (T < snap_every) this
+ * is gdn_chunk_prefill and the snapshot pointers are not read.
+ */
+gdn_status gdn_chunk_prefill_snapshots(const gdn_dims* dims, const gdn_opts* opts, const void* q,
+                                       const void* k, const void* v, const void* a,
+                                       const void* b, const float* A_log, const float* dt_bias,
+                                       const void* conv_weight, const void* conv_bias,
+                                       float* state, void* conv_state,
+                                       const int32_t* state_slots, void* out,
+                                       int32_t snap_every, float* snap_state,
+                                       void* snap_conv_state, int32_t num_snap_slots,
+                                       const int32_t* snap_slots, void* workspace,
+                                       size_t workspace_bytes, void* stream);
+
+/*
  * gdn_chunk_prefill_noalloc -- gdn_chunk_prefill for callers that cannot allocate device
  * memory.  The pages have no counterpart of this call; it is a convenience of this library.
  *

@@ -39,7 +39,7 @@ def test_status_strings_and_version(L):
     for code, name in gdn.STATUS_NAMES.items():
         assert gdn.gdn_status_string(code) == name
     assert gdn.gdn_status_string(99) == "GDN_UNKNOWN_STATUS"
-    assert L.gdn_version() == 100
+    assert L.gdn_version() == 101
 
 
 def _dims(**kw):
@@ -63,6 +63,33 @@ def _prefill(L, dims, opts, q=A, k=A, v=A, a=A, b=A, A_log=A, state=A, out=A, ws
              conv_w=None, conv_state=None):
     return L.gdn_chunk_prefill(ctypes.byref(dims), ctypes.byref(opts), q, k, v, a, b, A_log,
                                None, conv_w, None, state, conv_state, None, out, ws, wsb, None)
+
+
+def _snap(L, dims, opts, every, snap_state=A, snap_conv=None, nbank=4, snap_slots=A,
+          conv_w=None, conv_state=None, q=A, k=A, v=A):
+    return L.gdn_chunk_prefill_snapshots(ctypes.byref(dims), ctypes.byref(opts), q, k, v, A, A,
+                                         A, None, conv_w, None, A, conv_state, None, A, every,
+                                         snap_state, snap_conv, nbank, snap_slots, None, 0, None)
+
+
+def test_snapshot_prefill_rejects_bad_arguments(L):
+    d = _dims(seqlen=256)
+    # the boundary spacing: positive and a whole number of 64-token chunks
+    for every in (0, -64, 100, 32):
+        assert _snap(L, d, _opts(), every) == 1
+    # with at least one boundary inside T: bank, slot table and bank size are required
+    assert _snap(L, d, _opts(), 128, snap_state=None) == 1
+    assert _snap(L, d, _opts(), 128, snap_state=A + 4) == 1          # misaligned
+    assert _snap(L, d, _opts(), 128, snap_slots=None) == 1
+    assert _snap(L, d, _opts(), 128, nbank=0) == 1
+    # with a conv: the conv-state bank too (x arrives in q, k = v = NULL)
+    dc = _dims(seqlen=256, conv_width=4)
+    assert _snap(L, dc, _opts(), 128, conv_w=A, conv_state=A, k=None, v=None,
+                 snap_conv=None) == 1
+    # bad dims are still caught first
+    assert _snap(L, _dims(seqlen=256, head_dim=64), _opts(), 128) == 2
+    # an empty batch is a no-op
+    assert _snap(L, _dims(batch=0, seqlen=256), _opts(), 128) == 0
 
 
 @pytest.mark.parametrize("field,value,status", [
