@@ -554,26 +554,30 @@ __global__ void __launch_bounds__(LGT, 3)
 
 // ======================================================================= chain kernel
 // One CTA per (value head h, sequence b): eight epilogue warps (warp w: TMEM lane quarter
-// w % 4, column half w / 4) and one issuer warp, one elected lane of which issues every copy
-// and MMA, so that no epilogue thread ever stalls behind the tensor-core queue.  The two
-// sides meet only at mbarriers.  Per chunk: the five tiles of the local kernel plus V, double-buffered.
+// w % 4, column half w / 4), one issuer warp, one elected lane of which issues every copy
+// and MMA, so that no epilogue thread ever stalls behind the tensor-core queue, and four
+// store warps for the output.  They meet only at mbarriers.  Per chunk: the five tiles of the
+// local kernel plus V, double-buffered.
 //
 // The chain S -> S0 -> U -> S is the critical path; per chunk it runs
 //   C0 (S0 = bf16(S), S *= e^{G_C})  ->  U^T += S0 (-W)^T  ->  C2 (U^T -> bf16 hi / lo)
 //   ->  S += U^T K~
 // with one commit barrier after each of its two MMA groups.  The output MMAs (O^T = S0 Q~^T,
 // O^T += U^T P^T) and the state-independent U'^T = V^T T''^T of the next chunk are issued
-// behind them and run while the epilogue warps work on the next step; the finished output
-// tile of a chunk is transposed through shared memory (each warp its own 32 x 32 block)
-// and leaves with TMA stores while the next chunk's MMAs run.  A buffer's
-// tiles other than P are free once S of its chunk is final; P once the output MMAs are done.
+// behind them and run while the epilogue warps work on the next step.  The finished output
+// tile of a chunk (double-buffered in TMEM) is read by the store warps, which transpose it
+// through shared memory (each warp its 32 d_v rows) and send it with TMA stores, off the
+// epilogue's path.  A buffer's tiles other than P are free once S of its chunk is final; P
+// once the output MMAs are done.
 constexpr uint32_t CH_BUF = 96 * KB;            // unit tiles (80 KB) + V [2][64][128 B] (16 KB)
 constexpr uint32_t CH_V = 80 * KB;
-constexpr uint32_t CH_OUT = 2 * CH_BUF;         // output staging, 2 KB per epilogue warp
+constexpr uint32_t CH_OUT = 2 * CH_BUF;         // output staging, 4 KB per store warp
 constexpr uint32_t CH_MISC = CH_OUT + 16 * KB;  // e^{G_C} of the slice (2 KB), barriers
 constexpr uint32_t CH_SMEM = CH_MISC + 3 * KB + KB;
 constexpr int CH_EPI = 256;                     // epilogue threads
-constexpr int CH_THREADS = CH_EPI + 32;         // + the issuer warp
+constexpr int CH_ISSUER = CH_EPI / 32;          // the issuer warp
+constexpr int CH_STORE = CH_ISSUER + 1;         // first of the four store warps
+constexpr int CH_THREADS = CH_EPI + 32 + 128;
 constexpr int MAX_SLICE = 512;
 // TMEM columns: S fp32 | U^T fp32 | O^T fp32 x 2 | S0 bf16 packed | U^T bf16 hi | lo
 constexpr uint32_t TM_S = 0, TM_U = 128, TM_O = 192, TM_S0 = 320, TM_UH = 384, TM_UL = 416;
@@ -603,14 +607,16 @@ __global__ void __launch_bounds__(CH_THREADS, 1)
   const uint32_t bar_ld0 = smem_addr(&barmem[0]), bar_ld1 = smem_addr(&barmem[1]);
   const uint32_t bar_u = smem_addr(&barmem[2]);     // MMA: U^T += S0 (-W)^T done (and all before)
   const uint32_t bar_s = smem_addr(&barmem[3]);     // MMA: S += U^T K~ done (and all before)
-  const uint32_t bar_o = smem_addr(&barmem[4]);     // MMA: output MMAs done (and all before)
+  // MMA: output MMAs of a chunk done (and all before), one barrier per TMEM output buffer
+  const uint32_t bar_o0 = smem_addr(&barmem[4]), bar_o1 = smem_addr(&barmem[10]);
   const uint32_t bar_fin = smem_addr(&barmem[5]);   // MMA: teardown, everything issued done
   const uint32_t bar_c0 = smem_addr(&barmem[6]);    // epilogue: S0 packed, S rescaled
-  const uint32_t bar_c2 = smem_addr(&barmem[7]);    // epilogue: U^T hi / lo packed (and the
-                                                    // previous output tile read out of TMEM)
+  const uint32_t bar_c2 = smem_addr(&barmem[7]);    // epilogue: U^T hi / lo packed
   const uint32_t bar_p0 = smem_addr(&barmem[8]), bar_p1 = smem_addr(&barmem[9]);   // P copies
+  // store warps: the output tile of a TMEM output buffer has been read out
+  const uint32_t bar_r0 = smem_addr(&barmem[11]), bar_r1 = smem_addr(&barmem[12]);
   const size_t u0 = ((size_t)b * p.Hv + h) * p.ns;  // first unit of this head's slice
-  const bool issuer_warp = (warp == CH_EPI / 32);
+  const bool issuer_warp = (warp == CH_ISSUER);
 
   // copies of chunk nl into buffer nl & 1: everything but P, and P (16 KB, needed only by the
   // last MMA group) on a barrier of its own
@@ -632,11 +638,12 @@ __global__ void __launch_bounds__(CH_THREADS, 1)
   // per buffer (issuer warp): chunk of the main / P copy issued and not yet waited for, or -1
   int ld_chunk[2] = {-1, -1}, lp_chunk[2] = {-1, -1};
   if (tid == CH_EPI) {
-    for (int i = 0; i < 10; ++i) mbar_init(smem_addr(&barmem[i]), (i == 6 || i == 7) ? CH_EPI / 32 : 1);
+    for (int i = 0; i < 13; ++i)
+      mbar_init(smem_addr(&barmem[i]), (i == 6 || i == 7) ? CH_EPI / 32 : (i >= 11 ? 4 : 1));
     *sAbort = 0;
     fence_mbar_init();
   }
-  if (warp == CH_EPI / 32)
+  if (issuer_warp)
     for (int i = 0; i < 2 && i < p.ns; ++i) ld_chunk[i] = lp_chunk[i] = i;
   if (warp == 0) {
     tmem_alloc(smem_addr(sTmem), CH_TMEM);
@@ -710,7 +717,17 @@ __global__ void __launch_bounds__(CH_THREADS, 1)
         mma_commit(bar_u);
         // C0 waited for S of the previous chunk: the other buffer's tiles but P are free
         if (nl >= 1 && nl + 1 < p.ns) load_main(nl + 1);
-        // this O buffer was last read out for chunk nl - 2, before C2 of chunk nl - 1
+      }
+      __syncwarp();
+      if (nl >= 1 && nl + 1 < p.ns) ld_chunk[(nl + 1) & 1] = nl + 1;
+      // then O^T = S0 Q~^T, once the store warps have read this O buffer's tile of chunk nl - 2
+      if (nl >= 2 && !__all_sync(0xffffffffu, mbar_wait_or_abort((nl & 1) ? bar_r1 : bar_r0,
+                                                                  ((nl - 2) >> 1) & 1, sAbort))) {
+        *sAbort = 1;
+        break;
+      }
+      tc_fence_after();
+      if (leader) {
 #pragma unroll
         for (int k = 0; k < 8; ++k)
           mma_bf16_ta(tmO, tmem + TM_S0 + 8 * k,
@@ -718,7 +735,6 @@ __global__ void __launch_bounds__(CH_THREADS, 1)
                       ID_SQ, k > 0);
       }
       __syncwarp();
-      if (nl >= 1 && nl + 1 < p.ns) ld_chunk[(nl + 1) & 1] = nl + 1;
       // C3 once C2 is done: S += U^T K~ (Uh K~ + Ul K~; critical), then
       // O^T += U^T P^T (Uh Ph + Ul Ph + Uh Pl)
       if (!__all_sync(0xffffffffu, mbar_wait_or_abort(bar_c2, nl & 1, sAbort))) {
@@ -751,7 +767,7 @@ __global__ void __launch_bounds__(CH_THREADS, 1)
           mma_bf16_ta(tmO, tmem + ua + 8 * (k & 3),
                       sdesc_sw128(buf + U_P + pb + (k & 3) * 32, 16, 1024), ID_SQ, true);
         }
-        mma_commit(bar_o);
+        mma_commit((nl & 1) ? bar_o1 : bar_o0);
         if (refill_p) load_p(nl + 1);
       }
       __syncwarp();
@@ -762,32 +778,6 @@ __global__ void __launch_bounds__(CH_THREADS, 1)
     tmem_st32(tmem + lane_off + TM_S + 64 * hc, *reinterpret_cast<float(*)[32]>(&sv[0]));
     tmem_st32(tmem + lane_off + TM_S + 64 * hc + 32, *reinterpret_cast<float(*)[32]>(&sv[32]));
     tmem_wait_st();
-    constexpr int OUT_ROWS = (int)(2 * KB / (32 * sizeof(Tout)));   // tokens per staging pass
-    Tout* stg = reinterpret_cast<Tout*>(sm + CH_OUT + warp * 2 * KB);
-    // output tile of slice chunk nl (O^T in TMEM: lane = d_v index, column = token): this
-    // warp's 32 d_v x 32 tokens -> its staging block [token][32 d_v] -> HBM with a TMA store
-    // per pass (the store clips the rows past the sequence end).  Everything stays within
-    // the warp; lane 0 issues the stores and is the one that waits for their reads.
-    auto store_out = [&](int nl) {
-      float v[32];
-      tmem_ld32(tmem + lane_off + TM_O + 64 * (nl & 1) + 32 * hc, v);
-      tmem_wait_ld();
-#pragma unroll
-      for (int pass = 0; pass < 32 / OUT_ROWS; ++pass) {
-        if (lane == 0) tma_store_wait_read();
-        __syncwarp();
-#pragma unroll
-        for (int jj = 0; jj < OUT_ROWS; ++jj)
-          stg[jj * 32 + lane] = from_float<Tout>(v[pass * OUT_ROWS + jj]);
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) {
-          tma_store_3d(&tm_o, smem_addr(stg), h * D + 32 * gw,
-                       (p.n0 + nl) * C + 32 * hc + pass * OUT_ROWS, b);
-          tma_store_commit();
-        }
-      }
-    };
     // in-call snapshots: bank rows of the next boundary inside this slice (loaded a step or
     // more ahead of its use) and of the boundary at the slice end, -1 for none
     const int32_t* snap_row = p.se_c > 0 ? p.snap_slots + (size_t)b * p.n_snap - 1 : nullptr;
@@ -863,15 +853,6 @@ __global__ void __launch_bounds__(CH_THREADS, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar_c0);
-      // ---- while U^T is being finished: the output of the previous chunk
-      if (nl > 0) {
-        if (!__all_sync(0xffffffffu, mbar_wait_or_abort(bar_o, (nl - 1) & 1, sAbort))) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        store_out(nl - 1);
-      }
       // ---- C2: U^T (fp32) -> bf16 hi / lo, packed into TMEM as A operands
       if (!__all_sync(0xffffffffu, mbar_wait_or_abort(bar_u, nl & 1, sAbort))) {
         ok = false;
@@ -894,7 +875,7 @@ __global__ void __launch_bounds__(CH_THREADS, 1)
       if (lane == 0) mbar_arrive(bar_c2);
     }
     if (ok && p.ns > 0) {
-      // the leaving state, as soon as the last S update is done (the last output update may
+      // the leaving state, as soon as the last S update is done (the last output MMAs may
       // still run): TMEM -> this warp's 32 rows x 64 columns, staged as two 128-byte-swizzled
       // 32 x 32 blocks in the tile buffer the last chunk does not use (its readers are done)
       // -> two TMA tensor stores (whole rows per request)
@@ -927,21 +908,58 @@ __global__ void __launch_bounds__(CH_THREADS, 1)
           }
           tma_store_commit();
         }
-        // then the last output tile
-        if (__all_sync(0xffffffffu, mbar_wait_or_abort(bar_o, (p.ns - 1) & 1, sAbort))) {
-          tc_fence_after();
-          store_out(p.ns - 1);
-        } else {
-          ok = false;
-        }
       } else {
         ok = false;
       }
     }
+    // the state stores must have read their staging before the CTA exits (their writes
+    // complete with the grid)
+    if (lane == 0) tma_store_wait_read();
+    if (!ok) *sAbort = 1;
+  } else {
+    // ======================= store warps: the output tile of each chunk (O^T in TMEM: lane =
+    // d_v index, column = token).  Warp w reads TMEM lane quarter w % 4, i.e. 32 d_v rows x 64
+    // tokens, tells the issuer that the buffer is free, then sends the rows through its 4 KB
+    // staging block [token][32 d_v] with one TMA store per pass (the store clips the rows
+    // past the sequence end).  Lane 0 issues the stores and is the one that waits for their
+    // reads.
+    constexpr int OUT_ROWS = (int)(4 * KB / (32 * sizeof(Tout)));   // tokens per pass
+    const int q = warp & 3;
+    const uint32_t lq = static_cast<uint32_t>(q * 32) << 16;
+    Tout* stg = reinterpret_cast<Tout*>(sm + CH_OUT + (warp - CH_STORE) * 4 * KB);
+    bool ok = true;
+    for (int nl = 0; nl < p.ns; ++nl) {
+      if (!__all_sync(0xffffffffu, mbar_wait_or_abort((nl & 1) ? bar_o1 : bar_o0,
+                                                      (nl >> 1) & 1, sAbort))) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      float v[64];
+      tmem_ld32(tmem + lq + TM_O + 64 * (nl & 1), *reinterpret_cast<float(*)[32]>(&v[0]));
+      tmem_ld32(tmem + lq + TM_O + 64 * (nl & 1) + 32, *reinterpret_cast<float(*)[32]>(&v[32]));
+      tmem_wait_ld();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive((nl & 1) ? bar_r1 : bar_r0);
+#pragma unroll
+      for (int pass = 0; pass < 64 / OUT_ROWS; ++pass) {
+        if (lane == 0) tma_store_wait_read();
+        __syncwarp();
+#pragma unroll
+        for (int jj = 0; jj < OUT_ROWS; ++jj)
+          stg[jj * 32 + lane] = from_float<Tout>(v[pass * OUT_ROWS + jj]);
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          tma_store_3d(&tm_o, smem_addr(stg), h * D + 32 * q, (p.n0 + nl) * C + pass * OUT_ROWS,
+                       b);
+          tma_store_commit();
+        }
+      }
+    }
     // everything this kernel writes has been issued: a kernel after it may start its set-up
     pdl_trigger();
-    // the output stores must have read this warp's staging block before the CTA exits (their
-    // writes complete with the grid)
     if (lane == 0) tma_store_wait_read();
     if (!ok) *sAbort = 1;
   }
@@ -979,7 +997,7 @@ int slice_chunks(int B, int Hv, int nch) {
 template <typename Tout>
 cudaError_t launch_tc_t(const GdnLayerArgs& L, cudaStream_t stream) {
   CUtensorMap mq, mk, mv, mo, ms;
-  constexpr int out_rows = (int)(2 * KB / (32 * sizeof(Tout)));
+  constexpr int out_rows = (int)(4 * KB / (32 * sizeof(Tout)));
   const bool ok =
       gdn_make_map(&mq, L.q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, L.Hk * D, L.T, L.B, L.q_tok_stride,
                64, 64, true) &&
