@@ -60,6 +60,9 @@ def lib():
         L.gdn_oracle_unit_lower_inverse.restype = None
         L.gdn_oracle_unit_lower_inverse.argtypes = [ctypes.c_int, _dp, _dp]
         L.gdn_oracle_layer.restype = ctypes.c_int
+        L.gdn_oracle_gated_rmsnorm.restype = None
+        L.gdn_oracle_gated_rmsnorm.argtypes = [ctypes.c_int, ctypes.c_int, _dp, _dp, _dp,
+                                               ctypes.c_double, _dp]
         L.gdn_oracle_layer.argtypes = [ctypes.POINTER(OracleCfg)] + [_dp] * 13 + [ctypes.c_int]
         _lib = L
     return _lib
@@ -151,6 +154,18 @@ class LayerOut:
     out: np.ndarray          # [B,T,Hv,dv]
     state: np.ndarray        # [B,Hv,dv,dk]
     conv_state: Optional[np.ndarray]   # [B,W-1,C_conv]
+
+
+def gated_rmsnorm(o, z, w, eps: float = 1e-6) -> np.ndarray:
+    """Gated RMS norm over the last axis (length n): w * o / sqrt(mean(o^2) + eps) * silu(z)."""
+    o, z, w = _f64(o), _f64(z), _f64(w)
+    assert o.shape == z.shape and w.shape == (o.shape[-1],)
+    n = o.shape[-1]
+    rows = o.size // n if n else 0
+    y = np.zeros(o.shape)
+    lib().gdn_oracle_gated_rmsnorm(int(rows), int(n), _p(np.ascontiguousarray(o)),
+                                   _p(np.ascontiguousarray(z)), _p(w), float(eps), _p(y))
+    return y
 
 
 def layer(*, num_k_heads: int, num_v_heads: int, q=None, k=None, v=None, x=None, a, b,

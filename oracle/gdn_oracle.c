@@ -30,6 +30,13 @@
  *     W-1 pre-conv inputs, oldest first); optional SiLU after the conv.
  *   - softplus(x) = max(x,0) + log1p(exp(-|x|)) (the exact function, no threshold).
  *   - GQA: value head h reads key head h / (Hv/Hk) (contiguous groups).
+ *   - The gated output norm (gdn_oracle_gated_rmsnorm): the card lists an "RMS norm" among
+ *     the operations around the kernel and gives no formula.  Read as the gated RMS norm of
+ *     these layers, per (token, value head) output vector o of length n:
+ *         y_i = w_i * o_i / sqrt((1/n) sum_j o_j^2 + eps) * silu(z_i),  silu(z) = z / (1 + e^-z),
+ *     with w the effective per-channel weight (a checkpoint that stores w - 1, the
+ *     "RMSNorm +1 conversion" of PR #164 "Add Qwen3.6-27B contrib model with vLLM APC
+ *     baseline", "Unit Coverage", is converted by the caller).
  *
  * Everything is IEEE double, no fast-math, straight loops in the order the definitions give.
  * Work units (batch row, value head) are independent and spread over pthreads.
@@ -67,6 +74,26 @@ void gdn_oracle_l2norm(int n, const double* x, double eps, double scale, double*
   for (int i = 0; i < n; ++i) ss += x[i] * x[i];
   double inv = scale / sqrt(ss + eps);
   for (int i = 0; i < n; ++i) y[i] = x[i] * inv;
+}
+
+/* ---------------------------------------------------------------- gated output norm */
+
+/* rows vectors of length n: o, z, y [rows][n] (y may alias o), w [n].  The mean of squares,
+ * its root with eps inside, the per-channel weight, then the SiLU gate of z, in that order. */
+void gdn_oracle_gated_rmsnorm(int rows, int n, const double* o, const double* z,
+                              const double* w, double eps, double* y) {
+  for (int r = 0; r < rows; ++r) {
+    const double* orow = o + (size_t)r * n;
+    const double* zrow = z + (size_t)r * n;
+    double ms = 0.0;
+    for (int i = 0; i < n; ++i) ms += orow[i] * orow[i];
+    ms /= (double)n;
+    double inv = 1.0 / sqrt(ms + eps);
+    for (int i = 0; i < n; ++i) {
+      double gate = zrow[i] * gdn_oracle_sigmoid(zrow[i]);
+      y[(size_t)r * n + i] = w[i] * (orow[i] * inv) * gate;
+    }
+  }
 }
 
 /* ---------------------------------------------------------------- causal depthwise conv */

@@ -38,6 +38,12 @@ MUTATIONS = {
                        "int W = c->conv_width, r = Hv / Hk, kh = h % Hk;"),
     "l2norm_no_sqrt": ("double inv = scale / sqrt(ss + eps);", "double inv = scale / (ss + eps);"),
     "conv_state_off_by_one": ("int idx = (W - 1) + tau;", "int idx = (W - 2) + tau;"),
+    "rmsnorm_sum_not_mean": ("ms /= (double)n;", "ms /= 1.0;"),
+    "rmsnorm_no_sqrt": ("double inv = 1.0 / sqrt(ms + eps);", "double inv = 1.0 / (ms + eps);"),
+    "rmsnorm_gate_sign": ("double gate = zrow[i] * gdn_oracle_sigmoid(zrow[i]);",
+                          "double gate = zrow[i] * gdn_oracle_sigmoid(-zrow[i]);"),
+    "rmsnorm_no_weight": ("y[(size_t)r * n + i] = w[i] * (orow[i] * inv) * gate;",
+                          "y[(size_t)r * n + i] = (orow[i] * inv) * gate;"),
 }
 
 

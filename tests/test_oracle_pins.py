@@ -377,3 +377,54 @@ def test_layer_rejects_bad_geometry():
     kw = _layer_case(50, 1, 3, 2, 3, 8, 0)   # Hv % Hk != 0
     with pytest.raises(ValueError):
         oracle.layer(**kw)
+
+
+# ------------------------------------------------------------------ gated output norm
+
+def test_gated_rmsnorm_worked_example():
+    """o = (3, 4), w = 1, z = ln 3 in both channels: mean square 12.5 and
+    silu(ln 3) = ln 3 * sigmoid(ln 3) = (3/4) ln 3, so y = o / sqrt(12.5) * (3/4) ln 3."""
+    y = oracle.gated_rmsnorm(np.array([[3.0, 4.0]]), np.full((1, 2), math.log(3.0)),
+                             np.ones(2), eps=0.0)
+    g = 0.75 * math.log(3.0)
+    np.testing.assert_allclose(y[0], [3.0 / math.sqrt(12.5) * g, 4.0 / math.sqrt(12.5) * g],
+                               rtol=1e-15)
+
+
+def test_gated_rmsnorm_closed_forms():
+    """A constant vector c has RMS |c|: y = sign(c) * w * silu(z).  z = 0 closes the gate
+    (silu(0) = 0); a large z opens it to z itself; a very negative z closes it."""
+    rng = np.random.default_rng(11)
+    n = 128
+    w = rng.uniform(0.5, 2.0, n)
+    z = rng.standard_normal((2, n))
+    o = np.stack([np.full(n, 0.37), np.full(n, -5.0)])
+    y = oracle.gated_rmsnorm(o, z, w, eps=0.0)
+    silu = z * sps.expit(z)
+    np.testing.assert_allclose(y[0], w * silu[0], rtol=1e-14)
+    np.testing.assert_allclose(y[1], -w * silu[1], rtol=1e-14)
+    o = rng.standard_normal((3, n))
+    assert np.all(oracle.gated_rmsnorm(o, np.zeros((3, n)), w, eps=0.0) == 0.0)
+    big = oracle.gated_rmsnorm(o, np.full((3, n), 60.0), np.ones(n), eps=0.0)
+    rms = np.sqrt(np.mean(o * o, axis=1, keepdims=True))
+    np.testing.assert_allclose(big, o / rms * 60.0, rtol=1e-13)
+    assert np.all(np.abs(oracle.gated_rmsnorm(o, np.full((3, n), -60.0), np.ones(n))) < 1e-20)
+
+
+def test_gated_rmsnorm_invariants():
+    """Without eps: invariant to positive scaling of o, odd in o, and the normalised vector
+    y / (w silu(z)) has mean square exactly 1 (mean over n channels, not a sum).  With eps,
+    o = 0 gives 0 (no division by zero) and a tiny o is damped, not blown up."""
+    rng = np.random.default_rng(12)
+    n = 128
+    o = rng.standard_normal((5, n))
+    z = rng.standard_normal((5, n))
+    w = rng.uniform(0.5, 2.0, n)
+    y = oracle.gated_rmsnorm(o, z, w, eps=0.0)
+    np.testing.assert_allclose(oracle.gated_rmsnorm(7.5 * o, z, w, eps=0.0), y, rtol=1e-13)
+    np.testing.assert_allclose(oracle.gated_rmsnorm(-o, z, w, eps=0.0), -y, rtol=1e-15)
+    unit = y / (w * z * sps.expit(z))
+    np.testing.assert_allclose(np.mean(unit * unit, axis=1), 1.0, rtol=1e-13)
+    assert np.all(oracle.gated_rmsnorm(np.zeros((1, n)), z[:1], w, eps=1e-6) == 0.0)
+    tiny = oracle.gated_rmsnorm(1e-6 * o, z, w, eps=1e-6)
+    assert np.max(np.abs(tiny)) < np.max(np.abs(y)) * 2e-3
