@@ -168,16 +168,22 @@ def prefill_step(gdn, wl):
                                  wl["rows"], wl["slots"][i:i + 1], num_k_heads=HK)
 
 
-def prefill_calls_only(gdn, wl):
-    """The 256 bucket prefill calls of a step without the checkpoints (kernel timing)."""
+def prefill_calls_only(gdn, wl, gate=None):
+    """The 256 bucket prefill calls of a step without the checkpoints (kernel timing); with
+    `gate` = (z [1, T, Hv, d], weight [d]) the gated-norm entry point instead."""
     inp = wl["inp"]
     for i in range(T_TOTAL // BUCKET):
         t0 = i * BUCKET
-        gdn.gdn_chunk_prefill(inp.x[:, t0:t0 + BUCKET], None, None, inp.a[:, t0:t0 + BUCKET],
-                              inp.b[:, t0:t0 + BUCKET], inp.A_log, inp.dt_bias, inp.state,
-                              wl["out"][:, t0:t0 + BUCKET], num_k_heads=HK,
-                              conv_weight=inp.conv_weight, conv_state=inp.conv_state,
-                              workspace=wl["ws"])
+        args = (inp.x[:, t0:t0 + BUCKET], None, None, inp.a[:, t0:t0 + BUCKET],
+                inp.b[:, t0:t0 + BUCKET], inp.A_log, inp.dt_bias, inp.state,
+                wl["out"][:, t0:t0 + BUCKET])
+        kw = dict(num_k_heads=HK, conv_weight=inp.conv_weight, conv_state=inp.conv_state,
+                  workspace=wl["ws"])
+        if gate is None:
+            gdn.gdn_chunk_prefill(*args, **kw)
+        else:
+            gdn.gdn_chunk_prefill_gated(*args, gate_z=gate[0][:, t0:t0 + BUCKET],
+                                        gate_weight=gate[1], **kw)
 
 
 def make_decode_workload(device):
@@ -195,16 +201,22 @@ def make_decode_workload(device):
                 dt_bias=dt_bias, out=out)
 
 
-def decode_steps(gdn, wl, events=None):
+def decode_steps(gdn, wl, events=None, gate=None):
+    """DECODE_STEPS decode steps; with `gate` = (z [steps, B, Hv, d], weight [d]) the
+    gated-norm entry point instead."""
     dec = wl["dec"]
     for t in range(DECODE_STEPS):
         if events is not None:
             events[t][0].record()
-        gdn.gdn_decode_step(dec["x"][t].view(DECODE_B, 1, C_CONV), None, None,
-                            dec["a"][t].view(DECODE_B, 1, HV), dec["b"][t].view(DECODE_B, 1, HV),
-                            wl["A_log"], wl["dt_bias"], wl["state"],
-                            wl["out"][t].view(DECODE_B, 1, HV, D), num_k_heads=HK,
-                            conv_weight=wl["cw"], conv_state=wl["conv_state"])
+        args = (dec["x"][t].view(DECODE_B, 1, C_CONV), None, None,
+                dec["a"][t].view(DECODE_B, 1, HV), dec["b"][t].view(DECODE_B, 1, HV),
+                wl["A_log"], wl["dt_bias"], wl["state"], wl["out"][t].view(DECODE_B, 1, HV, D))
+        kw = dict(num_k_heads=HK, conv_weight=wl["cw"], conv_state=wl["conv_state"])
+        if gate is None:
+            gdn.gdn_decode_step(*args, **kw)
+        else:
+            gdn.gdn_decode_step_gated(*args, gate_z=gate[0][t].view(DECODE_B, 1, HV, D),
+                                      gate_weight=gate[1], **kw)
         if events is not None:
             events[t][1].record()
 
@@ -286,6 +298,8 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-decode-sweep", action="store_true")
     ap.add_argument("--no-prefill-4b", action="store_true")
+    ap.add_argument("--no-gated", action="store_true",
+                    help="skip the gated-norm prefill / decode variants")
     ap.add_argument("--no-single-call", action="store_true",
                     help="skip the one-call 27B prefill with in-kernel snapshots")
     ap.add_argument("--e2e-streams", type=int, default=1, help="upload streams of the e2e pipeline")
@@ -482,6 +496,48 @@ def main():
     st = gdn.gdn_get_device_error()
     if st != 0:
         raise RuntimeError(f"device error in decode: {gdn.gdn_status_string(st)}")
+    # the same decode with the gated RMS norm fused into the output (z adds B Hv d bf16 bytes)
+    gated = None
+    if not args.no_gated:
+        gz = (torch.randn(DECODE_STEPS, DECODE_B, HV, D, device=device).to(torch.bfloat16),
+              torch.rand(D, device=device) + 0.5)
+        decode_steps(gdn, dwl, gate=gz)
+        g_gd = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g_gd):
+            decode_steps(gdn, dwl, gate=gz)
+        for _ in range(3):
+            g_gd.replay()
+        d0.record()
+        for _ in range(dreps):
+            g_gd.replay()
+        d1.record()
+        torch.cuda.synchronize()
+        gd_ms = d0.elapsed_time(d1) / (dreps * DECODE_STEPS)
+        gd_bytes = dec_bytes + DECODE_B * HV * D * 2
+        # and the 27B bucket prefill calls with the norm (z [1, T, Hv, d] bf16)
+        gzp = (torch.randn(1, T_TOTAL, HV, D, device=device).to(torch.bfloat16), gz[1])
+        prefill_calls_only(gdn, wl, gate=gzp)
+        g_gp = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g_gp):
+            prefill_calls_only(gdn, wl, gate=gzp)
+        for _ in range(2):
+            g_gp.replay()
+        d0.record()
+        for _ in range(3):
+            g_gp.replay()
+        d1.record()
+        torch.cuda.synchronize()
+        gp_ms = d0.elapsed_time(d1) / 3
+        st = gdn.gdn_get_device_error()
+        if st != 0:
+            raise RuntimeError(f"device error in the gated runs: {gdn.gdn_status_string(st)}")
+        gated = {"what": "gated RMS norm fused into the output (w o / rms(o) silu(z))",
+                 "prefill_tokens_per_s": T_TOTAL / (gp_ms / 1e3),
+                 "prefill_call_ms": gp_ms / nbk,
+                 "decode_step_ms": gd_ms,
+                 "decode_gbs": gd_bytes / (gd_ms / 1e3) / 1e9,
+                 "decode_frac_of_hbm": gd_bytes / (gd_ms / 1e3) / 1e9 / peaks["hbm_gbs"]}
+        del g_gd, g_gp, gz, gzp
     del g_dec, dwl
     # the other batch sizes of the 27B decode workload (64-step graphs), for latency
     dec_batches = []
@@ -640,6 +696,7 @@ def main():
                                     "traffic": measured_traffic("decode_step", f"qwen36_27b_decode_B{DECODE_B}"),
                                     "peak_source": peaks["source"]},
                        "l2": "state 805 MB > L2", "other_batches": dec_batches},
+            "gated_rmsnorm": gated,
             "e2e": e2e,
             "cpu_baseline": cpu,
             "clocks": clocks,

@@ -27,8 +27,8 @@ STATUS_NAMES = {0: "GDN_OK", 1: "GDN_ERR_INVALID_ARGUMENT", 2: "GDN_ERR_UNSUPPOR
 
 EXPORTED = ("gdn_prefill_workspace_size", "gdn_chunk_prefill", "gdn_decode_step",
             "causal_conv1d_update", "gdn_state_checkpoint", "gdn_chunk_prefill_noalloc",
-            "gdn_chunk_prefill_snapshots", "gdn_get_device_error", "gdn_status_string",
-            "gdn_version")
+            "gdn_chunk_prefill_snapshots", "gdn_chunk_prefill_gated", "gdn_decode_step_gated",
+            "gdn_get_device_error", "gdn_status_string", "gdn_version")
 NOALLOC_SCRATCH_BYTES = 64 << 20   # GDN_NOALLOC_SCRATCH_BYTES in include/gdn.h
 
 
@@ -50,6 +50,10 @@ class GdnOpts(ctypes.Structure):
                 ("qk_l2norm", ctypes.c_int32), ("l2_eps", ctypes.c_float),
                 ("scale", ctypes.c_float), ("conv_silu", ctypes.c_int32),
                 ("gates_precomputed", ctypes.c_int32)]
+
+
+class GdnOutGate(ctypes.Structure):
+    _fields_ = [("z", ctypes.c_void_p), ("weight", ctypes.c_void_p), ("eps", ctypes.c_float)]
 
 
 _vp = ctypes.c_void_p
@@ -74,6 +78,11 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     L.gdn_chunk_prefill_snapshots.argtypes = ([dp, op] + [_vp] * 13 +
                                               [ctypes.c_int32, _vp, _vp, ctypes.c_int32, _vp,
                                                _vp, ctypes.c_size_t, _vp])
+    gp = ctypes.POINTER(GdnOutGate)
+    L.gdn_chunk_prefill_gated.restype = ctypes.c_int
+    L.gdn_chunk_prefill_gated.argtypes = [dp, op] + [_vp] * 13 + [gp, _vp, ctypes.c_size_t, _vp]
+    L.gdn_decode_step_gated.restype = ctypes.c_int
+    L.gdn_decode_step_gated.argtypes = [dp, op] + [_vp] * 13 + [gp, _vp]
     L.gdn_chunk_prefill_noalloc.restype = ctypes.c_int
     L.gdn_chunk_prefill_noalloc.argtypes = [dp, op] + [_vp] * 13 + [_vp]
     L.gdn_decode_step.restype = ctypes.c_int
@@ -312,6 +321,70 @@ def gdn_decode_step(q, k, v, a, b, A_log, dt_bias, state, out, *, num_k_heads=No
                            _ptr(conv_bias), _ptr(state), _ptr(conv_state), _ptr(state_slots),
                            _ptr(out), _stream(stream))
     _check(st, "gdn_decode_step")
+    return out
+
+
+def _out_gate(gate_z, gate_weight, gate_eps, out, in_dtype) -> GdnOutGate:
+    dev = out.device
+    _need(gate_z, "gate_z", tuple(out.shape), in_dtype, dev)
+    _need(gate_weight, "gate_weight", (HEAD_DIM,), torch.float32, dev)
+    return GdnOutGate(_ptr(gate_z), _ptr(gate_weight), float(gate_eps))
+
+
+def gdn_chunk_prefill_gated(q, k, v, a, b, A_log, dt_bias, state, out, *, gate_z, gate_weight,
+                            gate_eps: float = 1e-6, num_k_heads=None, conv_weight=None,
+                            conv_bias=None, conv_state=None, state_slots=None,
+                            scale: float = 1.0, eps: float = 1e-6, qk_l2norm: bool = True,
+                            conv_silu: bool = True, gates_precomputed: bool = False,
+                            workspace: Optional[torch.Tensor] = None,
+                            stream=None) -> torch.Tensor:
+    """gdn_chunk_prefill with the gated RMS norm on the output (see gdn_out_gate in
+    include/gdn.h): out = gate_weight * o / sqrt(mean(o^2) + gate_eps) * silu(gate_z) per
+    (token, value head); gate_z has the shape of out and the input dtype."""
+    L = load_library()
+    B, T, Hk, Hv, W, num_slots = _layer_dims(q, k, v, a, num_k_heads, conv_weight, conv_state,
+                                             state, state_slots, None)
+    _check_layer(q, k, v, a, b, A_log, dt_bias, conv_weight, conv_bias, state, conv_state,
+                 state_slots, out, B, T, Hk, Hv, W, num_slots, gates_precomputed)
+    gate = _out_gate(gate_z, gate_weight, gate_eps, out, q.dtype)
+    dims = GdnDims(B, T, Hk, Hv, HEAD_DIM, 64, W, num_slots)
+    opts = _opts(_dt(q), _dt(out), qk_l2norm, eps, scale, conv_silu, gates_precomputed)
+    need = int(L.gdn_prefill_workspace_size(ctypes.byref(dims), ctypes.byref(opts)))
+    if need and workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    st = L.gdn_chunk_prefill_gated(ctypes.byref(dims), ctypes.byref(opts), _ptr(q), _ptr(k),
+                                   _ptr(v), _ptr(a), _ptr(b), _ptr(A_log), _ptr(dt_bias),
+                                   _ptr(conv_weight), _ptr(conv_bias), _ptr(state),
+                                   _ptr(conv_state), _ptr(state_slots), _ptr(out),
+                                   ctypes.byref(gate), _ptr(workspace), ws_bytes,
+                                   _stream(stream))
+    _check(st, "gdn_chunk_prefill_gated")
+    return out
+
+
+def gdn_decode_step_gated(q, k, v, a, b, A_log, dt_bias, state, out, *, gate_z, gate_weight,
+                          gate_eps: float = 1e-6, num_k_heads=None, conv_weight=None,
+                          conv_bias=None, conv_state=None, state_slots=None, scale: float = 1.0,
+                          eps: float = 1e-6, qk_l2norm: bool = True, conv_silu: bool = True,
+                          gates_precomputed: bool = False, stream=None) -> torch.Tensor:
+    """gdn_decode_step with the gated RMS norm on the output (gate_z shaped like out)."""
+    L = load_library()
+    B, T, Hk, Hv, W, num_slots = _layer_dims(q, k, v, a, num_k_heads, conv_weight, conv_state,
+                                             state, state_slots, None)
+    if T != 1:
+        raise ValueError("gdn_decode_step_gated takes exactly one token per sequence")
+    _check_layer(q, k, v, a, b, A_log, dt_bias, conv_weight, conv_bias, state, conv_state,
+                 state_slots, out, B, T, Hk, Hv, W, num_slots, gates_precomputed)
+    gate = _out_gate(gate_z, gate_weight, gate_eps, out, q.dtype)
+    dims = GdnDims(B, 1, Hk, Hv, HEAD_DIM, 64, W, num_slots)
+    opts = _opts(_dt(q), _dt(out), qk_l2norm, eps, scale, conv_silu, gates_precomputed)
+    st = L.gdn_decode_step_gated(ctypes.byref(dims), ctypes.byref(opts), _ptr(q), _ptr(k),
+                                 _ptr(v), _ptr(a), _ptr(b), _ptr(A_log), _ptr(dt_bias),
+                                 _ptr(conv_weight), _ptr(conv_bias), _ptr(state),
+                                 _ptr(conv_state), _ptr(state_slots), _ptr(out),
+                                 ctypes.byref(gate), _stream(stream))
+    _check(st, "gdn_decode_step_gated")
     return out
 
 

@@ -39,6 +39,9 @@ __device__ __forceinline__ float softplus_f(float x) {
 }
 __device__ __forceinline__ float sigmoid_f(float x) { return 1.0f / (1.0f + expf(-x)); }
 __device__ __forceinline__ float silu_f(float x) { return x * sigmoid_f(x); }
+// SiLU for the output gate: z / (1 + e^-z) with the fast exponential and division (for
+// z -> -inf the denominator overflows to inf and the quotient is 0).
+__device__ __forceinline__ float silu_gate(float z) { return __fdividef(z, 1.0f + __expf(-z)); }
 
 // Gate of the model card's correctness contract: g = -exp(A_log) * softplus(a + dt_bias).
 __device__ __forceinline__ float gate_g(float a, float A_log, float dt_bias) {
@@ -140,6 +143,11 @@ struct GdnLayerArgs {
   int snap_every, n_snap, num_snap_slots;
   float* snap_state;
   const int32_t* snap_slots;
+  // gated RMS norm of the output (gate != 0): out = w * o / sqrt(mean(o^2) + eps) * silu(z)
+  int gate;
+  const void* gate_z;         // [B, T, Hv, d] in the input type
+  const float* gate_w;        // [d]
+  float gate_eps;
 };
 
 // Workspace bytes the tensor-core prefill needs for B sequences of T tokens, Hv value heads.
@@ -170,6 +178,13 @@ cudaError_t gdn_launch_checkpoint(int op, int Hv, int d, int conv_elems, int con
                                   float* slot_state, void* slot_conv_state, int num_bank,
                                   const int32_t* rows, const int32_t* slots, int n,
                                   cudaStream_t stream);
+
+// The gated RMS norm as a pass of its own over out [B][T][Hv][d] (in place, fp32), for the
+// FMA-pipe prefill; z [B][T][Hv][d] in fp32; rows of batch entries that `slots` skips are
+// left alone.
+cudaError_t gdn_launch_gated_norm_f32(float* out, const float* z, const float* w, float eps,
+                                      int B, long long rows_per_seq, const int32_t* slots,
+                                      int num_slots, cudaStream_t stream);
 
 // Per-translation-unit device error words: read and clear (host side, synchronous copy).
 unsigned gdn_take_error_decode();

@@ -17,6 +17,10 @@
 // blocks of 16 KB: a three-stage ring of TMA bulk copies (loads run two blocks ahead, across
 // item boundaries, while the updated blocks leave with bulk stores).  In shared memory one
 // warp handles a 512-byte row with 128-bit accesses and two warp-wide dot products.
+//
+// With the gated output norm (out = w o / sqrt(mean(o^2) + eps) silu(z) over the 128 outputs
+// of a value head) the outputs of an item wait in shared memory, in the slots of the v values
+// they replace, and the head's last block normalises and stores all 128 of them.
 #include "common.cuh"
 #include "sm100_ptx.cuh"
 
@@ -165,11 +169,14 @@ __global__ void __launch_bounds__(DEC_THREADS, DEC_CPS) gdn_decode_stream_kernel
   DecCursor c;
   dec_first(p, nitems, c);
   float kq = 0.f;
+  float zg = 0.f;                                      // gate of output channel tid (< 128)
   int k = 0;                                           // ordinal of the block being consumed
   for (; c.item < nitems; ++k) {
     const int b = c.item / p.Hk, kh = c.item % p.Hk;
     const int slot = p.slots ? p.slots[b] : b;
     if (c.blk == 0) {
+      // (gated: the previous item's last head may still be reading its outputs out of sv)
+      if (p.gate) __syncthreads();
       // ---- item prologue: conv (+SiLU) of q, k (threads 0..127: q_j, 128..255: k_j) and of
       //      the r value heads' v channels, their new conv state, norms, k.q, gates
       const int j = tid & (D - 1);
@@ -230,6 +237,8 @@ __global__ void __launch_bounds__(DEC_THREADS, DEC_CPS) gdn_decode_stream_kernel
     // ---- the block: rows r0 .. r0 + DEC_RB - 1 of value head hh
     const int hh = c.blk / DEC_BPH, r0 = (c.blk % DEC_BPH) * DEC_RB;
     const int h = kh * r + hh;
+    if (p.gate && c.blk % DEC_BPH == 0 && tid < D)      // used at the head's last block
+      zg = ld_elem((const Tin*)p.gate_z + ((size_t)b * p.Hv + h) * D + tid);
     const float eg = sg[2 * hh], beta = sg[2 * hh + 1];
     const float4 k4 = reinterpret_cast<const float4*>(sk)[lane];
     const float4 q4 = reinterpret_cast<const float4*>(sq)[lane];
@@ -243,17 +252,24 @@ __global__ void __launch_bounds__(DEC_THREADS, DEC_CPS) gdn_decode_stream_kernel
     float* sob = so + (k & 1) * DEC_RB;
 #pragma unroll
     for (int i = 0; i < RPW; ++i) {
+      const int row = warp * RPW + i;
+      const float vi = sv[hh * D + r0 + row];
       const float al = warp_sum(dot4(s[i], k4));
       const float ga = warp_sum(dot4(s[i], q4));
-      const int row = warp * RPW + i;
-      const float delta = beta * (sv[hh * D + r0 + row] - eg * al);
+      const float delta = beta * (vi - eg * al);
       float4 t;
       t.x = fmaf(eg, s[i].x, delta * k4.x);
       t.y = fmaf(eg, s[i].y, delta * k4.y);
       t.z = fmaf(eg, s[i].z, delta * k4.z);
       t.w = fmaf(eg, s[i].w, delta * k4.w);
       reinterpret_cast<float4*>(Sw + i * D)[lane] = t;
-      if (lane == 0) sob[row] = fmaf(eg, ga, delta * kq);
+      const float o = fmaf(eg, ga, delta * kq);
+      if (p.gate) {
+        __syncwarp();                                  // every lane has read v_i
+        if (lane == 0) sv[hh * D + r0 + row] = o;
+      } else if (lane == 0) {
+        sob[row] = o;
+      }
     }
     fence_proxy_async_smem();
     if (!__syncthreads_and(ok)) {
@@ -274,9 +290,20 @@ __global__ void __launch_bounds__(DEC_THREADS, DEC_CPS) gdn_decode_stream_kernel
         ++pk;
       }
     }
-    if (tid < DEC_RB) {
-      Tout* o = (Tout*)p.out + ((size_t)b * p.Hv + h) * D + r0 + tid;
-      *o = from_float<Tout>(sob[tid]);
+    if (!p.gate) {
+      if (tid < DEC_RB) {
+        Tout* o = (Tout*)p.out + ((size_t)b * p.Hv + h) * D + r0 + tid;
+        *o = from_float<Tout>(sob[tid]);
+      }
+    } else if (c.blk % DEC_BPH == DEC_BPH - 1 && tid < D) {
+      // the head's 128 outputs are complete: gated RMS norm over them (warps 0-3)
+      const float ov = sv[hh * D + tid];
+      const float ssum = warp_sum(ov * ov);
+      if (lane == 0) red[16 + warp] = ssum;
+      named_bar_sync(1, D);
+      const float inv = rsqrtf((red[16] + red[17] + red[18] + red[19]) * (1.0f / D) + p.gate_eps);
+      Tout* o = (Tout*)p.out + ((size_t)b * p.Hv + h) * D + tid;
+      *o = from_float<Tout>(p.gate_w[tid] * (ov * inv) * silu_gate(zg));
     }
     dec_advance(p, nitems, nblk, c);
   }
@@ -306,6 +333,18 @@ __device__ __forceinline__ void cluster_arrive_relaxed() {
 }
 __device__ __forceinline__ void cluster_wait_acquire() {
   asm volatile("barrier.cluster.wait.acquire.aligned;\n" ::: "memory");
+}
+__device__ __forceinline__ void cluster_arrive_release() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n" ::: "memory");
+}
+// A float in the shared memory of cluster CTA `rank`, at the offset of `local` here.
+__device__ __forceinline__ float ld_cluster_f32(const float* local, uint32_t rank) {
+  uint32_t remote;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;\n"
+               : "=r"(remote) : "r"(smem_addr(local)), "r"(rank));
+  float v;
+  asm volatile("ld.shared::cluster.f32 %0, [%1];\n" : "=f"(v) : "r"(remote) : "memory");
+  return v;
 }
 
 template <typename Tin, typename Tout, int R>
@@ -352,6 +391,11 @@ __global__ void __launch_bounds__(256) gdn_decode_cluster_kernel(GdnLayerArgs p,
   __shared__ float so[R];
   __shared__ float red[16];
   __shared__ float sgate[2];
+  __shared__ float spart;                        // gated norm: sum of squares of this CTA's outputs
+  // gated norm: the gate of this CTA's output channel r0 + tid
+  const float zg = (p.gate && tid < R)
+                       ? ld_elem((const Tin*)p.gate_z + ((size_t)b * p.Hv + h) * D + r0 + tid)
+                       : 0.f;
 
   // ---- 1. conv (+SiLU) or plain load of q, k (threads 0..127: q_j, 128..255: k_j)
   const int j = tid & (D - 1);
@@ -445,13 +489,40 @@ __global__ void __launch_bounds__(256) gdn_decode_cluster_kernel(GdnLayerArgs p,
     tma_store_commit();
   }
   // ---- 4. outputs and conv state
-  if (tid < R) {
-    Tout* o = (Tout*)p.out + ((size_t)b * p.Hv + h) * D + r0 + tid;
-    *o = from_float<Tout>(so[tid]);
-    if (p.W > 1) conv_store_state<Tin>(p, slot, chv, winv);
+  if (!p.gate) {
+    if (tid < R) {
+      Tout* o = (Tout*)p.out + ((size_t)b * p.Hv + h) * D + r0 + tid;
+      *o = from_float<Tout>(so[tid]);
+      if (p.W > 1) conv_store_state<Tin>(p, slot, chv, winv);
+    }
+    cluster_wait_acquire();
+    if (p.W > 1 && hh == 0 && sp == 0) conv_store_state<Tin>(p, slot, ch, win);
+  } else {
+    // gated RMS norm over the head's 128 outputs, spread over its nsplit CTAs: each CTA's
+    // sum of squares goes to its shared memory, a cluster barrier publishes it, every CTA
+    // adds the head's partial sums, and a last barrier keeps every CTA (and its partial sum)
+    // alive until all reads are done
+    if (warp == 0) {
+      float acc = 0.f;
+      for (int i = lane; i < R; i += 32) acc = fmaf(so[i], so[i], acc);
+      acc = warp_sum(acc);
+      if (lane == 0) spart = acc;
+    }
+    if (tid < R && p.W > 1) conv_store_state<Tin>(p, slot, chv, winv);
+    cluster_wait_acquire();
+    if (p.W > 1 && hh == 0 && sp == 0) conv_store_state<Tin>(p, slot, ch, win);
+    cluster_arrive_release();
+    cluster_wait_acquire();
+    float tot = 0.f;
+    for (int s2 = 0; s2 < nsplit; ++s2) tot += ld_cluster_f32(&spart, (uint32_t)(hh * nsplit + s2));
+    const float inv = rsqrtf(tot * (1.0f / D) + p.gate_eps);
+    if (tid < R) {
+      Tout* o = (Tout*)p.out + ((size_t)b * p.Hv + h) * D + r0 + tid;
+      *o = from_float<Tout>(p.gate_w[r0 + tid] * (so[tid] * inv) * silu_gate(zg));
+    }
+    cluster_arrive_relaxed();
+    cluster_wait_acquire();
   }
-  cluster_wait_acquire();
-  if (p.W > 1 && hh == 0 && sp == 0) conv_store_state<Tin>(p, slot, ch, win);
   if (tid == 0) tma_store_wait_read();    // the bulk store has read shared memory
 }
 

@@ -7,7 +7,7 @@
 
 namespace {
 
-constexpr int32_t kVersion = 101;
+constexpr int32_t kVersion = 102;
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
@@ -109,6 +109,19 @@ size_t workspace_bytes_for(const Checked& c, const gdn_opts* o) {
   return n;
 }
 
+// Copies a valid output gate into L (gate may be NULL: no norm).
+gdn_status set_gate(const gdn_out_gate* gate, bool required, GdnLayerArgs* L) {
+  if (!gate) return required ? GDN_ERR_INVALID_ARGUMENT : GDN_OK;
+  if (!gate->z || !aligned16(gate->z) || !gate->weight || !aligned4(gate->weight) ||
+      !(gate->eps >= 0.0f) || !(gate->eps < 3.0e38f))
+    return GDN_ERR_INVALID_ARGUMENT;
+  L->gate = 1;
+  L->gate_z = gate->z;
+  L->gate_w = gate->weight;
+  L->gate_eps = gate->eps;
+  return GDN_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -142,7 +155,8 @@ static gdn_status prefill_impl(const gdn_dims* dims, const gdn_opts* opts, const
                                void* conv_state, const int32_t* state_slots, void* out,
                                int32_t snap_every, float* snap_state, void* snap_conv_state,
                                int32_t num_snap_slots, const int32_t* snap_slots,
-                               void* workspace, size_t workspace_bytes, void* stream) {
+                               const gdn_out_gate* gate, bool gated, void* workspace,
+                               size_t workspace_bytes, void* stream) {
   Checked c;
   gdn_status st = check_dims(dims, opts, false, &c);
   if (st != GDN_OK) return st;
@@ -151,6 +165,8 @@ static gdn_status prefill_impl(const gdn_dims* dims, const gdn_opts* opts, const
   GdnLayerArgs L;
   st = check_layer_ptrs(c, opts, q, k, v, a, b, A_log, dt_bias, conv_weight, conv_bias, state,
                         conv_state, state_slots, out, &L);
+  if (st != GDN_OK) return st;
+  st = set_gate(gate, gated, &L);
   if (st != GDN_OK) return st;
   const int n_snap = snap_every > 0 ? c.T / snap_every : 0;
   if (n_snap > 0) {
@@ -187,6 +203,13 @@ static gdn_status prefill_impl(const gdn_dims* dims, const gdn_opts* opts, const
   }
   cudaError_t e = L.in_bf16 ? gdn_launch_prefill_tc(L, s) : gdn_launch_prefill_simt(L, s);
   if (e != cudaSuccess) return GDN_ERR_CUDA;
+  if (L.gate && !L.in_bf16) {
+    // the FMA-pipe path (fp32 in and out) applies the norm as a pass of its own
+    e = gdn_launch_gated_norm_f32(static_cast<float*>(out), static_cast<const float*>(L.gate_z),
+                                  L.gate_w, L.gate_eps, c.B, (long long)c.T * c.Hv, state_slots,
+                                  c.num_slots, s);
+    if (e != cudaSuccess) return GDN_ERR_CUDA;
+  }
   if (n_snap > 0 && c.W > 1) {
     // the conv state at each boundary: W-1 rows of the call's pre-conv input
     e = gdn_launch_conv_snapshots(c.B, c.T, c.Cc * c.in_elem, (long long)c.Cc * c.in_elem,
@@ -204,8 +227,20 @@ gdn_status gdn_chunk_prefill(const gdn_dims* dims, const gdn_opts* opts, const v
                              const int32_t* state_slots, void* out, void* workspace,
                              size_t workspace_bytes, void* stream) {
   return prefill_impl(dims, opts, q, k, v, a, b, A_log, dt_bias, conv_weight, conv_bias, state,
-                      conv_state, state_slots, out, 0, nullptr, nullptr, 0, nullptr, workspace,
-                      workspace_bytes, stream);
+                      conv_state, state_slots, out, 0, nullptr, nullptr, 0, nullptr, nullptr,
+                      false, workspace, workspace_bytes, stream);
+}
+
+gdn_status gdn_chunk_prefill_gated(const gdn_dims* dims, const gdn_opts* opts, const void* q,
+                                   const void* k, const void* v, const void* a, const void* b,
+                                   const float* A_log, const float* dt_bias,
+                                   const void* conv_weight, const void* conv_bias, float* state,
+                                   void* conv_state, const int32_t* state_slots, void* out,
+                                   const gdn_out_gate* gate, void* workspace,
+                                   size_t workspace_bytes, void* stream) {
+  return prefill_impl(dims, opts, q, k, v, a, b, A_log, dt_bias, conv_weight, conv_bias, state,
+                      conv_state, state_slots, out, 0, nullptr, nullptr, 0, nullptr, gate, true,
+                      workspace, workspace_bytes, stream);
 }
 
 gdn_status gdn_chunk_prefill_snapshots(const gdn_dims* dims, const gdn_opts* opts, const void* q,
@@ -221,14 +256,17 @@ gdn_status gdn_chunk_prefill_snapshots(const gdn_dims* dims, const gdn_opts* opt
   if (snap_every <= 0) return GDN_ERR_INVALID_ARGUMENT;
   return prefill_impl(dims, opts, q, k, v, a, b, A_log, dt_bias, conv_weight, conv_bias, state,
                       conv_state, state_slots, out, snap_every, snap_state, snap_conv_state,
-                      num_snap_slots, snap_slots, workspace, workspace_bytes, stream);
+                      num_snap_slots, snap_slots, nullptr, false, workspace, workspace_bytes,
+                      stream);
 }
 
-gdn_status gdn_decode_step(const gdn_dims* dims, const gdn_opts* opts, const void* q,
-                           const void* k, const void* v, const void* a, const void* b,
-                           const float* A_log, const float* dt_bias, const void* conv_weight,
-                           const void* conv_bias, float* state, void* conv_state,
-                           const int32_t* state_slots, void* out, void* stream) {
+// gdn_decode_step, with the output gate when `gated`
+static gdn_status decode_impl(const gdn_dims* dims, const gdn_opts* opts, const void* q,
+                              const void* k, const void* v, const void* a, const void* b,
+                              const float* A_log, const float* dt_bias, const void* conv_weight,
+                              const void* conv_bias, float* state, void* conv_state,
+                              const int32_t* state_slots, void* out, const gdn_out_gate* gate,
+                              bool gated, void* stream) {
   Checked c;
   gdn_status st = check_dims(dims, opts, true, &c);
   if (st != GDN_OK) return st;
@@ -237,8 +275,29 @@ gdn_status gdn_decode_step(const gdn_dims* dims, const gdn_opts* opts, const voi
   st = check_layer_ptrs(c, opts, q, k, v, a, b, A_log, dt_bias, conv_weight, conv_bias, state,
                         conv_state, state_slots, out, &L);
   if (st != GDN_OK) return st;
+  st = set_gate(gate, gated, &L);
+  if (st != GDN_OK) return st;
   cudaError_t e = gdn_launch_decode(L, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+}
+
+gdn_status gdn_decode_step(const gdn_dims* dims, const gdn_opts* opts, const void* q,
+                           const void* k, const void* v, const void* a, const void* b,
+                           const float* A_log, const float* dt_bias, const void* conv_weight,
+                           const void* conv_bias, float* state, void* conv_state,
+                           const int32_t* state_slots, void* out, void* stream) {
+  return decode_impl(dims, opts, q, k, v, a, b, A_log, dt_bias, conv_weight, conv_bias, state,
+                     conv_state, state_slots, out, nullptr, false, stream);
+}
+
+gdn_status gdn_decode_step_gated(const gdn_dims* dims, const gdn_opts* opts, const void* q,
+                                 const void* k, const void* v, const void* a, const void* b,
+                                 const float* A_log, const float* dt_bias,
+                                 const void* conv_weight, const void* conv_bias, float* state,
+                                 void* conv_state, const int32_t* state_slots, void* out,
+                                 const gdn_out_gate* gate, void* stream) {
+  return decode_impl(dims, opts, q, k, v, a, b, A_log, dt_bias, conv_weight, conv_bias, state,
+                     conv_state, state_slots, out, gate, true, stream);
 }
 
 gdn_status causal_conv1d_update(int32_t batch, int32_t seqlen, int32_t channels, int32_t width,

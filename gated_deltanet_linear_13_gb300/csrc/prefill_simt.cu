@@ -270,3 +270,42 @@ cudaError_t gdn_launch_prefill_simt(const GdnLayerArgs& p, cudaStream_t stream) 
   }
   return launch_simt_t<float, float>(p, stream);
 }
+
+// ======================================================================= gated output norm
+// out_i = w_i * o_i / sqrt(mean(o^2) + eps) * silu(z_i) per (token, value head) vector of 128,
+// in place: one warp per vector, four channels per lane.
+__global__ void __launch_bounds__(256) gdn_gated_norm_f32_kernel(
+    float* out, const float* __restrict__ z, const float* __restrict__ w, float eps,
+    long long rows, long long rows_per_seq, const int32_t* slots, int num_slots) {
+  const long long r = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (r >= rows) return;
+  if (slots) {
+    const int s = slots[r / rows_per_seq];
+    if (s < 0 || s >= num_slots) return;           // a skipped batch entry keeps its rows
+  }
+  float4* o4 = reinterpret_cast<float4*>(out + r * D) + lane;
+  const float4 o = *o4;
+  const float4 zz = reinterpret_cast<const float4*>(z + r * D)[lane];
+  const float4 ww = reinterpret_cast<const float4*>(w)[lane];
+  const float ss = warp_sum(o.x * o.x + o.y * o.y + o.z * o.z + o.w * o.w);
+  const float inv = rsqrtf(ss * (1.0f / D) + eps);
+  float4 y;
+  y.x = ww.x * (o.x * inv) * silu_gate(zz.x);
+  y.y = ww.y * (o.y * inv) * silu_gate(zz.y);
+  y.z = ww.z * (o.z * inv) * silu_gate(zz.z);
+  y.w = ww.w * (o.w * inv) * silu_gate(zz.w);
+  *o4 = y;
+}
+
+cudaError_t gdn_launch_gated_norm_f32(float* out, const float* z, const float* w, float eps,
+                                      int B, long long rows_per_seq, const int32_t* slots,
+                                      int num_slots, cudaStream_t stream) {
+  const long long rows = (long long)B * rows_per_seq;
+  if (rows == 0) return cudaSuccess;
+  const long long blocks = (rows + 7) / 8;
+  if (blocks > 0x7fffffffLL) return cudaErrorInvalidValue;
+  gdn_gated_norm_f32_kernel<<<(unsigned)blocks, 256, 0, stream>>>(out, z, w, eps, rows,
+                                                                  rows_per_seq, slots, num_slots);
+  return cudaGetLastError();
+}

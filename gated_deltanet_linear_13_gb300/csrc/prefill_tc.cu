@@ -95,6 +95,10 @@ struct TcParams {
   // to bank row snap_slots[b * n_snap + n / se_c - 1]; se_c == 0: none
   int se_c, n_snap, n_snap_slots;
   const int32_t* snap_slots;
+  // gated RMS norm of the output (the gate z arrives by TMA): out = w o / rms(o) silu(z)
+  int gate;
+  const float* gw;
+  float geps;
 };
 
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
@@ -552,6 +556,54 @@ __global__ void __launch_bounds__(LGT, 3)
   }
 }
 
+// One level of a transposing warp reduction: lanes with bit M set keep the upper half of
+// s[0, L) and send the lower half to lane ^ M, the others the reverse; afterwards s[0, L/2)
+// holds the sums of the kept half.
+template <int M, int L>
+__device__ __forceinline__ void butterfly_half(float (&s)[32], int lane) {
+  const bool up = lane & M;
+#pragma unroll
+  for (int i = 0; i < L / 2; ++i) {
+    const float send = up ? s[i] : s[i + L / 2];
+    const float keep = up ? s[i + L / 2] : s[i];
+    s[i] = keep + __shfl_xor_sync(0xffffffffu, send, M);
+  }
+}
+
+// SiLU of the output gate: for a bf16 output z sigmoid(z) = z (1 + tanh(z / 2)) / 2 with the
+// hardware tanh (one special-function op, relative error ~2^-11, below the output's rounding);
+// for an fp32 output the exponential and division form.
+template <typename Tout> __device__ __forceinline__ float silu_out(float z);
+template <> __device__ __forceinline__ float silu_out<__nv_bfloat16>(float z) {
+  float t;
+  asm("tanh.approx.f32 %0, %1;\n" : "=f"(t) : "f"(0.5f * z));
+  const float hz = 0.5f * z;
+  return fmaf(hz, t, hz);
+}
+template <> __device__ __forceinline__ float silu_out<float>(float z) { return silu_gate(z); }
+
+// A warp's 32 rows x 64 tokens of output (v[t] = row lane, token t) through its staging block
+// [ROWS tokens][32 rows] to HBM, one TMA store of ROWS tokens per pass; lane 0 issues the
+// stores and waits for the previous pass's read of the block.
+template <typename Tout, int ROWS>
+__device__ __forceinline__ void store_tile_passes(const CUtensorMap* tm, Tout* stg,
+                                                  const float (&v)[64], int lane, int c0,
+                                                  int tok0, int b) {
+#pragma unroll
+  for (int pass = 0; pass < 64 / ROWS; ++pass) {
+    if (lane == 0) tma_store_wait_read();
+    __syncwarp();
+#pragma unroll
+    for (int jj = 0; jj < ROWS; ++jj) stg[jj * 32 + lane] = from_float<Tout>(v[pass * ROWS + jj]);
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) {
+      tma_store_3d(tm, smem_addr(stg), c0, tok0 + pass * ROWS, b);
+      tma_store_commit();
+    }
+  }
+}
+
 // ======================================================================= chain kernel
 // One CTA per (value head h, sequence b): eight epilogue warps (warp w: TMEM lane quarter
 // w % 4, column half w / 4), one issuer warp, one elected lane of which issues every copy
@@ -571,8 +623,12 @@ __global__ void __launch_bounds__(LGT, 3)
 // once the output MMAs are done.
 constexpr uint32_t CH_BUF = 96 * KB;            // unit tiles (80 KB) + V [2][64][128 B] (16 KB)
 constexpr uint32_t CH_V = 80 * KB;
-constexpr uint32_t CH_OUT = 2 * CH_BUF;         // output staging, 4 KB per store warp
-constexpr uint32_t CH_MISC = CH_OUT + 16 * KB;  // e^{G_C} of the slice (2 KB), barriers
+// output staging: 2 KB per store warp with the gated norm, else 4 KB (over the gate tiles)
+constexpr uint32_t CH_OUT = 2 * CH_BUF;
+constexpr uint32_t CH_Z = CH_OUT + 8 * KB;      // gate tiles z [64 tokens][32 d_v], 4 KB per store warp
+constexpr uint32_t CH_SQ = CH_Z + 16 * KB;      // per-token sums of squares [2][4 warps][64]
+constexpr uint32_t CH_RI = CH_SQ + 2 * KB;      // per-token 1 / rms, [4 warps][64]
+constexpr uint32_t CH_MISC = CH_RI + KB;        // e^{G_C} of the slice (2 KB), barriers
 constexpr uint32_t CH_SMEM = CH_MISC + 3 * KB + KB;
 constexpr int CH_EPI = 256;                     // epilogue threads
 constexpr int CH_ISSUER = CH_EPI / 32;          // the issuer warp
@@ -588,7 +644,8 @@ __global__ void __launch_bounds__(CH_THREADS, 1)
     gdn_chunk_chain_kernel(const __grid_constant__ CUtensorMap tm_v,
                            const __grid_constant__ CUtensorMap tm_o,
                            const __grid_constant__ CUtensorMap tm_s,
-                           const __grid_constant__ CUtensorMap tm_snap, const TcParams p) {
+                           const __grid_constant__ CUtensorMap tm_snap,
+                           const __grid_constant__ CUtensorMap tm_z, const TcParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
   const uint32_t sb = smem_addr(sm);
@@ -602,8 +659,8 @@ __global__ void __launch_bounds__(CH_THREADS, 1)
   }
   float* sEgc = reinterpret_cast<float*>(sm + CH_MISC);
   uint64_t* barmem = reinterpret_cast<uint64_t*>(sm + CH_MISC + 2048);
-  uint32_t* sTmem = reinterpret_cast<uint32_t*>(sm + CH_MISC + 2048 + 128);
-  volatile int* sAbort = reinterpret_cast<volatile int*>(sm + CH_MISC + 2048 + 132);
+  uint32_t* sTmem = reinterpret_cast<uint32_t*>(sm + CH_MISC + 2048 + 256);
+  volatile int* sAbort = reinterpret_cast<volatile int*>(sm + CH_MISC + 2048 + 260);
   const uint32_t bar_ld0 = smem_addr(&barmem[0]), bar_ld1 = smem_addr(&barmem[1]);
   const uint32_t bar_u = smem_addr(&barmem[2]);     // MMA: U^T += S0 (-W)^T done (and all before)
   const uint32_t bar_s = smem_addr(&barmem[3]);     // MMA: S += U^T K~ done (and all before)
@@ -615,6 +672,8 @@ __global__ void __launch_bounds__(CH_THREADS, 1)
   const uint32_t bar_p0 = smem_addr(&barmem[8]), bar_p1 = smem_addr(&barmem[9]);   // P copies
   // store warps: the output tile of a TMEM output buffer has been read out
   const uint32_t bar_r0 = smem_addr(&barmem[11]), bar_r1 = smem_addr(&barmem[12]);
+  // store warps, gated norm: barmem[13 + w] = gate tile of store warp w landed;
+  // barmem[17 + (chunk & 1)] = the four warps' sums of squares written (every lane arrives)
   const size_t u0 = ((size_t)b * p.Hv + h) * p.ns;  // first unit of this head's slice
   const bool issuer_warp = (warp == CH_ISSUER);
 
@@ -638,8 +697,9 @@ __global__ void __launch_bounds__(CH_THREADS, 1)
   // per buffer (issuer warp): chunk of the main / P copy issued and not yet waited for, or -1
   int ld_chunk[2] = {-1, -1}, lp_chunk[2] = {-1, -1};
   if (tid == CH_EPI) {
-    for (int i = 0; i < 13; ++i)
-      mbar_init(smem_addr(&barmem[i]), (i == 6 || i == 7) ? CH_EPI / 32 : (i >= 11 ? 4 : 1));
+    for (int i = 0; i < 19; ++i)
+      mbar_init(smem_addr(&barmem[i]), (i == 6 || i == 7) ? CH_EPI / 32
+                                       : (i == 11 || i == 12) ? 4 : (i >= 17 ? 128 : 1));
     *sAbort = 0;
     fence_mbar_init();
   }
@@ -919,14 +979,35 @@ __global__ void __launch_bounds__(CH_THREADS, 1)
   } else {
     // ======================= store warps: the output tile of each chunk (O^T in TMEM: lane =
     // d_v index, column = token).  Warp w reads TMEM lane quarter w % 4, i.e. 32 d_v rows x 64
-    // tokens, tells the issuer that the buffer is free, then sends the rows through its 4 KB
-    // staging block [token][32 d_v] with one TMA store per pass (the store clips the rows
-    // past the sequence end).  Lane 0 issues the stores and is the one that waits for their
-    // reads.
-    constexpr int OUT_ROWS = (int)(4 * KB / (32 * sizeof(Tout)));   // tokens per pass
+    // tokens, tells the issuer that the buffer is free, optionally applies the gated RMS norm,
+    // then sends the rows through its staging block [token][32 d_v] (2 KB with the norm, whose
+    // gate tiles take the rest of the area, else 4 KB) with one TMA store per pass (the store
+    // clips the rows past the sequence end).  Lane 0 issues the copies and is the one that
+    // waits for their reads.
+    const int sw = warp - CH_STORE;
     const int q = warp & 3;
     const uint32_t lq = static_cast<uint32_t>(q * 32) << 16;
-    Tout* stg = reinterpret_cast<Tout*>(sm + CH_OUT + (warp - CH_STORE) * 4 * KB);
+    Tout* stg = reinterpret_cast<Tout*>(sm + CH_OUT + sw * (p.gate ? 2 : 4) * KB);
+    // gated norm: this warp's gate tile z [64 tokens][32 d_v] (bf16, one TMA copy per chunk,
+    // a chunk ahead), the four warps' per-token partial sums of squares, this lane's weight
+    const uint32_t zst = sb + CH_Z + sw * 4 * KB;
+    const __nv_bfloat16* zs = reinterpret_cast<const __nv_bfloat16*>(sm + CH_Z + sw * 4 * KB);
+    float* sqp = reinterpret_cast<float*>(sm + CH_SQ);
+    float* rinv = reinterpret_cast<float*>(sm + CH_RI) + sw * 64;
+    const uint32_t bar_zw = smem_addr(&barmem[13 + sw]);
+    const float wgt = p.gate ? p.gw[32 * q + lane] : 0.f;
+    int z_chunk = -1;                                  // gate copy in flight, or -1
+    auto load_z = [&](int nl) {
+      if (lane == 0) {
+        fence_proxy_async_smem();                      // after this warp's reads of the tile
+        mbar_arrive_expect_tx(bar_zw, 4 * KB);
+        tma_load_3d(zst, &tm_z, h * D + 32 * q, (p.n0 + nl) * C, b, bar_zw);
+        // and the tile after it into L2, so that its own copy is an L2 hit
+        if (nl + 1 < p.ns) tma_prefetch_l2_3d(&tm_z, h * D + 32 * q, (p.n0 + nl + 1) * C, b);
+      }
+      z_chunk = nl;
+    };
+    if (p.gate && p.ns > 0) load_z(0);
     bool ok = true;
     for (int nl = 0; nl < p.ns; ++nl) {
       if (!__all_sync(0xffffffffu, mbar_wait_or_abort((nl & 1) ? bar_o1 : bar_o0,
@@ -942,25 +1023,72 @@ __global__ void __launch_bounds__(CH_THREADS, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive((nl & 1) ? bar_r1 : bar_r0);
+      if (p.gate) {
+        // per-token sums of squares over this warp's 32 rows: a transposing butterfly leaves
+        // lane l with the sums of tokens 2l and 2l + 1; the four warps meet at a barrier
+        float s2[32];
+        {
+          const bool up = lane & 16;
 #pragma unroll
-      for (int pass = 0; pass < 64 / OUT_ROWS; ++pass) {
-        if (lane == 0) tma_store_wait_read();
-        __syncwarp();
-#pragma unroll
-        for (int jj = 0; jj < OUT_ROWS; ++jj)
-          stg[jj * 32 + lane] = from_float<Tout>(v[pass * OUT_ROWS + jj]);
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) {
-          tma_store_3d(&tm_o, smem_addr(stg), h * D + 32 * q, (p.n0 + nl) * C + pass * OUT_ROWS,
-                       b);
-          tma_store_commit();
+          for (int i = 0; i < 32; ++i) {
+            const float lo = v[i] * v[i], hi = v[i + 32] * v[i + 32];
+            s2[i] = (up ? hi : lo) + __shfl_xor_sync(0xffffffffu, up ? lo : hi, 16);
+          }
         }
+        butterfly_half<8, 32>(s2, lane);
+        butterfly_half<4, 16>(s2, lane);
+        butterfly_half<2, 8>(s2, lane);
+        butterfly_half<1, 4>(s2, lane);
+        float* sqb = sqp + (nl & 1) * 256;
+        *reinterpret_cast<float2*>(sqb + q * 64 + 2 * lane) = make_float2(s2[0], s2[1]);
+        const uint32_t bsq = smem_addr(&barmem[17 + (nl & 1)]);
+        mbar_arrive(bsq);
+        if (!__all_sync(0xffffffffu, mbar_wait_or_abort(bsq, (nl >> 1) & 1, sAbort) &&
+                                         mbar_wait_or_abort(bar_zw, nl & 1, sAbort))) {
+          ok = false;
+          break;
+        }
+        z_chunk = -1;
+        float tot0 = 0.f, tot1 = 0.f;
+#pragma unroll
+        for (int w4 = 0; w4 < 4; ++w4) {
+          const float2 pp = *reinterpret_cast<const float2*>(sqb + w4 * 64 + 2 * lane);
+          tot0 += pp.x;
+          tot1 += pp.y;
+        }
+        // this lane's two tokens' 1 / rms, then all 64 back as broadcast vector loads
+        *reinterpret_cast<float2*>(rinv + 2 * lane) =
+            make_float2(rsqrtf(tot0 * (1.0f / D) + p.geps), rsqrtf(tot1 * (1.0f / D) + p.geps));
+        __syncwarp();
+#pragma unroll
+        for (int t4 = 0; t4 < 16; ++t4) {
+          const float4 r4 = reinterpret_cast<const float4*>(rinv)[t4];
+          const float rr[4] = {r4.x, r4.y, r4.z, r4.w};
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const int t = 4 * t4 + u;
+            const float zt = __bfloat162float(zs[t * 32 + lane]);
+            v[t] = wgt * (v[t] * rr[u]) * silu_out<Tout>(zt);
+          }
+        }
+        __syncwarp();
+        if (nl + 1 < p.ns) load_z(nl + 1);
       }
+      const int tok0 = (p.n0 + nl) * C;
+      if (p.gate)
+        store_tile_passes<Tout, (int)(2 * KB / (32 * sizeof(Tout)))>(&tm_o, stg, v, lane,
+                                                                     h * D + 32 * q, tok0, b);
+      else
+        store_tile_passes<Tout, (int)(4 * KB / (32 * sizeof(Tout)))>(&tm_o, stg, v, lane,
+                                                                     h * D + 32 * q, tok0, b);
     }
     // everything this kernel writes has been issued: a kernel after it may start its set-up
     pdl_trigger();
-    if (lane == 0) tma_store_wait_read();
+    if (lane == 0) {
+      tma_store_wait_read();
+      // a gate copy issued ahead of a chunk that an abort left unprocessed must land first
+      if (z_chunk >= 0) mbar_wait_bounded(bar_zw, z_chunk & 1, 1u << 16);
+    }
     if (!ok) *sAbort = 1;
   }
   if (tid == CH_EPI) {
@@ -997,7 +1125,8 @@ int slice_chunks(int B, int Hv, int nch) {
 template <typename Tout>
 cudaError_t launch_tc_t(const GdnLayerArgs& L, cudaStream_t stream) {
   CUtensorMap mq, mk, mv, mo, ms;
-  constexpr int out_rows = (int)(4 * KB / (32 * sizeof(Tout)));
+  // tokens per output store: a 2 KB staging block with the gated norm, else 4 KB
+  const int out_rows = (int)((L.gate ? 2 : 4) * KB / (32 * sizeof(Tout)));
   const bool ok =
       gdn_make_map(&mq, L.q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, L.Hk * D, L.T, L.B, L.q_tok_stride,
                64, 64, true) &&
@@ -1012,6 +1141,12 @@ cudaError_t launch_tc_t(const GdnLayerArgs& L, cudaStream_t stream) {
       gdn_make_map(&ms, L.state, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, D,
                    L.num_slots * L.Hv * D, 1, D, 32, 32, true);
   if (!ok) return cudaErrorInvalidValue;
+  // the output gate z [B][T][Hv d] bf16: box = 32 channels x 64 tokens (the V map stands in
+  // when there is no gate)
+  CUtensorMap mz = mv;
+  if (L.gate && !gdn_make_map(&mz, L.gate_z, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, L.Hv * D, L.T,
+                              L.B, (long long)L.Hv * D, 32, 64, false))
+    return cudaErrorInvalidValue;
   // the snapshot bank, the same way (the state map stands in when nothing is recorded)
   CUtensorMap msn = ms;
   const bool snaps = L.snap_every > 0 && L.n_snap > 0;
@@ -1043,6 +1178,9 @@ cudaError_t launch_tc_t(const GdnLayerArgs& L, cudaStream_t stream) {
   p.n_snap = snaps ? L.n_snap : 0;
   p.n_snap_slots = snaps ? L.num_snap_slots : 0;
   p.snap_slots = snaps ? L.snap_slots : nullptr;
+  p.gate = L.gate;
+  p.gw = L.gate_w;
+  p.geps = L.gate_eps;
   for (int n0 = 0; n0 < nch; n0 += ns_max) {
     p.n0 = n0;
     p.ns = nch - n0 < ns_max ? nch - n0 : ns_max;
@@ -1053,7 +1191,7 @@ cudaError_t launch_tc_t(const GdnLayerArgs& L, cudaStream_t stream) {
                    mq, mk, p);
     if (e != cudaSuccess) return e;
     e = launch_pdl(true, gdn_chunk_chain_kernel<Tout>, dim3((unsigned)(L.B * L.Hv)), dim3(CH_THREADS),
-                   CH_SMEM, stream, mv, mo, ms, msn, p);
+                   CH_SMEM, stream, mv, mo, ms, msn, mz, p);
     if (e != cudaSuccess) return e;
   }
   return cudaSuccess;

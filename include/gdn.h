@@ -188,6 +188,44 @@ gdn_status gdn_state_checkpoint(int32_t op, const gdn_dims* dims, gdn_dtype conv
                                 void* stream);
 
 /*
+ * Optional gated RMS norm fused into the output of gdn_chunk_prefill_gated and
+ * gdn_decode_step_gated.  Definition: the model card (section "How It Works") lists an RMS norm
+ * among the operations that run around the kernel, without a formula; this is the gated form
+ * these layers use, per (token, value head) output vector o of length d:
+ *     out_i = weight_i * o_i / sqrt(mean_j(o_j^2) + eps) * silu(z_i),  silu(z) = z sigmoid(z),
+ * computed in fp32 and rounded once to out_dtype.  `weight` is the effective per-channel
+ * factor: a checkpoint storing weight - 1 (the "RMSNorm +1 conversion" of PR #164 "Add
+ * Qwen3.6-27B contrib model with vLLM APC baseline", "Unit Coverage") is converted by the
+ * caller.
+ */
+typedef struct {
+  const void* z;          /* [B, T, Hv, d] in in_dtype, 16-byte aligned: the output gate */
+  const float* weight;    /* [d] fp32 */
+  float eps;              /* >= 0, inside the square root (e.g. 1e-6) */
+} gdn_out_gate;
+
+/*
+ * gdn_chunk_prefill_gated / gdn_decode_step_gated -- gdn_chunk_prefill / gdn_decode_step with
+ * the gated RMS norm above applied to every output vector before it is stored (the plain
+ * output is never written).  All other arguments, layouts, workspace and errors are those of
+ * the plain calls.  `gate` must be non-NULL with non-NULL z and weight, z 16-byte aligned and
+ * eps >= 0, else GDN_ERR_INVALID_ARGUMENT.  (For the decode step T = 1: z is [B, Hv, d].)
+ */
+gdn_status gdn_chunk_prefill_gated(const gdn_dims* dims, const gdn_opts* opts, const void* q,
+                                   const void* k, const void* v, const void* a, const void* b,
+                                   const float* A_log, const float* dt_bias,
+                                   const void* conv_weight, const void* conv_bias, float* state,
+                                   void* conv_state, const int32_t* state_slots, void* out,
+                                   const gdn_out_gate* gate, void* workspace,
+                                   size_t workspace_bytes, void* stream);
+gdn_status gdn_decode_step_gated(const gdn_dims* dims, const gdn_opts* opts, const void* q,
+                                 const void* k, const void* v, const void* a, const void* b,
+                                 const float* A_log, const float* dt_bias,
+                                 const void* conv_weight, const void* conv_bias, float* state,
+                                 void* conv_state, const int32_t* state_slots, void* out,
+                                 const gdn_out_gate* gate, void* stream);
+
+/*
  * gdn_chunk_prefill_snapshots -- gdn_chunk_prefill over a whole prompt in one call that also
  * records the recurrent and conv state every `snap_every` tokens, in-kernel.
  * Definition: the prefix checkpoints of hybrid automatic prefix caching (PR #164 "Hybrid APC

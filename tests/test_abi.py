@@ -39,7 +39,7 @@ def test_status_strings_and_version(L):
     for code, name in gdn.STATUS_NAMES.items():
         assert gdn.gdn_status_string(code) == name
     assert gdn.gdn_status_string(99) == "GDN_UNKNOWN_STATUS"
-    assert L.gdn_version() == 101
+    assert L.gdn_version() == 102
 
 
 def _dims(**kw):
@@ -90,6 +90,25 @@ def test_snapshot_prefill_rejects_bad_arguments(L):
     assert _snap(L, _dims(seqlen=256, head_dim=64), _opts(), 128) == 2
     # an empty batch is a no-op
     assert _snap(L, _dims(batch=0, seqlen=256), _opts(), 128) == 0
+
+
+def test_gated_entries_reject_bad_gate(L):
+    d = _dims()
+    g = gdn.GdnOutGate(A, A, 1e-6)
+    args = [ctypes.byref(d), ctypes.byref(_opts()), A, A, A, A, A, A, None, None, None, A, None,
+            None, A]
+    # a gate is required, with z and weight present and aligned and eps >= 0
+    for bad in (None, gdn.GdnOutGate(None, A, 1e-6), gdn.GdnOutGate(A + 4, A, 1e-6),
+                gdn.GdnOutGate(A, None, 1e-6), gdn.GdnOutGate(A, A + 2, 1e-6),
+                gdn.GdnOutGate(A, A, -1.0), gdn.GdnOutGate(A, A, float("nan"))):
+        ref = None if bad is None else ctypes.byref(bad)
+        assert L.gdn_chunk_prefill_gated(*args, ref, None, 0, None) == 1
+        dd = _dims(seqlen=1)
+        dargs = [ctypes.byref(dd)] + args[1:]
+        assert L.gdn_decode_step_gated(*dargs, ref, None) == 1
+    # the layer's own checks still come first
+    bad_dims = [ctypes.byref(_dims(head_dim=64))] + args[1:]
+    assert L.gdn_chunk_prefill_gated(*bad_dims, ctypes.byref(g), None, 0, None) == 2
 
 
 @pytest.mark.parametrize("field,value,status", [
