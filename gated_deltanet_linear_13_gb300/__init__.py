@@ -28,6 +28,7 @@ STATUS_NAMES = {0: "GDN_OK", 1: "GDN_ERR_INVALID_ARGUMENT", 2: "GDN_ERR_UNSUPPOR
 EXPORTED = ("gdn_prefill_workspace_size", "gdn_chunk_prefill", "gdn_decode_step",
             "causal_conv1d_update", "gdn_state_checkpoint", "gdn_chunk_prefill_noalloc",
             "gdn_chunk_prefill_snapshots", "gdn_chunk_prefill_gated", "gdn_decode_step_gated",
+            "gdn_prefill_varlen_workspace_size", "gdn_chunk_prefill_varlen",
             "gdn_get_device_error", "gdn_status_string", "gdn_version")
 NOALLOC_SCRATCH_BYTES = 64 << 20   # GDN_NOALLOC_SCRATCH_BYTES in include/gdn.h
 
@@ -83,6 +84,10 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     L.gdn_chunk_prefill_gated.argtypes = [dp, op] + [_vp] * 13 + [gp, _vp, ctypes.c_size_t, _vp]
     L.gdn_decode_step_gated.restype = ctypes.c_int
     L.gdn_decode_step_gated.argtypes = [dp, op] + [_vp] * 13 + [gp, _vp]
+    L.gdn_prefill_varlen_workspace_size.restype = ctypes.c_size_t
+    L.gdn_prefill_varlen_workspace_size.argtypes = [dp, op]
+    L.gdn_chunk_prefill_varlen.restype = ctypes.c_int
+    L.gdn_chunk_prefill_varlen.argtypes = [dp, op] + [_vp] * 14 + [gp, _vp, ctypes.c_size_t, _vp]
     L.gdn_chunk_prefill_noalloc.restype = ctypes.c_int
     L.gdn_chunk_prefill_noalloc.argtypes = [dp, op] + [_vp] * 13 + [_vp]
     L.gdn_decode_step.restype = ctypes.c_int
@@ -360,6 +365,62 @@ def gdn_chunk_prefill_gated(q, k, v, a, b, A_log, dt_bias, state, out, *, gate_z
                                    ctypes.byref(gate), _ptr(workspace), ws_bytes,
                                    _stream(stream))
     _check(st, "gdn_chunk_prefill_gated")
+    return out
+
+
+def gdn_prefill_varlen_workspace_size(num_seqs: int, total_tokens: int, num_k_heads: int,
+                                      num_v_heads: int, conv_width: int,
+                                      in_dtype=torch.bfloat16) -> int:
+    L = load_library()
+    dims = GdnDims(num_seqs, total_tokens, num_k_heads, num_v_heads, HEAD_DIM, 64, conv_width, 0)
+    dt = GDN_BF16 if in_dtype == torch.bfloat16 else GDN_F32
+    opts = _opts(dt, dt, 1, 1e-6, 1.0, 1, 0)
+    return int(L.gdn_prefill_varlen_workspace_size(ctypes.byref(dims), ctypes.byref(opts)))
+
+
+def gdn_chunk_prefill_varlen(q, k, v, a, b, A_log, dt_bias, state, out, *, cu_seqlens,
+                             num_k_heads=None, conv_weight=None, conv_bias=None,
+                             conv_state=None, state_slots=None, gate_z=None, gate_weight=None,
+                             gate_eps: float = 1e-6, scale: float = 1.0, eps: float = 1e-6,
+                             qk_l2norm: bool = True, conv_silu: bool = True,
+                             gates_precomputed: bool = False,
+                             workspace: Optional[torch.Tensor] = None,
+                             stream=None) -> torch.Tensor:
+    """Prefill of a packed variable-length batch (see gdn_chunk_prefill_varlen in
+    include/gdn.h): every tensor has the layout of a one-sequence call over all T packed
+    tokens ([1, T, ...]); sequence n is tokens cu_seqlens[n] .. cu_seqlens[n+1] - 1 and uses
+    state row state_slots[n] (or n).  Optional gated output norm (gate_z shaped like out)."""
+    L = load_library()
+    _, T, Hk, Hv, W, num_slots = _layer_dims(q, k, v, a, num_k_heads, conv_weight, conv_state,
+                                             state, None, None)
+    if a.shape[0] != 1:
+        raise ValueError("a packed batch has all its tokens in one row: a must be [1, T, Hv]")
+    N = cu_seqlens.numel() - 1
+    if N < 0:
+        raise ValueError("cu_seqlens needs N + 1 >= 1 entries")
+    _need(cu_seqlens, "cu_seqlens", (N + 1,), torch.int32, q.device)
+    if state_slots is None and num_slots < N:
+        raise ValueError("state has fewer rows than sequences and no state_slots given")
+    _check_layer(q, k, v, a, b, A_log, dt_bias, conv_weight, conv_bias, state, conv_state,
+                 None, out, 1, T, Hk, Hv, W, num_slots, gates_precomputed)
+    if state_slots is not None:
+        _need(state_slots, "state_slots", (N,), torch.int32, q.device)
+    gate = None
+    if gate_z is not None:
+        gate = _out_gate(gate_z, gate_weight, gate_eps, out, q.dtype)
+    dims = GdnDims(N, T, Hk, Hv, HEAD_DIM, 64, W, num_slots)
+    opts = _opts(_dt(q), _dt(out), qk_l2norm, eps, scale, conv_silu, gates_precomputed)
+    need = int(L.gdn_prefill_varlen_workspace_size(ctypes.byref(dims), ctypes.byref(opts)))
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
+    ws_bytes = workspace.numel() * workspace.element_size()
+    st = L.gdn_chunk_prefill_varlen(ctypes.byref(dims), ctypes.byref(opts), _ptr(q), _ptr(k),
+                                    _ptr(v), _ptr(a), _ptr(b), _ptr(A_log), _ptr(dt_bias),
+                                    _ptr(conv_weight), _ptr(conv_bias), _ptr(state),
+                                    _ptr(conv_state), _ptr(state_slots), _ptr(cu_seqlens),
+                                    _ptr(out), None if gate is None else ctypes.byref(gate),
+                                    _ptr(workspace), ws_bytes, _stream(stream))
+    _check(st, "gdn_chunk_prefill_varlen")
     return out
 
 

@@ -148,6 +148,13 @@ struct GdnLayerArgs {
   const void* gate_z;         // [B, T, Hv, d] in the input type
   const float* gate_w;        // [d]
   float gate_eps;
+  // packed variable-length batch (cu != nullptr): B sequences on one axis of T tokens,
+  // sequence n on [cu[n], cu[n+1]) (validated offsets), global chunks [ccs[n], ccs[n+1]),
+  // chunk table ctab[n_chunks] of int4 {first token, tokens, sequence, 0}
+  const int32_t* cu;
+  const int32_t* ccs;
+  const void* ctab;
+  int n_chunks;
 };
 
 // Workspace bytes the tensor-core prefill needs for B sequences of T tokens, Hv value heads.
@@ -173,6 +180,16 @@ cudaError_t gdn_launch_conv_snapshots(int B, int T, int row_bytes, long long x_t
                                       int rows, const void* x, int every, int n_snap,
                                       void* bank, int num_bank, const int32_t* slots,
                                       const int32_t* row_slots, cudaStream_t stream);
+// Packed variable-length batches: validate the offsets and lay out the chunk table (above).
+cudaError_t gdn_launch_varlen_prep(const int32_t* cu, int N, int T, int U, int32_t* cu_ok,
+                                   int32_t* ccs, void* ctab, cudaStream_t stream);
+// Conv of a packed batch (x, y: [T][C] with token strides), sequence n on [cu[n], cu[n+1]),
+// then its new conv states.
+cudaError_t gdn_launch_conv_varlen(int N, int T, int C, int W, int bf16, const int32_t* cu,
+                                   const void* x, long long x_tok_stride, const void* w,
+                                   const void* bias, void* conv_state, int num_slots,
+                                   const int32_t* slots, int silu, void* y,
+                                   long long y_tok_stride, cudaStream_t stream);
 cudaError_t gdn_launch_checkpoint(int op, int Hv, int d, int conv_elems, int conv_elem_bytes,
                                   float* state, void* conv_state, int num_rows,
                                   float* slot_state, void* slot_conv_state, int num_bank,
@@ -184,7 +201,8 @@ cudaError_t gdn_launch_checkpoint(int op, int Hv, int d, int conv_elems, int con
 // left alone.
 cudaError_t gdn_launch_gated_norm_f32(float* out, const float* z, const float* w, float eps,
                                       int B, long long rows_per_seq, const int32_t* slots,
-                                      int num_slots, cudaStream_t stream);
+                                      int num_slots, cudaStream_t stream,
+                                      const int32_t* cu = nullptr, int Hv = 0);
 
 // Per-translation-unit device error words: read and clear (host side, synchronous copy).
 unsigned gdn_take_error_decode();
@@ -192,3 +210,4 @@ unsigned gdn_take_error_conv();
 unsigned gdn_take_error_checkpoint();
 unsigned gdn_take_error_prefill_simt();
 unsigned gdn_take_error_prefill_tc();
+unsigned gdn_take_error_varlen();

@@ -219,3 +219,208 @@ cudaError_t gdn_launch_conv(int B, int T, int C, int W, int bf16, const void* x,
                          slots, silu, (float*)y, y_tok_stride);
   return cudaGetLastError();
 }
+
+// ======================================================================= packed sequences
+// Variable-length batches: N sequences packed back to back in x [T_total][C], sequence n on
+// tokens [cu[n], cu[n+1]) (cu validated by the prep kernel), each with its own conv-state
+// row.  The tile and the sliding window are those above; a thread finds the sequence of its
+// first token by bisection and, when its window crosses into the next sequence, restarts the
+// window from that sequence's old conv state.  The per-token arithmetic is the same as above,
+// so each sequence's outputs equal those of a call of its own, bit for bit.  The new conv
+// states are written by the kernel after this one (every old state is read here first).
+
+template <typename T, int H>
+__device__ __forceinline__ void conv_state_word(const T* cs, int C, int num_slots,
+                                                const int32_t* slots, int n, int idx, int c0,
+                                                float (&v)[8 / sizeof(T)]) {
+  const int slot = slots ? slots[n] : n;
+  if (slot < 0 || slot >= num_slots) {
+#pragma unroll
+    for (int e = 0; e < (int)(8 / sizeof(T)); ++e) v[e] = 0.f;
+    return;
+  }
+  ld_word(cs + ((size_t)slot * H + idx) * C + c0, v);
+}
+
+template <typename T, int W>
+__global__ void __launch_bounds__(CONV_THREADS, 3) gdn_conv_varlen_kernel(
+    const __grid_constant__ CUtensorMap tm_x, int N, int T_, int C, const int32_t* cu,
+    const T* w, const T* bias, const T* cs, int num_slots, const int32_t* slots, int silu,
+    T* y, long long ys) {
+  constexpr int CC = TILE_BYTES / (int)sizeof(T);
+  constexpr int CPT = 8 / (int)sizeof(T);
+  constexpr int H = W - 1;
+  __shared__ __align__(128) uint8_t tile[TILE_ROWS * TILE_BYTES];
+  __shared__ uint64_t bar;
+  const int t0 = blockIdx.x * TT, cb = blockIdx.y * CC;
+  const int tid = threadIdx.x;
+  pdl_trigger();
+  const int nt = min(TT, T_ - t0);
+  const uint32_t bar_a = smem_addr(&bar);
+  if (tid == 0) {
+    mbar_init(bar_a, 1);
+    fence_mbar_init();
+    mbar_arrive_expect_tx(bar_a, (uint32_t)((TT + H) * TILE_BYTES));
+    tma_load_3d(smem_addr(tile), &tm_x, cb, t0 - H, 0, bar_a);
+  }
+  const int wi = tid % WORDS, tg = tid / WORDS;
+  const int c0 = cb + wi * CPT;
+  float wt[W][CPT], bi[CPT];
+#pragma unroll
+  for (int e = 0; e < CPT; ++e) {
+    const bool ok = c0 + e < C;
+    bi[e] = (bias && ok) ? ld_elem(bias + c0 + e) : 0.f;
+#pragma unroll
+    for (int j = 0; j < W; ++j) wt[j][e] = ok ? ld_elem(w + (size_t)(c0 + e) * W + j) : 0.f;
+  }
+  __syncthreads();
+  if (!__syncthreads_and(mbar_wait_bounded(bar_a, 0))) {
+    if (tid == 0) atomicOr(&g_err_conv, kErrTimeout);
+    return;
+  }
+  const int tb = tg * TG;
+  const int tfirst = t0 + tb;
+  if (c0 >= C || tb >= nt || tfirst >= cu[N]) return;
+  // the sequence holding tfirst: cu[lo] <= tfirst < cu[lo + 1]
+  int lo = 0, hi = N;
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (cu[mid] <= tfirst) lo = mid; else hi = mid;
+  }
+  int n = lo, s0 = cu[n], s1 = cu[n + 1];
+  const T* col = reinterpret_cast<const T*>(tile) + wi * CPT;
+  float win[W][CPT];
+#pragma unroll
+  for (int i = 0; i < H; ++i) {
+    const int pos = tfirst - H + i;
+    if (pos >= s0) ld_word(col + (tb + i) * CC, win[i]);
+    else conv_state_word<T, H>(cs, C, num_slots, slots, n, pos - s0 + H, c0, win[i]);
+  }
+  T* yp = y + (size_t)tfirst * ys + c0;
+  const int cnt = min(TG, nt - tb);
+#pragma unroll
+  for (int t = 0; t < TG; ++t) {
+    if (t < cnt) {
+      const int tt = tfirst + t;
+      if (tt >= s1) {
+        // the next non-empty sequence starts at tt: its window history is its conv state
+        while (tt >= s1 && n < N - 1) {
+          ++n;
+          s0 = s1;
+          s1 = cu[n + 1];
+        }
+#pragma unroll
+        for (int i = 0; i < H; ++i) conv_state_word<T, H>(cs, C, num_slots, slots, n, i, c0, win[i]);
+      }
+      ld_word(col + (tb + t + H) * CC, win[H]);
+      float out[CPT];
+#pragma unroll
+      for (int e = 0; e < CPT; ++e) {
+        float acc = bi[e];
+#pragma unroll
+        for (int j = 0; j < W; ++j) acc = fmaf(wt[j][e], win[j][e], acc);
+        out[e] = silu ? silu_fast(acc) : acc;
+      }
+      st_word(yp, out);
+      yp += ys;
+#pragma unroll
+      for (int j = 0; j < H; ++j)
+#pragma unroll
+        for (int e = 0; e < CPT; ++e) win[j][e] = win[j + 1][e];
+    }
+  }
+}
+
+// New conv state of each packed sequence: its last W-1 inputs, the older ones from its old
+// state when it is shorter than W-1.  One CTA per sequence; a thread owns whole words.
+template <typename T, int W>
+__global__ void __launch_bounds__(256) gdn_conv_state_varlen_kernel(
+    int N, int C, const int32_t* cu, const T* x, long long xs, T* cs, int num_slots,
+    const int32_t* slots) {
+  constexpr int CPT = 8 / (int)sizeof(T);
+  constexpr int H = W - 1;
+  pdl_wait();
+  const int n = blockIdx.x;
+  const int slot = slots ? slots[n] : n;
+  if (slot < 0) return;
+  if (slot >= num_slots) {
+    if (threadIdx.x == 0) atomicOr(&g_err_conv, kErrIndex);
+    return;
+  }
+  const int s0 = cu[n], s1 = cu[n + 1];
+  T* csn = cs + (size_t)slot * H * C;
+  for (int c0 = threadIdx.x * CPT; c0 < C; c0 += blockDim.x * CPT) {
+    float old[H > 0 ? H : 1][CPT], nst[H > 0 ? H : 1][CPT];
+#pragma unroll
+    for (int i = 0; i < H; ++i) ld_word(csn + (size_t)i * C + c0, old[i]);
+#pragma unroll
+    for (int i = 0; i < H; ++i) {
+      const int pos = s1 - H + i;
+      if (pos >= s0) {
+        ld_word(x + (size_t)pos * xs + c0, nst[i]);
+      } else {
+#pragma unroll
+        for (int j = 0; j < H; ++j)
+          if (j == pos - s0 + H) {
+#pragma unroll
+            for (int e = 0; e < CPT; ++e) nst[i][e] = old[j][e];
+          }
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < H; ++i) st_word(csn + (size_t)i * C + c0, nst[i]);
+  }
+}
+
+template <typename T, int W>
+static cudaError_t launch_conv_varlen_w(const CUtensorMap& m, int N, int Tn, int C,
+                                        const int32_t* cu, const T* x, long long xs, const T* w,
+                                        const T* bias, T* cs, int ns, const int32_t* slots,
+                                        int silu, T* y, long long ys, cudaStream_t stream) {
+  static unsigned done = 0;
+  cudaError_t e = set_carveout_once(gdn_conv_varlen_kernel<T, W>, 100, &done);
+  if (e != cudaSuccess) return e;
+  constexpr int cc = TILE_BYTES / (int)sizeof(T);
+  dim3 grid((unsigned)((Tn + TT - 1) / TT), (unsigned)((C + cc - 1) / cc), 1);
+  gdn_conv_varlen_kernel<T, W><<<grid, CONV_THREADS, 0, stream>>>(m, N, Tn, C, cu, w, bias, cs,
+                                                                   ns, slots, silu, y, ys);
+  e = cudaGetLastError();
+  if (e != cudaSuccess || W < 2) return e;
+  return launch_pdl(true, gdn_conv_state_varlen_kernel<T, W>, dim3((unsigned)N), dim3(256), 0,
+                    stream, N, C, cu, x, xs, cs, ns, slots);
+}
+
+template <typename T>
+static cudaError_t launch_conv_varlen_t(const CUtensorMap& m, int N, int Tn, int C, int W,
+                                        const int32_t* cu, const T* x, long long xs, const T* w,
+                                        const T* bias, T* cs, int ns, const int32_t* slots,
+                                        int silu, T* y, long long ys, cudaStream_t stream) {
+  switch (W) {
+    case 1: return launch_conv_varlen_w<T, 1>(m, N, Tn, C, cu, x, xs, w, bias, cs, ns, slots, silu, y, ys, stream);
+    case 2: return launch_conv_varlen_w<T, 2>(m, N, Tn, C, cu, x, xs, w, bias, cs, ns, slots, silu, y, ys, stream);
+    case 3: return launch_conv_varlen_w<T, 3>(m, N, Tn, C, cu, x, xs, w, bias, cs, ns, slots, silu, y, ys, stream);
+    default: return launch_conv_varlen_w<T, 4>(m, N, Tn, C, cu, x, xs, w, bias, cs, ns, slots, silu, y, ys, stream);
+  }
+}
+
+cudaError_t gdn_launch_conv_varlen(int N, int T, int C, int W, int bf16, const int32_t* cu,
+                                   const void* x, long long x_tok_stride, const void* w,
+                                   const void* bias, void* conv_state, int num_slots,
+                                   const int32_t* slots, int silu, void* y,
+                                   long long y_tok_stride, cudaStream_t stream) {
+  if (N == 0 || T == 0) return cudaSuccess;
+  if (W < 1 || W > 4) return cudaErrorInvalidValue;
+  const int eb = bf16 ? 2 : 4, cc = TILE_BYTES / eb;
+  CUtensorMap m;
+  if (!gdn_make_map(&m, x, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
+                    eb, C, T, 1, x_tok_stride, cc, TT + W - 1, false))
+    return cudaErrorInvalidValue;
+  if (bf16)
+    return launch_conv_varlen_t<__nv_bfloat16>(
+        m, N, T, C, W, cu, (const __nv_bfloat16*)x, x_tok_stride, (const __nv_bfloat16*)w,
+        (const __nv_bfloat16*)bias, (__nv_bfloat16*)conv_state, num_slots, slots, silu,
+        (__nv_bfloat16*)y, y_tok_stride, stream);
+  return launch_conv_varlen_t<float>(m, N, T, C, W, cu, (const float*)x, x_tok_stride,
+                                     (const float*)w, (const float*)bias, (float*)conv_state,
+                                     num_slots, slots, silu, (float*)y, y_tok_stride, stream);
+}

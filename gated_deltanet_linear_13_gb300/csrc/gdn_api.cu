@@ -7,7 +7,7 @@
 
 namespace {
 
-constexpr int32_t kVersion = 102;
+constexpr int32_t kVersion = 103;
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
@@ -107,6 +107,31 @@ size_t workspace_bytes_for(const Checked& c, const gdn_opts* o) {
   size_t n = conv_bytes_for(c);
   if (o->in_dtype == GDN_BF16) n += gdn_prefill_tc_scratch_bytes(c.B, c.T, c.Hv);
   return n;
+}
+
+// Workspace of a packed variable-length call: [post-conv activations of the T tokens]
+// [validated offsets, chunk offsets (N+1 int32 each), chunk table (U int4)][tensor-core
+// tiles for a slice of U chunks], U = ceil(T / 64) + N bounding the chunk count.
+struct VarlenLayout {
+  size_t cu_ok, ccs, ctab, tc, total;
+  int U;
+};
+VarlenLayout varlen_layout(const Checked& c, const gdn_opts* o) {
+  auto up = [](size_t n) { return (n + 255) & ~(size_t)255; };
+  VarlenLayout v;
+  v.U = (c.T + gdn::kChunk - 1) / gdn::kChunk + c.B;
+  size_t off = 0;
+  if (c.W > 0) off = ((size_t)c.T * c.Cc * c.in_elem + 1023) & ~(size_t)1023;
+  v.cu_ok = off;
+  off += up(sizeof(int32_t) * ((size_t)c.B + 1));
+  v.ccs = off;
+  off += up(sizeof(int32_t) * ((size_t)c.B + 1));
+  v.ctab = off;
+  off += up((size_t)16 * v.U);
+  v.tc = off;
+  if (o->in_dtype == GDN_BF16) off += gdn_prefill_tc_scratch_bytes(1, v.U * gdn::kChunk, c.Hv);
+  v.total = off;
+  return v;
 }
 
 // Copies a valid output gate into L (gate may be NULL: no norm).
@@ -260,6 +285,68 @@ gdn_status gdn_chunk_prefill_snapshots(const gdn_dims* dims, const gdn_opts* opt
                       stream);
 }
 
+size_t gdn_prefill_varlen_workspace_size(const gdn_dims* dims, const gdn_opts* opts) {
+  Checked c;
+  if (check_dims(dims, opts, false, &c) != GDN_OK) return 0;
+  return varlen_layout(c, opts).total;
+}
+
+gdn_status gdn_chunk_prefill_varlen(const gdn_dims* dims, const gdn_opts* opts, const void* q,
+                                    const void* k, const void* v, const void* a, const void* b,
+                                    const float* A_log, const float* dt_bias,
+                                    const void* conv_weight, const void* conv_bias,
+                                    float* state, void* conv_state, const int32_t* state_slots,
+                                    const int32_t* cu_seqlens, void* out,
+                                    const gdn_out_gate* gate, void* workspace,
+                                    size_t workspace_bytes, void* stream) {
+  Checked c;
+  gdn_status st = check_dims(dims, opts, false, &c);
+  if (st != GDN_OK) return st;
+  if (!cu_seqlens || !aligned4(cu_seqlens)) return GDN_ERR_INVALID_ARGUMENT;
+  if (c.B == 0 || c.T == 0) return GDN_OK;
+  GdnLayerArgs L;
+  st = check_layer_ptrs(c, opts, q, k, v, a, b, A_log, dt_bias, conv_weight, conv_bias, state,
+                        conv_state, state_slots, out, &L);
+  if (st != GDN_OK) return st;
+  st = set_gate(gate, false, &L);
+  if (st != GDN_OK) return st;
+  const VarlenLayout lay = varlen_layout(c, opts);
+  if (!workspace || workspace_bytes < lay.total || !aligned16(workspace))
+    return GDN_ERR_WORKSPACE;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  char* ws = static_cast<char*>(workspace);
+  int32_t* cu_ok = reinterpret_cast<int32_t*>(ws + lay.cu_ok);
+  int32_t* ccs = reinterpret_cast<int32_t*>(ws + lay.ccs);
+  cudaError_t e = gdn_launch_varlen_prep(cu_seqlens, c.B, c.T, lay.U, cu_ok, ccs, ws + lay.ctab, s);
+  if (e != cudaSuccess) return GDN_ERR_CUDA;
+  if (c.W > 0) {
+    // conv (+SiLU) of the packed tokens into the workspace, every sequence's conv state
+    e = gdn_launch_conv_varlen(c.B, c.T, c.Cc, c.W, L.in_bf16, cu_ok, q, c.Cc, conv_weight,
+                               conv_bias, conv_state, c.num_slots, state_slots, L.silu, ws,
+                               c.Cc, s);
+    if (e != cudaSuccess) return GDN_ERR_CUDA;
+    L.q = ws;
+    L.k = ws + (size_t)c.Hk * gdn::kHeadDim * c.in_elem;
+    L.v = ws + (size_t)2 * c.Hk * gdn::kHeadDim * c.in_elem;
+    L.q_tok_stride = L.k_tok_stride = L.v_tok_stride = c.Cc;
+  }
+  L.cu = cu_ok;
+  L.ccs = ccs;
+  L.ctab = ws + lay.ctab;
+  L.n_chunks = lay.U;
+  L.scratch = L.in_bf16 ? ws + lay.tc : nullptr;
+  L.scratch_bytes = lay.total - lay.tc;
+  e = L.in_bf16 ? gdn_launch_prefill_tc(L, s) : gdn_launch_prefill_simt(L, s);
+  if (e != cudaSuccess) return GDN_ERR_CUDA;
+  if (L.gate && !L.in_bf16) {
+    e = gdn_launch_gated_norm_f32(static_cast<float*>(out), static_cast<const float*>(L.gate_z),
+                                  L.gate_w, L.gate_eps, c.B, (long long)c.T * c.Hv, state_slots,
+                                  c.num_slots, s, cu_ok, c.Hv);
+    if (e != cudaSuccess) return GDN_ERR_CUDA;
+  }
+  return GDN_OK;
+}
+
 // gdn_decode_step, with the output gate when `gated`
 static gdn_status decode_impl(const gdn_dims* dims, const gdn_opts* opts, const void* q,
                               const void* k, const void* v, const void* a, const void* b,
@@ -359,7 +446,8 @@ gdn_status gdn_state_checkpoint(int32_t op, const gdn_dims* dims, gdn_dtype conv
 gdn_status gdn_get_device_error(void* stream) {
   if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return GDN_ERR_CUDA;
   unsigned bits = gdn_take_error_decode() | gdn_take_error_conv() | gdn_take_error_checkpoint() |
-                  gdn_take_error_prefill_simt() | gdn_take_error_prefill_tc();
+                  gdn_take_error_prefill_simt() | gdn_take_error_prefill_tc() |
+                  gdn_take_error_varlen();
   if (cudaGetLastError() != cudaSuccess) return GDN_ERR_CUDA;
   if (bits & gdn::kErrTimeout) return GDN_ERR_DEVICE_TIMEOUT;
   if (bits & gdn::kErrIndex) return GDN_ERR_DEVICE_INDEX;

@@ -68,9 +68,12 @@ __global__ void __launch_bounds__(THREADS) gdn_prefill_simt_kernel(GdnLayerArgs 
     if (tid == 0 && sp == 0) atomicOr(&g_err_simt, kErrIndex);
     return;
   }
-  const Tin* qg = (const Tin*)p.q + (size_t)b * p.T * p.q_tok_stride + kh * D;
-  const Tin* kg = (const Tin*)p.k + (size_t)b * p.T * p.k_tok_stride + kh * D;
-  const Tin* vg = (const Tin*)p.v + (size_t)b * p.T * p.v_tok_stride + h * D + r0;
+  // tokens of sequence b: [tokb, tokb + Tb) of its own row, or of the packed axis
+  const long long tokb = p.cu ? p.cu[b] : (long long)b * p.T;
+  const int Tb = p.cu ? p.cu[b + 1] - p.cu[b] : p.T;
+  const Tin* qg = (const Tin*)p.q + (size_t)tokb * p.q_tok_stride + kh * D;
+  const Tin* kg = (const Tin*)p.k + (size_t)tokb * p.k_tok_stride + kh * D;
+  const Tin* vg = (const Tin*)p.v + (size_t)tokb * p.v_tok_stride + h * D + r0;
   float* Sg = p.state + (((size_t)slot * p.Hv + h) * D + r0) * D;
 
   for (int idx = tid; idx < R * D; idx += THREADS) Ss[(idx / D) * LD + idx % D] = Sg[idx];
@@ -87,8 +90,8 @@ __global__ void __launch_bounds__(THREADS) gdn_prefill_simt_kernel(GdnLayerArgs 
     for (int idx = tid; idx < R * D; idx += THREADS) dst[idx] = Ss[(idx / D) * LD + idx % D];
   };
 
-  for (int t0 = 0; t0 < p.T; t0 += C) {
-    const int n = min(C, p.T - t0);
+  for (int t0 = 0; t0 < Tb; t0 += C) {
+    const int n = min(C, Tb - t0);
     if (p.snap_every > 0 && t0 > 0 && t0 % p.snap_every == 0) snapshot(t0 / p.snap_every - 1);
     // ---- load the chunk (zero padded)
     for (int idx = tid; idx < C * D; idx += THREADS) {
@@ -108,7 +111,7 @@ __global__ void __launch_bounds__(THREADS) gdn_prefill_simt_kernel(GdnLayerArgs 
     if (tid < C) {
       float g = 0.f, beta = 0.f;
       if (tid < n) {
-        const size_t gi = ((size_t)b * p.T + t0 + tid) * p.Hv + h;
+        const size_t gi = ((size_t)tokb + t0 + tid) * p.Hv + h;
         if (p.gates_pre) {
           g = ((const float*)p.a)[gi];
           beta = ((const float*)p.b)[gi];
@@ -230,7 +233,7 @@ __global__ void __launch_bounds__(THREADS) gdn_prefill_simt_kernel(GdnLayerArgs 
       float intra = 0.f;
       for (int s = 0; s <= rr; ++s) intra = fmaf(Ps[rr * LT + s], Us[s * LV + i], intra);
       const float o = fmaf(Eg[rr], inter, intra);
-      Tout* og = (Tout*)p.out + (((size_t)b * p.T + t0 + rr) * p.Hv + h) * D + r0 + i;
+      Tout* og = (Tout*)p.out + (((size_t)tokb + t0 + rr) * p.Hv + h) * D + r0 + i;
       *og = from_float<Tout>(o);
     }
     __syncthreads();
@@ -276,12 +279,23 @@ cudaError_t gdn_launch_prefill_simt(const GdnLayerArgs& p, cudaStream_t stream) 
 // in place: one warp per vector, four channels per lane.
 __global__ void __launch_bounds__(256) gdn_gated_norm_f32_kernel(
     float* out, const float* __restrict__ z, const float* __restrict__ w, float eps,
-    long long rows, long long rows_per_seq, const int32_t* slots, int num_slots) {
+    long long rows, long long rows_per_seq, const int32_t* slots, int num_slots,
+    const int32_t* cu, int nseq, int Hv) {
   const long long r = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (r >= rows) return;
   if (slots) {
-    const int s = slots[r / rows_per_seq];
+    long long seq = r / rows_per_seq;
+    if (cu) {                                      // packed batch: the sequence of the token
+      const long long tok = r / Hv;
+      int lo = 0, hi = nseq;
+      while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (cu[mid] <= tok) lo = mid; else hi = mid;
+      }
+      seq = lo;
+    }
+    const int s = slots[seq];
     if (s < 0 || s >= num_slots) return;           // a skipped batch entry keeps its rows
   }
   float4* o4 = reinterpret_cast<float4*>(out + r * D) + lane;
@@ -300,12 +314,14 @@ __global__ void __launch_bounds__(256) gdn_gated_norm_f32_kernel(
 
 cudaError_t gdn_launch_gated_norm_f32(float* out, const float* z, const float* w, float eps,
                                       int B, long long rows_per_seq, const int32_t* slots,
-                                      int num_slots, cudaStream_t stream) {
-  const long long rows = (long long)B * rows_per_seq;
+                                      int num_slots, cudaStream_t stream, const int32_t* cu,
+                                      int Hv) {
+  // (a packed batch passes B = 1, rows_per_seq = T Hv and its B sequences' offsets in cu)
+  const long long rows = (long long)(cu ? 1 : B) * rows_per_seq;
   if (rows == 0) return cudaSuccess;
   const long long blocks = (rows + 7) / 8;
   if (blocks > 0x7fffffffLL) return cudaErrorInvalidValue;
-  gdn_gated_norm_f32_kernel<<<(unsigned)blocks, 256, 0, stream>>>(out, z, w, eps, rows,
-                                                                  rows_per_seq, slots, num_slots);
+  gdn_gated_norm_f32_kernel<<<(unsigned)blocks, 256, 0, stream>>>(
+      out, z, w, eps, rows, rows_per_seq, slots, num_slots, cu, B, Hv);
   return cudaGetLastError();
 }

@@ -99,6 +99,13 @@ struct TcParams {
   int gate;
   const float* gw;
   float geps;
+  // packed variable-length batch (cu != nullptr): all tokens on one axis (batch index 0 of
+  // the tensor maps); global chunk u of a slice is ctab[n0 + u] = {first token, tokens,
+  // sequence}; sequence s owns global chunks [ccs[s], ccs[s+1]) and tokens [cu[s], cu[s+1])
+  const int32_t* cu;
+  const int32_t* ccs;
+  const int4* ctab;
+  void* out;              // for the ragged last chunk of a packed sequence (plain stores)
 };
 
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
@@ -290,9 +297,17 @@ __global__ void __launch_bounds__(LGT, 3)
   const uint32_t sb = smem_addr(sm);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int jc = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
-  const int n = p.n0 + jc;                       // chunk index within the sequence
   const int kh = h / (p.Hv / p.Hk);
-  const int slot = p.slots ? p.slots[b] : b;
+  // this unit's tokens: chunk n0 + jc of sequence b, or of a packed batch, entry n0 + jc
+  int tok0 = (p.n0 + jc) * C, ntok = min(C, p.T - tok0), seq = b;
+  if (p.cu) {
+    const int4 e = p.ctab[p.n0 + jc];
+    tok0 = e.x;
+    ntok = e.y;
+    seq = e.z;
+    if (ntok <= 0) return;                       // past the last chunk
+  }
+  const int slot = p.slots ? p.slots[seq] : seq;
   if (slot < 0 || slot >= p.num_slots) return;  // the chain kernel reports bad slots
   const size_t u = ((size_t)b * p.Hv + h) * p.ns + jc;
   uint8_t* unit = p.units + u * UNIT_BYTES;
@@ -327,9 +342,9 @@ __global__ void __launch_bounds__(LGT, 3)
     float g2[2] = {0.f, 0.f}, b2[2] = {0.f, 0.f};
 #pragma unroll
     for (int e = 0; e < 2; ++e) {
-      const int t = n * C + 2 * lane + e;
-      if (t < p.T) {
-        const size_t gi = ((size_t)b * p.T + t) * p.Hv + h;
+      const int r = 2 * lane + e;
+      if (r < ntok) {
+        const size_t gi = ((size_t)b * p.T + tok0 + r) * p.Hv + h;
         if (p.gates_pre) {
           g2[e] = reinterpret_cast<const float*>(p.a)[gi];
           b2[e] = reinterpret_cast<const float*>(p.b)[gi];
@@ -359,8 +374,8 @@ __global__ void __launch_bounds__(LGT, 3)
     mbar_arrive_expect_tx(bar_in, 32 * KB);
 #pragma unroll
     for (int kb = 0; kb < 2; ++kb) {
-      tma_load_3d(sb + L_KQ + kb * 16 * KB, &tm_k, kh * D + 64 * kb, n * C, b, bar_in);
-      tma_load_3d(sb + L_KQ + kb * 16 * KB + 8 * KB, &tm_q, kh * D + 64 * kb, n * C, b, bar_in);
+      tma_load_3d(sb + L_KQ + kb * 16 * KB, &tm_k, kh * D + 64 * kb, tok0, b, bar_in);
+      tma_load_3d(sb + L_KQ + kb * 16 * KB + 8 * KB, &tm_q, kh * D + 64 * kb, tok0, b, bar_in);
     }
   }
   tc_fence_before();
@@ -651,10 +666,25 @@ __global__ void __launch_bounds__(CH_THREADS, 1)
   const uint32_t sb = smem_addr(sm);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int b = blockIdx.x / p.Hv, h = blockIdx.x % p.Hv;
+  // this CTA's chunks: chunks n0 .. n0 + ns - 1 of sequence b; for a packed batch, the part
+  // of sequence b's chunks [ccs[b], ccs[b+1]) inside this slice (tokens from tbase, batch
+  // coordinate 0; the last one may hold fewer than C tokens of this sequence)
+  int ns = p.ns, tbase = p.n0 * C, bt = b, last_tok = C;
+  size_t u0 = ((size_t)b * p.Hv + h) * p.ns;      // first unit of this CTA's chunks
+  if (p.cu) {
+    const int cb0 = p.ccs[b], cb1 = p.ccs[b + 1];
+    const int c0 = max(cb0, p.n0), c1 = min(cb1, p.n0 + p.ns);
+    if (c0 >= c1) return;
+    ns = c1 - c0;
+    tbase = p.cu[b] + (c0 - cb0) * C;
+    bt = 0;
+    u0 = (size_t)h * p.ns + (c0 - p.n0);
+    last_tok = min(C, p.cu[b + 1] - (tbase + (ns - 1) * C));
+  }
   const int slot = p.slots ? p.slots[b] : b;
   if (slot < 0) return;
   if (slot >= p.num_slots) {
-    if (tid == 0 && p.n0 == 0) atomicOr(&g_err_tc, kErrIndex);
+    if (tid == 0 && (p.cu || p.n0 == 0)) atomicOr(&g_err_tc, kErrIndex);
     return;
   }
   float* sEgc = reinterpret_cast<float*>(sm + CH_MISC);
@@ -674,7 +704,6 @@ __global__ void __launch_bounds__(CH_THREADS, 1)
   const uint32_t bar_r0 = smem_addr(&barmem[11]), bar_r1 = smem_addr(&barmem[12]);
   // store warps, gated norm: barmem[13 + w] = gate tile of store warp w landed;
   // barmem[17 + (chunk & 1)] = the four warps' sums of squares written (every lane arrives)
-  const size_t u0 = ((size_t)b * p.Hv + h) * p.ns;  // first unit of this head's slice
   const bool issuer_warp = (warp == CH_ISSUER);
 
   // copies of chunk nl into buffer nl & 1: everything but P, and P (16 KB, needed only by the
@@ -686,8 +715,8 @@ __global__ void __launch_bounds__(CH_THREADS, 1)
     mbar_arrive_expect_tx(bar, 80 * KB);
     bulk_load(buf + U_NW, unit + U_NW, 32 * KB, bar);     // -W^T, Q~
     bulk_load(buf + U_KT, unit + U_KT, 32 * KB, bar);     // K~, T''
-    tma_load_3d(buf + CH_V, &tm_v, h * D, (p.n0 + nl) * C, b, bar);
-    tma_load_3d(buf + CH_V + 8 * KB, &tm_v, h * D + 64, (p.n0 + nl) * C, b, bar);
+    tma_load_3d(buf + CH_V, &tm_v, h * D, tbase + nl * C, bt, bar);
+    tma_load_3d(buf + CH_V + 8 * KB, &tm_v, h * D + 64, tbase + nl * C, bt, bar);
   };
   auto load_p = [&](int nl) {
     const uint32_t bar = (nl & 1) ? bar_p1 : bar_p0;
@@ -704,7 +733,7 @@ __global__ void __launch_bounds__(CH_THREADS, 1)
     fence_mbar_init();
   }
   if (issuer_warp)
-    for (int i = 0; i < 2 && i < p.ns; ++i) ld_chunk[i] = lp_chunk[i] = i;
+    for (int i = 0; i < 2 && i < ns; ++i) ld_chunk[i] = lp_chunk[i] = i;
   if (warp == 0) {
     tmem_alloc(smem_addr(sTmem), CH_TMEM);
     tmem_relinquish();
@@ -728,11 +757,11 @@ __global__ void __launch_bounds__(CH_THREADS, 1)
   // the local kernel's tiles and e^{G_C} (and the conv output V) from here on
   pdl_wait();
   if (tid == CH_EPI)
-    for (int i = 0; i < 2 && i < p.ns; ++i) {
+    for (int i = 0; i < 2 && i < ns; ++i) {
       load_main(i);
       load_p(i);
     }
-  for (int i = tid; i < p.ns; i += CH_THREADS) sEgc[i] = p.egc[u0 + i];
+  for (int i = tid; i < ns; i += CH_THREADS) sEgc[i] = p.egc[u0 + i];
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -742,7 +771,7 @@ __global__ void __launch_bounds__(CH_THREADS, 1)
     // ======================= issuer warp: the whole warp runs the loop and waits, one
     // elected lane issues the copies and MMAs (in chain order)
     const bool leader = elect_one();
-    for (int nl = 0; nl < p.ns; ++nl) {
+    for (int nl = 0; nl < ns; ++nl) {
       const uint32_t buf = sb + (nl & 1) * CH_BUF;
       const uint32_t tmO = tmem + TM_O + 64 * (nl & 1);
       // U'^T = V^T T''^T of this chunk (T'' as hi + lo; M = d_v, N = K = 64 tokens).  TM_U
@@ -776,10 +805,10 @@ __global__ void __launch_bounds__(CH_THREADS, 1)
                       sdesc_sw128(buf + U_NW + k * 2048, 8 * KB, 1024), ID_SW, true);
         mma_commit(bar_u);
         // C0 waited for S of the previous chunk: the other buffer's tiles but P are free
-        if (nl >= 1 && nl + 1 < p.ns) load_main(nl + 1);
+        if (nl >= 1 && nl + 1 < ns) load_main(nl + 1);
       }
       __syncwarp();
-      if (nl >= 1 && nl + 1 < p.ns) ld_chunk[(nl + 1) & 1] = nl + 1;
+      if (nl >= 1 && nl + 1 < ns) ld_chunk[(nl + 1) & 1] = nl + 1;
       // then O^T = S0 Q~^T, once the store warps have read this O buffer's tile of chunk nl - 2
       if (nl >= 2 && !__all_sync(0xffffffffu, mbar_wait_or_abort((nl & 1) ? bar_r1 : bar_r0,
                                                                   ((nl - 2) >> 1) & 1, sAbort))) {
@@ -818,7 +847,7 @@ __global__ void __launch_bounds__(CH_THREADS, 1)
       lp_chunk[nl & 1] = -1;
       // C2 waited for U^T, i.e. for every MMA before it, the previous output MMAs included:
       // the other buffer's P is free
-      const bool refill_p = nl >= 1 && nl + 1 < p.ns;
+      const bool refill_p = nl >= 1 && nl + 1 < ns;
       if (leader) {
 #pragma unroll
         for (int k = 0; k < 12; ++k) {
@@ -842,14 +871,14 @@ __global__ void __launch_bounds__(CH_THREADS, 1)
     // more ahead of its use) and of the boundary at the slice end, -1 for none
     const int32_t* snap_row = p.se_c > 0 ? p.snap_slots + (size_t)b * p.n_snap - 1 : nullptr;
     int snap_nb = p.se_c > 0 ? (p.n0 / p.se_c + 1) * p.se_c : 0x7fffffff;   // chunk index
-    int snap_next = snap_nb < p.n0 + p.ns ? snap_row[snap_nb / p.se_c] : -1;
-    const int n_end = p.n0 + p.ns;
+    int snap_next = snap_nb < p.n0 + ns ? snap_row[snap_nb / p.se_c] : -1;
+    const int n_end = p.n0 + ns;
     const int snap_end =
         (p.se_c > 0 && n_end % p.se_c == 0 && n_end * C <= p.T) ? snap_row[n_end / p.se_c] : -1;
     if (tid == 0 && (snap_next >= p.n_snap_slots || snap_end >= p.n_snap_slots))
       atomicOr(&g_err_tc, kErrIndex);
     bool ok = true;
-    for (int nl = 0; nl < p.ns && ok; ++nl) {
+    for (int nl = 0; nl < ns && ok; ++nl) {
       // ---- C0: S -> S0 (bf16, packed into TMEM as the A operand);  S <- e^{G_C} S
       // (every wait is decided warp-uniformly: the warp syncs below must not split)
       if (nl > 0 && !__all_sync(0xffffffffu, mbar_wait_or_abort(bar_s, (nl - 1) & 1, sAbort))) {
@@ -934,14 +963,14 @@ __global__ void __launch_bounds__(CH_THREADS, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(bar_c2);
     }
-    if (ok && p.ns > 0) {
+    if (ok && ns > 0) {
       // the leaving state, as soon as the last S update is done (the last output MMAs may
       // still run): TMEM -> this warp's 32 rows x 64 columns, staged as two 128-byte-swizzled
       // 32 x 32 blocks in the tile buffer the last chunk does not use (its readers are done)
       // -> two TMA tensor stores (whole rows per request)
-      if (__all_sync(0xffffffffu, mbar_wait_or_abort(bar_s, (p.ns - 1) & 1, sAbort))) {
+      if (__all_sync(0xffffffffu, mbar_wait_or_abort(bar_s, (ns - 1) & 1, sAbort))) {
         tc_fence_after();
-        const uint32_t stg = sb + ((((p.ns - 1) & 1) ^ 1) * CH_BUF) + warp * 8 * KB;
+        const uint32_t stg = sb + ((((ns - 1) & 1) ^ 1) * CH_BUF) + warp * 8 * KB;
 #pragma unroll
         for (int g = 0; g < 2; ++g) {
           float v[32];
@@ -1001,15 +1030,15 @@ __global__ void __launch_bounds__(CH_THREADS, 1)
       if (lane == 0) {
         fence_proxy_async_smem();                      // after this warp's reads of the tile
         mbar_arrive_expect_tx(bar_zw, 4 * KB);
-        tma_load_3d(zst, &tm_z, h * D + 32 * q, (p.n0 + nl) * C, b, bar_zw);
+        tma_load_3d(zst, &tm_z, h * D + 32 * q, tbase + nl * C, bt, bar_zw);
         // and the tile after it into L2, so that its own copy is an L2 hit
-        if (nl + 1 < p.ns) tma_prefetch_l2_3d(&tm_z, h * D + 32 * q, (p.n0 + nl + 1) * C, b);
+        if (nl + 1 < ns) tma_prefetch_l2_3d(&tm_z, h * D + 32 * q, tbase + (nl + 1) * C, bt);
       }
       z_chunk = nl;
     };
-    if (p.gate && p.ns > 0) load_z(0);
+    if (p.gate && ns > 0) load_z(0);
     bool ok = true;
-    for (int nl = 0; nl < p.ns; ++nl) {
+    for (int nl = 0; nl < ns; ++nl) {
       if (!__all_sync(0xffffffffu, mbar_wait_or_abort((nl & 1) ? bar_o1 : bar_o0,
                                                       (nl >> 1) & 1, sAbort))) {
         ok = false;
@@ -1072,15 +1101,24 @@ __global__ void __launch_bounds__(CH_THREADS, 1)
           }
         }
         __syncwarp();
-        if (nl + 1 < p.ns) load_z(nl + 1);
+        if (nl + 1 < ns) load_z(nl + 1);
       }
-      const int tok0 = (p.n0 + nl) * C;
-      if (p.gate)
+      const int tok0 = tbase + nl * C;
+      if (p.cu && nl == ns - 1 && last_tok < C) {
+        // the ragged last chunk of a packed sequence: the next sequence's tokens follow it,
+        // so only this sequence's rows are written, with plain stores (a warp's 32 lanes are
+        // 32 consecutive channels of a token row)
+        Tout* o = reinterpret_cast<Tout*>(p.out) + (size_t)tok0 * p.Hv * D + h * D + 32 * q +
+                  lane;
+#pragma unroll
+        for (int t = 0; t < 64; ++t)
+          if (t < last_tok) o[(size_t)t * p.Hv * D] = from_float<Tout>(v[t]);
+      } else if (p.gate)
         store_tile_passes<Tout, (int)(2 * KB / (32 * sizeof(Tout)))>(&tm_o, stg, v, lane,
-                                                                     h * D + 32 * q, tok0, b);
+                                                                     h * D + 32 * q, tok0, bt);
       else
         store_tile_passes<Tout, (int)(4 * KB / (32 * sizeof(Tout)))>(&tm_o, stg, v, lane,
-                                                                     h * D + 32 * q, tok0, b);
+                                                                     h * D + 32 * q, tok0, bt);
     }
     // everything this kernel writes has been issued: a kernel after it may start its set-up
     pdl_trigger();
@@ -1127,16 +1165,18 @@ cudaError_t launch_tc_t(const GdnLayerArgs& L, cudaStream_t stream) {
   CUtensorMap mq, mk, mv, mo, ms;
   // tokens per output store: a 2 KB staging block with the gated norm, else 4 KB
   const int out_rows = (int)((L.gate ? 2 : 4) * KB / (32 * sizeof(Tout)));
+  // a packed batch has all its tokens on one axis: batch extent 1 in the tensor maps
+  const int MB = L.cu ? 1 : L.B;
   const bool ok =
-      gdn_make_map(&mq, L.q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, L.Hk * D, L.T, L.B, L.q_tok_stride,
+      gdn_make_map(&mq, L.q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, L.Hk * D, L.T, MB, L.q_tok_stride,
                64, 64, true) &&
-      gdn_make_map(&mk, L.k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, L.Hk * D, L.T, L.B, L.k_tok_stride,
+      gdn_make_map(&mk, L.k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, L.Hk * D, L.T, MB, L.k_tok_stride,
                64, 64, true) &&
-      gdn_make_map(&mv, L.v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, L.Hv * D, L.T, L.B, L.v_tok_stride,
+      gdn_make_map(&mv, L.v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, L.Hv * D, L.T, MB, L.v_tok_stride,
                64, 64, true) &&
       gdn_make_map(&mo, L.out,
                sizeof(Tout) == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
-               (int)sizeof(Tout), L.Hv * D, L.T, L.B, (long long)L.Hv * D, 32, out_rows, false) &&
+               (int)sizeof(Tout), L.Hv * D, L.T, MB, (long long)L.Hv * D, 32, out_rows, false) &&
       // the state as rows of 128 fp32: box = 32 columns x 32 rows, 128-byte swizzle
       gdn_make_map(&ms, L.state, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, D,
                    L.num_slots * L.Hv * D, 1, D, 32, 32, true);
@@ -1145,7 +1185,7 @@ cudaError_t launch_tc_t(const GdnLayerArgs& L, cudaStream_t stream) {
   // when there is no gate)
   CUtensorMap mz = mv;
   if (L.gate && !gdn_make_map(&mz, L.gate_z, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, L.Hv * D, L.T,
-                              L.B, (long long)L.Hv * D, 32, 64, false))
+                              MB, (long long)L.Hv * D, 32, 64, false))
     return cudaErrorInvalidValue;
   // the snapshot bank, the same way (the state map stands in when nothing is recorded)
   CUtensorMap msn = ms;
@@ -1163,10 +1203,11 @@ cudaError_t launch_tc_t(const GdnLayerArgs& L, cudaStream_t stream) {
   if (e != cudaSuccess) return e;
   e = set_smem_once(gdn_chunk_chain_kernel<Tout>, (int)CH_SMEM, &done_c);
   if (e != cudaSuccess) return e;
-  const int nch = (L.T + C - 1) / C;
-  const int ns_max = slice_chunks(L.B, L.Hv, nch);
-  const size_t units = (size_t)ns_max * L.B * L.Hv;
-  if (!L.scratch || L.scratch_bytes < gdn_prefill_tc_scratch_bytes(L.B, L.T, L.Hv))
+  // chunks per sequence, or of a packed batch (its chunk table's length, an upper bound)
+  const int nch = L.cu ? L.n_chunks : (L.T + C - 1) / C;
+  const int ns_max = slice_chunks(MB, L.Hv, nch);
+  const size_t units = (size_t)ns_max * MB * L.Hv;
+  if (!L.scratch || L.scratch_bytes < gdn_prefill_tc_scratch_bytes(MB, nch * C, L.Hv))
     return cudaErrorInvalidValue;
   TcParams p;
   p.T = L.T; p.Hk = L.Hk; p.Hv = L.Hv; p.num_slots = L.num_slots; p.l2norm = L.l2norm;
@@ -1181,13 +1222,18 @@ cudaError_t launch_tc_t(const GdnLayerArgs& L, cudaStream_t stream) {
   p.gate = L.gate;
   p.gw = L.gate_w;
   p.geps = L.gate_eps;
+  p.cu = L.cu;
+  p.ccs = L.ccs;
+  p.ctab = static_cast<const int4*>(L.ctab);
+  p.out = L.out;
   for (int n0 = 0; n0 < nch; n0 += ns_max) {
     p.n0 = n0;
     p.ns = nch - n0 < ns_max ? nch - n0 : ns_max;
-    // (the first slice's local kernel reads the caller's gate inputs before its grid wait: it
-    // may start early only behind this call's own conv kernel)
+    // (the first slice's local kernel reads the caller's gate inputs, and a packed batch's
+    // chunk table, before its grid wait: it may start early only behind this call's own conv
+    // kernels, which began after everything earlier had completed)
     e = launch_pdl(n0 > 0 || L.W > 0, gdn_chunk_local_kernel<__nv_bfloat16>,
-                   dim3((unsigned)p.ns, (unsigned)L.Hv, (unsigned)L.B), dim3(LGT), L_SMEM, stream,
+                   dim3((unsigned)p.ns, (unsigned)L.Hv, (unsigned)MB), dim3(LGT), L_SMEM, stream,
                    mq, mk, p);
     if (e != cudaSuccess) return e;
     e = launch_pdl(true, gdn_chunk_chain_kernel<Tout>, dim3((unsigned)(L.B * L.Hv)), dim3(CH_THREADS),

@@ -226,6 +226,34 @@ gdn_status gdn_decode_step_gated(const gdn_dims* dims, const gdn_opts* opts, con
                                  const gdn_out_gate* gate, void* stream);
 
 /*
+ * gdn_chunk_prefill_varlen -- gdn_chunk_prefill for a packed variable-length batch: N
+ * sequences back to back on one token axis, sequence n on tokens [cu_seqlens[n],
+ * cu_seqlens[n+1]).  Each sequence is its own recurrence (its own state and conv-state row,
+ * its own chunk grid starting at its first token), so the results equal one
+ * gdn_chunk_prefill call per sequence, bit for bit.  This is the packed-prefill half of the
+ * mixed batches of PR #164 ("Hybrid APC Runtime": prefill and decode rows addressed through
+ * state slots); a decode row is a sequence of length 1.
+ *   dims         batch = N (>= 0), seqlen = T = the packed token count.
+ *   q, k, v, x, a, b, out, gate->z   as gdn_chunk_prefill with B = 1: [1, T, ...].
+ *   state_slots  [N] device int32 or NULL (identity, num_slots >= N): sequence n's row.
+ *   cu_seqlens   [N+1] device int32: 0 = cu[0] <= cu[1] <= ... <= cu[N] = T.  Offsets that
+ *                break this are reported as GDN_ERR_DEVICE_INDEX and nothing is computed
+ *                (checked on the device: the host never reads them).  Empty sequences are
+ *                allowed and leave their rows untouched.
+ *   gate         NULL, or the gated output norm as for gdn_chunk_prefill_gated.
+ *   workspace    at least gdn_prefill_varlen_workspace_size(dims, opts) bytes.
+ */
+size_t gdn_prefill_varlen_workspace_size(const gdn_dims* dims, const gdn_opts* opts);
+gdn_status gdn_chunk_prefill_varlen(const gdn_dims* dims, const gdn_opts* opts, const void* q,
+                                    const void* k, const void* v, const void* a, const void* b,
+                                    const float* A_log, const float* dt_bias,
+                                    const void* conv_weight, const void* conv_bias,
+                                    float* state, void* conv_state, const int32_t* state_slots,
+                                    const int32_t* cu_seqlens, void* out,
+                                    const gdn_out_gate* gate, void* workspace,
+                                    size_t workspace_bytes, void* stream);
+
+/*
  * gdn_chunk_prefill_snapshots -- gdn_chunk_prefill over a whole prompt in one call that also
  * records the recurrent and conv state every `snap_every` tokens, in-kernel.
  * Definition: the prefix checkpoints of hybrid automatic prefix caching (PR #164 "Hybrid APC

@@ -39,7 +39,7 @@ def test_status_strings_and_version(L):
     for code, name in gdn.STATUS_NAMES.items():
         assert gdn.gdn_status_string(code) == name
     assert gdn.gdn_status_string(99) == "GDN_UNKNOWN_STATUS"
-    assert L.gdn_version() == 102
+    assert L.gdn_version() == 103
 
 
 def _dims(**kw):
@@ -109,6 +109,29 @@ def test_gated_entries_reject_bad_gate(L):
     # the layer's own checks still come first
     bad_dims = [ctypes.byref(_dims(head_dim=64))] + args[1:]
     assert L.gdn_chunk_prefill_gated(*bad_dims, ctypes.byref(g), None, 0, None) == 2
+
+
+def test_varlen_rejects_bad_arguments(L):
+    d = _dims(batch=3, seqlen=200)
+    args = [ctypes.byref(d), ctypes.byref(_opts()), A, A, A, A, A, A, None, None, None, A, None,
+            None]
+    # offsets are required and 4-byte aligned
+    assert L.gdn_chunk_prefill_varlen(*args, None, A, None, A, 1 << 30, None) == 1
+    assert L.gdn_chunk_prefill_varlen(*args, A + 2, A, None, A, 1 << 30, None) == 1
+    # the workspace must hold the offsets' tables and the tiles
+    need = L.gdn_prefill_varlen_workspace_size(ctypes.byref(d), ctypes.byref(_opts()))
+    assert need > 0
+    assert L.gdn_chunk_prefill_varlen(*args, A, A, None, A, need - 1, None) == 3
+    assert L.gdn_chunk_prefill_varlen(*args, A, A, None, None, need, None) == 3
+    # a bad gate is rejected; bad dims first
+    bad = gdn.GdnOutGate(None, A, 1e-6)
+    assert L.gdn_chunk_prefill_varlen(*args, A, A, ctypes.byref(bad), A, need, None) == 1
+    bd = [ctypes.byref(_dims(batch=3, seqlen=200, head_dim=64))] + args[1:]
+    assert L.gdn_chunk_prefill_varlen(*bd, A, A, None, A, need, None) == 2
+    # no sequences or no tokens: nothing to do
+    for dd in (_dims(batch=0, seqlen=200), _dims(batch=3, seqlen=0)):
+        a0 = [ctypes.byref(dd)] + args[1:]
+        assert L.gdn_chunk_prefill_varlen(*a0, A, A, None, None, 0, None) == 0
 
 
 @pytest.mark.parametrize("field,value,status", [
