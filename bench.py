@@ -298,6 +298,8 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-decode-sweep", action="store_true")
     ap.add_argument("--no-prefill-4b", action="store_true")
+    ap.add_argument("--no-varlen", action="store_true",
+                    help="skip the packed variable-length prefill")
     ap.add_argument("--no-gated", action="store_true",
                     help="skip the gated-norm prefill / decode variants")
     ap.add_argument("--no-single-call", action="store_true",
@@ -463,6 +465,52 @@ def main():
                               "tokens_per_s": tok1, "ms_per_call": ms1, "tflops": tf1,
                               "frac_of_bf16_sustained": tf1 / peaks["bf16_sustained"]})
         del g1, ws1
+
+    # ---------------- a packed variable-length batch of the 27B shape: 16 sequences of seeded
+    #                  lengths in [64, 2048] (about 17k tokens) in one call
+    if not args.no_varlen:
+        lens = torch.randint(64, 2049, (16,), generator=torch.Generator().manual_seed(77))
+        cu = torch.zeros(17, dtype=torch.int32)
+        cu[1:] = torch.cumsum(lens, 0).to(torch.int32)
+        Tv = int(cu[-1])
+        shv = gi.GDNShape(1, Tv, HK, HV, conv_width=W)
+        inv = gi.make_inputs_device(shv, seed=4600, device=device)
+        stv = torch.zeros(16, HV, D, D, device=device)
+        csv = torch.zeros(16, W - 1, C_CONV, dtype=torch.bfloat16, device=device)
+        outv = torch.empty(1, Tv, HV, D, dtype=torch.bfloat16, device=device)
+        cud = cu.to(device)
+        wsv = torch.empty(gdn.gdn_prefill_varlen_workspace_size(16, Tv, HK, HV, W),
+                          dtype=torch.uint8, device=device)
+
+        def callv():
+            gdn.gdn_chunk_prefill_varlen(inv.x, None, None, inv.a, inv.b, inv.A_log,
+                                         inv.dt_bias, stv, outv, cu_seqlens=cud, num_k_heads=HK,
+                                         conv_weight=inv.conv_weight, conv_state=csv,
+                                         workspace=wsv)
+        callv()
+        gv = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gv):
+            callv()
+        for _ in range(3):
+            gv.replay()
+        q0 = torch.cuda.Event(enable_timing=True)
+        q1 = torch.cuda.Event(enable_timing=True)
+        q0.record()
+        for _ in range(5):
+            gv.replay()
+        q1.record()
+        torch.cuda.synchronize()
+        msv = q0.elapsed_time(q1) / 5
+        st = gdn.gdn_get_device_error()
+        if st != 0:
+            raise RuntimeError(f"device error in the packed prefill: {gdn.gdn_status_string(st)}")
+        tokv = Tv / (msv / 1e3)
+        tfv = tokv * FLOP_PER_TOKEN / 1e12
+        other_prefill.append({"workload": f"qwen36_27b_prefill_varlen_16seq_T{Tv}",
+                              "tokens_per_s": tokv, "ms_per_call": msv, "tflops": tfv,
+                              "frac_of_bf16_sustained": tfv / peaks["bf16_sustained"],
+                              "lengths": [int(x) for x in lens]})
+        del gv, inv, stv, csv, outv, wsv
 
     # ---------------- decode (same run, HBM-resident state), 256 steps as one CUDA graph
     dwl = make_decode_workload(device)
