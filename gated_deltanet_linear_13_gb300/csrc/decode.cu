@@ -123,7 +123,9 @@ __device__ __forceinline__ void dec_advance(const GdnLayerArgs& p, int nitems, i
   } while (c.item < nitems && !dec_item_valid(p, c.item));
 }
 
-template <typename Tin, typename Tout>
+// GATE: the gated output norm (a separate instantiation, so that the plain step keeps its
+// own schedule).
+template <typename Tin, typename Tout, bool GATE>
 __global__ void __launch_bounds__(DEC_THREADS, DEC_CPS) gdn_decode_stream_kernel(GdnLayerArgs p) {
   constexpr int D = kHeadDim;
   constexpr int RPW = DEC_RB / (DEC_THREADS / 32);    // rows per warp in a block
@@ -176,7 +178,7 @@ __global__ void __launch_bounds__(DEC_THREADS, DEC_CPS) gdn_decode_stream_kernel
     const int slot = p.slots ? p.slots[b] : b;
     if (c.blk == 0) {
       // (gated: the previous item's last head may still be reading its outputs out of sv)
-      if (p.gate) __syncthreads();
+      if (GATE) __syncthreads();
       // ---- item prologue: conv (+SiLU) of q, k (threads 0..127: q_j, 128..255: k_j) and of
       //      the r value heads' v channels, their new conv state, norms, k.q, gates
       const int j = tid & (D - 1);
@@ -237,7 +239,7 @@ __global__ void __launch_bounds__(DEC_THREADS, DEC_CPS) gdn_decode_stream_kernel
     // ---- the block: rows r0 .. r0 + DEC_RB - 1 of value head hh
     const int hh = c.blk / DEC_BPH, r0 = (c.blk % DEC_BPH) * DEC_RB;
     const int h = kh * r + hh;
-    if (p.gate && c.blk % DEC_BPH == 0 && tid < D)      // used at the head's last block
+    if (GATE && c.blk % DEC_BPH == 0 && tid < D)        // used at the head's last block
       zg = ld_elem((const Tin*)p.gate_z + ((size_t)b * p.Hv + h) * D + tid);
     const float eg = sg[2 * hh], beta = sg[2 * hh + 1];
     const float4 k4 = reinterpret_cast<const float4*>(sk)[lane];
@@ -253,9 +255,11 @@ __global__ void __launch_bounds__(DEC_THREADS, DEC_CPS) gdn_decode_stream_kernel
 #pragma unroll
     for (int i = 0; i < RPW; ++i) {
       const int row = warp * RPW + i;
-      const float vi = sv[hh * D + r0 + row];
+      float vi = 0.f;
+      if (GATE) vi = sv[hh * D + r0 + row];
       const float al = warp_sum(dot4(s[i], k4));
       const float ga = warp_sum(dot4(s[i], q4));
+      if (!GATE) vi = sv[hh * D + r0 + row];
       const float delta = beta * (vi - eg * al);
       float4 t;
       t.x = fmaf(eg, s[i].x, delta * k4.x);
@@ -264,7 +268,7 @@ __global__ void __launch_bounds__(DEC_THREADS, DEC_CPS) gdn_decode_stream_kernel
       t.w = fmaf(eg, s[i].w, delta * k4.w);
       reinterpret_cast<float4*>(Sw + i * D)[lane] = t;
       const float o = fmaf(eg, ga, delta * kq);
-      if (p.gate) {
+      if (GATE) {
         __syncwarp();                                  // every lane has read v_i
         if (lane == 0) sv[hh * D + r0 + row] = o;
       } else if (lane == 0) {
@@ -290,7 +294,7 @@ __global__ void __launch_bounds__(DEC_THREADS, DEC_CPS) gdn_decode_stream_kernel
         ++pk;
       }
     }
-    if (!p.gate) {
+    if (!GATE) {
       if (tid < DEC_RB) {
         Tout* o = (Tout*)p.out + ((size_t)b * p.Hv + h) * D + r0 + tid;
         *o = from_float<Tout>(sob[tid]);
@@ -570,9 +574,19 @@ static cudaError_t launch_decode_cluster(const GdnLayerArgs& p, cudaStream_t str
 #undef GDN_DEC
 }
 
+template <typename Tin, typename Tout, bool GATE>
+static cudaError_t launch_stream(const GdnLayerArgs& p, int grid, unsigned (*done)[2],
+                                 cudaStream_t stream) {
+  cudaError_t e = set_smem_once(gdn_decode_stream_kernel<Tin, Tout, GATE>, (int)DEC_SMEM,
+                                &(*done)[GATE ? 1 : 0]);
+  if (e != cudaSuccess) return e;
+  gdn_decode_stream_kernel<Tin, Tout, GATE><<<grid, DEC_THREADS, DEC_SMEM, stream>>>(p);
+  return cudaGetLastError();
+}
+
 cudaError_t gdn_launch_decode(const GdnLayerArgs& p, cudaStream_t stream) {
   if (p.B == 0) return cudaSuccess;
-  static unsigned done_bb = 0, done_bf = 0, done_ff = 0;
+  static unsigned done_bb[2] = {0, 0}, done_bf[2] = {0, 0}, done_ff[2] = {0, 0};
   int dev = 0, sms = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
@@ -581,18 +595,12 @@ cudaError_t gdn_launch_decode(const GdnLayerArgs& p, cudaStream_t stream) {
   const int nitems = p.B * p.Hk;
   if (nitems < 2 * sms) return launch_decode_cluster(p, stream);
   const int grid = nitems < sms * DEC_CPS ? nitems : sms * DEC_CPS;
-  if (p.in_bf16 && p.out_bf16) {
-    e = set_smem_once(gdn_decode_stream_kernel<__nv_bfloat16, __nv_bfloat16>, (int)DEC_SMEM, &done_bb);
-    if (e != cudaSuccess) return e;
-    gdn_decode_stream_kernel<__nv_bfloat16, __nv_bfloat16><<<grid, DEC_THREADS, DEC_SMEM, stream>>>(p);
-  } else if (p.in_bf16) {
-    e = set_smem_once(gdn_decode_stream_kernel<__nv_bfloat16, float>, (int)DEC_SMEM, &done_bf);
-    if (e != cudaSuccess) return e;
-    gdn_decode_stream_kernel<__nv_bfloat16, float><<<grid, DEC_THREADS, DEC_SMEM, stream>>>(p);
-  } else {
-    e = set_smem_once(gdn_decode_stream_kernel<float, float>, (int)DEC_SMEM, &done_ff);
-    if (e != cudaSuccess) return e;
-    gdn_decode_stream_kernel<float, float><<<grid, DEC_THREADS, DEC_SMEM, stream>>>(p);
-  }
-  return cudaGetLastError();
+  if (p.in_bf16 && p.out_bf16)
+    return p.gate ? launch_stream<__nv_bfloat16, __nv_bfloat16, true>(p, grid, &done_bb, stream)
+                  : launch_stream<__nv_bfloat16, __nv_bfloat16, false>(p, grid, &done_bb, stream);
+  if (p.in_bf16)
+    return p.gate ? launch_stream<__nv_bfloat16, float, true>(p, grid, &done_bf, stream)
+                  : launch_stream<__nv_bfloat16, float, false>(p, grid, &done_bf, stream);
+  return p.gate ? launch_stream<float, float, true>(p, grid, &done_ff, stream)
+                : launch_stream<float, float, false>(p, grid, &done_ff, stream);
 }
