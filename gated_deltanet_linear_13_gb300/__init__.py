@@ -28,7 +28,7 @@ STATUS_NAMES = {0: "GDN_OK", 1: "GDN_ERR_INVALID_ARGUMENT", 2: "GDN_ERR_UNSUPPOR
 EXPORTED = ("gdn_prefill_workspace_size", "gdn_chunk_prefill", "gdn_decode_step",
             "causal_conv1d_update", "gdn_state_checkpoint", "gdn_chunk_prefill_noalloc",
             "gdn_chunk_prefill_snapshots", "gdn_chunk_prefill_gated", "gdn_decode_step_gated",
-            "gdn_prefill_varlen_workspace_size", "gdn_chunk_prefill_varlen",
+            "gdn_prefill_varlen_workspace_size", "gdn_chunk_prefill_varlen", "gdn_decode_multi",
             "gdn_get_device_error", "gdn_status_string", "gdn_version")
 NOALLOC_SCRATCH_BYTES = 64 << 20   # GDN_NOALLOC_SCRATCH_BYTES in include/gdn.h
 
@@ -88,6 +88,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     L.gdn_prefill_varlen_workspace_size.argtypes = [dp, op]
     L.gdn_chunk_prefill_varlen.restype = ctypes.c_int
     L.gdn_chunk_prefill_varlen.argtypes = [dp, op] + [_vp] * 14 + [gp, _vp, ctypes.c_size_t, _vp]
+    L.gdn_decode_multi.restype = ctypes.c_int
+    L.gdn_decode_multi.argtypes = [dp, op] + [_vp] * 15 + [ctypes.c_int32, _vp, _vp]
     L.gdn_chunk_prefill_noalloc.restype = ctypes.c_int
     L.gdn_chunk_prefill_noalloc.argtypes = [dp, op] + [_vp] * 13 + [_vp]
     L.gdn_decode_step.restype = ctypes.c_int
@@ -421,6 +423,41 @@ def gdn_chunk_prefill_varlen(q, k, v, a, b, A_log, dt_bias, state, out, *, cu_se
                                     _ptr(out), None if gate is None else ctypes.byref(gate),
                                     _ptr(workspace), ws_bytes, _stream(stream))
     _check(st, "gdn_chunk_prefill_varlen")
+    return out
+
+
+def gdn_decode_multi(q, k, v, a, b, A_log, dt_bias, state, out, *, num_k_heads=None,
+                     conv_weight=None, conv_bias=None, conv_state=None, state_slots=None,
+                     snap_state=None, snap_conv_state=None, snap_slots=None,
+                     scale: float = 1.0, eps: float = 1e-6, qk_l2norm: bool = True,
+                     conv_silu: bool = True, gates_precomputed: bool = False,
+                     stream=None) -> torch.Tensor:
+    """A decode step over T <= 16 tokens per sequence (see gdn_decode_multi in
+    include/gdn.h); inputs shaped as for gdn_chunk_prefill with seqlen T.  With snap_slots
+    [B, T] the state (and conv state) after every token go to those rows of snap_state
+    (snap_conv_state)."""
+    L = load_library()
+    B, T, Hk, Hv, W, num_slots = _layer_dims(q, k, v, a, num_k_heads, conv_weight, conv_state,
+                                             state, state_slots, None)
+    _check_layer(q, k, v, a, b, A_log, dt_bias, conv_weight, conv_bias, state, conv_state,
+                 state_slots, out, B, T, Hk, Hv, W, num_slots, gates_precomputed)
+    nb = 0
+    if snap_slots is not None:
+        dev = q.device
+        nb = snap_state.shape[0]
+        _need(snap_slots, "snap_slots", (B, T), torch.int32, dev)
+        _need(snap_state, "snap_state", (nb, Hv, HEAD_DIM, HEAD_DIM), torch.float32, dev)
+        if W > 1:
+            _need(snap_conv_state, "snap_conv_state", (nb, W - 1, (2 * Hk + Hv) * HEAD_DIM),
+                  q.dtype, dev)
+    dims = GdnDims(B, T, Hk, Hv, HEAD_DIM, 64, W, num_slots)
+    opts = _opts(_dt(q), _dt(out), qk_l2norm, eps, scale, conv_silu, gates_precomputed)
+    st = L.gdn_decode_multi(ctypes.byref(dims), ctypes.byref(opts), _ptr(q), _ptr(k), _ptr(v),
+                            _ptr(a), _ptr(b), _ptr(A_log), _ptr(dt_bias), _ptr(conv_weight),
+                            _ptr(conv_bias), _ptr(state), _ptr(conv_state), _ptr(state_slots),
+                            _ptr(out), _ptr(snap_state), _ptr(snap_conv_state), nb,
+                            _ptr(snap_slots), _stream(stream))
+    _check(st, "gdn_decode_multi")
     return out
 
 

@@ -161,6 +161,11 @@ struct GdnLayerArgs {
 size_t gdn_prefill_tc_scratch_bytes(int B, int T, int Hv);
 
 cudaError_t gdn_launch_decode(const GdnLayerArgs& args, cudaStream_t stream);
+// A decode step over args.T <= 16 tokens per sequence; with snap_slots ([B][T]) the state and
+// conv state after every token go to those bank rows.
+cudaError_t gdn_launch_decode_multi(const GdnLayerArgs& args, float* snap_state, int num_snap,
+                                    const int32_t* snap_slots, void* snap_conv,
+                                    cudaStream_t stream);
 cudaError_t gdn_launch_prefill_simt(const GdnLayerArgs& args, cudaStream_t stream);
 cudaError_t gdn_launch_prefill_tc(const GdnLayerArgs& args, cudaStream_t stream);
 // 3-D tensor map over [B][T][width] elements starting at `base`, token stride `tok_stride`
@@ -211,3 +216,4 @@ unsigned gdn_take_error_checkpoint();
 unsigned gdn_take_error_prefill_simt();
 unsigned gdn_take_error_prefill_tc();
 unsigned gdn_take_error_varlen();
+unsigned gdn_take_error_decode_multi();

@@ -1,0 +1,337 @@
+// A decode step over T <= 16 new tokens per sequence (speculative multi-token verification,
+// short prefill): the gated delta rule on the fp32 state already in HBM, as in the decode
+// step, with the conv, the L2 norms and the gates fused in front, and optionally the state
+// after every token written to checkpoint slots (so that a verifier can keep any accepted
+// prefix).
+//
+// For the T tokens of one (sequence, value head) the chunked form of the recurrence holds
+// with a T x T chunk (the same algebra as the prefill's 64-token chunks): with G_t the
+// cumulative log-decay, A_ts = beta_t e^{G_t - G_s} (k_t . k_s) for s < t and
+// P_ts = e^{G_t - G_s} (q_t . k_s) for s <= t,
+//     u = (I + A)^{-1} (beta (v_i - e^{G} (k . s0_i)))          (per state row i)
+//     o_t = e^{G_t} (q_t . s0_i) + sum_{s<=t} P_ts u_s
+//     s_i <- e^{g_t} s_i + u_t k_t   after token t (t = 0 .. T-1).
+// Row independence again: row i needs only its own T values of v, and its 2T dot products
+// with the k_t and q_t are independent of each other, so a warp forms all 2T at once and one
+// transposing warp reduction (31 shuffles) leaves lane l with dot product l.
+//
+// One CTA per (sequence, key head): the prologue convolves the T tokens of the key head's
+// q/k channels and its r value heads' v channels (and writes the new conv state), forms the
+// norms, the gates and, per value head, (I + A)^{-1} and P in shared memory.  Then each warp
+// streams state rows: one 512-byte row per warp access, coalesced.
+#include "common.cuh"
+
+using namespace gdn;
+
+static __device__ unsigned int g_err_multi;
+
+unsigned gdn_take_error_decode_multi() {
+  unsigned v = 0, z = 0;
+  cudaMemcpyFromSymbol(&v, g_err_multi, sizeof(v));
+  cudaMemcpyToSymbol(g_err_multi, &z, sizeof(z));
+  return v;
+}
+
+namespace {
+
+constexpr int D = kHeadDim;
+constexpr int MT_THREADS = 256;
+constexpr int MT_MAXT = 16;
+
+__device__ __forceinline__ float dot4(float4 a, float4 b) {
+  return fmaf(a.x, b.x, fmaf(a.y, b.y, fmaf(a.z, b.z, a.w * b.w)));
+}
+
+// transposing warp reduction of 32 values per lane: lane l ends with the sum over lanes of
+// value l (five levels of halving, 31 shuffles)
+__device__ __forceinline__ float transpose_reduce32(float (&x)[32], int lane) {
+#pragma unroll
+  for (int lvl = 0; lvl < 5; ++lvl) {
+    const int m = 16 >> lvl, L = 32 >> lvl;
+    const bool up = lane & m;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      if (i < L / 2) {
+        const float send = up ? x[i] : x[i + L / 2];
+        const float keep = up ? x[i + L / 2] : x[i];
+        x[i] = keep + __shfl_xor_sync(0xffffffffu, send, m);
+      }
+    }
+  }
+  return x[0];
+}
+
+// shared-memory layout (floats) for T tokens and r value heads
+struct MtLayout {
+  int qh, kh, vv, kk, qk, mats, ostage, red, total;
+  __host__ __device__ MtLayout(int T, int r) {
+    qh = 0;
+    kh = qh + T * D;
+    vv = kh + T * D;
+    kk = vv + T * r * D;
+    qk = kk + T * T;
+    mats = qk + T * T;                       // per value head: Tm [T][T], P [T][T], 4 x [T]
+    ostage = mats + r * (2 * T * T + 4 * T);
+    red = ostage + T * D;
+    total = red + 64;
+  }
+};
+
+template <typename Tin, typename Tout>
+__global__ void __launch_bounds__(MT_THREADS) gdn_decode_multi_kernel(GdnLayerArgs p, int T,
+                                                                      float* snap_state,
+                                                                      int num_snap,
+                                                                      const int32_t* snap_slots,
+                                                                      Tin* snap_conv) {
+  extern __shared__ __align__(16) float ms[];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int r = p.Hv / p.Hk;
+  const int b = blockIdx.x / p.Hk, kh = blockIdx.x % p.Hk;
+  const int slot = p.slots ? p.slots[b] : b;
+  if (slot < 0) return;
+  if (slot >= p.num_slots) {
+    if (tid == 0 && kh == 0) atomicOr(&g_err_multi, kErrIndex);
+    return;
+  }
+  const MtLayout lay(T, r);
+  float* qh = ms + lay.qh;
+  float* khat = ms + lay.kh;
+  float* vv = ms + lay.vv;
+  float* KK = ms + lay.kk;
+  float* QK = ms + lay.qk;
+  float* red = ms + lay.red;
+  const int W = p.W, H = W > 0 ? W - 1 : 0, C = p.C_conv;
+  const int ch_qk = 2 * D, ch_all = ch_qk + r * D;
+  // ---- 1. conv (+SiLU) of this item's channels over the T tokens, or plain loads; the new
+  //      conv state, and the conv state after every token for the snapshots
+  for (int cl = tid; cl < ch_all; cl += MT_THREADS) {
+    // local channel cl: q (0..127), k (128..255), v of value head cl / 128 - 2
+    const int ch = cl < D ? kh * D + cl
+                   : cl < ch_qk ? p.Hk * D + kh * D + (cl - D)
+                                : 2 * p.Hk * D + kh * r * D + (cl - ch_qk);
+    float win[3 + MT_MAXT];
+    if (W > 0) {
+      const Tin* cs = (const Tin*)p.conv_state + (size_t)slot * H * C + ch;
+      for (int i = 0; i < H; ++i) win[i] = ld_elem(cs + (size_t)i * C);
+      for (int t = 0; t < T; ++t)
+        win[H + t] = ld_elem((const Tin*)p.x + ((size_t)b * T + t) * C + ch);
+      const float bias = p.conv_b ? ld_elem((const Tin*)p.conv_b + ch) : 0.f;
+      const Tin* w = (const Tin*)p.conv_w + (size_t)ch * W;
+      float wt[4];
+      for (int j = 0; j < W; ++j) wt[j] = ld_elem(w + j);
+      for (int t = 0; t < T; ++t) {
+        float y = bias;
+        for (int j = 0; j < W; ++j) y = fmaf(wt[j], win[t + j], y);
+        y = p.silu ? silu_f(y) : y;
+        if (cl < D) qh[t * D + cl] = y;
+        else if (cl < ch_qk) khat[t * D + cl - D] = y;
+        else vv[t * r * D + cl - ch_qk] = y;
+      }
+      // new conv state: the last W-1 window entries; after token t: entries t+1 .. t+W-1
+      Tin* csw = (Tin*)p.conv_state + (size_t)slot * H * C + ch;
+      for (int i = 0; i < H; ++i) st_elem(csw + (size_t)i * C, win[T + i]);
+      if (snap_conv && snap_slots)
+        for (int t = 0; t < T; ++t) {
+          const int sl = snap_slots[b * T + t];
+          if (sl >= 0 && sl < num_snap)
+            for (int i = 0; i < H; ++i)
+              st_elem(snap_conv + ((size_t)sl * H + i) * C + ch, win[t + 1 + i]);
+        }
+    } else {
+      for (int t = 0; t < T; ++t) {
+        float y;
+        if (cl < D) {
+          y = ld_elem((const Tin*)p.q + (((size_t)b * T + t) * p.Hk + kh) * D + cl);
+          qh[t * D + cl] = y;
+        } else if (cl < ch_qk) {
+          y = ld_elem((const Tin*)p.k + (((size_t)b * T + t) * p.Hk + kh) * D + cl - D);
+          khat[t * D + cl - D] = y;
+        } else {
+          y = ld_elem((const Tin*)p.v + (((size_t)b * T + t) * p.Hv + kh * r) * D + cl - ch_qk);
+          vv[t * r * D + cl - ch_qk] = y;
+        }
+      }
+    }
+  }
+  __syncthreads();
+  // ---- 2. L2 norms of q_t and k_t (one warp per vector), q also times `scale`
+  for (int vec = warp; vec < 2 * T; vec += MT_THREADS / 32) {
+    float* x = (vec < T ? qh : khat) + (vec % T) * D;
+    float4 v4 = reinterpret_cast<float4*>(x)[lane];
+    const float ss = warp_sum(dot4(v4, v4));
+    const float inv = (p.l2norm ? 1.0f / sqrtf(ss + p.eps) : 1.0f) * (vec < T ? p.scale : 1.0f);
+    v4.x *= inv; v4.y *= inv; v4.z *= inv; v4.w *= inv;
+    reinterpret_cast<float4*>(x)[lane] = v4;
+  }
+  __syncthreads();
+  // ---- 3. KK_ts = k_t . k_s and QK_ts = q_t . k_s (one warp per pair)
+  for (int pr = warp; pr < 2 * T * T; pr += MT_THREADS / 32) {
+    const int which = pr / (T * T), t = (pr / T) % T, s2 = pr % T;
+    const float4 a4 = reinterpret_cast<const float4*>((which ? qh : khat) + t * D)[lane];
+    const float4 k4 = reinterpret_cast<const float4*>(khat + s2 * D)[lane];
+    const float d = warp_sum(dot4(a4, k4));
+    if (lane == 0) (which ? QK : KK)[t * T + s2] = d;
+  }
+  __syncthreads();
+  // ---- 4. per value head: gates, G, (I + A)^{-1} and P (warp hh, lanes = tokens)
+  for (int hh = warp; hh < r; hh += MT_THREADS / 32) {
+    float* Tm = ms + lay.mats + hh * (2 * T * T + 4 * T);
+    float* P = Tm + T * T;
+    float* eG = P + T * T;          // e^{G_t}
+    float* bt = eG + T;             // beta_t
+    float* dk = bt + T;             // e^{G_{T-1} - G_t}
+    float* eg = dk + T;             // e^{g_t}
+    const int h = kh * r + hh;
+    float g = 0.f, beta = 0.f;
+    if (lane < T) {
+      const size_t gi = ((size_t)b * T + lane) * p.Hv + h;
+      if (p.gates_pre) {
+        g = ((const float*)p.a)[gi];
+        beta = ((const float*)p.b)[gi];
+      } else {
+        g = gate_g(ld_elem((const Tin*)p.a + gi), p.A_log[h], p.dt_bias ? p.dt_bias[h] : 0.f);
+        beta = sigmoid_f(ld_elem((const Tin*)p.b + gi));
+      }
+    }
+    float G = g;                    // inclusive prefix over tokens
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const float y = __shfl_up_sync(0xffffffffu, G, o);
+      if (lane >= o) G += y;
+    }
+    const float GT = __shfl_sync(0xffffffffu, G, T - 1);
+    if (lane < T) {
+      eG[lane] = expf(G);
+      bt[lane] = beta;
+      dk[lane] = expf(GT - G);
+      eg[lane] = expf(g);
+    }
+    // A and P rows (lane t), then (I + A)^{-1} by forward substitution, column by column
+    // (lane j owns column j; rows t > j in order)
+    for (int s2 = 0; s2 < MT_MAXT; ++s2) {
+      const float Gs = __shfl_sync(0xffffffffu, G, s2 & 31);
+      float a = 0.f, pp = 0.f;
+      if (lane < T && s2 < T && s2 <= lane) {
+        const float e = expf(G - Gs);
+        if (s2 < lane) a = beta * e * KK[lane * T + s2];
+        pp = e * QK[lane * T + s2];
+      }
+      if (lane < T && s2 < T) P[lane * T + s2] = pp;
+      if (lane < T && s2 < T) Tm[lane * T + s2] = a;     // A for now
+    }
+    __syncwarp();
+    if (lane < T) {
+      const int j = lane;
+      float col[MT_MAXT];
+      for (int t = 0; t < MT_MAXT; ++t) col[t] = (t == j) ? 1.f : 0.f;
+      for (int t = 0; t < MT_MAXT; ++t) {
+        if (t > j && t < T) {
+          float acc = 0.f;
+          for (int s2 = 0; s2 < MT_MAXT; ++s2)
+            if (s2 >= j && s2 < t) acc = fmaf(Tm[t * T + s2], col[s2], acc);
+          col[t] = -acc;
+        }
+      }
+      __syncwarp(__activemask());
+      for (int t = 0; t < T; ++t) Tm[t * T + j] = col[t];
+    }
+  }
+  __syncthreads();
+  // ---- 5. the state rows: value head hh, rows warp, warp + 8, ...
+  for (int hh = 0; hh < r; ++hh) {
+    const int h = kh * r + hh;
+    const float* Tm = ms + lay.mats + hh * (2 * T * T + 4 * T);
+    const float* P = Tm + T * T;
+    const float* eG = P + T * T;
+    const float* bt = eG + T;
+    const float* eg = bt + 2 * T;
+    float* ost = ms + lay.ostage;
+    float* Sh = p.state + ((size_t)slot * p.Hv + h) * D * D;
+    for (int i = warp; i < D; i += MT_THREADS / 32) {
+      float4 s = reinterpret_cast<const float4*>(Sh + (size_t)i * D)[lane];
+      float x[32];
+#pragma unroll
+      for (int t = 0; t < 16; ++t) {
+        const bool on = t < T;
+        x[t] = on ? dot4(s, reinterpret_cast<const float4*>(khat + t * D)[lane]) : 0.f;
+        x[16 + t] = on ? dot4(s, reinterpret_cast<const float4*>(qh + t * D)[lane]) : 0.f;
+      }
+      // lane l: l < 16: k_l . s0_i;  16 <= l: q_{l-16} . s0_i
+      const float red_l = transpose_reduce32(x, lane);
+      const float ci = __shfl_sync(0xffffffffu, red_l, (lane + 16) & 31);
+      const int t = lane;
+      float rhs = 0.f;
+      if (t < T) rhs = bt[t] * (vv[t * r * D + hh * D + i] - eG[t] * red_l);
+      // u = (I + A)^{-1} rhs, lane t
+      float u = 0.f;
+#pragma unroll
+      for (int s2 = 0; s2 < 16; ++s2) {
+        const float rs = __shfl_sync(0xffffffffu, rhs, s2);
+        if (s2 < T && t < T && s2 <= t) u = fmaf(Tm[t * T + s2], rs, u);
+      }
+      // outputs and the state after each token
+      float o = (t < T) ? eG[t] * ci : 0.f;
+#pragma unroll
+      for (int s2 = 0; s2 < 16; ++s2) {
+        if (s2 < T) {
+          const float us = __shfl_sync(0xffffffffu, u, s2);
+          if (t < T && s2 <= t) o = fmaf(P[t * T + s2], us, o);
+          const float4 k4 = reinterpret_cast<const float4*>(khat + s2 * D)[lane];
+          const float e = eg[s2];
+          s.x = fmaf(e, s.x, us * k4.x);
+          s.y = fmaf(e, s.y, us * k4.y);
+          s.z = fmaf(e, s.z, us * k4.z);
+          s.w = fmaf(e, s.w, us * k4.w);
+          if (snap_state && snap_slots) {
+            const int sl = snap_slots[b * T + s2];
+            if (sl >= 0 && sl < num_snap)
+              reinterpret_cast<float4*>(snap_state + (((size_t)sl * p.Hv + h) * D + i) * D)[lane] = s;
+          }
+        }
+      }
+      reinterpret_cast<float4*>(Sh + (size_t)i * D)[lane] = s;
+      if (t < T) ost[t * D + i] = o;
+    }
+    __syncthreads();
+    // this head's outputs, token rows of 128 channels
+    for (int e = tid; e < T * D; e += MT_THREADS) {
+      const int tt = e / D, c = e % D;
+      st_elem((Tout*)p.out + (((size_t)b * T + tt) * p.Hv + h) * D + c, ost[e]);
+    }
+    __syncthreads();
+  }
+  if (tid == 0 && snap_slots)
+    for (int t = 0; t < T; ++t)
+      if (snap_slots[b * T + t] >= num_snap && kh == 0) atomicOr(&g_err_multi, kErrIndex);
+}
+
+template <typename Tin, typename Tout>
+cudaError_t launch_multi_t(const GdnLayerArgs& p, int T, float* snap_state, int num_snap,
+                           const int32_t* snap_slots, void* snap_conv, cudaStream_t stream) {
+  const MtLayout lay(T, p.Hv / p.Hk);
+  const size_t smem = sizeof(float) * lay.total;
+  static unsigned done = 0;
+  cudaError_t e = set_smem_once(gdn_decode_multi_kernel<Tin, Tout>,
+                                (int)(sizeof(float) * MtLayout(MT_MAXT, 8).total), &done);
+  if (e != cudaSuccess) return e;
+  gdn_decode_multi_kernel<Tin, Tout><<<(unsigned)(p.B * p.Hk), MT_THREADS, smem, stream>>>(
+      p, T, snap_state, num_snap, snap_slots, static_cast<Tin*>(snap_conv));
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t gdn_launch_decode_multi(const GdnLayerArgs& p, float* snap_state, int num_snap,
+                                    const int32_t* snap_slots, void* snap_conv,
+                                    cudaStream_t stream) {
+  if (p.B == 0 || p.T == 0) return cudaSuccess;
+  if (p.T > MT_MAXT) return cudaErrorInvalidValue;
+  if (p.in_bf16 && p.out_bf16)
+    return launch_multi_t<__nv_bfloat16, __nv_bfloat16>(p, p.T, snap_state, num_snap,
+                                                         snap_slots, snap_conv, stream);
+  if (p.in_bf16)
+    return launch_multi_t<__nv_bfloat16, float>(p, p.T, snap_state, num_snap, snap_slots,
+                                                snap_conv, stream);
+  return launch_multi_t<float, float>(p, p.T, snap_state, num_snap, snap_slots, snap_conv,
+                                      stream);
+}

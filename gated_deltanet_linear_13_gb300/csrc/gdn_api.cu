@@ -7,7 +7,7 @@
 
 namespace {
 
-constexpr int32_t kVersion = 103;
+constexpr int32_t kVersion = 104;
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
@@ -347,6 +347,35 @@ gdn_status gdn_chunk_prefill_varlen(const gdn_dims* dims, const gdn_opts* opts, 
   return GDN_OK;
 }
 
+gdn_status gdn_decode_multi(const gdn_dims* dims, const gdn_opts* opts, const void* q,
+                            const void* k, const void* v, const void* a, const void* b,
+                            const float* A_log, const float* dt_bias, const void* conv_weight,
+                            const void* conv_bias, float* state, void* conv_state,
+                            const int32_t* state_slots, void* out, float* snap_state,
+                            void* snap_conv_state, int32_t num_snap_slots,
+                            const int32_t* snap_slots, void* stream) {
+  Checked c;
+  gdn_status st = check_dims(dims, opts, false, &c);
+  if (st != GDN_OK) return st;
+  if (c.T > 16) return GDN_ERR_UNSUPPORTED;
+  if (c.B == 0 || c.T == 0) return GDN_OK;
+  GdnLayerArgs L;
+  st = check_layer_ptrs(c, opts, q, k, v, a, b, A_log, dt_bias, conv_weight, conv_bias, state,
+                        conv_state, state_slots, out, &L);
+  if (st != GDN_OK) return st;
+  if (snap_slots) {
+    if (!aligned4(snap_slots) || num_snap_slots <= 0 || !snap_state || !aligned16(snap_state))
+      return GDN_ERR_INVALID_ARGUMENT;
+    if (c.W > 1 && (!snap_conv_state || !aligned16(snap_conv_state)))
+      return GDN_ERR_INVALID_ARGUMENT;
+  }
+  cudaError_t e = gdn_launch_decode_multi(L, snap_slots ? snap_state : nullptr,
+                                          snap_slots ? num_snap_slots : 0, snap_slots,
+                                          (snap_slots && c.W > 1) ? snap_conv_state : nullptr,
+                                          static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+}
+
 // gdn_decode_step, with the output gate when `gated`
 static gdn_status decode_impl(const gdn_dims* dims, const gdn_opts* opts, const void* q,
                               const void* k, const void* v, const void* a, const void* b,
@@ -447,7 +476,7 @@ gdn_status gdn_get_device_error(void* stream) {
   if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return GDN_ERR_CUDA;
   unsigned bits = gdn_take_error_decode() | gdn_take_error_conv() | gdn_take_error_checkpoint() |
                   gdn_take_error_prefill_simt() | gdn_take_error_prefill_tc() |
-                  gdn_take_error_varlen();
+                  gdn_take_error_varlen() | gdn_take_error_decode_multi();
   if (cudaGetLastError() != cudaSuccess) return GDN_ERR_CUDA;
   if (bits & gdn::kErrTimeout) return GDN_ERR_DEVICE_TIMEOUT;
   if (bits & gdn::kErrIndex) return GDN_ERR_DEVICE_INDEX;

@@ -254,6 +254,32 @@ gdn_status gdn_chunk_prefill_varlen(const gdn_dims* dims, const gdn_opts* opts, 
                                     size_t workspace_bytes, void* stream);
 
 /*
+ * gdn_decode_multi -- a decode step over T = 1 .. 16 new tokens per sequence: speculative
+ * multi-token verification and short prefills on the state already in HBM.  Definition: the
+ * recurrence of gdn_chunk_prefill over the T tokens (the model card's "How It Works" loop);
+ * computed as one T-token chunk of the WY/UT form per (sequence, value head), streaming every
+ * state row once.  The model card's performance tables ("Performance") cover this 2-16 token
+ * regime; PR #164 lists native multi-token (MTP) speculative decoding as a follow-up ("Known
+ * limitations and follow-ups").
+ *   all arguments but the ones below: as gdn_chunk_prefill with seqlen = T <= 16 (T > 16
+ *                returns GDN_ERR_UNSUPPORTED; use gdn_chunk_prefill).
+ *   snap_slots   [B, T] device int32 or NULL: the bank row that receives the state (and conv
+ *                state) after token t of sequence b; negative = not recorded; >= num_snap_slots
+ *                is skipped and recorded as GDN_ERR_DEVICE_INDEX.  With it, a verifier that
+ *                accepts the first a tokens restores row snap_slots[b, a-1].
+ *   snap_state   [num_snap_slots, Hv, d, d] fp32 (required with snap_slots).
+ *   snap_conv_state  [num_snap_slots, W-1, C_conv] in in_dtype (required with snap_slots when
+ *                conv_width > 1).
+ */
+gdn_status gdn_decode_multi(const gdn_dims* dims, const gdn_opts* opts, const void* q,
+                            const void* k, const void* v, const void* a, const void* b,
+                            const float* A_log, const float* dt_bias, const void* conv_weight,
+                            const void* conv_bias, float* state, void* conv_state,
+                            const int32_t* state_slots, void* out, float* snap_state,
+                            void* snap_conv_state, int32_t num_snap_slots,
+                            const int32_t* snap_slots, void* stream);
+
+/*
  * gdn_chunk_prefill_snapshots -- gdn_chunk_prefill over a whole prompt in one call that also
  * records the recurrent and conv state every `snap_every` tokens, in-kernel.
  * Definition: the prefix checkpoints of hybrid automatic prefix caching (PR #164 "Hybrid APC

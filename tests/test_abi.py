@@ -39,7 +39,7 @@ def test_status_strings_and_version(L):
     for code, name in gdn.STATUS_NAMES.items():
         assert gdn.gdn_status_string(code) == name
     assert gdn.gdn_status_string(99) == "GDN_UNKNOWN_STATUS"
-    assert L.gdn_version() == 103
+    assert L.gdn_version() == 104
 
 
 def _dims(**kw):
@@ -109,6 +109,19 @@ def test_gated_entries_reject_bad_gate(L):
     # the layer's own checks still come first
     bad_dims = [ctypes.byref(_dims(head_dim=64))] + args[1:]
     assert L.gdn_chunk_prefill_gated(*bad_dims, ctypes.byref(g), None, 0, None) == 2
+
+
+def test_decode_multi_rejects_bad_arguments(L):
+    def call(d, snap_state=None, snap_conv=None, nb=0, snap_slots=None):
+        return L.gdn_decode_multi(ctypes.byref(d), ctypes.byref(_opts()), A, A, A, A, A, A, None,
+                                  None, None, A, None, None, A, snap_state, snap_conv, nb,
+                                  snap_slots, None)
+    assert call(_dims(seqlen=17)) == 2                      # more than 16 tokens: the prefill
+    assert call(_dims(seqlen=4, head_dim=64)) == 2
+    assert call(_dims(seqlen=4), snap_slots=A) == 1          # slots without a bank
+    assert call(_dims(seqlen=4), snap_state=A, nb=0, snap_slots=A) == 1
+    assert call(_dims(seqlen=4), snap_state=A + 4, nb=3, snap_slots=A) == 1
+    assert call(_dims(seqlen=0)) == 0 and call(_dims(batch=0, seqlen=4)) == 0
 
 
 def test_varlen_rejects_bad_arguments(L):

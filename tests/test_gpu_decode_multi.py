@@ -1,0 +1,136 @@
+"""gdn_decode_multi (a decode step over T <= 16 tokens) against the fp64 oracle, through the
+C ABI: outputs, final state and conv state for T = 1 .. 16 in bf16 and fp32, the 27B shape,
+skipped rows, and the per-token snapshots (the state and conv state after every token, as a
+speculative verifier restores them).
+"""
+import numpy as np
+import pytest
+import torch
+
+import gdn_inputs as gi
+import oracle
+from gdn_testutil import (assert_bf16_parity, assert_f32_parity, assert_state_parity,
+                          head_slice, oracle_full, to_device)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def gdn():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import gated_deltanet_linear_13_gb300 as m
+    from gated_deltanet_linear_13_gb300 import build_lib
+    build_lib.build()
+    m.load_library()
+    return m
+
+
+def _inputs(B, T, Hk, Hv, W, dtype, seed):
+    sh = gi.GDNShape(B, T, Hk, Hv, conv_width=W)
+    inp = gi.make_inputs(sh, seed=seed, dtype=dtype, state="normal", state_std=0.3)
+    if W > 0:
+        cs = np.random.default_rng(seed).standard_normal(inp.conv_state.shape).astype(np.float32)
+        inp.conv_state = gi.to_bf16(cs) if dtype == "bf16" else torch.from_numpy(cs)
+    return sh, inp
+
+
+def _run(gdn, dev, sh, out_dtype, state_slots=None, **snap):
+    out = torch.full((sh.batch, sh.seqlen, sh.num_v_heads, 128), 7.0, dtype=out_dtype,
+                     device="cuda")
+    if sh.conv_width > 0:
+        gdn.gdn_decode_multi(dev.x, None, None, dev.a, dev.b, dev.A_log, dev.dt_bias, dev.state,
+                             out, num_k_heads=sh.num_k_heads, conv_weight=dev.conv_weight,
+                             conv_state=dev.conv_state, state_slots=state_slots, **snap)
+    else:
+        gdn.gdn_decode_multi(dev.q, dev.k, dev.v, dev.a, dev.b, dev.A_log, dev.dt_bias,
+                             dev.state, out, state_slots=state_slots, **snap)
+    return out
+
+
+@pytest.mark.parametrize("T", [1, 2, 5, 16])
+def test_bf16_conv_matches_oracle(gdn, T):
+    sh, inp = _inputs(3, T, 2, 6, 4, "bf16", 8000 + T)
+    ref = oracle_full(inp)
+    dev = to_device(inp)
+    out = _run(gdn, dev, sh, torch.bfloat16)
+    assert gdn.gdn_get_device_error() == 0
+    assert_bf16_parity(out.cpu(), ref.out)
+    assert_state_parity(dev.state.cpu(), ref.state)
+    np.testing.assert_array_equal(dev.conv_state.float().cpu().numpy(), ref.conv_state)
+
+
+@pytest.mark.parametrize("T", [3, 16])
+def test_fp32_mode(gdn, T):
+    sh, inp = _inputs(2, T, 4, 4, 0, "f32", 8100 + T)
+    ref = oracle_full(inp)
+    dev = to_device(inp)
+    out = _run(gdn, dev, sh, torch.float32)
+    assert gdn.gdn_get_device_error() == 0
+    assert_f32_parity(out.cpu(), ref.out)
+    assert_state_parity(dev.state.cpu(), ref.state, fp32=True)
+
+
+def test_27b_shape_sampled(gdn):
+    """16/48 heads (GQA 1:3), width-4 conv, B = 32, T = 4: sampled units against the oracle."""
+    sh, inp = _inputs(32, 4, 16, 48, 4, "bf16", 8200)
+    dev = to_device(inp)
+    out = _run(gdn, dev, sh, torch.bfloat16)
+    assert gdn.gdn_get_device_error() == 0
+    for (b, h) in [(0, 0), (5, 47), (17, 23), (31, 30)]:
+        r = oracle.layer(**head_slice(inp, b, h))
+        assert_bf16_parity(out[b, :, h].cpu(), r.out[0, :, 0], what=f"out {b},{h}")
+        assert_state_parity(dev.state[b, h].cpu(), r.state[0, 0], what=f"state {b},{h}")
+
+
+def test_skipped_row(gdn):
+    sh, inp = _inputs(3, 4, 2, 4, 4, "bf16", 8300)
+    dev = to_device(inp)
+    before = dev.state.clone()
+    slots = torch.tensor([2, -1, 0], dtype=torch.int32, device="cuda")
+    st = dev.state.clone()
+    dev.state[2], dev.state[0] = st[0], st[2]
+    cs = dev.conv_state.clone()
+    dev.conv_state[2], dev.conv_state[0] = cs[0], cs[2]
+    ref = oracle_full(inp)
+    out = _run(gdn, dev, sh, torch.bfloat16, state_slots=slots)
+    assert gdn.gdn_get_device_error() == 0
+    assert torch.all(out[1].float() == 7.0)
+    assert torch.equal(dev.state[1], before[1])
+    assert_bf16_parity(out[0].cpu(), ref.out[0])
+    assert_bf16_parity(out[2].cpu(), ref.out[2])
+    assert_state_parity(dev.state[2].cpu(), ref.state[0])
+
+
+def test_per_token_snapshots(gdn):
+    """The state and conv state after every token of every row, into permuted bank rows with
+    one pair masked: each equals the oracle after that many tokens."""
+    B, T = 2, 5
+    sh, inp = _inputs(B, T, 2, 6, 4, "bf16", 8400)
+    nb = B * T + 2
+    perm = np.random.default_rng(1).permutation(nb)[:B * T].reshape(B, T)
+    perm[1, 2] = -1
+    slots = torch.tensor(perm, dtype=torch.int32, device="cuda")
+    bank = torch.full((nb, 6, 128, 128), 12345.0, device="cuda")
+    cbank = torch.zeros(nb, 3, sh.conv_channels, dtype=torch.bfloat16, device="cuda")
+    dev = to_device(inp)
+    _run(gdn, dev, sh, torch.bfloat16, snap_state=bank, snap_conv_state=cbank, snap_slots=slots)
+    assert gdn.gdn_get_device_error() == 0
+    for b in range(B):
+        for t in range(T):
+            row = int(perm[b, t])
+            if row < 0:
+                continue
+            sub = gi.GDNShape(1, t + 1, 2, 6, conv_width=4)
+            part = gi.GDNInputs(sub, "bf16", None, None, None, inp.x[b:b + 1, :t + 1],
+                                inp.a[b:b + 1, :t + 1], inp.b[b:b + 1, :t + 1], inp.A_log,
+                                inp.dt_bias, inp.conv_weight, inp.state[b:b + 1],
+                                inp.conv_state[b:b + 1])
+            r = oracle_full(part)
+            assert_state_parity(bank[row].cpu(), r.state[0], what=f"snapshot {b},{t}")
+            np.testing.assert_array_equal(cbank[row].float().cpu().numpy(), r.conv_state[0])
+    # the masked pair's row and the unused rows were not written
+    used = set(int(v) for v in perm.ravel() if v >= 0)
+    for row in range(nb):
+        if row not in used:
+            assert bool((bank[row] == 12345.0).all())
