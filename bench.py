@@ -298,6 +298,8 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-decode-sweep", action="store_true")
     ap.add_argument("--no-prefill-4b", action="store_true")
+    ap.add_argument("--no-multi", action="store_true",
+                    help="skip the multi-token decode steps")
     ap.add_argument("--no-varlen", action="store_true",
                     help="skip the packed variable-length prefill")
     ap.add_argument("--no-gated", action="store_true",
@@ -587,6 +589,43 @@ def main():
                  "decode_frac_of_hbm": gd_bytes / (gd_ms / 1e3) / 1e9 / peaks["hbm_gbs"]}
         del g_gd, g_gp, gz, gzp
     del g_dec, dwl
+    # multi-token steps (gdn_decode_multi) at B = 128: T = 4 and 16 new tokens per sequence in
+    # one step, against T single-token steps; bytes are those of one step plus the extra
+    # tokens' inputs and outputs
+    multi = []
+    if not args.no_multi:
+        for Tm in (4, 16):
+            shm = gi.GDNShape(DECODE_B, Tm, HK, HV, conv_width=W)
+            inm = gi.make_inputs_device(shm, seed=4700 + Tm, device=device)
+            stm = torch.randn(DECODE_B, HV, D, D, device=device) * 0.02
+            csm = torch.zeros(DECODE_B, W - 1, C_CONV, dtype=torch.bfloat16, device=device)
+            outm = torch.empty(DECODE_B, Tm, HV, D, dtype=torch.bfloat16, device=device)
+
+            def callm():
+                gdn.gdn_decode_multi(inm.x, None, None, inm.a, inm.b, inm.A_log, inm.dt_bias, stm,
+                                     outm, num_k_heads=HK, conv_weight=inm.conv_weight,
+                                     conv_state=csm)
+            callm()
+            gm = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(gm):
+                for _ in range(8):
+                    callm()
+            gm.replay()
+            d0.record()
+            for _ in range(3):
+                gm.replay()
+            d1.record()
+            torch.cuda.synchronize()
+            ms_m = d0.elapsed_time(d1) / 24
+            st = gdn.gdn_get_device_error()
+            if st != 0:
+                raise RuntimeError(f"device error in the multi-token step: {gdn.gdn_status_string(st)}")
+            mbytes = dec_bytes + (Tm - 1) * DECODE_B * (C_CONV * 2 + HV * D * 2 + 2 * HV * 2)
+            multi.append({"tokens": Tm, "step_us": 1e3 * ms_m,
+                          "us_per_token": 1e3 * ms_m / Tm,
+                          "vs_single_token_steps": Tm * mean_ms / ms_m,
+                          "gbs": mbytes / (ms_m / 1e3) / 1e9})
+            del gm, inm, stm, csm, outm
     # the other batch sizes of the 27B decode workload (64-step graphs), for latency
     dec_batches = []
     if not args.no_decode_sweep:
@@ -743,7 +782,8 @@ def main():
                                     "frac": dec_gbs / peaks["hbm_gbs"],
                                     "traffic": measured_traffic("decode_step", f"qwen36_27b_decode_B{DECODE_B}"),
                                     "peak_source": peaks["source"]},
-                       "l2": "state 805 MB > L2", "other_batches": dec_batches},
+                       "l2": "state 805 MB > L2", "other_batches": dec_batches,
+                       "multi_token": multi},
             "gated_rmsnorm": gated,
             "e2e": e2e,
             "cpu_baseline": cpu,
