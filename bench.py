@@ -80,6 +80,45 @@ def load_peaks():
     return dict(hbm_gbs=6800.0, bf16=1900.0, bf16_sustained=1700.0, source="fallback")
 
 
+# ------------------------------------------------------------------ ranks
+
+class ControlPlane:
+    """The ranks of one node (torchrun sets RANK / WORLD_SIZE / LOCAL_RANK / MASTER_*): each
+    runs the whole workload on its own GPU (independent sequences, no collective on the data
+    path); gloo carries only the host-side barrier and the max of the timings."""
+
+    def __init__(self):
+        self.world = int(os.environ.get("WORLD_SIZE", "1"))
+        self.rank = int(os.environ.get("RANK", "0"))
+        self.local = int(os.environ.get("LOCAL_RANK", "0"))
+        self.dist = None
+        if self.world > 1:
+            import torch.distributed as dist
+            dist.init_process_group("gloo")
+            self.dist = dist
+
+    def barrier(self):
+        if self.dist is not None:
+            self.dist.barrier()
+
+    def max_over_ranks(self, x: float) -> float:
+        if self.dist is None:
+            return x
+        t = torch.tensor([x], dtype=torch.float64)
+        self.dist.all_reduce(t, op=self.dist.ReduceOp.MAX)
+        return float(t.item())
+
+    def close(self):
+        if self.dist is not None:
+            self.dist.barrier()
+            self.dist.destroy_process_group()
+
+
+def whole_job_rate(world: int, units_per_rank: float, max_ms: float) -> float:
+    """Units per second of the whole job: every rank's units over the slowest rank's time."""
+    return world * units_per_rank / (max_ms / 1e3)
+
+
 # ------------------------------------------------------------------ clocks
 
 class ClockSampler:
@@ -318,28 +357,17 @@ def main():
     if args.impl == "reference":
         return run_reference(args)
 
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
-    dist = None
-    if world > 1:
-        import torch.distributed as dist
-        dist.init_process_group("gloo")
+    cp = ControlPlane()
+    world, rank, local = cp.world, cp.rank, cp.local
     torch.cuda.set_device(local)
     device = torch.device("cuda", local)
 
     def barrier():
         torch.cuda.synchronize()
-        if dist is not None:
-            dist.barrier()
+        cp.barrier()
         torch.cuda.synchronize()
 
-    def max_over_ranks(x: float) -> float:
-        if dist is None:
-            return x
-        t = torch.tensor([x], dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        return float(t.item())
+    max_over_ranks = cp.max_over_ranks
 
     import gated_deltanet_linear_13_gb300 as gdn
     from gated_deltanet_linear_13_gb300 import build_lib
@@ -389,7 +417,7 @@ def main():
         raise RuntimeError(f"device error in the timed region: {gdn.gdn_status_string(st)}")
     prefill_ms = max_over_ranks(prefill_ms)
     ms_per_step = prefill_ms / args.steps
-    value = world * T_TOTAL * args.steps / (prefill_ms / 1e3)
+    value = whole_job_rate(world, T_TOTAL * args.steps, prefill_ms)
     achieved_tflops = FLOP_PER_TOKEN * BUCKET / (call_ms / 1e3) / 1e12
 
     # ---------------- the 4B-shape prefill (16 / 32 heads, B = 4, T = 4096, conv, half the heads
@@ -733,7 +761,7 @@ def main():
         h2d = (hx.numel() * hx.element_size() + ha.numel() * ha.element_size() +
                hb.numel() * hb.element_size())
         d2h = hout.numel() * hout.element_size()
-        e2e = {"value": world * T_TOTAL * e2e_steps / (e2e_ms / 1e3), "unit": "tokens/s",
+        e2e = {"value": whole_job_rate(world, T_TOTAL * e2e_steps, e2e_ms), "unit": "tokens/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                "ms_per_step": e2e_ms / e2e_steps,
                "pipeline": f"per 512-token bucket: uploads on {args.e2e_streams} streams, compute, download"}
@@ -791,9 +819,7 @@ def main():
             "gpu_launches": launches_per_step * args.steps,
         }
         print(json.dumps(line))
-    if dist is not None:
-        dist.barrier()
-        dist.destroy_process_group()
+    cp.close()
     return 0
 
 
