@@ -346,6 +346,8 @@ def main():
     ap.add_argument("--no-single-call", action="store_true",
                     help="skip the one-call 27B prefill with in-kernel snapshots")
     ap.add_argument("--e2e-streams", type=int, default=1, help="upload streams of the e2e pipeline")
+    ap.add_argument("--e2e-group", type=int, default=4,
+                    help="buckets per host copy in the e2e pipeline")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--prefill-tokens", type=int, default=T_TOTAL,
                     help="tokens of the prefill workload (a multiple of 512; smaller only for "
@@ -695,16 +697,20 @@ def main():
         ha.copy_(inp.a)
         hb.copy_(inp.b)
         e2e_steps = max(1, min(args.steps, 3))
-        # A serving-style pipeline through the public API: bucket i's inputs go up on one
-        # stream while bucket i-1 computes and bucket i-2's output comes down on a third;
-        # every byte of every step's inputs and result crosses the host link inside the
-        # timed region.  The whole step is captured once as a CUDA graph.
+        # A serving-style pipeline through the public API: the gate inputs a, b of the step go
+        # up first (two copies), then x in groups of `e2e_group` buckets on one stream while
+        # earlier buckets compute, and each group's output comes down on another as soon as
+        # its last bucket is done; every byte of every step's inputs and result crosses the
+        # host link inside the timed region.  The whole step is captured once as a CUDA graph.
         n_up = args.e2e_streams
+        grp = max(1, args.e2e_group)
         s_ups = [torch.cuda.Stream() for _ in range(n_up)]
         s_down = torch.cuda.Stream()
         nbk = T_TOTAL // BUCKET
-        ev_in = [torch.cuda.Event() for _ in range(nbk)]
-        ev_out = [torch.cuda.Event() for _ in range(nbk)]
+        ngr = (nbk + grp - 1) // grp
+        ev_ab = torch.cuda.Event()
+        ev_in = [torch.cuda.Event() for _ in range(ngr)]
+        ev_out = [torch.cuda.Event() for _ in range(ngr)]
 
         def e2e_body():
             comp = torch.cuda.current_stream()
@@ -713,26 +719,31 @@ def main():
             s_down.wait_stream(comp)
             inp.state.zero_()
             inp.conv_state.zero_()
-            for i in range(nbk):
-                sl = slice(i * BUCKET, (i + 1) * BUCKET)
-                s_up = s_ups[i % n_up]
+            with torch.cuda.stream(s_ups[0]):
+                inp.a.copy_(ha, non_blocking=True)
+                inp.b.copy_(hb, non_blocking=True)
+                ev_ab.record(s_ups[0])
+            comp.wait_event(ev_ab)
+            for gi_ in range(ngr):
+                gs = slice(gi_ * grp * BUCKET, min(nbk, (gi_ + 1) * grp) * BUCKET)
+                s_up = s_ups[gi_ % n_up]
                 with torch.cuda.stream(s_up):
-                    inp.x[:, sl].copy_(hx[:, sl], non_blocking=True)
-                    inp.a[:, sl].copy_(ha[:, sl], non_blocking=True)
-                    inp.b[:, sl].copy_(hb[:, sl], non_blocking=True)
-                    ev_in[i].record(s_up)
-                comp.wait_event(ev_in[i])
-                gdn.gdn_chunk_prefill(inp.x[:, sl], None, None, inp.a[:, sl], inp.b[:, sl],
-                                      inp.A_log, inp.dt_bias, inp.state, wl["out"][:, sl],
-                                      num_k_heads=HK, conv_weight=inp.conv_weight,
-                                      conv_state=inp.conv_state, workspace=wl["ws"])
-                gdn.gdn_state_checkpoint("save", inp.state, inp.conv_state, wl["bank"],
-                                         wl["cbank"], wl["rows"], wl["slots"][i:i + 1],
-                                         num_k_heads=HK)
-                ev_out[i].record(comp)
+                    inp.x[:, gs].copy_(hx[:, gs], non_blocking=True)
+                    ev_in[gi_].record(s_up)
+                comp.wait_event(ev_in[gi_])
+                for i in range(gi_ * grp, min(nbk, (gi_ + 1) * grp)):
+                    sl = slice(i * BUCKET, (i + 1) * BUCKET)
+                    gdn.gdn_chunk_prefill(inp.x[:, sl], None, None, inp.a[:, sl], inp.b[:, sl],
+                                          inp.A_log, inp.dt_bias, inp.state, wl["out"][:, sl],
+                                          num_k_heads=HK, conv_weight=inp.conv_weight,
+                                          conv_state=inp.conv_state, workspace=wl["ws"])
+                    gdn.gdn_state_checkpoint("save", inp.state, inp.conv_state, wl["bank"],
+                                             wl["cbank"], wl["rows"], wl["slots"][i:i + 1],
+                                             num_k_heads=HK)
+                ev_out[gi_].record(comp)
                 with torch.cuda.stream(s_down):
-                    s_down.wait_event(ev_out[i])
-                    hout[:, sl].copy_(wl["out"][:, sl], non_blocking=True)
+                    s_down.wait_event(ev_out[gi_])
+                    hout[:, gs].copy_(wl["out"][:, gs], non_blocking=True)
             for su in s_ups:
                 comp.wait_stream(su)
             comp.wait_stream(s_down)
@@ -764,7 +775,8 @@ def main():
         e2e = {"value": whole_job_rate(world, T_TOTAL * e2e_steps, e2e_ms), "unit": "tokens/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                "ms_per_step": e2e_ms / e2e_steps,
-               "pipeline": f"per 512-token bucket: uploads on {args.e2e_streams} streams, compute, download"}
+               "pipeline": f"a, b up once; x up and out down per {grp} buckets "
+                           f"({args.e2e_streams} upload streams), compute per 512-token bucket"}
 
     # ---------------- CPU oracle baseline (rank 0, bounded sample)
     cpu = None

@@ -42,15 +42,21 @@ __device__ __forceinline__ float dot4(float4 a, float4 b) {
   return fmaf(a.x, b.x, fmaf(a.y, b.y, fmaf(a.z, b.z, a.w * b.w)));
 }
 
-// transposing warp reduction of 32 values per lane: lane l ends with the sum over lanes of
-// value l (five levels of halving, 31 shuffles)
-__device__ __forceinline__ float transpose_reduce32(float (&x)[32], int lane) {
+template <int V> struct Log2 { static constexpr int value = 1 + Log2<V / 2>::value; };
+template <> struct Log2<1> { static constexpr int value = 0; };
+
+// transposing warp reduction of V values per lane (V a power of two <= 32): log2 V halving
+// levels, then plain butterfly levels; value v ends in lanes v * 32/V .. (v+1) * 32/V - 1
+// (V - 1 + 5 - log2 V shuffles)
+template <int V>
+__device__ __forceinline__ float transpose_reduce(float (&x)[V], int lane) {
+  constexpr int LV = Log2<V>::value;
 #pragma unroll
-  for (int lvl = 0; lvl < 5; ++lvl) {
-    const int m = 16 >> lvl, L = 32 >> lvl;
+  for (int lvl = 0; lvl < LV; ++lvl) {
+    const int m = 16 >> lvl, L = V >> lvl;
     const bool up = lane & m;
 #pragma unroll
-    for (int i = 0; i < 16; ++i) {
+    for (int i = 0; i < V / 2; ++i) {
       if (i < L / 2) {
         const float send = up ? x[i] : x[i + L / 2];
         const float keep = up ? x[i + L / 2] : x[i];
@@ -58,7 +64,10 @@ __device__ __forceinline__ float transpose_reduce32(float (&x)[32], int lane) {
       }
     }
   }
-  return x[0];
+  float r = x[0];
+#pragma unroll
+  for (int lvl = LV; lvl < 5; ++lvl) r += __shfl_xor_sync(0xffffffffu, r, 16 >> lvl);
+  return r;
 }
 
 // shared-memory layout (floats) for T tokens and r value heads
@@ -77,7 +86,8 @@ struct MtLayout {
   }
 };
 
-template <typename Tin, typename Tout>
+// TM: the token capacity the loops are unrolled for (T <= TM)
+template <typename Tin, typename Tout, int TM>
 __global__ void __launch_bounds__(MT_THREADS) gdn_decode_multi_kernel(GdnLayerArgs p, int T,
                                                                       float* snap_state,
                                                                       int num_snap,
@@ -109,7 +119,7 @@ __global__ void __launch_bounds__(MT_THREADS) gdn_decode_multi_kernel(GdnLayerAr
     const int ch = cl < D ? kh * D + cl
                    : cl < ch_qk ? p.Hk * D + kh * D + (cl - D)
                                 : 2 * p.Hk * D + kh * r * D + (cl - ch_qk);
-    float win[3 + MT_MAXT];
+    float win[3 + TM];
     if (W > 0) {
       const Tin* cs = (const Tin*)p.conv_state + (size_t)slot * H * C + ch;
       for (int i = 0; i < H; ++i) win[i] = ld_elem(cs + (size_t)i * C);
@@ -208,7 +218,7 @@ __global__ void __launch_bounds__(MT_THREADS) gdn_decode_multi_kernel(GdnLayerAr
     }
     // A and P rows (lane t), then (I + A)^{-1} by forward substitution, column by column
     // (lane j owns column j; rows t > j in order)
-    for (int s2 = 0; s2 < MT_MAXT; ++s2) {
+    for (int s2 = 0; s2 < TM; ++s2) {
       const float Gs = __shfl_sync(0xffffffffu, G, s2 & 31);
       float a = 0.f, pp = 0.f;
       if (lane < T && s2 < T && s2 <= lane) {
@@ -222,12 +232,12 @@ __global__ void __launch_bounds__(MT_THREADS) gdn_decode_multi_kernel(GdnLayerAr
     __syncwarp();
     if (lane < T) {
       const int j = lane;
-      float col[MT_MAXT];
-      for (int t = 0; t < MT_MAXT; ++t) col[t] = (t == j) ? 1.f : 0.f;
-      for (int t = 0; t < MT_MAXT; ++t) {
+      float col[TM];
+      for (int t = 0; t < TM; ++t) col[t] = (t == j) ? 1.f : 0.f;
+      for (int t = 0; t < TM; ++t) {
         if (t > j && t < T) {
           float acc = 0.f;
-          for (int s2 = 0; s2 < MT_MAXT; ++s2)
+          for (int s2 = 0; s2 < TM; ++s2)
             if (s2 >= j && s2 < t) acc = fmaf(Tm[t * T + s2], col[s2], acc);
           col[t] = -acc;
         }
@@ -237,7 +247,12 @@ __global__ void __launch_bounds__(MT_THREADS) gdn_decode_multi_kernel(GdnLayerAr
     }
   }
   __syncthreads();
-  // ---- 5. the state rows: value head hh, rows warp, warp + 8, ...
+  // ---- 5. the state rows: value head hh, rows warp, warp + 8, ... (the next row's load is
+  //      issued before the current row's arithmetic)
+  int* ssl = reinterpret_cast<int*>(red);              // this sequence's snapshot rows
+  if (tid < TM) ssl[tid] = (snap_state && snap_slots && tid < T) ? snap_slots[b * T + tid] : -1;
+  __syncthreads();
+  constexpr int V = 2 * TM, SV = 32 / V;               // reduced values; lanes per value
   for (int hh = 0; hh < r; ++hh) {
     const int h = kh * r + hh;
     const float* Tm = ms + lay.mats + hh * (2 * T * T + 4 * T);
@@ -247,32 +262,36 @@ __global__ void __launch_bounds__(MT_THREADS) gdn_decode_multi_kernel(GdnLayerAr
     const float* eg = bt + 2 * T;
     float* ost = ms + lay.ostage;
     float* Sh = p.state + ((size_t)slot * p.Hv + h) * D * D;
+    float4 s_next = reinterpret_cast<const float4*>(Sh + (size_t)warp * D)[lane];
     for (int i = warp; i < D; i += MT_THREADS / 32) {
-      float4 s = reinterpret_cast<const float4*>(Sh + (size_t)i * D)[lane];
-      float x[32];
+      float4 s = s_next;
+      if (i + MT_THREADS / 32 < D)
+        s_next = reinterpret_cast<const float4*>(Sh + (size_t)(i + MT_THREADS / 32) * D)[lane];
+      float x[V];
 #pragma unroll
-      for (int t = 0; t < 16; ++t) {
+      for (int t = 0; t < TM; ++t) {
         const bool on = t < T;
         x[t] = on ? dot4(s, reinterpret_cast<const float4*>(khat + t * D)[lane]) : 0.f;
-        x[16 + t] = on ? dot4(s, reinterpret_cast<const float4*>(qh + t * D)[lane]) : 0.f;
+        x[TM + t] = on ? dot4(s, reinterpret_cast<const float4*>(qh + t * D)[lane]) : 0.f;
       }
-      // lane l: l < 16: k_l . s0_i;  16 <= l: q_{l-16} . s0_i
-      const float red_l = transpose_reduce32(x, lane);
-      const float ci = __shfl_sync(0xffffffffu, red_l, (lane + 16) & 31);
+      // value v (v < TM: k_v . s0_i; TM <= v: q_{v-TM} . s0_i) lands in lanes v * SV ..
+      const float red_v = transpose_reduce<V>(x, lane);
       const int t = lane;
+      const float ai = __shfl_sync(0xffffffffu, red_v, (t * SV) & 31);
+      const float ci = __shfl_sync(0xffffffffu, red_v, ((TM + t) * SV) & 31);
       float rhs = 0.f;
-      if (t < T) rhs = bt[t] * (vv[t * r * D + hh * D + i] - eG[t] * red_l);
+      if (t < T) rhs = bt[t] * (vv[t * r * D + hh * D + i] - eG[t] * ai);
       // u = (I + A)^{-1} rhs, lane t
       float u = 0.f;
 #pragma unroll
-      for (int s2 = 0; s2 < 16; ++s2) {
+      for (int s2 = 0; s2 < TM; ++s2) {
         const float rs = __shfl_sync(0xffffffffu, rhs, s2);
         if (s2 < T && t < T && s2 <= t) u = fmaf(Tm[t * T + s2], rs, u);
       }
       // outputs and the state after each token
       float o = (t < T) ? eG[t] * ci : 0.f;
 #pragma unroll
-      for (int s2 = 0; s2 < 16; ++s2) {
+      for (int s2 = 0; s2 < TM; ++s2) {
         if (s2 < T) {
           const float us = __shfl_sync(0xffffffffu, u, s2);
           if (t < T && s2 <= t) o = fmaf(P[t * T + s2], us, o);
@@ -282,11 +301,9 @@ __global__ void __launch_bounds__(MT_THREADS) gdn_decode_multi_kernel(GdnLayerAr
           s.y = fmaf(e, s.y, us * k4.y);
           s.z = fmaf(e, s.z, us * k4.z);
           s.w = fmaf(e, s.w, us * k4.w);
-          if (snap_state && snap_slots) {
-            const int sl = snap_slots[b * T + s2];
-            if (sl >= 0 && sl < num_snap)
-              reinterpret_cast<float4*>(snap_state + (((size_t)sl * p.Hv + h) * D + i) * D)[lane] = s;
-          }
+          const int sl = ssl[s2];
+          if (sl >= 0 && sl < num_snap)
+            reinterpret_cast<float4*>(snap_state + (((size_t)sl * p.Hv + h) * D + i) * D)[lane] = s;
         }
       }
       reinterpret_cast<float4*>(Sh + (size_t)i * D)[lane] = s;
@@ -305,18 +322,27 @@ __global__ void __launch_bounds__(MT_THREADS) gdn_decode_multi_kernel(GdnLayerAr
       if (snap_slots[b * T + t] >= num_snap && kh == 0) atomicOr(&g_err_multi, kErrIndex);
 }
 
-template <typename Tin, typename Tout>
-cudaError_t launch_multi_t(const GdnLayerArgs& p, int T, float* snap_state, int num_snap,
-                           const int32_t* snap_slots, void* snap_conv, cudaStream_t stream) {
+template <typename Tin, typename Tout, int TM>
+cudaError_t launch_multi_tm(const GdnLayerArgs& p, int T, float* snap_state, int num_snap,
+                            const int32_t* snap_slots, void* snap_conv, cudaStream_t stream) {
   const MtLayout lay(T, p.Hv / p.Hk);
   const size_t smem = sizeof(float) * lay.total;
   static unsigned done = 0;
-  cudaError_t e = set_smem_once(gdn_decode_multi_kernel<Tin, Tout>,
-                                (int)(sizeof(float) * MtLayout(MT_MAXT, 8).total), &done);
+  cudaError_t e = set_smem_once(gdn_decode_multi_kernel<Tin, Tout, TM>,
+                                (int)(sizeof(float) * MtLayout(TM, 8).total), &done);
   if (e != cudaSuccess) return e;
-  gdn_decode_multi_kernel<Tin, Tout><<<(unsigned)(p.B * p.Hk), MT_THREADS, smem, stream>>>(
+  gdn_decode_multi_kernel<Tin, Tout, TM><<<(unsigned)(p.B * p.Hk), MT_THREADS, smem, stream>>>(
       p, T, snap_state, num_snap, snap_slots, static_cast<Tin*>(snap_conv));
   return cudaGetLastError();
+}
+
+template <typename Tin, typename Tout>
+cudaError_t launch_multi_t(const GdnLayerArgs& p, int T, float* snap_state, int num_snap,
+                           const int32_t* snap_slots, void* snap_conv, cudaStream_t stream) {
+  if (T <= 2) return launch_multi_tm<Tin, Tout, 2>(p, T, snap_state, num_snap, snap_slots, snap_conv, stream);
+  if (T <= 4) return launch_multi_tm<Tin, Tout, 4>(p, T, snap_state, num_snap, snap_slots, snap_conv, stream);
+  if (T <= 8) return launch_multi_tm<Tin, Tout, 8>(p, T, snap_state, num_snap, snap_slots, snap_conv, stream);
+  return launch_multi_tm<Tin, Tout, 16>(p, T, snap_state, num_snap, snap_slots, snap_conv, stream);
 }
 
 }  // namespace
