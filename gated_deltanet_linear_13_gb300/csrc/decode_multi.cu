@@ -262,52 +262,81 @@ __global__ void __launch_bounds__(MT_THREADS) gdn_decode_multi_kernel(GdnLayerAr
     const float* eg = bt + 2 * T;
     float* ost = ms + lay.ostage;
     float* Sh = p.state + ((size_t)slot * p.Hv + h) * D * D;
-    float4 s_next = reinterpret_cast<const float4*>(Sh + (size_t)warp * D)[lane];
-    for (int i = warp; i < D; i += MT_THREADS / 32) {
-      float4 s = s_next;
-      if (i + MT_THREADS / 32 < D)
-        s_next = reinterpret_cast<const float4*>(Sh + (size_t)(i + MT_THREADS / 32) * D)[lane];
-      float x[V];
+    // rows i, i + 8, ... two at a time for short token counts (independent chains that the
+    // scheduler interleaves), one at a time for long ones (registers)
+    constexpr int RPI = TM <= 8 ? 2 : 1;
+    constexpr int STEP = RPI * (MT_THREADS / 32);
+    float4 s_next[RPI];
 #pragma unroll
-      for (int t = 0; t < TM; ++t) {
-        const bool on = t < T;
-        x[t] = on ? dot4(s, reinterpret_cast<const float4*>(khat + t * D)[lane]) : 0.f;
-        x[TM + t] = on ? dot4(s, reinterpret_cast<const float4*>(qh + t * D)[lane]) : 0.f;
+    for (int q = 0; q < RPI; ++q)
+      s_next[q] = reinterpret_cast<const float4*>(Sh + (size_t)(warp + q * 8) * D)[lane];
+    for (int i0 = warp; i0 < D; i0 += STEP) {
+      float4 sr[RPI];
+#pragma unroll
+      for (int q = 0; q < RPI; ++q) {
+        sr[q] = s_next[q];
+        if (i0 + STEP < D)
+          s_next[q] = reinterpret_cast<const float4*>(Sh + (size_t)(i0 + STEP + q * 8) * D)[lane];
       }
-      // value v (v < TM: k_v . s0_i; TM <= v: q_{v-TM} . s0_i) lands in lanes v * SV ..
-      const float red_v = transpose_reduce<V>(x, lane);
+      float red_v[RPI];
+#pragma unroll
+      for (int q = 0; q < RPI; ++q) {
+        float x[V];
+#pragma unroll
+        for (int t = 0; t < TM; ++t) {
+          const bool on = t < T;
+          x[t] = on ? dot4(sr[q], reinterpret_cast<const float4*>(khat + t * D)[lane]) : 0.f;
+          x[TM + t] = on ? dot4(sr[q], reinterpret_cast<const float4*>(qh + t * D)[lane]) : 0.f;
+        }
+        // value v (v < TM: k_v . s0_i; TM <= v: q_{v-TM} . s0_i) lands in lanes v * SV ..
+        red_v[q] = transpose_reduce<V>(x, lane);
+      }
       const int t = lane;
-      const float ai = __shfl_sync(0xffffffffu, red_v, (t * SV) & 31);
-      const float ci = __shfl_sync(0xffffffffu, red_v, ((TM + t) * SV) & 31);
-      float rhs = 0.f;
-      if (t < T) rhs = bt[t] * (vv[t * r * D + hh * D + i] - eG[t] * ai);
+      float rhs[RPI], u[RPI], o[RPI];
+#pragma unroll
+      for (int q = 0; q < RPI; ++q) {
+        const int i = i0 + q * 8;
+        const float ai = __shfl_sync(0xffffffffu, red_v[q], (t * SV) & 31);
+        const float ci = __shfl_sync(0xffffffffu, red_v[q], ((TM + t) * SV) & 31);
+        rhs[q] = (t < T) ? bt[t] * (vv[t * r * D + hh * D + i] - eG[t] * ai) : 0.f;
+        o[q] = (t < T) ? eG[t] * ci : 0.f;
+        u[q] = 0.f;
+      }
       // u = (I + A)^{-1} rhs, lane t
-      float u = 0.f;
 #pragma unroll
       for (int s2 = 0; s2 < TM; ++s2) {
-        const float rs = __shfl_sync(0xffffffffu, rhs, s2);
-        if (s2 < T && t < T && s2 <= t) u = fmaf(Tm[t * T + s2], rs, u);
+        const float tm = (s2 < T && t < T && s2 <= t) ? Tm[t * T + s2] : 0.f;
+#pragma unroll
+        for (int q = 0; q < RPI; ++q) u[q] = fmaf(tm, __shfl_sync(0xffffffffu, rhs[q], s2), u[q]);
       }
       // outputs and the state after each token
-      float o = (t < T) ? eG[t] * ci : 0.f;
 #pragma unroll
       for (int s2 = 0; s2 < TM; ++s2) {
         if (s2 < T) {
-          const float us = __shfl_sync(0xffffffffu, u, s2);
-          if (t < T && s2 <= t) o = fmaf(P[t * T + s2], us, o);
+          const float pv = (t < T && s2 <= t) ? P[t * T + s2] : 0.f;
           const float4 k4 = reinterpret_cast<const float4*>(khat + s2 * D)[lane];
           const float e = eg[s2];
-          s.x = fmaf(e, s.x, us * k4.x);
-          s.y = fmaf(e, s.y, us * k4.y);
-          s.z = fmaf(e, s.z, us * k4.z);
-          s.w = fmaf(e, s.w, us * k4.w);
           const int sl = ssl[s2];
-          if (sl >= 0 && sl < num_snap)
-            reinterpret_cast<float4*>(snap_state + (((size_t)sl * p.Hv + h) * D + i) * D)[lane] = s;
+#pragma unroll
+          for (int q = 0; q < RPI; ++q) {
+            const float us = __shfl_sync(0xffffffffu, u[q], s2);
+            o[q] = fmaf(pv, us, o[q]);
+            sr[q].x = fmaf(e, sr[q].x, us * k4.x);
+            sr[q].y = fmaf(e, sr[q].y, us * k4.y);
+            sr[q].z = fmaf(e, sr[q].z, us * k4.z);
+            sr[q].w = fmaf(e, sr[q].w, us * k4.w);
+            if (sl >= 0 && sl < num_snap)
+              reinterpret_cast<float4*>(snap_state +
+                                        (((size_t)sl * p.Hv + h) * D + i0 + q * 8) * D)[lane] = sr[q];
+          }
         }
       }
-      reinterpret_cast<float4*>(Sh + (size_t)i * D)[lane] = s;
-      if (t < T) ost[t * D + i] = o;
+#pragma unroll
+      for (int q = 0; q < RPI; ++q) {
+        const int i = i0 + q * 8;
+        reinterpret_cast<float4*>(Sh + (size_t)i * D)[lane] = sr[q];
+        if (t < T) ost[t * D + i] = o[q];
+      }
     }
     __syncthreads();
     // this head's outputs, token rows of 128 channels

@@ -60,6 +60,16 @@ def test_bf16_conv_matches_oracle(gdn, T):
     np.testing.assert_array_equal(dev.conv_state.float().cpu().numpy(), ref.conv_state)
 
 
+def test_bf16_in_fp32_out(gdn):
+    sh, inp = _inputs(2, 7, 2, 4, 4, "bf16", 8050)
+    ref = oracle_full(inp)
+    dev = to_device(inp)
+    out = _run(gdn, dev, sh, torch.float32)
+    assert gdn.gdn_get_device_error() == 0
+    assert_bf16_parity(out.cpu(), ref.out)
+    assert_state_parity(dev.state.cpu(), ref.state)
+
+
 @pytest.mark.parametrize("T", [3, 16])
 def test_fp32_mode(gdn, T):
     sh, inp = _inputs(2, T, 4, 4, 0, "f32", 8100 + T)

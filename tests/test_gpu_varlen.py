@@ -168,3 +168,15 @@ def test_bad_offsets_compute_nothing(gdn):
     assert torch.equal(dev.state, before)
     assert torch.equal(dev.conv_state, cbefore)
     assert torch.all(out.float() == SENT)
+
+
+def test_packed_fp32_gated_norm(gdn):
+    """fp32 mode with the gated norm: the norm runs as a pass of its own that finds each
+    token's sequence (and skips the skipped one) by bisection on the offsets."""
+    sh, inp, cu = _packed_inputs([40, 0, 77, 64, 5], 4, 8, 0, "f32", 7600)
+    g = torch.Generator().manual_seed(11)
+    z = torch.randn(1, sh.seqlen, 8, 128, generator=g).cuda()
+    w = (torch.rand(128, generator=g) + 0.5).cuda()
+    _, out = _compare(gdn, sh, inp, cu, [3, 4, -1, 0, 1], torch.float32, gate=(z, w))
+    t0, t1 = int(cu[2]), int(cu[3])
+    assert torch.all(out[:, t0:t1] == SENT)
