@@ -323,6 +323,55 @@ def run_reference(args):
     return 0
 
 
+# ------------------------------------------------------------------ profiler cases
+
+def varlen16_inputs(device):
+    """The packed 27B-shape batch of the bench: 16 sequences of seeded lengths in [64, 2048]."""
+    lens = torch.randint(64, 2049, (16,), generator=torch.Generator().manual_seed(77))
+    cu = torch.zeros(17, dtype=torch.int32)
+    cu[1:] = torch.cumsum(lens, 0).to(torch.int32)
+    Tv = int(cu[-1])
+    inv = gi.make_inputs_device(gi.GDNShape(1, Tv, HK, HV, conv_width=W), seed=4600,
+                                device=device)
+    return lens, cu, Tv, inv
+
+
+def run_case(args):
+    """One workload, three calls, nothing printed but a status line (for ncu captures)."""
+    import gated_deltanet_linear_13_gb300 as gdn
+    from gated_deltanet_linear_13_gb300 import build_lib
+    build_lib.build()
+    gdn.load_library()
+    device = torch.device("cuda", 0)
+    if args.case == "decode_multi_T4":
+        B, Tm = DECODE_B, 4
+        inm = gi.make_inputs_device(gi.GDNShape(B, Tm, HK, HV, conv_width=W), seed=4704,
+                                    device=device)
+        st = torch.randn(B, HV, D, D, device=device) * 0.02
+        cs = torch.zeros(B, W - 1, C_CONV, dtype=torch.bfloat16, device=device)
+        out = torch.empty(B, Tm, HV, D, dtype=torch.bfloat16, device=device)
+        for _ in range(3):
+            gdn.gdn_decode_multi(inm.x, None, None, inm.a, inm.b, inm.A_log, inm.dt_bias, st,
+                                 out, num_k_heads=HK, conv_weight=inm.conv_weight,
+                                 conv_state=cs)
+    else:
+        lens, cu, Tv, inv = varlen16_inputs(device)
+        st = torch.zeros(16, HV, D, D, device=device)
+        cs = torch.zeros(16, W - 1, C_CONV, dtype=torch.bfloat16, device=device)
+        out = torch.empty(1, Tv, HV, D, dtype=torch.bfloat16, device=device)
+        for _ in range(3):
+            gdn.gdn_chunk_prefill_varlen(inv.x, None, None, inv.a, inv.b, inv.A_log,
+                                         inv.dt_bias, st, out, cu_seqlens=cu.to(device),
+                                         num_k_heads=HK, conv_weight=inv.conv_weight,
+                                         conv_state=cs)
+    torch.cuda.synchronize()
+    st = gdn.gdn_get_device_error()
+    if st != 0:
+        raise RuntimeError(f"device error in case {args.case}: {gdn.gdn_status_string(st)}")
+    print(f"case {args.case}: ok")
+    return 0
+
+
 # ------------------------------------------------------------------ main
 
 def main():
@@ -353,11 +402,15 @@ def main():
                     help="tokens of the prefill workload (a multiple of 512; smaller only for "
                          "profiling captures, the reported workload is 131072)")
     ap.add_argument("--decode-batch", type=int, default=DECODE_B)
+    ap.add_argument("--case", default=None, choices=["decode_multi_T4", "varlen16"],
+                    help="run one workload three times and exit (for profiler captures)")
     args = ap.parse_args()
     globals()["T_TOTAL"] = args.prefill_tokens
     globals()["DECODE_B"] = args.decode_batch
     if args.impl == "reference":
         return run_reference(args)
+    if args.case:
+        return run_case(args)
 
     cp = ControlPlane()
     world, rank, local = cp.world, cp.rank, cp.local
@@ -501,12 +554,7 @@ def main():
     # ---------------- a packed variable-length batch of the 27B shape: 16 sequences of seeded
     #                  lengths in [64, 2048] (about 17k tokens) in one call
     if not args.no_varlen:
-        lens = torch.randint(64, 2049, (16,), generator=torch.Generator().manual_seed(77))
-        cu = torch.zeros(17, dtype=torch.int32)
-        cu[1:] = torch.cumsum(lens, 0).to(torch.int32)
-        Tv = int(cu[-1])
-        shv = gi.GDNShape(1, Tv, HK, HV, conv_width=W)
-        inv = gi.make_inputs_device(shv, seed=4600, device=device)
+        lens, cu, Tv, inv = varlen16_inputs(device)
         stv = torch.zeros(16, HV, D, D, device=device)
         csv = torch.zeros(16, W - 1, C_CONV, dtype=torch.bfloat16, device=device)
         outv = torch.empty(1, Tv, HV, D, dtype=torch.bfloat16, device=device)

@@ -332,7 +332,7 @@ __global__ void __launch_bounds__(CONV_THREADS, 3) gdn_conv_varlen_kernel(
 }
 
 // New conv state of each packed sequence: its last W-1 inputs, the older ones from its old
-// state when it is shorter than W-1.  One CTA per sequence; a thread owns whole words.
+// state when it is shorter than W-1.  CTA (sequence, block of words); a thread owns a word.
 template <typename T, int W>
 __global__ void __launch_bounds__(256) gdn_conv_state_varlen_kernel(
     int N, int C, const int32_t* cu, const T* x, long long xs, T* cs, int num_slots,
@@ -344,12 +344,13 @@ __global__ void __launch_bounds__(256) gdn_conv_state_varlen_kernel(
   const int slot = slots ? slots[n] : n;
   if (slot < 0) return;
   if (slot >= num_slots) {
-    if (threadIdx.x == 0) atomicOr(&g_err_conv, kErrIndex);
+    if (threadIdx.x == 0 && blockIdx.y == 0) atomicOr(&g_err_conv, kErrIndex);
     return;
   }
   const int s0 = cu[n], s1 = cu[n + 1];
   T* csn = cs + (size_t)slot * H * C;
-  for (int c0 = threadIdx.x * CPT; c0 < C; c0 += blockDim.x * CPT) {
+  const int c0 = (blockIdx.y * blockDim.x + threadIdx.x) * CPT;
+  if (c0 < C) {
     float old[H > 0 ? H : 1][CPT], nst[H > 0 ? H : 1][CPT];
 #pragma unroll
     for (int i = 0; i < H; ++i) ld_word(csn + (size_t)i * C + c0, old[i]);
@@ -386,8 +387,10 @@ static cudaError_t launch_conv_varlen_w(const CUtensorMap& m, int N, int Tn, int
                                                                    ns, slots, silu, y, ys);
   e = cudaGetLastError();
   if (e != cudaSuccess || W < 2) return e;
-  return launch_pdl(true, gdn_conv_state_varlen_kernel<T, W>, dim3((unsigned)N), dim3(256), 0,
-                    stream, N, C, cu, x, xs, cs, ns, slots);
+  constexpr int cpt = 8 / (int)sizeof(T);
+  const unsigned wblocks = (unsigned)((C + 256 * cpt - 1) / (256 * cpt));
+  return launch_pdl(true, gdn_conv_state_varlen_kernel<T, W>, dim3((unsigned)N, wblocks),
+                    dim3(256), 0, stream, N, C, cu, x, xs, cs, ns, slots);
 }
 
 template <typename T>
