@@ -386,6 +386,8 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-decode-sweep", action="store_true")
     ap.add_argument("--no-prefill-4b", action="store_true")
+    ap.add_argument("--no-latency", action="store_true",
+                    help="skip the small-call latency sweep")
     ap.add_argument("--no-multi", action="store_true",
                     help="skip the multi-token decode steps")
     ap.add_argument("--no-varlen", action="store_true",
@@ -591,6 +593,57 @@ def main():
                               "frac_of_bf16_sustained": tfv / peaks["bf16_sustained"],
                               "lengths": [int(x) for x in lens]})
         del gv, inv, stv, csv, outv, wsv
+
+    # ---------------- small calls: the 0.8B-shape prefill (16 / 16 heads, no conv, bf16, B = 1)
+    #                  per T of its sweep, and the tiny fp32 layer (B = 1, T = 16): device time
+    #                  per call, from a CUDA graph of 10 calls (so that host launch overhead is
+    #                  not timed), median of 50 replays after 5 warm-ups; for T <= 16 also the
+    #                  multi-token step on the same inputs
+    latency = []
+    if not args.no_latency:
+        def lat_ms(fn):
+            fn()
+            gl = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(gl):
+                for _ in range(10):
+                    fn()
+            for _ in range(5):
+                gl.replay()
+            evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                   for _ in range(50)]
+            for a0, a1 in evs:
+                a0.record()
+                gl.replay()
+                a1.record()
+            torch.cuda.synchronize()
+            return statistics.median(a0.elapsed_time(a1) for a0, a1 in evs) / 10
+        for Tl, f32 in [(t, False) for t in gi.SEQLEN_SWEEP_08B] + [(16, True)]:
+            shl = gi.GDNShape(1, Tl, 16, 16, conv_width=0)
+            inl = gi.make_inputs_device(shl, seed=4900 + Tl, device=device,
+                                        dtype="f32" if f32 else "bf16")
+            stl = torch.randn(1, 16, D, D, device=device) * 0.02
+            outl = torch.empty(1, Tl, 16, D, dtype=torch.float32 if f32 else torch.bfloat16,
+                               device=device)
+            wsl = torch.empty(max(16, gdn.gdn_prefill_workspace_size(
+                1, Tl, 16, 16, 0, torch.float32 if f32 else torch.bfloat16)),
+                dtype=torch.uint8, device=device)
+
+            def callp():
+                gdn.gdn_chunk_prefill(inl.q, inl.k, inl.v, inl.a, inl.b, inl.A_log, inl.dt_bias,
+                                      stl, outl, workspace=wsl)
+
+            row = {"workload": ("tiny_fp32_B1_T16_16h" if f32 else f"qwen35_08b_prefill_T{Tl}"),
+                   "T": Tl, "prefill_call_us": 1e3 * lat_ms(callp)}
+            if Tl <= 16:
+                def callm():
+                    gdn.gdn_decode_multi(inl.q, inl.k, inl.v, inl.a, inl.b, inl.A_log,
+                                         inl.dt_bias, stl, outl)
+                row["decode_multi_us"] = 1e3 * lat_ms(callm)
+            latency.append(row)
+            del inl, stl, outl, wsl
+        st = gdn.gdn_get_device_error()
+        if st != 0:
+            raise RuntimeError(f"device error in the latency sweep: {gdn.gdn_status_string(st)}")
 
     # ---------------- decode (same run, HBM-resident state), 256 steps as one CUDA graph
     dwl = make_decode_workload(device)
@@ -861,6 +914,7 @@ def main():
                          "flop_per_launch": FLOP_PER_TOKEN * BUCKET,
                          "launch_ms": call_ms, "peak_source": peaks["source"] + " sustained"},
             "other_prefill": other_prefill,
+            "latency": latency,
             "decode": {"metric": "decode state-update HBM GB/s", "value": dec_gbs,
                        "unit": "GB/s", "batch": DECODE_B, "steps": DECODE_STEPS,
                        "step_ms_graph_mean": mean_ms, "step_ms_eager_median": eager_ms,

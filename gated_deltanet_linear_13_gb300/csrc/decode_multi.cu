@@ -15,10 +15,13 @@
 // with the k_t and q_t are independent of each other, so a warp forms all 2T at once and one
 // transposing warp reduction (31 shuffles) leaves lane l with dot product l.
 //
-// One CTA per (sequence, key head): the prologue convolves the T tokens of the key head's
-// q/k channels and its r value heads' v channels (and writes the new conv state), forms the
-// norms, the gates and, per value head, (I + A)^{-1} and P in shared memory.  Then each warp
-// streams state rows: one 512-byte row per warp access, coalesced.
+// One CTA per (sequence, key head), or, at small batches, a thread-block cluster of nsplit
+// CTAs that split the rows of each value head.  The prologue convolves the T tokens of the
+// key head's q/k channels and of its own rows' v channels (and writes their new conv state),
+// forms the norms, the gates and, per value head, (I + A)^{-1} and P in shared memory.  Then
+// each warp streams state rows: one 512-byte row per warp access, coalesced.  All CTAs of a
+// cluster read the old q/k conv state; a cluster barrier orders those reads before the one
+// CTA (rank 0) that writes the new one.
 #include "common.cuh"
 
 using namespace gdn;
@@ -37,6 +40,13 @@ namespace {
 constexpr int D = kHeadDim;
 constexpr int MT_THREADS = 256;
 constexpr int MT_MAXT = 16;
+
+__device__ __forceinline__ void cluster_arrive_relaxed_mt() {
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;\n" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait_mt() {
+  asm volatile("barrier.cluster.wait.acquire.aligned;\n" ::: "memory");
+}
 
 __device__ __forceinline__ float dot4(float4 a, float4 b) {
   return fmaf(a.x, b.x, fmaf(a.y, b.y, fmaf(a.z, b.z, a.w * b.w)));
@@ -92,15 +102,18 @@ __global__ void __launch_bounds__(MT_THREADS) gdn_decode_multi_kernel(GdnLayerAr
                                                                       float* snap_state,
                                                                       int num_snap,
                                                                       const int32_t* snap_slots,
-                                                                      Tin* snap_conv) {
+                                                                      Tin* snap_conv,
+                                                                      int nsplit) {
   extern __shared__ __align__(16) float ms[];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int r = p.Hv / p.Hk;
-  const int b = blockIdx.x / p.Hk, kh = blockIdx.x % p.Hk;
+  const int item = blockIdx.x / nsplit, sp = blockIdx.x % nsplit;
+  const int b = item / p.Hk, kh = item % p.Hk;
+  const int R = D / nsplit, r_lo = sp * R;          // this CTA's rows of every value head
   const int slot = p.slots ? p.slots[b] : b;
   if (slot < 0) return;
-  if (slot >= p.num_slots) {
-    if (tid == 0 && kh == 0) atomicOr(&g_err_multi, kErrIndex);
+  if (slot >= p.num_slots) {            // (decided per sequence: a whole cluster leaves)
+    if (tid == 0 && kh == 0 && sp == 0) atomicOr(&g_err_multi, kErrIndex);
     return;
   }
   const MtLayout lay(T, r);
@@ -111,14 +124,18 @@ __global__ void __launch_bounds__(MT_THREADS) gdn_decode_multi_kernel(GdnLayerAr
   float* QK = ms + lay.qk;
   float* red = ms + lay.red;
   const int W = p.W, H = W > 0 ? W - 1 : 0, C = p.C_conv;
-  const int ch_qk = 2 * D, ch_all = ch_qk + r * D;
-  // ---- 1. conv (+SiLU) of this item's channels over the T tokens, or plain loads; the new
-  //      conv state, and the conv state after every token for the snapshots
+  const int ch_qk = 2 * D, ch_all = ch_qk + r * R;
+  // ---- 1. conv (+SiLU) of this CTA's channels over the T tokens, or plain loads; the new
+  //      conv state, and the conv state after every token for the snapshots (for the q/k
+  //      channels, which every CTA of a cluster reads, once the cluster's reads are done)
+  float qkwin[3 + TM];                                  // this thread's q/k channel (tid < 256)
+  int qkch = -1;
   for (int cl = tid; cl < ch_all; cl += MT_THREADS) {
-    // local channel cl: q (0..127), k (128..255), v of value head cl / 128 - 2
+    // local channel cl: q (0..127), k (128..255), then v of value head vh, row r_lo + vi
+    const int vh = (cl - ch_qk) / R, vi = r_lo + (cl - ch_qk) % R;
     const int ch = cl < D ? kh * D + cl
                    : cl < ch_qk ? p.Hk * D + kh * D + (cl - D)
-                                : 2 * p.Hk * D + kh * r * D + (cl - ch_qk);
+                                : 2 * p.Hk * D + (kh * r + vh) * D + vi;
     float win[3 + TM];
     if (W > 0) {
       const Tin* cs = (const Tin*)p.conv_state + (size_t)slot * H * C + ch;
@@ -135,18 +152,23 @@ __global__ void __launch_bounds__(MT_THREADS) gdn_decode_multi_kernel(GdnLayerAr
         y = p.silu ? silu_f(y) : y;
         if (cl < D) qh[t * D + cl] = y;
         else if (cl < ch_qk) khat[t * D + cl - D] = y;
-        else vv[t * r * D + cl - ch_qk] = y;
+        else vv[t * r * D + vh * D + vi] = y;
       }
       // new conv state: the last W-1 window entries; after token t: entries t+1 .. t+W-1
-      Tin* csw = (Tin*)p.conv_state + (size_t)slot * H * C + ch;
-      for (int i = 0; i < H; ++i) st_elem(csw + (size_t)i * C, win[T + i]);
-      if (snap_conv && snap_slots)
-        for (int t = 0; t < T; ++t) {
-          const int sl = snap_slots[b * T + t];
-          if (sl >= 0 && sl < num_snap)
-            for (int i = 0; i < H; ++i)
-              st_elem(snap_conv + ((size_t)sl * H + i) * C + ch, win[t + 1 + i]);
-        }
+      if (cl < ch_qk) {
+        qkch = ch;
+        for (int i = 0; i < H + T; ++i) qkwin[i] = win[i];
+      } else {
+        Tin* csw = (Tin*)p.conv_state + (size_t)slot * H * C + ch;
+        for (int i = 0; i < H; ++i) st_elem(csw + (size_t)i * C, win[T + i]);
+        if (snap_conv && snap_slots)
+          for (int t = 0; t < T; ++t) {
+            const int sl = snap_slots[b * T + t];
+            if (sl >= 0 && sl < num_snap)
+              for (int i = 0; i < H; ++i)
+                st_elem(snap_conv + ((size_t)sl * H + i) * C + ch, win[t + 1 + i]);
+          }
+      }
     } else {
       for (int t = 0; t < T; ++t) {
         float y;
@@ -157,12 +179,14 @@ __global__ void __launch_bounds__(MT_THREADS) gdn_decode_multi_kernel(GdnLayerAr
           y = ld_elem((const Tin*)p.k + (((size_t)b * T + t) * p.Hk + kh) * D + cl - D);
           khat[t * D + cl - D] = y;
         } else {
-          y = ld_elem((const Tin*)p.v + (((size_t)b * T + t) * p.Hv + kh * r) * D + cl - ch_qk);
-          vv[t * r * D + cl - ch_qk] = y;
+          y = ld_elem((const Tin*)p.v + (((size_t)b * T + t) * p.Hv + kh * r + vh) * D + vi);
+          vv[t * r * D + vh * D + vi] = y;
         }
       }
     }
   }
+  // every CTA of the cluster has read the old q/k conv state (the values are consumed)
+  if (nsplit > 1) cluster_arrive_relaxed_mt();
   __syncthreads();
   // ---- 2. L2 norms of q_t and k_t (one warp per vector), q also times `scale`
   for (int vec = warp; vec < 2 * T; vec += MT_THREADS / 32) {
@@ -174,13 +198,20 @@ __global__ void __launch_bounds__(MT_THREADS) gdn_decode_multi_kernel(GdnLayerAr
     reinterpret_cast<float4*>(x)[lane] = v4;
   }
   __syncthreads();
-  // ---- 3. KK_ts = k_t . k_s and QK_ts = q_t . k_s (one warp per pair)
-  for (int pr = warp; pr < 2 * T * T; pr += MT_THREADS / 32) {
+  // ---- 3. KK_ts = k_t . k_s and QK_ts = q_t . k_s (a thread per pair, 2 T^2 <= 512; the
+  //      thread walks its two vectors from rotated starting points so that a warp's lanes
+  //      read different banks)
+  for (int pr = tid; pr < 2 * T * T; pr += MT_THREADS) {
     const int which = pr / (T * T), t = (pr / T) % T, s2 = pr % T;
-    const float4 a4 = reinterpret_cast<const float4*>((which ? qh : khat) + t * D)[lane];
-    const float4 k4 = reinterpret_cast<const float4*>(khat + s2 * D)[lane];
-    const float d = warp_sum(dot4(a4, k4));
-    if (lane == 0) (which ? QK : KK)[t * T + s2] = d;
+    const float4* a4 = reinterpret_cast<const float4*>((which ? qh : khat) + t * D);
+    const float4* k4 = reinterpret_cast<const float4*>(khat + s2 * D);
+    float d = 0.f;
+#pragma unroll 8
+    for (int j = 0; j < D / 4; ++j) {
+      const int jj = (j + lane) & (D / 4 - 1);
+      d += dot4(a4[jj], k4[jj]);
+    }
+    (which ? QK : KK)[t * T + s2] = d;
   }
   __syncthreads();
   // ---- 4. per value head: gates, G, (I + A)^{-1} and P (warp hh, lanes = tokens)
@@ -269,13 +300,13 @@ __global__ void __launch_bounds__(MT_THREADS) gdn_decode_multi_kernel(GdnLayerAr
     float4 s_next[RPI];
 #pragma unroll
     for (int q = 0; q < RPI; ++q)
-      s_next[q] = reinterpret_cast<const float4*>(Sh + (size_t)(warp + q * 8) * D)[lane];
-    for (int i0 = warp; i0 < D; i0 += STEP) {
+      s_next[q] = reinterpret_cast<const float4*>(Sh + (size_t)(r_lo + warp + q * 8) * D)[lane];
+    for (int i0 = r_lo + warp; i0 < r_lo + R; i0 += STEP) {
       float4 sr[RPI];
 #pragma unroll
       for (int q = 0; q < RPI; ++q) {
         sr[q] = s_next[q];
-        if (i0 + STEP < D)
+        if (i0 + STEP < r_lo + R)
           s_next[q] = reinterpret_cast<const float4*>(Sh + (size_t)(i0 + STEP + q * 8) * D)[lane];
       }
       float red_v[RPI];
@@ -340,13 +371,27 @@ __global__ void __launch_bounds__(MT_THREADS) gdn_decode_multi_kernel(GdnLayerAr
     }
     __syncthreads();
     // this head's outputs, token rows of 128 channels
-    for (int e = tid; e < T * D; e += MT_THREADS) {
-      const int tt = e / D, c = e % D;
-      st_elem((Tout*)p.out + (((size_t)b * T + tt) * p.Hv + h) * D + c, ost[e]);
+    for (int e = tid; e < T * R; e += MT_THREADS) {
+      const int tt = e / R, c = r_lo + e % R;
+      st_elem((Tout*)p.out + (((size_t)b * T + tt) * p.Hv + h) * D + c, ost[tt * D + c]);
     }
     __syncthreads();
   }
-  if (tid == 0 && snap_slots)
+  // the q/k channels' new conv state (and per-token snapshots): rank 0, after the cluster's
+  // reads of the old one
+  if (nsplit > 1) cluster_wait_mt();
+  if (sp == 0 && W > 0 && qkch >= 0) {
+    Tin* csw = (Tin*)p.conv_state + (size_t)slot * H * C + qkch;
+    for (int i = 0; i < H; ++i) st_elem(csw + (size_t)i * C, qkwin[T + i]);
+    if (snap_conv && snap_slots)
+      for (int t = 0; t < T; ++t) {
+        const int sl = snap_slots[b * T + t];
+        if (sl >= 0 && sl < num_snap)
+          for (int i = 0; i < H; ++i)
+            st_elem(snap_conv + ((size_t)sl * H + i) * C + qkch, qkwin[t + 1 + i]);
+      }
+  }
+  if (tid == 0 && sp == 0 && snap_slots)
     for (int t = 0; t < T; ++t)
       if (snap_slots[b * T + t] >= num_snap && kh == 0) atomicOr(&g_err_multi, kErrIndex);
 }
@@ -360,9 +405,29 @@ cudaError_t launch_multi_tm(const GdnLayerArgs& p, int T, float* snap_state, int
   cudaError_t e = set_smem_once(gdn_decode_multi_kernel<Tin, Tout, TM>,
                                 (int)(sizeof(float) * MtLayout(TM, 8).total), &done);
   if (e != cudaSuccess) return e;
-  gdn_decode_multi_kernel<Tin, Tout, TM><<<(unsigned)(p.B * p.Hk), MT_THREADS, smem, stream>>>(
-      p, T, snap_state, num_snap, snap_slots, static_cast<Tin*>(snap_conv));
-  return cudaGetLastError();
+  // rows of each value head split over a cluster of nsplit CTAs when the (sequence, key head)
+  // items alone would leave most SMs idle
+  int dev = 0, sms = 0;
+  if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+  if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+    return e;
+  const int nitems = p.B * p.Hk;
+  int nsplit = 1;
+  while (nsplit < 8 && nitems * nsplit * 2 <= 2 * sms) nsplit *= 2;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(nitems * nsplit), 1, 1);
+  cfg.blockDim = dim3(MT_THREADS, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = (unsigned)nsplit;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = nsplit > 1 ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, gdn_decode_multi_kernel<Tin, Tout, TM>, p, T, snap_state,
+                            num_snap, snap_slots, static_cast<Tin*>(snap_conv), nsplit);
 }
 
 template <typename Tin, typename Tout>
