@@ -29,10 +29,13 @@
 //     in the swizzled layouts the chain's MMAs read, written with bulk copies to a workspace
 //     slice small enough to stay in L2, plus e^{G_C}.
 //   * gdn_chunk_chain_kernel, one CTA per (value head, sequence): the state chain only, with
-//     eight epilogue warps and one MMA / copy issuer warp.  Per chunk: U'^T (MMA), S0 =
-//     bf16(S) into TMEM, S <- e^{G_C} S, U^T += S0 (-W)^T, O^T = S0 Q~^T, U^T -> bf16 hi/lo in
-//     TMEM, S += U^T K~, O^T += U^T P^T; the next chunk's tiles stream in meanwhile and the
-//     previous chunk's output leaves through TMA stores, as does the leaving state.
+//     eight epilogue warps, one MMA / copy issuer warp and four store warps.  Per chunk: U'^T
+//     (MMA), S0 = bf16(S) into TMEM, S <- e^{G_C} S, U^T += S0 (-W)^T, O^T = S0 Q~^T, U^T ->
+//     bf16 hi/lo in TMEM, S += U^T K~, O^T += U^T P^T; the next chunk's tiles stream in
+//     meanwhile, the store warps send the previous chunk's output (optionally through the
+//     gated RMS norm) by TMA, and the epilogue warps send the leaving state (and any in-call
+//     snapshot).  A packed variable-length batch runs the same kernels on one token axis
+//     with a per-chunk table (each sequence keeps its own chunk grid).
 // Both kernels are launched with programmatic dependent launch (set-up overlaps the tail of
 // the kernel before).  The fp32 state stays in TMEM for a whole slice.  Every mbarrier wait
 // is bounded: on timeout the CTA records GDN_ERR_DEVICE_TIMEOUT, waits (bounded) for its own
