@@ -11,15 +11,24 @@
 //     u = (I + A)^{-1} (beta (v_i - e^{G} (k . s0_i)))          (per state row i)
 //     o_t = e^{G_t} (q_t . s0_i) + sum_{s<=t} P_ts u_s
 //     s_i <- e^{g_t} s_i + u_t k_t   after token t (t = 0 .. T-1).
-// Row independence again: row i needs only its own T values of v, and its 2T dot products
-// with the k_t and q_t are independent of each other, so a warp forms all 2T at once and one
-// transposing warp reduction (31 shuffles) leaves lane l with dot product l.
+// Row independence again: row i needs only its own T values of v and its 2T dot products
+// with the k_t and q_t.  Eight lanes share a row (16 elements each), and a lane carries RL
+// rows (two when T <= 8, else one), so that each k_t / q_t slice it reads from shared memory
+// serves RL rows: a 128-bit shared load costs the same four wavefronts however many lanes
+// share its addresses, so rows per lane is what sets the operand traffic.  A warp pass covers
+// 4 RL rows.  The 2T partial sums of a row meet in a transposing reduction over its eight
+// lanes (TM = T rounded up to 4, 8 or 16), after which each lane holds TM RL / 4 of one row's
+// k_t . s0_i or q_t . s0_i.  With M = [(I + A)^{-1}; P (I + A)^{-1}], one pass of broadcasts
+// of the right-hand side gives u in the lanes of the k-dots and the P u part of the outputs in
+// those of the q-dots.  Without per-token snapshots the state update is taken relative to the
+// last token, s_i <- e^{G_{T-1}} s_i + sum_t e^{G_{T-1} - G_t} u_t k_t (one FMA per element and
+// token, no factor above 1); with them, token by token.
 //
 // One CTA per (sequence, key head), or, at small batches, a thread-block cluster of nsplit
 // CTAs that split the rows of each value head.  The prologue convolves the T tokens of the
 // key head's q/k channels and of its own rows' v channels (and writes their new conv state),
-// forms the norms, the gates and, per value head, (I + A)^{-1} and P in shared memory.  Then
-// each warp streams state rows: one 512-byte row per warp access, coalesced.  All CTAs of a
+// forms the norms, the gates and, per value head, M in shared memory.  Then each warp
+// streams state rows, 512 contiguous bytes per eight lanes, coalesced.  All CTAs of a
 // cluster read the old q/k conv state; a cluster barrier orders those reads before the one
 // CTA (rank 0) that writes the new one.
 #include "common.cuh"
@@ -51,19 +60,19 @@ __device__ __forceinline__ void cluster_wait_mt() {
 __device__ __forceinline__ float dot4(float4 a, float4 b) {
   return fmaf(a.x, b.x, fmaf(a.y, b.y, fmaf(a.z, b.z, a.w * b.w)));
 }
+// acc + a . b
+__device__ __forceinline__ float fma4(float4 a, float4 b, float acc) {
+  return fmaf(a.w, b.w, fmaf(a.z, b.z, fmaf(a.y, b.y, fmaf(a.x, b.x, acc))));
+}
 
-template <int V> struct Log2 { static constexpr int value = 1 + Log2<V / 2>::value; };
-template <> struct Log2<1> { static constexpr int value = 0; };
-
-// transposing warp reduction of V values per lane (V a power of two <= 32): log2 V halving
-// levels, then plain butterfly levels; value v ends in lanes v * 32/V .. (v+1) * 32/V - 1
-// (V - 1 + 5 - log2 V shuffles)
+// transposing reduction of V values (a power of two >= 8) over the eight lanes of a row
+// group: three halving levels (xor 4, 2, 1; 7 V / 8 shuffles); afterwards x[i], i < V / 8,
+// holds value gl * V / 8 + i summed over the group (gl = lane & 7)
 template <int V>
-__device__ __forceinline__ float transpose_reduce(float (&x)[V], int lane) {
-  constexpr int LV = Log2<V>::value;
+__device__ __forceinline__ void transpose_reduce8(float (&x)[V], int lane) {
 #pragma unroll
-  for (int lvl = 0; lvl < LV; ++lvl) {
-    const int m = 16 >> lvl, L = V >> lvl;
+  for (int lvl = 0; lvl < 3; ++lvl) {
+    const int m = 4 >> lvl, L = V >> lvl;
     const bool up = lane & m;
 #pragma unroll
     for (int i = 0; i < V / 2; ++i) {
@@ -74,31 +83,30 @@ __device__ __forceinline__ float transpose_reduce(float (&x)[V], int lane) {
       }
     }
   }
-  float r = x[0];
-#pragma unroll
-  for (int lvl = LV; lvl < 5; ++lvl) r += __shfl_xor_sync(0xffffffffu, r, 16 >> lvl);
-  return r;
 }
 
-// shared-memory layout (floats) for T tokens and r value heads
+// shared-memory layout (floats) for T tokens, TM >= T the unrolled capacity, r value heads
 struct MtLayout {
   int qh, kh, vv, kk, qk, mats, ostage, red, total;
-  __host__ __device__ MtLayout(int T, int r) {
+  // per value head: Mt [TM][2 TM] (column s of (I + A)^{-1}, then of P (I + A)^{-1}),
+  // P [TM][TM], e^{G_t}, beta_t, e^{G_{T-1} - G_t}, e^{g_t}
+  static __host__ __device__ int head_block(int TM) { return 3 * TM * TM + 4 * TM; }
+  __host__ __device__ MtLayout(int T, int TM, int r) {
     qh = 0;
     kh = qh + T * D;
     vv = kh + T * D;
     kk = vv + T * r * D;
     qk = kk + T * T;
-    mats = qk + T * T;                       // per value head: Tm [T][T], P [T][T], 4 x [T]
-    ostage = mats + r * (2 * T * T + 4 * T);
-    red = ostage + T * D;
+    mats = (qk + T * T + 3) & ~3;
+    ostage = mats + r * head_block(TM);      // outputs [T][r][D]
+    red = ostage + T * r * D;
     total = red + 64;
   }
 };
 
 // TM: the token capacity the loops are unrolled for (T <= TM)
 template <typename Tin, typename Tout, int TM>
-__global__ void __launch_bounds__(MT_THREADS) gdn_decode_multi_kernel(GdnLayerArgs p, int T,
+__global__ void __launch_bounds__(MT_THREADS, 2) gdn_decode_multi_kernel(GdnLayerArgs p, int T,
                                                                       float* snap_state,
                                                                       int num_snap,
                                                                       const int32_t* snap_slots,
@@ -116,7 +124,32 @@ __global__ void __launch_bounds__(MT_THREADS) gdn_decode_multi_kernel(GdnLayerAr
     if (tid == 0 && kh == 0 && sp == 0) atomicOr(&g_err_multi, kErrIndex);
     return;
   }
-  const MtLayout lay(T, r);
+  const MtLayout lay(T, TM, r);
+  constexpr int HB = 3 * TM * TM + 4 * TM;
+  // state-row geometry of step 5; the first pass's rows are loaded now, so that they are in
+  // flight while the prologue runs
+  constexpr int RL = TM <= 8 ? 2 : 1;                  // state rows per lane
+  constexpr int V = RL * 2 * TM, VPL = V / 8;          // reduced values; values per lane
+  const int gl = lane & 7, grp = lane >> 3;
+  const int QO = R / (4 * RL), NQ = r * QO;            // warp passes per head; in all
+  auto pass_base = [&](int q, int& hh) {               // first row of pass q; its head
+    hh = q / QO;
+    return r_lo + (q - hh * QO) * 4 * RL + grp;
+  };
+  auto row_ptr = [&](int hh, int i) {
+    return reinterpret_cast<float4*>(p.state + (((size_t)slot * p.Hv + kh * r + hh) * D + i) * D);
+  };
+  float4 s_next[RL][4];
+  if (warp < NQ) {
+    int hh;
+    const int i0 = pass_base(warp, hh);
+#pragma unroll
+    for (int rr = 0; rr < RL; ++rr) {
+      const float4* src = row_ptr(hh, i0 + 4 * rr);
+#pragma unroll
+      for (int m = 0; m < 4; ++m) s_next[rr][m] = src[gl + 8 * m];
+    }
+  }
   float* qh = ms + lay.qh;
   float* khat = ms + lay.kh;
   float* vv = ms + lay.vv;
@@ -128,6 +161,16 @@ __global__ void __launch_bounds__(MT_THREADS) gdn_decode_multi_kernel(GdnLayerAr
   // ---- 1. conv (+SiLU) of this CTA's channels over the T tokens, or plain loads; the new
   //      conv state, and the conv state after every token for the snapshots (for the q/k
   //      channels, which every CTA of a cluster reads, once the cluster's reads are done)
+  // the window of a channel, right-aligned in 3 + TM registers: conv-state entries at
+  // 3 - H .. 2, the new inputs at 3 .. 3 + T - 1 (zeros elsewhere), so that every register
+  // index is a compile-time constant; window entries shift .. shift + H - 1 are a conv state
+  auto store_window = [&](const float (&wv)[3 + TM], Tin* dst, int shift) {
+#pragma unroll
+    for (int pos = 0; pos < 3 + TM; ++pos) {
+      const int i = pos - shift;
+      if (i >= 0 && i < H) st_elem(dst + (size_t)i * C, wv[pos]);
+    }
+  };
   float qkwin[3 + TM];                                  // this thread's q/k channel (tid < 256)
   int qkch = -1;
   for (int cl = tid; cl < ch_all; cl += MT_THREADS) {
@@ -136,37 +179,42 @@ __global__ void __launch_bounds__(MT_THREADS) gdn_decode_multi_kernel(GdnLayerAr
     const int ch = cl < D ? kh * D + cl
                    : cl < ch_qk ? p.Hk * D + kh * D + (cl - D)
                                 : 2 * p.Hk * D + (kh * r + vh) * D + vi;
-    float win[3 + TM];
     if (W > 0) {
       const Tin* cs = (const Tin*)p.conv_state + (size_t)slot * H * C + ch;
-      for (int i = 0; i < H; ++i) win[i] = ld_elem(cs + (size_t)i * C);
-      for (int t = 0; t < T; ++t)
-        win[H + t] = ld_elem((const Tin*)p.x + ((size_t)b * T + t) * C + ch);
+      float win[3 + TM], w4[4];
+#pragma unroll
+      for (int j = 0; j < 3; ++j) win[j] = j >= 3 - H ? ld_elem(cs + (size_t)(j - 3 + H) * C) : 0.f;
+#pragma unroll
+      for (int t = 0; t < TM; ++t)
+        win[3 + t] = t < T ? ld_elem((const Tin*)p.x + ((size_t)b * T + t) * C + ch) : 0.f;
       const float bias = p.conv_b ? ld_elem((const Tin*)p.conv_b + ch) : 0.f;
       const Tin* w = (const Tin*)p.conv_w + (size_t)ch * W;
-      float wt[4];
-      for (int j = 0; j < W; ++j) wt[j] = ld_elem(w + j);
-      for (int t = 0; t < T; ++t) {
-        float y = bias;
-        for (int j = 0; j < W; ++j) y = fmaf(wt[j], win[t + j], y);
-        y = p.silu ? silu_f(y) : y;
-        if (cl < D) qh[t * D + cl] = y;
-        else if (cl < ch_qk) khat[t * D + cl - D] = y;
-        else vv[t * r * D + vh * D + vi] = y;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) w4[j] = j >= 4 - W ? ld_elem(w + j - 4 + W) : 0.f;
+#pragma unroll
+      for (int t = 0; t < TM; ++t) {
+        if (t < T) {
+          float y = bias;
+#pragma unroll
+          for (int j = 0; j < 4; ++j) y = fmaf(w4[j], win[t + j], y);
+          y = p.silu ? silu_f(y) : y;
+          if (cl < D) qh[t * D + cl] = y;
+          else if (cl < ch_qk) khat[t * D + cl - D] = y;
+          else vv[t * r * D + vh * D + vi] = y;
+        }
       }
-      // new conv state: the last W-1 window entries; after token t: entries t+1 .. t+W-1
+      // new conv state: window entries T + 3 - H ..; after token t: t + 4 - H ..
       if (cl < ch_qk) {
         qkch = ch;
-        for (int i = 0; i < H + T; ++i) qkwin[i] = win[i];
+#pragma unroll
+        for (int i = 0; i < 3 + TM; ++i) qkwin[i] = win[i];
       } else {
-        Tin* csw = (Tin*)p.conv_state + (size_t)slot * H * C + ch;
-        for (int i = 0; i < H; ++i) st_elem(csw + (size_t)i * C, win[T + i]);
+        store_window(win, (Tin*)p.conv_state + (size_t)slot * H * C + ch, T + 3 - H);
         if (snap_conv && snap_slots)
           for (int t = 0; t < T; ++t) {
             const int sl = snap_slots[b * T + t];
             if (sl >= 0 && sl < num_snap)
-              for (int i = 0; i < H; ++i)
-                st_elem(snap_conv + ((size_t)sl * H + i) * C + ch, win[t + 1 + i]);
+              store_window(win, snap_conv + (size_t)sl * H * C + ch, t + 4 - H);
           }
       }
     } else {
@@ -214,14 +262,15 @@ __global__ void __launch_bounds__(MT_THREADS) gdn_decode_multi_kernel(GdnLayerAr
     (which ? QK : KK)[t * T + s2] = d;
   }
   __syncthreads();
-  // ---- 4. per value head: gates, G, (I + A)^{-1} and P (warp hh, lanes = tokens)
+  // ---- 4. per value head: gates, G, (I + A)^{-1}, P and P (I + A)^{-1} (warp hh, lanes =
+  //      tokens); entries of tokens T .. TM-1 are zero
   for (int hh = warp; hh < r; hh += MT_THREADS / 32) {
-    float* Tm = ms + lay.mats + hh * (2 * T * T + 4 * T);
-    float* P = Tm + T * T;
-    float* eG = P + T * T;          // e^{G_t}
-    float* bt = eG + T;             // beta_t
-    float* dk = bt + T;             // e^{G_{T-1} - G_t}
-    float* eg = dk + T;             // e^{g_t}
+    float* Mt = ms + lay.mats + hh * HB;
+    float* P = Mt + 2 * TM * TM;
+    float* eG = P + TM * TM;        // e^{G_t}
+    float* bt = eG + TM;            // beta_t
+    float* dk = bt + TM;            // e^{G_{T-1} - G_t}
+    float* eg = dk + TM;            // e^{g_t}
     const int h = kh * r + hh;
     float g = 0.f, beta = 0.f;
     if (lane < T) {
@@ -241,154 +290,251 @@ __global__ void __launch_bounds__(MT_THREADS) gdn_decode_multi_kernel(GdnLayerAr
       if (lane >= o) G += y;
     }
     const float GT = __shfl_sync(0xffffffffu, G, T - 1);
-    if (lane < T) {
-      eG[lane] = expf(G);
-      bt[lane] = beta;
-      dk[lane] = expf(GT - G);
-      eg[lane] = expf(g);
+    if (lane < TM) {
+      const bool on = lane < T;
+      eG[lane] = on ? expf(G) : 0.f;
+      bt[lane] = on ? beta : 0.f;
+      dk[lane] = on ? expf(GT - G) : 0.f;
+      eg[lane] = on ? expf(g) : 1.f;
     }
-    // A and P rows (lane t), then (I + A)^{-1} by forward substitution, column by column
-    // (lane j owns column j; rows t > j in order)
+    // A (strictly lower) into the Mt area for now, and P (lower with the diagonal): row t in
+    // lane t
+#pragma unroll
     for (int s2 = 0; s2 < TM; ++s2) {
-      const float Gs = __shfl_sync(0xffffffffu, G, s2 & 31);
+      const float Gs = __shfl_sync(0xffffffffu, G, s2);
       float a = 0.f, pp = 0.f;
       if (lane < T && s2 < T && s2 <= lane) {
         const float e = expf(G - Gs);
         if (s2 < lane) a = beta * e * KK[lane * T + s2];
         pp = e * QK[lane * T + s2];
       }
-      if (lane < T && s2 < T) P[lane * T + s2] = pp;
-      if (lane < T && s2 < T) Tm[lane * T + s2] = a;     // A for now
+      if (lane < TM) {
+        Mt[lane * TM + s2] = a;
+        P[lane * TM + s2] = pp;
+      }
     }
     __syncwarp();
-    if (lane < T) {
-      const int j = lane;
-      float col[TM];
-      for (int t = 0; t < TM; ++t) col[t] = (t == j) ? 1.f : 0.f;
+    // column j of (I + A)^{-1} by forward substitution (lane j), then column j of
+    // P (I + A)^{-1}
+    const int j = lane;
+    float col[TM], pt[TM];
+#pragma unroll
+    for (int t = 0; t < TM; ++t) col[t] = (t == j && j < T) ? 1.f : 0.f;
+    if (j < TM) {
+#pragma unroll
       for (int t = 0; t < TM; ++t) {
         if (t > j && t < T) {
           float acc = 0.f;
+#pragma unroll
           for (int s2 = 0; s2 < TM; ++s2)
-            if (s2 >= j && s2 < t) acc = fmaf(Tm[t * T + s2], col[s2], acc);
+            if (s2 >= j && s2 < t) acc = fmaf(Mt[t * TM + s2], col[s2], acc);
           col[t] = -acc;
         }
       }
-      __syncwarp(__activemask());
-      for (int t = 0; t < T; ++t) Tm[t * T + j] = col[t];
+#pragma unroll
+      for (int t = 0; t < TM; ++t) {
+        float acc = 0.f;
+#pragma unroll
+        for (int s2 = 0; s2 <= t; ++s2) acc = fmaf(P[t * TM + s2], col[s2], acc);
+        pt[t] = acc;
+      }
+    }
+    __syncwarp();                   // every lane has read A
+    if (j < TM) {
+#pragma unroll
+      for (int t = 0; t < TM; ++t) {
+        Mt[j * 2 * TM + t] = col[t];
+        Mt[j * 2 * TM + TM + t] = pt[t];
+      }
     }
   }
   __syncthreads();
-  // ---- 5. the state rows: value head hh, rows warp, warp + 8, ... (the next row's load is
-  //      issued before the current row's arithmetic)
+  // ---- 5. the state rows: eight lanes a row (elements 4 (gl + 8 m) .. + 3, m < 4) and RL
+  //      rows a lane (rows i0 + 4 rho + grp), so that each k / q slice read from shared memory
+  //      serves RL rows; a warp pass covers 4 RL rows of one value head, warp w taking passes
+  //      w, w + 8, ...; the next pass's rows are loaded before this one's arithmetic
   int* ssl = reinterpret_cast<int*>(red);              // this sequence's snapshot rows
   if (tid < TM) ssl[tid] = (snap_state && snap_slots && tid < T) ? snap_slots[b * T + tid] : -1;
   __syncthreads();
-  constexpr int V = 2 * TM, SV = 32 / V;               // reduced values; lanes per value
-  for (int hh = 0; hh < r; ++hh) {
-    const int h = kh * r + hh;
-    const float* Tm = ms + lay.mats + hh * (2 * T * T + 4 * T);
-    const float* P = Tm + T * T;
-    const float* eG = P + T * T;
-    const float* bt = eG + T;
-    const float* eg = bt + 2 * T;
-    float* ost = ms + lay.ostage;
-    float* Sh = p.state + ((size_t)slot * p.Hv + h) * D * D;
-    // rows i, i + 8, ... two at a time for short token counts (independent chains that the
-    // scheduler interleaves), one at a time for long ones (registers)
-    constexpr int RPI = TM <= 8 ? 2 : 1;
-    constexpr int STEP = RPI * (MT_THREADS / 32);
-    float4 s_next[RPI];
+  // after the reduction lane gl holds values gl VPL .. + VPL-1 of [row rho][k-dots, q-dots]
+  const int rho = gl * VPL / (2 * TM), tr0 = gl * VPL - rho * 2 * TM;
+  const bool role_a = tr0 < TM;                        // k-dots (-> u) or q-dots (-> o)
+  const int tk0 = role_a ? tr0 : tr0 - TM;             // token of value slot 0
+  const bool per_token = snap_state != nullptr && snap_slots != nullptr;
+  const float4* q4 = reinterpret_cast<const float4*>(qh);
+  const float4* k4 = reinterpret_cast<const float4*>(khat);
+  float* ost = ms + lay.ostage;
+  for (int q = warp; q < NQ; q += MT_THREADS / 32) {
+    int hh;
+    const int i0 = pass_base(q, hh);
+    const int h = kh * r + hh, irow = i0 + 4 * rho;
+    float4 st[RL][4];
 #pragma unroll
-    for (int q = 0; q < RPI; ++q)
-      s_next[q] = reinterpret_cast<const float4*>(Sh + (size_t)(r_lo + warp + q * 8) * D)[lane];
-    for (int i0 = r_lo + warp; i0 < r_lo + R; i0 += STEP) {
-      float4 sr[RPI];
+    for (int rr = 0; rr < RL; ++rr)
 #pragma unroll
-      for (int q = 0; q < RPI; ++q) {
-        sr[q] = s_next[q];
-        if (i0 + STEP < r_lo + R)
-          s_next[q] = reinterpret_cast<const float4*>(Sh + (size_t)(i0 + STEP + q * 8) * D)[lane];
+      for (int m = 0; m < 4; ++m) st[rr][m] = s_next[rr][m];
+    if (q + MT_THREADS / 32 < NQ) {
+      int hn;
+      const int in = pass_base(q + MT_THREADS / 32, hn);
+#pragma unroll
+      for (int rr = 0; rr < RL; ++rr) {
+        const float4* src = row_ptr(hn, in + 4 * rr);
+#pragma unroll
+        for (int m = 0; m < 4; ++m) s_next[rr][m] = src[gl + 8 * m];
       }
-      float red_v[RPI];
+    }
+    const float* Mt = ms + lay.mats + hh * HB;
+    const float* eG = Mt + 3 * TM * TM;
+    const float* bt = eG + TM;
+    const float* dk = bt + TM;
+    const float* eg = dk + TM;
+    // 2T partial dot products per row over this lane's 16 elements, reduced over the row's
+    // eight lanes
+    float x[V];
 #pragma unroll
-      for (int q = 0; q < RPI; ++q) {
-        float x[V];
+    for (int t = 0; t < TM; ++t) {
+      float a[RL], c[RL];
 #pragma unroll
-        for (int t = 0; t < TM; ++t) {
-          const bool on = t < T;
-          x[t] = on ? dot4(sr[q], reinterpret_cast<const float4*>(khat + t * D)[lane]) : 0.f;
-          x[TM + t] = on ? dot4(sr[q], reinterpret_cast<const float4*>(qh + t * D)[lane]) : 0.f;
-        }
-        // value v (v < TM: k_v . s0_i; TM <= v: q_{v-TM} . s0_i) lands in lanes v * SV ..
-        red_v[q] = transpose_reduce<V>(x, lane);
-      }
-      const int t = lane;
-      float rhs[RPI], u[RPI], o[RPI];
+      for (int rr = 0; rr < RL; ++rr) a[rr] = c[rr] = 0.f;
+      if (t < T) {
 #pragma unroll
-      for (int q = 0; q < RPI; ++q) {
-        const int i = i0 + q * 8;
-        const float ai = __shfl_sync(0xffffffffu, red_v[q], (t * SV) & 31);
-        const float ci = __shfl_sync(0xffffffffu, red_v[q], ((TM + t) * SV) & 31);
-        rhs[q] = (t < T) ? bt[t] * (vv[t * r * D + hh * D + i] - eG[t] * ai) : 0.f;
-        o[q] = (t < T) ? eG[t] * ci : 0.f;
-        u[q] = 0.f;
-      }
-      // u = (I + A)^{-1} rhs, lane t
+        for (int m = 0; m < 4; ++m) {
+          const float4 kv = k4[t * (D / 4) + gl + 8 * m];
+          const float4 qv = q4[t * (D / 4) + gl + 8 * m];
 #pragma unroll
-      for (int s2 = 0; s2 < TM; ++s2) {
-        const float tm = (s2 < T && t < T && s2 <= t) ? Tm[t * T + s2] : 0.f;
-#pragma unroll
-        for (int q = 0; q < RPI; ++q) u[q] = fmaf(tm, __shfl_sync(0xffffffffu, rhs[q], s2), u[q]);
-      }
-      // outputs and the state after each token
-#pragma unroll
-      for (int s2 = 0; s2 < TM; ++s2) {
-        if (s2 < T) {
-          const float pv = (t < T && s2 <= t) ? P[t * T + s2] : 0.f;
-          const float4 k4 = reinterpret_cast<const float4*>(khat + s2 * D)[lane];
-          const float e = eg[s2];
-          const int sl = ssl[s2];
-#pragma unroll
-          for (int q = 0; q < RPI; ++q) {
-            const float us = __shfl_sync(0xffffffffu, u[q], s2);
-            o[q] = fmaf(pv, us, o[q]);
-            sr[q].x = fmaf(e, sr[q].x, us * k4.x);
-            sr[q].y = fmaf(e, sr[q].y, us * k4.y);
-            sr[q].z = fmaf(e, sr[q].z, us * k4.z);
-            sr[q].w = fmaf(e, sr[q].w, us * k4.w);
-            if (sl >= 0 && sl < num_snap)
-              reinterpret_cast<float4*>(snap_state +
-                                        (((size_t)sl * p.Hv + h) * D + i0 + q * 8) * D)[lane] = sr[q];
+          for (int rr = 0; rr < RL; ++rr) {
+            a[rr] = fma4(st[rr][m], kv, a[rr]);
+            c[rr] = fma4(st[rr][m], qv, c[rr]);
           }
         }
       }
 #pragma unroll
-      for (int q = 0; q < RPI; ++q) {
-        const int i = i0 + q * 8;
-        reinterpret_cast<float4*>(Sh + (size_t)i * D)[lane] = sr[q];
-        if (t < T) ost[t * D + i] = o[q];
+      for (int rr = 0; rr < RL; ++rr) {
+        x[rr * 2 * TM + t] = a[rr];
+        x[rr * 2 * TM + TM + t] = c[rr];
       }
     }
-    __syncthreads();
-    // this head's outputs, token rows of 128 channels
-    for (int e = tid; e < T * R; e += MT_THREADS) {
-      const int tt = e / R, c = r_lo + e % R;
-      st_elem((Tout*)p.out + (((size_t)b * T + tt) * p.Hv + h) * D + c, ost[tt * D + c]);
+    transpose_reduce8<V>(x, lane);
+    // x[k]: k_t . s0 (role_a) or q_t . s0 of row irow, t = tk0 + k
+    float rhs[VPL], acc[VPL];
+#pragma unroll
+    for (int k = 0; k < VPL; ++k) {
+      const int t = tk0 + k;
+      rhs[k] = (role_a && t < T) ? bt[t] * (vv[(t * r + hh) * D + irow] - eG[t] * x[k]) : 0.f;
+      acc[k] = 0.f;
     }
-    __syncthreads();
+    // role_a lanes: u = (I + A)^{-1} rhs; the others: P (I + A)^{-1} rhs
+#pragma unroll
+    for (int s2 = 0; s2 < TM; ++s2) {
+      if (s2 < T) {
+        const float rs =
+            __shfl_sync(0xffffffffu, rhs[s2 % VPL], (rho * 2 * TM + s2) / VPL, 8);
+        const float* mrow = Mt + s2 * 2 * TM + tr0;
+#pragma unroll
+        for (int k = 0; k < VPL; ++k) acc[k] = fmaf(mrow[k], rs, acc[k]);
+      }
+    }
+    if (!role_a) {
+#pragma unroll
+      for (int k = 0; k < VPL; ++k) {
+        const int t = tk0 + k;
+        if (t < T) ost[(t * r + hh) * D + irow] = fmaf(eG[t], x[k], acc[k]);
+      }
+    }
+    // the state: token by token with snapshots, else relative to the last token; u_s of row
+    // rr sits in lane (rr 2 TM + s) / VPL, slot s % VPL
+    if (per_token) {
+#pragma unroll
+      for (int s2 = 0; s2 < TM; ++s2) {
+        if (s2 < T) {
+          float us[RL];
+#pragma unroll
+          for (int rr = 0; rr < RL; ++rr)
+            us[rr] = __shfl_sync(0xffffffffu, acc[s2 % VPL], (rr * 2 * TM + s2) / VPL, 8);
+          const float e = eg[s2];
+          const int sl = ssl[s2];
+#pragma unroll
+          for (int m = 0; m < 4; ++m) {
+            const float4 kv = k4[s2 * (D / 4) + gl + 8 * m];
+#pragma unroll
+            for (int rr = 0; rr < RL; ++rr) {
+              st[rr][m].x = fmaf(e, st[rr][m].x, us[rr] * kv.x);
+              st[rr][m].y = fmaf(e, st[rr][m].y, us[rr] * kv.y);
+              st[rr][m].z = fmaf(e, st[rr][m].z, us[rr] * kv.z);
+              st[rr][m].w = fmaf(e, st[rr][m].w, us[rr] * kv.w);
+            }
+          }
+          if (sl >= 0 && sl < num_snap) {
+#pragma unroll
+            for (int rr = 0; rr < RL; ++rr) {
+              float4* dst = reinterpret_cast<float4*>(
+                  snap_state + (((size_t)sl * p.Hv + h) * D + i0 + 4 * rr) * D);
+#pragma unroll
+              for (int m = 0; m < 4; ++m) dst[gl + 8 * m] = st[rr][m];
+            }
+          }
+        }
+      }
+    } else {
+      const float eT = eG[T - 1];
+#pragma unroll
+      for (int rr = 0; rr < RL; ++rr)
+#pragma unroll
+        for (int m = 0; m < 4; ++m) {
+          st[rr][m].x *= eT; st[rr][m].y *= eT; st[rr][m].z *= eT; st[rr][m].w *= eT;
+        }
+#pragma unroll
+      for (int s2 = 0; s2 < TM; ++s2) {
+        if (s2 < T) {
+          float us[RL];
+#pragma unroll
+          for (int rr = 0; rr < RL; ++rr)
+            us[rr] = __shfl_sync(0xffffffffu, acc[s2 % VPL], (rr * 2 * TM + s2) / VPL, 8) *
+                     dk[s2];
+#pragma unroll
+          for (int m = 0; m < 4; ++m) {
+            const float4 kv = k4[s2 * (D / 4) + gl + 8 * m];
+#pragma unroll
+            for (int rr = 0; rr < RL; ++rr) {
+              st[rr][m].x = fmaf(us[rr], kv.x, st[rr][m].x);
+              st[rr][m].y = fmaf(us[rr], kv.y, st[rr][m].y);
+              st[rr][m].z = fmaf(us[rr], kv.z, st[rr][m].z);
+              st[rr][m].w = fmaf(us[rr], kv.w, st[rr][m].w);
+            }
+          }
+        }
+      }
+    }
+#pragma unroll
+    for (int rr = 0; rr < RL; ++rr) {
+      float4* Sr = row_ptr(hh, i0 + 4 * rr);
+#pragma unroll
+      for (int m = 0; m < 4; ++m) Sr[gl + 8 * m] = st[rr][m];
+    }
+  }
+  __syncthreads();
+  // the outputs, token rows of Hv x 128 channels: this CTA's rows of its r value heads
+  {
+    const int lgR = __ffs(R) - 1;                      // R is a power of two
+    for (int tt = 0; tt < T; ++tt) {
+      Tout* orow = (Tout*)p.out + (((size_t)b * T + tt) * p.Hv + kh * r) * D;
+      const float* srow = ost + tt * r * D;
+      for (int j = tid; j < r * R; j += MT_THREADS) {
+        const int e = (j >> lgR) * D + r_lo + (j & (R - 1));       // hh * D + c
+        st_elem(orow + e, srow[e]);
+      }
+    }
   }
   // the q/k channels' new conv state (and per-token snapshots): rank 0, after the cluster's
   // reads of the old one
   if (nsplit > 1) cluster_wait_mt();
   if (sp == 0 && W > 0 && qkch >= 0) {
-    Tin* csw = (Tin*)p.conv_state + (size_t)slot * H * C + qkch;
-    for (int i = 0; i < H; ++i) st_elem(csw + (size_t)i * C, qkwin[T + i]);
+    store_window(qkwin, (Tin*)p.conv_state + (size_t)slot * H * C + qkch, T + 3 - H);
     if (snap_conv && snap_slots)
       for (int t = 0; t < T; ++t) {
         const int sl = snap_slots[b * T + t];
         if (sl >= 0 && sl < num_snap)
-          for (int i = 0; i < H; ++i)
-            st_elem(snap_conv + ((size_t)sl * H + i) * C + qkch, qkwin[t + 1 + i]);
+          store_window(qkwin, snap_conv + (size_t)sl * H * C + qkch, t + 4 - H);
       }
   }
   if (tid == 0 && sp == 0 && snap_slots)
@@ -399,11 +545,11 @@ __global__ void __launch_bounds__(MT_THREADS) gdn_decode_multi_kernel(GdnLayerAr
 template <typename Tin, typename Tout, int TM>
 cudaError_t launch_multi_tm(const GdnLayerArgs& p, int T, float* snap_state, int num_snap,
                             const int32_t* snap_slots, void* snap_conv, cudaStream_t stream) {
-  const MtLayout lay(T, p.Hv / p.Hk);
+  const MtLayout lay(T, TM, p.Hv / p.Hk);
   const size_t smem = sizeof(float) * lay.total;
   static unsigned done = 0;
   cudaError_t e = set_smem_once(gdn_decode_multi_kernel<Tin, Tout, TM>,
-                                (int)(sizeof(float) * MtLayout(TM, 8).total), &done);
+                                (int)(sizeof(float) * MtLayout(TM, TM, 8).total), &done);
   if (e != cudaSuccess) return e;
   // rows of each value head split over a cluster of nsplit CTAs when the (sequence, key head)
   // items alone would leave most SMs idle
@@ -433,10 +579,14 @@ cudaError_t launch_multi_tm(const GdnLayerArgs& p, int T, float* snap_state, int
 template <typename Tin, typename Tout>
 cudaError_t launch_multi_t(const GdnLayerArgs& p, int T, float* snap_state, int num_snap,
                            const int32_t* snap_slots, void* snap_conv, cudaStream_t stream) {
-  if (T <= 2) return launch_multi_tm<Tin, Tout, 2>(p, T, snap_state, num_snap, snap_slots, snap_conv, stream);
-  if (T <= 4) return launch_multi_tm<Tin, Tout, 4>(p, T, snap_state, num_snap, snap_slots, snap_conv, stream);
-  if (T <= 8) return launch_multi_tm<Tin, Tout, 8>(p, T, snap_state, num_snap, snap_slots, snap_conv, stream);
-  return launch_multi_tm<Tin, Tout, 16>(p, T, snap_state, num_snap, snap_slots, snap_conv, stream);
+  if (T <= 4)
+    return launch_multi_tm<Tin, Tout, 4>(p, T, snap_state, num_snap, snap_slots, snap_conv,
+                                         stream);
+  if (T <= 8)
+    return launch_multi_tm<Tin, Tout, 8>(p, T, snap_state, num_snap, snap_slots, snap_conv,
+                                         stream);
+  return launch_multi_tm<Tin, Tout, 16>(p, T, snap_state, num_snap, snap_slots, snap_conv,
+                                        stream);
 }
 
 }  // namespace
