@@ -37,7 +37,11 @@
 //     snapshot).  A packed variable-length batch runs the same kernels on one token axis
 //     with a per-chunk table (each sequence keeps its own chunk grid).
 // Both kernels are launched with programmatic dependent launch (set-up overlaps the tail of
-// the kernel before).  The fp32 state stays in TMEM for a whole slice.  Every mbarrier wait
+// the kernel before).  In a call of several slices the workspace is double-buffered and the
+// local kernel of slice i+1 runs beside the chain of slice i: the chain releases its
+// dependents right after its own grid wait, and the local kernel's last block waits for that
+// chain before it exits, so that the grid (whose completion starts the next chain) cannot
+// complete first.  No kernel spins on another's data.  The fp32 state stays in TMEM for a whole slice.  Every mbarrier wait
 // is bounded: on timeout the CTA records GDN_ERR_DEVICE_TIMEOUT, waits (bounded) for its own
 // copies and MMAs, frees TMEM and returns.
 #include "common.cuh"
@@ -109,6 +113,10 @@ struct TcParams {
   const int32_t* ccs;
   const int4* ctab;
   void* out;              // for the ragged last chunk of a packed sequence (plain stores)
+  // slices after the first of a call: the local kernel waits for the kernel before it (the
+  // previous slice's chain) only at the end of its last block; every slice but the last: the
+  // chain lets the next slice's local kernel start as soon as its own grid wait has returned
+  int late_wait, early_trigger;
 };
 
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
@@ -301,6 +309,11 @@ __global__ void __launch_bounds__(LGT, 3)
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int jc = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
   const int kh = h / (p.Hv / p.Hk);
+  // a later slice of the call: the grid's last block alone waits for the previous slice's
+  // chain, at its end; that keeps the grid from completing before the chain has, and lets
+  // every other block finish and free its SM for the blocks behind it
+  const bool wait_late = p.late_wait && jc == (int)gridDim.x - 1 &&
+                         h == (int)gridDim.y - 1 && b == (int)gridDim.z - 1;
   // this unit's tokens: chunk n0 + jc of sequence b, or of a packed batch, entry n0 + jc
   int tok0 = (p.n0 + jc) * C, ntok = min(C, p.T - tok0), seq = b;
   if (p.cu) {
@@ -308,10 +321,16 @@ __global__ void __launch_bounds__(LGT, 3)
     tok0 = e.x;
     ntok = e.y;
     seq = e.z;
-    if (ntok <= 0) return;                       // past the last chunk
+    if (ntok <= 0) {                             // past the last chunk
+      if (wait_late) pdl_wait();
+      return;
+    }
   }
   const int slot = p.slots ? p.slots[seq] : seq;
-  if (slot < 0 || slot >= p.num_slots) return;  // the chain kernel reports bad slots
+  if (slot < 0 || slot >= p.num_slots) {        // the chain kernel reports bad slots
+    if (wait_late) pdl_wait();
+    return;
+  }
   const size_t u = ((size_t)b * p.Hv + h) * p.ns + jc;
   uint8_t* unit = p.units + u * UNIT_BYTES;
 
@@ -370,9 +389,13 @@ __global__ void __launch_bounds__(LGT, 3)
   }
   // the conv output (K, Q) and this slice's workspace belong to the kernels before until
   // here.  Only then may the state-chain kernel start its set-up, which reads the state: the
-  // chain that last wrote it is then complete and visible.
-  pdl_wait();
-  pdl_trigger();
+  // chain that last wrote it is then complete and visible.  A later slice of the call (its
+  // own half of a double-buffered workspace; the conv output complete since the first slice)
+  // skips this and waits at its end instead, running beside the previous slice's chain.
+  if (!p.late_wait) {
+    pdl_wait();
+    pdl_trigger();
+  }
   if (tid == 0) {
     mbar_arrive_expect_tx(bar_in, 32 * KB);
 #pragma unroll
@@ -572,6 +595,9 @@ __global__ void __launch_bounds__(LGT, 3)
     tc_fence_after();
     tmem_dealloc(tmem, L_TMEM);
   }
+  // a later slice: this grid completes only after the previous slice's chain has, so that the
+  // next chain (started by this grid's completion) reads the state that chain left
+  if (wait_late) pdl_wait();
 }
 
 // One level of a transposing warp reduction: lanes with bit M set keep the upper half of
@@ -759,6 +785,9 @@ __global__ void __launch_bounds__(CH_THREADS, 1)
   }
   // the local kernel's tiles and e^{G_C} (and the conv output V) from here on
   pdl_wait();
+  // another slice follows: its local kernel may run beside this chain now (it writes the
+  // other half of the workspace and waits for this grid before it completes)
+  if (p.early_trigger) pdl_trigger();
   if (tid == CH_EPI)
     for (int i = 0; i < 2 && i < ns; ++i) {
       load_main(i);
@@ -1153,6 +1182,11 @@ __global__ void __launch_bounds__(CH_THREADS, 1)
 
 // ======================================================================= host side
 
+// One slice's workspace: its units' tiles, then e^{G_C} per unit (256-byte aligned size).
+size_t scratch_half_bytes(size_t units) {
+  return units * UNIT_BYTES + ((units * sizeof(float) + 255) & ~(size_t)255);
+}
+
 // Chunks per slice: as many as keep one slice's tiles within SLICE_BUDGET bytes.
 int slice_chunks(int B, int Hv, int nch) {
   const size_t per_chunk = (size_t)B * Hv * UNIT_BYTES;
@@ -1212,12 +1246,12 @@ cudaError_t launch_tc_t(const GdnLayerArgs& L, cudaStream_t stream) {
   const size_t units = (size_t)ns_max * MB * L.Hv;
   if (!L.scratch || L.scratch_bytes < gdn_prefill_tc_scratch_bytes(MB, nch * C, L.Hv))
     return cudaErrorInvalidValue;
+  const int nslices = (nch + ns_max - 1) / ns_max;
+  const size_t half_bytes = scratch_half_bytes(units);
   TcParams p;
   p.T = L.T; p.Hk = L.Hk; p.Hv = L.Hv; p.num_slots = L.num_slots; p.l2norm = L.l2norm;
   p.gates_pre = L.gates_pre; p.eps = L.eps; p.scale = L.scale; p.a = L.a; p.b = L.b;
   p.A_log = L.A_log; p.dt_bias = L.dt_bias; p.state = L.state; p.slots = L.slots;
-  p.units = static_cast<uint8_t*>(L.scratch);
-  p.egc = reinterpret_cast<float*>(p.units + units * UNIT_BYTES);
   p.se_c = snaps ? L.snap_every / C : 0;
   p.n_snap = snaps ? L.n_snap : 0;
   p.n_snap_slots = snaps ? L.num_snap_slots : 0;
@@ -1229,9 +1263,16 @@ cudaError_t launch_tc_t(const GdnLayerArgs& L, cudaStream_t stream) {
   p.ccs = L.ccs;
   p.ctab = static_cast<const int4*>(L.ctab);
   p.out = L.out;
-  for (int n0 = 0; n0 < nch; n0 += ns_max) {
+  for (int si = 0; si < nslices; ++si) {
+    const int n0 = si * ns_max;
     p.n0 = n0;
     p.ns = nch - n0 < ns_max ? nch - n0 : ns_max;
+    // workspace half (si & 1) when the call has several slices
+    p.units = static_cast<uint8_t*>(L.scratch) +
+              (nslices > 1 ? (size_t)(si & 1) * half_bytes : 0);
+    p.egc = reinterpret_cast<float*>(p.units + units * UNIT_BYTES);
+    p.late_wait = si > 0;
+    p.early_trigger = si + 1 < nslices;
     // (the first slice's local kernel reads the caller's gate inputs, and a packed batch's
     // chunk table, before its grid wait: it may start early only behind this call's own conv
     // kernels, which began after everything earlier had completed)
@@ -1251,8 +1292,9 @@ cudaError_t launch_tc_t(const GdnLayerArgs& L, cudaStream_t stream) {
 size_t gdn_prefill_tc_scratch_bytes(int B, int T, int Hv) {
   const int nch = (T + C - 1) / C;
   if (B <= 0 || nch <= 0 || Hv <= 0) return 0;
-  const size_t units = (size_t)slice_chunks(B, Hv, nch) * B * Hv;
-  return units * UNIT_BYTES + ((units * sizeof(float) + 255) & ~(size_t)255);
+  const int ns = slice_chunks(B, Hv, nch);
+  const size_t half = scratch_half_bytes((size_t)ns * B * Hv);
+  return ns < nch ? 2 * half : half;        // two halves when the call has several slices
 }
 
 cudaError_t gdn_launch_prefill_tc(const GdnLayerArgs& L, cudaStream_t stream) {
