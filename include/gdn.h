@@ -95,8 +95,9 @@ typedef struct {
  * Bytes of device workspace gdn_chunk_prefill needs for these dims/opts (0 when none): the
  * post-conv activations when conv_width > 0, plus, for bf16 inputs, the per-chunk operand
  * tiles the tensor-core prefill passes from its chunk-local kernel to its state-chain kernel
- * (80 KB per chunk and value head for a slice of at most ~96 MB).  Returns 0 for invalid
- * dims.
+ * (80 KB per chunk and value head for a slice of at most ~96 MB; twice that when the call
+ * spans several slices, so that one slice's tiles are written while the previous slice's are
+ * read).  Returns 0 for invalid dims.
  */
 size_t gdn_prefill_workspace_size(const gdn_dims* dims, const gdn_opts* opts);
 
