@@ -28,7 +28,9 @@
 // CTAs that split the rows of each value head.  The prologue convolves the T tokens of the
 // key head's q/k channels and of its own rows' v channels (and writes their new conv state),
 // forms the norms, the gates and, per value head, M in shared memory.  Then each warp
-// streams state rows, 512 contiguous bytes per eight lanes, coalesced.  All CTAs of a
+// streams state rows, 512 contiguous bytes per eight lanes, coalesced: asynchronous copies
+// put the next pass's rows into one of two per-warp shared buffers a pass ahead (the first
+// pass's at kernel entry, in flight during the prologue), and stores write the new rows.  All CTAs of a
 // cluster read the old q/k conv state; a cluster barrier orders those reads before the one
 // CTA (rank 0) that writes the new one.
 #include "common.cuh"
@@ -60,6 +62,18 @@ __device__ __forceinline__ void cluster_wait_mt() {
 __device__ __forceinline__ float dot4(float4 a, float4 b) {
   return fmaf(a.x, b.x, fmaf(a.y, b.y, fmaf(a.z, b.z, a.w * b.w)));
 }
+// 16-byte asynchronous copy global -> shared (no registers held while it is in flight)
+__device__ __forceinline__ void cp_async16(void* smem_dst, const void* gsrc) {
+  const uint32_t d = static_cast<uint32_t>(__cvta_generic_to_shared(smem_dst));
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(d), "l"(gsrc) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;\n" ::: "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+  asm volatile("cp.async.wait_group 0;\n" ::: "memory");
+}
+
 // acc + a . b
 __device__ __forceinline__ float fma4(float4 a, float4 b, float acc) {
   return fmaf(a.w, b.w, fmaf(a.z, b.z, fmaf(a.y, b.y, fmaf(a.x, b.x, acc))));
@@ -87,7 +101,7 @@ __device__ __forceinline__ void transpose_reduce8(float (&x)[V], int lane) {
 
 // shared-memory layout (floats) for T tokens, TM >= T the unrolled capacity, r value heads
 struct MtLayout {
-  int qh, kh, vv, kk, qk, mats, ostage, red, total;
+  int qh, kh, vv, kk, qk, mats, ostage, red, stage, total;
   // per value head: Mt [TM][2 TM] (column s of (I + A)^{-1}, then of P (I + A)^{-1}),
   // P [TM][TM], e^{G_t}, beta_t, e^{G_{T-1} - G_t}, e^{g_t}
   static __host__ __device__ int head_block(int TM) { return 3 * TM * TM + 4 * TM; }
@@ -100,7 +114,8 @@ struct MtLayout {
     mats = (qk + T * T + 3) & ~3;
     ostage = mats + r * head_block(TM);      // outputs [T][r][D]
     red = ostage + T * r * D;
-    total = red + 64;
+    stage = red + 64;                        // per warp: two buffers of one pass's rows
+    total = stage + (MT_THREADS / 32) * 2 * 4 * (TM <= 8 ? 2 : 1) * D;
   }
 };
 
@@ -126,7 +141,7 @@ __global__ void __launch_bounds__(MT_THREADS, 2) gdn_decode_multi_kernel(GdnLaye
   }
   const MtLayout lay(T, TM, r);
   constexpr int HB = 3 * TM * TM + 4 * TM;
-  // state-row geometry of step 5; the first pass's rows are loaded now, so that they are in
+  // state-row geometry of step 5; the first pass's rows are copied now, so that they are in
   // flight while the prologue runs
   constexpr int RL = TM <= 8 ? 2 : 1;                  // state rows per lane
   constexpr int V = RL * 2 * TM, VPL = V / 8;          // reduced values; values per lane
@@ -139,17 +154,25 @@ __global__ void __launch_bounds__(MT_THREADS, 2) gdn_decode_multi_kernel(GdnLaye
   auto row_ptr = [&](int hh, int i) {
     return reinterpret_cast<float4*>(p.state + (((size_t)slot * p.Hv + kh * r + hh) * D + i) * D);
   };
-  float4 s_next[RL][4];
-  if (warp < NQ) {
+  // a pass's rows go to one of this warp's two staging buffers by asynchronous copies, each
+  // lane copying (and later reading) only its own 16-byte pieces: element
+  // (rr, grp, 4 (gl + 8 m)); the pass k-th of this warp uses buffer k & 1
+  constexpr int SBUF = 4 * RL * D / 4;                 // float4s per buffer
+  float4* stg = reinterpret_cast<float4*>(ms + lay.stage) + warp * 2 * SBUF;
+  auto prefetch_pass = [&](int q, int buf) {
     int hh;
-    const int i0 = pass_base(warp, hh);
+    const int i0 = pass_base(q, hh);
+    float4* dst = stg + buf * SBUF;
 #pragma unroll
     for (int rr = 0; rr < RL; ++rr) {
       const float4* src = row_ptr(hh, i0 + 4 * rr);
 #pragma unroll
-      for (int m = 0; m < 4; ++m) s_next[rr][m] = src[gl + 8 * m];
+      for (int m = 0; m < 4; ++m)
+        cp_async16(dst + (rr * 4 + grp) * (D / 4) + gl + 8 * m, src + gl + 8 * m);
     }
-  }
+    cp_async_commit();
+  };
+  if (warp < NQ) prefetch_pass(warp, 0);
   float* qh = ms + lay.qh;
   float* khat = ms + lay.kh;
   float* vv = ms + lay.vv;
@@ -352,7 +375,8 @@ __global__ void __launch_bounds__(MT_THREADS, 2) gdn_decode_multi_kernel(GdnLaye
   // ---- 5. the state rows: eight lanes a row (elements 4 (gl + 8 m) .. + 3, m < 4) and RL
   //      rows a lane (rows i0 + 4 rho + grp), so that each k / q slice read from shared memory
   //      serves RL rows; a warp pass covers 4 RL rows of one value head, warp w taking passes
-  //      w, w + 8, ...; the next pass's rows are loaded before this one's arithmetic
+  //      w, w + 8, ...; the next pass's rows are copied to shared memory (cp.async, no
+  //      registers held) while this one's arithmetic runs
   int* ssl = reinterpret_cast<int*>(red);              // this sequence's snapshot rows
   if (tid < TM) ssl[tid] = (snap_state && snap_slots && tid < T) ? snap_slots[b * T + tid] : -1;
   __syncthreads();
@@ -364,25 +388,19 @@ __global__ void __launch_bounds__(MT_THREADS, 2) gdn_decode_multi_kernel(GdnLaye
   const float4* q4 = reinterpret_cast<const float4*>(qh);
   const float4* k4 = reinterpret_cast<const float4*>(khat);
   float* ost = ms + lay.ostage;
-  for (int q = warp; q < NQ; q += MT_THREADS / 32) {
+  for (int q = warp, pk = 0; q < NQ; q += MT_THREADS / 32, pk ^= 1) {
     int hh;
     const int i0 = pass_base(q, hh);
     const int h = kh * r + hh, irow = i0 + 4 * rho;
     float4 st[RL][4];
+    cp_async_wait_all();                               // this pass's rows (buffer pk)
 #pragma unroll
     for (int rr = 0; rr < RL; ++rr)
 #pragma unroll
-      for (int m = 0; m < 4; ++m) st[rr][m] = s_next[rr][m];
-    if (q + MT_THREADS / 32 < NQ) {
-      int hn;
-      const int in = pass_base(q + MT_THREADS / 32, hn);
-#pragma unroll
-      for (int rr = 0; rr < RL; ++rr) {
-        const float4* src = row_ptr(hn, in + 4 * rr);
-#pragma unroll
-        for (int m = 0; m < 4; ++m) s_next[rr][m] = src[gl + 8 * m];
-      }
-    }
+      for (int m = 0; m < 4; ++m)
+        st[rr][m] = stg[pk * SBUF + (rr * 4 + grp) * (D / 4) + gl + 8 * m];
+    // the next pass's rows into the other buffer (read by this lane a pass ago)
+    if (q + MT_THREADS / 32 < NQ) prefetch_pass(q + MT_THREADS / 32, pk ^ 1);
     const float* Mt = ms + lay.mats + hh * HB;
     const float* eG = Mt + 3 * TM * TM;
     const float* bt = eG + TM;
