@@ -156,7 +156,7 @@ __global__ void __launch_bounds__(MT_THREADS, 2) gdn_decode_multi_kernel(GdnLaye
   };
   // a pass's rows go to one of this warp's two staging buffers by asynchronous copies, each
   // lane copying (and later reading) only its own 16-byte pieces: element
-  // (rr, grp, 4 (gl + 8 m)); the pass k-th of this warp uses buffer k & 1
+  // (rr, grp, 4 (gl + 8 m)); the k-th pass of this warp uses buffer k & 1
   constexpr int SBUF = 4 * RL * D / 4;                 // float4s per buffer
   float4* stg = reinterpret_cast<float4*>(ms + lay.stage) + warp * 2 * SBUF;
   auto prefetch_pass = [&](int q, int buf) {
