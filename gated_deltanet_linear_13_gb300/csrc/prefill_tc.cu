@@ -41,9 +41,10 @@
 // local kernel of slice i+1 runs beside the chain of slice i: the chain releases its
 // dependents right after its own grid wait, and the local kernel's last block waits for that
 // chain before it exits, so that the grid (whose completion starts the next chain) cannot
-// complete first.  No kernel spins on another's data.  The fp32 state stays in TMEM for a whole slice.  Every mbarrier wait
-// is bounded: on timeout the CTA records GDN_ERR_DEVICE_TIMEOUT, waits (bounded) for its own
-// copies and MMAs, frees TMEM and returns.
+// complete first.  No kernel spins on another's data.  The fp32 state stays in TMEM for a
+// whole slice.  Every mbarrier wait is bounded: on timeout the CTA records
+// GDN_ERR_DEVICE_TIMEOUT, waits (bounded) for its own copies and MMAs, frees TMEM and
+// returns.
 #include "common.cuh"
 #include "sm100_ptx.cuh"
 
