@@ -181,6 +181,21 @@ def test_prefill_rejects_bad_pointers(L):
     assert _prefill(L, _dims(batch=4, num_slots=2), o) == 1
 
 
+def test_prefill_workspace_two_halves_past_one_slice(L):
+    """The 27B shape (48 value heads) holds floor(96 MiB / (48 x 80 KiB)) = 25 chunks of tiles
+    per slice. A call of 25 chunks needs one slice's tiles; one more chunk makes two slices,
+    and the workspace then holds two slices' worth (one written while the other is read)."""
+    o = _opts()
+    half = 25 * 48 * 80 * 1024 + ((25 * 48 * 4 + 255) // 256) * 256
+    one = _dims(seqlen=25 * 64, num_v_heads=48)
+    two = _dims(seqlen=26 * 64, num_v_heads=48)
+    assert L.gdn_prefill_workspace_size(ctypes.byref(one), ctypes.byref(o)) == half
+    assert L.gdn_prefill_workspace_size(ctypes.byref(two), ctypes.byref(o)) == 2 * half
+    # a longer call keeps the same two halves
+    long_ = _dims(seqlen=2048 * 64, num_v_heads=48)
+    assert L.gdn_prefill_workspace_size(ctypes.byref(long_), ctypes.byref(o)) == 2 * half
+
+
 def test_prefill_workspace_checked(L):
     dc, o = _dims(conv_width=4), _opts()
     need = L.gdn_prefill_workspace_size(ctypes.byref(dc), ctypes.byref(o))
