@@ -24,6 +24,7 @@ import os
 import statistics
 import subprocess
 import sys
+import tempfile
 import time
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
@@ -122,9 +123,13 @@ def whole_job_rate(world: int, units_per_rank: float, max_ms: float) -> float:
 # ------------------------------------------------------------------ clocks
 
 class ClockSampler:
+    """nvidia-smi clock / throttle samples every 200 ms while the timed region runs, written
+    as CSV to $GDN_CLOCK_LOG_DIR (default: the system temp directory)."""
+
     def __init__(self, gpu_index: int):
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{gpu_index}.csv")
+        log_dir = os.environ.get("GDN_CLOCK_LOG_DIR") or tempfile.gettempdir()
+        self.path = os.path.join(log_dir, f"clocks_rank{gpu_index}.csv")
         self.gpu = gpu_index
 
     def __enter__(self):

@@ -70,8 +70,9 @@ def test_single_process_has_no_collective():
 
 
 def test_reference_arm_under_torchrun():
-    """`bench.py --impl reference` launched as the driver launches N > 1: rank 0 alone runs
-    the oracle and prints one JSON line; the other rank exits 0 without work."""
+    """`bench.py --impl reference` launched under torchrun with two ranks, as an N > 1 run
+    is launched: rank 0 alone runs the oracle and prints one JSON line; the other rank exits
+    0 without work."""
     port = _free_port()
     cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node", "2",
            "--master-addr", "127.0.0.1", "--master-port", str(port), "bench.py", "--impl",
