@@ -29,7 +29,8 @@ EXPORTED = ("gdn_prefill_workspace_size", "gdn_chunk_prefill", "gdn_decode_step"
             "causal_conv1d_update", "gdn_state_checkpoint", "gdn_chunk_prefill_noalloc",
             "gdn_chunk_prefill_snapshots", "gdn_chunk_prefill_gated", "gdn_decode_step_gated",
             "gdn_prefill_varlen_workspace_size", "gdn_chunk_prefill_varlen", "gdn_decode_multi",
-            "gdn_get_device_error", "gdn_status_string", "gdn_version")
+            "gdn_get_device_error", "gdn_status_string", "gdn_version",
+            "gdn_selftest_device_timeout")
 NOALLOC_SCRATCH_BYTES = 64 << 20   # GDN_NOALLOC_SCRATCH_BYTES in include/gdn.h
 
 
@@ -102,6 +103,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
                                        [ctypes.c_int32, _vp, _vp, ctypes.c_int32, _vp])
     L.gdn_get_device_error.restype = ctypes.c_int
     L.gdn_get_device_error.argtypes = [_vp]
+    L.gdn_selftest_device_timeout.restype = ctypes.c_int
+    L.gdn_selftest_device_timeout.argtypes = [ctypes.c_uint32, _vp]
     L.gdn_status_string.restype = ctypes.c_char_p
     L.gdn_status_string.argtypes = [ctypes.c_int]
     L.gdn_version.restype = ctypes.c_int32
@@ -543,6 +546,13 @@ def gdn_state_checkpoint(op: str, state, conv_state, slot_state, slot_conv_state
 def gdn_get_device_error(stream=None) -> int:
     """Synchronise the stream and return (and clear) the device error status code."""
     return int(load_library().gdn_get_device_error(_stream(stream)))
+
+
+def gdn_selftest_device_timeout(max_iters: int = 1024, stream=None) -> None:
+    """Enqueue the bounded-wait self-test (a wait that nothing ends, on no copy or MMA): the
+    next gdn_get_device_error() returns GDN_ERR_DEVICE_TIMEOUT."""
+    st = load_library().gdn_selftest_device_timeout(int(max_iters), _stream(stream))
+    _check(st, "gdn_selftest_device_timeout")
 
 
 def gdn_status_string(status: int) -> str:

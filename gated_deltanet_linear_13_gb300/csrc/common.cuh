@@ -168,6 +168,8 @@ cudaError_t gdn_launch_decode_multi(const GdnLayerArgs& args, float* snap_state,
                                     cudaStream_t stream);
 cudaError_t gdn_launch_prefill_simt(const GdnLayerArgs& args, cudaStream_t stream);
 cudaError_t gdn_launch_prefill_tc(const GdnLayerArgs& args, cudaStream_t stream);
+// The bounded-wait self-test (one CTA, an mbarrier nothing arrives at, max_iters polls).
+cudaError_t gdn_launch_selftest_wait(uint32_t max_iters, cudaStream_t stream);
 // 3-D tensor map over [B][T][width] elements starting at `base`, token stride `tok_stride`
 // elements; box = {box0, box1 tokens, 1 sequence}; 128-byte swizzle or none.
 bool gdn_make_map(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int elem_bytes,

@@ -472,6 +472,13 @@ gdn_status gdn_state_checkpoint(int32_t op, const gdn_dims* dims, gdn_dtype conv
   return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
 }
 
+gdn_status gdn_selftest_device_timeout(uint32_t max_iters, void* stream) {
+  if (max_iters == 0 || max_iters > (1u << 20)) return GDN_ERR_INVALID_ARGUMENT;
+  return gdn_launch_selftest_wait(max_iters, static_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? GDN_OK
+             : GDN_ERR_CUDA;
+}
+
 gdn_status gdn_get_device_error(void* stream) {
   if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return GDN_ERR_CUDA;
   unsigned bits = gdn_take_error_decode() | gdn_take_error_conv() | gdn_take_error_checkpoint() |

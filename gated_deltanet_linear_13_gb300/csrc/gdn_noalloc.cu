@@ -11,7 +11,9 @@
 //
 // The array's name is only a host-side stand-in in host code, so its device address is
 // obtained with cudaGetSymbolAddress, once per device, with that device current, on the first
-// call made on that device, and cached.
+// call made on that device, and cached for the life of the process (a device reset that
+// destroys the context makes the cached address stale; the header tells callers not to call
+// this entry point again on that device).
 #include <mutex>
 
 #include "common.cuh"

@@ -1181,6 +1181,27 @@ __global__ void __launch_bounds__(CH_THREADS, 1)
   }
 }
 
+// ======================================================================= self-test
+// One CTA waits on an mbarrier that nothing arrives at, with nothing in flight (no copy, no
+// MMA, no TMEM), through the same bounded wait, abort flag and error word as the prefill
+// kernels: each thread gives up after max_iters polls (or once another has raised the
+// flag), and the CTA records kErrTimeout, which gdn_get_device_error then reports as
+// GDN_ERR_DEVICE_TIMEOUT.
+__global__ void __launch_bounds__(128, 1) gdn_selftest_wait_kernel(uint32_t max_iters) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int abort_flag;
+  const uint32_t b = smem_addr(&bar);
+  if (threadIdx.x == 0) {
+    mbar_init(b, 1);
+    abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (!mbar_wait_or_abort(b, 0, &abort_flag, max_iters)) abort_flag = 1;
+  __syncthreads();
+  if (threadIdx.x == 0 && abort_flag) atomicOr(&g_err_tc, kErrTimeout);
+}
+
 // ======================================================================= host side
 
 // One slice's workspace: its units' tiles, then e^{G_C} per unit (256-byte aligned size).
@@ -1296,6 +1317,11 @@ size_t gdn_prefill_tc_scratch_bytes(int B, int T, int Hv) {
   const int ns = slice_chunks(B, Hv, nch);
   const size_t half = scratch_half_bytes((size_t)ns * B * Hv);
   return ns < nch ? 2 * half : half;        // two halves when the call has several slices
+}
+
+cudaError_t gdn_launch_selftest_wait(uint32_t max_iters, cudaStream_t stream) {
+  gdn_selftest_wait_kernel<<<1, 128, 0, stream>>>(max_iters);
+  return cudaGetLastError();
 }
 
 cudaError_t gdn_launch_prefill_tc(const GdnLayerArgs& L, cudaStream_t stream) {

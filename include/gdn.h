@@ -335,6 +335,10 @@ gdn_status gdn_chunk_prefill_snapshots(const gdn_dims* dims, const gdn_opts* opt
  *     returns GDN_ERR_WORKSPACE and launches nothing.
  *   - Set-up: the first call on a device looks up the array's device address (with that
  *     device current) and caches it; make that first call before any stream capture.
+ *   - Device reset: the cached address belongs to the device context of that first call.
+ *     cudaDeviceReset (or anything else that destroys the device's primary context) makes it
+ *     stale, and the library is not told: after such a reset do not call this entry point on
+ *     that device again in the same process.
  *   - Sharing: all calls share the one array and it keeps the last call's contents (nothing
  *     in it has to start at zero: each call writes every byte it reads).  Calls that overlap
  *     on the GPU (different streams, concurrent graph replays) race on it: serialise them.
@@ -353,6 +357,23 @@ gdn_status gdn_chunk_prefill_noalloc(const gdn_dims* dims, const gdn_opts* opts,
  * GDN_ERR_DEVICE_TIMEOUT), or GDN_ERR_CUDA if the synchronisation itself failed.
  */
 gdn_status gdn_get_device_error(void* stream);
+
+/*
+ * gdn_selftest_device_timeout -- exercises the failure-detection path of the kernels without
+ * faulting or hanging anything.  The pages have no counterpart of this call.  Every wait of
+ * the library's copy / tensor-core pipelines is bounded: when a copy or MMA never completes,
+ * the CTA gives up, records the condition in the device error word and returns, and the next
+ * gdn_get_device_error reports GDN_ERR_DEVICE_TIMEOUT.  This call enqueues one CTA on `stream`
+ * that waits on an mbarrier that nothing ever arrives at (no copy, MMA or TMEM in flight),
+ * with the given poll limit, through the same bounded wait and the same error word as the
+ * prefill kernels.
+ *   max_iters: polls before giving up, 1 .. 2^20 (each poll may suspend for a short,
+ *     hardware-chosen time; 2^10 ends in well under a millisecond).
+ * Returns GDN_OK once enqueued (the timeout is then reported by the next
+ * gdn_get_device_error), GDN_ERR_INVALID_ARGUMENT for a limit out of range, GDN_ERR_CUDA if the
+ * launch failed.
+ */
+gdn_status gdn_selftest_device_timeout(uint32_t max_iters, void* stream);
 
 /* Static text for a status code (never NULL). */
 const char* gdn_status_string(gdn_status status);

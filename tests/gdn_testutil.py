@@ -10,6 +10,10 @@ Tolerances (gated-delta-rule targets):
 """
 from __future__ import annotations
 
+import concurrent.futures as cf
+import json
+import os
+
 import numpy as np
 import torch
 
@@ -41,6 +45,99 @@ def metrics(x, ref) -> dict:
     maxrms = float(np.abs(x - ref).max() / rms) if rms > 0 else 0.0
     return dict(cos=cos, maxrel=maxrel, relf=relf, max_over_rms=maxrms,
                 finite=bool(np.isfinite(x).all()))
+
+
+# ------------------------------------------------------------------ measured figures
+
+def record(case: str, **figures):
+    """Print one measured parity figure set (visible with ``pytest -s`` or in a failure report)
+    and, when the environment variable GDN_PARITY_LOG names a file, append it there as one
+    JSON line, so that a run leaves the worst errors it saw next to its pass/fail verdict."""
+    line = {"case": case}
+    for k, v in figures.items():
+        line[k] = float(v) if isinstance(v, (float, np.floating)) else v
+    print("[parity]", json.dumps(line))
+    path = os.environ.get("GDN_PARITY_LOG")
+    if path:
+        with open(path, "a") as f:
+            f.write(json.dumps(line) + "\n")
+
+
+def unit_metrics(x, ref):
+    """Per-unit figures of two arrays shaped [U, n] (row u = every element of unit u):
+    max|x - ref| / max|ref| (the unit's outputs scaled to unit range), cosine and relative
+    Frobenius error, each an array of U values, plus the sums they come from (so that the
+    pieces of one unit can be merged, see :func:`merge_units`)."""
+    x = _np(x)
+    ref = _np(ref)
+    U = ref.shape[0]
+    x = x.reshape(U, -1)
+    ref = ref.reshape(U, -1)
+    diff = x - ref
+    raw = dict(maxerr=np.abs(diff).max(axis=1), scale=np.abs(ref).max(axis=1),
+               xr=(x * ref).sum(axis=1), xx=(x * x).sum(axis=1), rr=(ref * ref).sum(axis=1),
+               dd=(diff * diff).sum(axis=1), finite=bool(np.isfinite(x).all()))
+    return _figures(raw)
+
+
+def _figures(raw):
+    scale, nr, nx = raw["scale"], np.sqrt(raw["rr"]), np.sqrt(raw["xx"])
+    with np.errstate(divide="ignore", invalid="ignore"):
+        maxrel = np.where(scale > 0, raw["maxerr"] / scale, raw["maxerr"])
+        cos = np.where((nr > 0) & (nx > 0), raw["xr"] / (nx * nr), np.where(nr == nx, 1.0, 0.0))
+        relf = np.where(nr > 0, np.sqrt(raw["dd"]) / nr, np.sqrt(raw["dd"]))
+    return dict(raw, maxrel=maxrel, cos=cos, relf=relf)
+
+
+def merge_units(pieces):
+    """Merge :func:`unit_metrics` results that cover different elements of the same U units
+    (e.g. consecutive segments of tokens) into the figures of the whole units."""
+    raw = dict(maxerr=np.max([p["maxerr"] for p in pieces], axis=0),
+               scale=np.max([p["scale"] for p in pieces], axis=0),
+               finite=all(p["finite"] for p in pieces))
+    for k in ("xr", "xx", "rr", "dd"):
+        raw[k] = np.sum([p[k] for p in pieces], axis=0)
+    return _figures(raw)
+
+
+def concat_units(pieces):
+    """Concatenate :func:`unit_metrics` results of different units into one result."""
+    out = {k: np.concatenate([p[k] for p in pieces])
+           for k in ("maxerr", "scale", "xr", "xx", "rr", "dd")}
+    out["finite"] = all(p["finite"] for p in pieces)
+    return _figures(out)
+
+
+def check_units(parts, case: str, maxrel: float = None, cos: float = BF16_COS,
+                relf: float = None):
+    """Every unit of a list of :func:`unit_metrics` results against its own bound: worst
+    per-unit max|err|/max|ref| <= maxrel, worst cosine >= cos, worst relative Frobenius error
+    <= relf (each when given).  The worst figures are recorded (see :func:`record`) before
+    anything is asserted."""
+    if isinstance(parts, dict):
+        parts = [parts]
+    m = dict(maxrel=np.concatenate([p["maxrel"] for p in parts]),
+             cos=np.concatenate([p["cos"] for p in parts]),
+             relf=np.concatenate([p["relf"] for p in parts]),
+             finite=all(p["finite"] for p in parts))
+    worst = dict(units=int(m["maxrel"].size), maxrel=float(m["maxrel"].max()),
+                 cos=float(m["cos"].min()), relf=float(m["relf"].max()),
+                 worst_unit=int(m["maxrel"].argmax()))
+    record(case, **worst)
+    assert m["finite"], f"{case}: non-finite values"
+    if maxrel is not None:
+        assert worst["maxrel"] <= maxrel, f"{case}: max|err|/max|ref| {worst}"
+    if cos is not None:
+        assert worst["cos"] >= cos, f"{case}: cosine {worst}"
+    if relf is not None:
+        assert worst["relf"] <= relf, f"{case}: rel-F {worst}"
+    return worst
+
+
+def assert_units(x, ref, case: str, maxrel: float = None, cos: float = BF16_COS,
+                 relf: float = None):
+    """:func:`check_units` of two [U, n] arrays (row u = every element of unit u)."""
+    return check_units(unit_metrics(x, ref), case, maxrel=maxrel, cos=cos, relf=relf)
 
 
 def assert_bf16_parity(out, ref, what="out"):
@@ -101,6 +198,45 @@ def head_slice(inp, b: int, h: int, t0: int = 0, t1=None):
         kw["k"] = cpu(inp.k[b:b + 1, t0:t1, kh:kh + 1])
         kw["v"] = cpu(inp.v[b:b + 1, t0:t1, h:h + 1])
     return kw
+
+
+def kh_slice(inp, b: int, kh: int, t0: int = 0, t1=None, state=None, conv_state=None):
+    """Inputs of key head kh of batch row b with its r value heads, as a 1-key-head /
+    r-value-head layer (exact: the conv is depthwise and value head h reads key head h / r).
+    ``state`` [1, r, d, d] / ``conv_state`` [1, W-1, (2 + r) d] replace the inputs' own."""
+    sh = inp.shape
+    d, Hk, Hv = sh.head_dim, sh.num_k_heads, sh.num_v_heads
+    r = Hv // Hk
+    h0 = kh * r
+    t1 = sh.seqlen if t1 is None else t1
+    cpu = lambda t: t.detach().to("cpu")
+    kw = dict(num_k_heads=1, num_v_heads=r, head_dim=d, nthreads=r,
+              a=cpu(inp.a[b:b + 1, t0:t1, h0:h0 + r]), b=cpu(inp.b[b:b + 1, t0:t1, h0:h0 + r]),
+              A_log=cpu(inp.A_log[h0:h0 + r]), dt_bias=cpu(inp.dt_bias[h0:h0 + r]),
+              state=cpu(inp.state[b:b + 1, h0:h0 + r]) if state is None else state)
+    if sh.conv_width > 0:
+        idx = torch.cat([torch.arange(kh * d, (kh + 1) * d),
+                         torch.arange(Hk * d + kh * d, Hk * d + (kh + 1) * d),
+                         torch.arange(2 * Hk * d + h0 * d, 2 * Hk * d + (h0 + r) * d)])
+        idx_dev = idx.to(inp.x.device)
+        kw["x"] = cpu(inp.x[b:b + 1, t0:t1].index_select(2, idx_dev))
+        kw["conv_weight"] = cpu(inp.conv_weight.index_select(0, idx_dev))
+        kw["conv_state"] = (cpu(inp.conv_state[b:b + 1].index_select(2, idx_dev))
+                            if conv_state is None else conv_state)
+    else:
+        kw["q"] = cpu(inp.q[b:b + 1, t0:t1, kh:kh + 1])
+        kw["k"] = cpu(inp.k[b:b + 1, t0:t1, kh:kh + 1])
+        kw["v"] = cpu(inp.v[b:b + 1, t0:t1, h0:h0 + r])
+    return kw
+
+
+def oracle_many(jobs, workers: int = None):
+    """oracle.layer over a list of keyword sets, several at a time (the C oracle runs outside
+    the interpreter lock); results in order."""
+    if workers is None:
+        workers = max(1, len(os.sched_getaffinity(0)) // 3)
+    with cf.ThreadPoolExecutor(max_workers=workers) as ex:
+        return list(ex.map(lambda kw: oracle.layer(**kw), jobs))
 
 
 def oracle_full(inp, **opts):

@@ -261,3 +261,9 @@ def test_checkpoint_rejects_bad_arguments(L):
     assert ck(ss=A + 8) == 1
     assert ck(n=70000) == 2
     assert ck(n=0, st=None) == 0
+
+
+def test_selftest_rejects_bad_limits(L):
+    # out-of-range poll limits are refused before any launch
+    for n in (0, (1 << 20) + 1, 0xFFFFFFFF):
+        assert L.gdn_selftest_device_timeout(n, None) == 1

@@ -4,16 +4,21 @@ The conv is checked against the oracle's conv (numpy.convolve-pinned) within one
 rounding of the output; its state, and every checkpoint copy, bit for bit.  The resume
 test runs the 27B-shape layer over 131072 tokens in 512-token buckets with a checkpoint
 after every bucket, restores a middle checkpoint, continues, and requires the continuation
-to equal the uninterrupted run bit for bit (hybrid prefix-reuse semantics); sampled units
-of that long run are checked against the oracle.
+to equal the uninterrupted run bit for bit (hybrid prefix-reuse semantics); every unit of
+that long run is checked against the oracle, with bf16 and with fp32 outputs.
 """
+import concurrent.futures as cf
+import os
+
 import numpy as np
 import pytest
 import torch
 
 import gdn_inputs as gi
 import oracle
-from gdn_testutil import assert_bf16_parity, assert_state_parity, head_slice, to_device
+from gdn_testutil import (BF16_MAXREL, BF16_OUT_ROUNDING, BF16_STATE_RELF, assert_bf16_parity,
+                          assert_state_parity, check_units, concat_units, kh_slice, merge_units,
+                          to_device, unit_metrics)
 
 pytestmark = pytest.mark.gpu
 
@@ -119,19 +124,26 @@ def _bucket_run(gdn, dev, T_total, bucket, first_bucket, bank, cbank, out):
                                  num_k_heads=Hk)
 
 
+CKPTS = (0, 15, 127, 255)
+
+
 def test_27b_long_context_bucketed_with_resume(gdn):
     """27B shape (16/48 heads, conv), B=1, T=131072 = 256 buckets of 512 with a checkpoint
     after each; restore checkpoint 127 and continue: bit-identical to the uninterrupted run.
-    Two sampled heads over all 131072 tokens against the oracle (state at 4 checkpoints)."""
+    The same bucketed run with fp32 outputs too; then every one of the 48 heads against the
+    oracle over all 131072 tokens (outputs per segment, state at checkpoints 0, 15, 127, 255):
+    fp32 outputs within max|o - o_ref| / max|o_ref| <= 5e-3 per unit and segment, bf16
+    outputs within that plus their own rounding, cosine >= 0.9999; states cosine >= 0.9999
+    and rel-F <= 5e-3."""
     T, bucket = 131072, 512
     nbk = T // bucket
-    sh = gi.GDNShape(1, T, 16, 48, conv_width=4)
+    Hk, Hv, d = 16, 48, 128
+    r = Hv // Hk
+    sh = gi.GDNShape(1, T, Hk, Hv, conv_width=4)
     dev = gi.make_inputs_device(sh, seed=4000, device="cuda")
-    # x slices along T must be contiguous per bucket for the C ABI: keep [B=1, T, C] layout
-    bank = torch.empty(nbk, 48, 128, 128, device="cuda")
+    bank = torch.empty(nbk, Hv, d, d, device="cuda")
     cbank = torch.empty(nbk, 3, sh.conv_channels, dtype=torch.bfloat16, device="cuda")
-    out = torch.empty(1, T, 48, 128, dtype=torch.bfloat16, device="cuda")
-    x0 = dev.x
+    out = torch.empty(1, T, Hv, d, dtype=torch.bfloat16, device="cuda")
     _bucket_run(gdn, dev, T, bucket, 0, bank, cbank, out)
     assert gdn.gdn_get_device_error() == 0
     final_state = dev.state.clone()
@@ -153,23 +165,64 @@ def test_27b_long_context_bucketed_with_resume(gdn):
     assert torch.equal(out2[:, t_mid:], out[:, t_mid:])
     assert torch.equal(dev.state, final_state)
     assert torch.equal(dev.conv_state, final_conv)
-    # oracle on two sampled heads, in segments ending at checkpoints 0, 15, 127, 255
-    out_h = out
-    for (b, h) in [(0, 5), (0, 40)]:
-        st, cst = None, None
-        t0 = 0
-        for ck in (0, 15, 127, 255):
+    del out2, bank2, cbank2
+    # the same bucketed run with fp32 outputs, from the zero state
+    dev.state = torch.zeros_like(final_state)
+    dev.conv_state = torch.zeros_like(final_conv)
+    out32 = torch.empty(1, T, Hv, d, dtype=torch.float32, device="cuda")
+    bank32 = torch.empty_like(bank)
+    cbank32 = torch.empty_like(cbank)
+    _bucket_run(gdn, dev, T, bucket, 0, bank32, cbank32, out32)
+    assert gdn.gdn_get_device_error() == 0
+    # fp32 outputs do not change the recurrence: the same states, bit for bit
+    assert torch.equal(dev.state, final_state)
+    assert torch.equal(bank32[list(CKPTS)], bank[list(CKPTS)])
+    del bank32, cbank32
+    dev.state = torch.zeros_like(final_state)
+    dev.conv_state = torch.zeros_like(final_conv)
+
+    # the oracle: every key head (with its 3 value heads) in segments ending at the checkpoints
+    bank_h = bank[list(CKPTS)].double().cpu().numpy()          # [4, Hv, d, d]
+    parts = {k: [] for k in ("o32", "o16", "state")}    # [segment][key head] -> r units
+
+    def unit_rows(o):       # [t, r, d] -> [r, t*d]
+        return np.ascontiguousarray(np.asarray(o, dtype=np.float64).transpose(1, 0, 2)
+                                    .reshape(o.shape[1], -1))
+
+    def job(kh, t0, t1, st, cst, ci):
+        kw = kh_slice(dev, 0, kh, t0, t1,
+                      state=torch.zeros(1, r, d, d) if st is None else st,
+                      conv_state=torch.zeros(1, 3, (2 + r) * d) if cst is None else cst)
+        res = oracle.layer(**kw)
+        ref = unit_rows(res.out[0])
+        got32 = unit_rows(out32[0, t0:t1, kh * r:(kh + 1) * r].double().cpu().numpy())
+        got16 = unit_rows(out[0, t0:t1, kh * r:(kh + 1) * r].double().cpu().numpy())
+        m = (unit_metrics(got32, ref), unit_metrics(got16, ref),
+             unit_metrics(bank_h[ci, kh * r:(kh + 1) * r].reshape(r, -1),
+                          res.state[0].reshape(r, -1)))
+        return m, res.state, res.conv_state
+
+    carry = [(None, None)] * Hk
+    t0 = 0
+    with cf.ThreadPoolExecutor(max_workers=max(1, len(os.sched_getaffinity(0)) // r)) as ex:
+        for ci, ck in enumerate(CKPTS):
             t1 = (ck + 1) * bucket
-            kw = head_slice(dev, b, h, t0, t1)
-            kw["x"] = kw["x"]  # pre-conv slice of [t0, t1)
-            if st is not None:
-                kw["state"], kw["conv_state"] = st, cst
-            else:
-                kw["state"] = torch.zeros(1, 1, 128, 128)
-                kw["conv_state"] = torch.zeros(1, 3, 384)
-            r = oracle.layer(**kw)
-            assert_bf16_parity(out_h[0, t0:t1, h].cpu(), r.out[0, :, 0], what=f"out h{h} <{t1}")
-            assert_state_parity(bank[ck, h].cpu(), r.state[0, 0], what=f"state h{h} @ ckpt {ck}")
-            st, cst = r.state, r.conv_state
+            res = list(ex.map(lambda kh: job(kh, t0, t1, carry[kh][0], carry[kh][1], ci),
+                              range(Hk)))
+            for kh, (m, st, cst) in enumerate(res):
+                parts["o32"].append(m[0])
+                parts["o16"].append(m[1])
+                parts["state"].append(m[2])
+                carry[kh] = (torch.from_numpy(st), torch.from_numpy(cst))
             t0 = t1
-    del x0
+    # per unit over the whole call (the segments of a unit merged), then per segment
+    for key, tag, bound in (("o32", "f32 out", BF16_MAXREL),
+                            ("o16", "bf16 out", BF16_MAXREL + BF16_OUT_ROUNDING)):
+        segs = parts[key]
+        per_seg = [concat_units(segs[ci * Hk:(ci + 1) * Hk]) for ci in range(len(CKPTS))]
+        check_units(merge_units(per_seg), f"qwen36_27b T131072 bucket512 out ({tag}), per unit",
+                    maxrel=bound)
+        check_units(per_seg, f"qwen36_27b T131072 bucket512 out ({tag}), per unit and segment",
+                    maxrel=None, cos=None)
+    check_units(parts["state"], "qwen36_27b T131072 bucket512 state at checkpoints 0/15/127/255",
+                relf=BF16_STATE_RELF)

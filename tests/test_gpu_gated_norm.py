@@ -14,8 +14,7 @@ import torch
 import gdn_inputs as gi
 import gdn_testutil
 import oracle
-from gdn_testutil import (assert_bf16_parity, assert_f32_parity, head_slice, oracle_full,
-                          to_device)
+from gdn_testutil import assert_f32_parity, oracle_full, to_device
 
 pytestmark = pytest.mark.gpu
 
@@ -77,13 +76,50 @@ def _assert_norm_of(y, o32, z, w, bf16_out, what):
     assert not bad.any(), f"{what}: {bad.sum()} elements off, worst {(err - tol).max():.3e}"
 
 
-def _assert_end_to_end(y, want, what):
-    """Against the oracle all the way (recurrence, then norm).  The norm rescales each token
-    to unit RMS, so a token whose output is small next to the state's scale carries the
-    recurrence's bf16-operand error amplified by that ratio: the whole-tensor cosine is the
-    bar here (the per-element bound is the one above, on the kernel's own output)."""
-    m = gdn_testutil.metrics(y.float().cpu(), want)
+def _assert_end_to_end(y, o_plain, o_ref, z, w, bf16_out, what):
+    """Against the oracle all the way (its recurrence, then its norm), element by element.
+
+    The gated call runs the same recurrence as the plain call (its states are bit-identical)
+    and normalises that fp32 output o' = o + e, where e is the recurrence's error, itself held
+    to the parity bar by the plain-call tests.  Per token, with delta = max_i |e_i| (measured:
+    the plain call's fp32 output against the oracle) and r = sqrt(mean(o^2) + eps) of the
+    oracle's vector, |rms(o') - r| <= delta (triangle inequality of the RMS), and
+    o'/rms(o') - o/r = e/rms(o') + o (1/rms(o') - 1/r) give, for delta < r,
+        |u'_i - u_i| <= delta / (r - delta) * (1 + |o_i| / r),      u = o / r,
+    which y = w silu(z) u inherits times |w_i silu(z_i)|.  On top come the norm's own fp32
+    arithmetic, the output rounding and the hardware-tanh SiLU (as in _assert_norm_of).  A
+    token whose recurrence error reaches half its own rms (delta >= r/2: an output vector far
+    smaller than the state's scale, e.g. a query almost orthogonal to the stored keys, where
+    the bf16 snapshot of the state costs more than the vector itself) has no useful bound:
+    such tokens are counted and must stay below 1% (their gated value is still held to the
+    norm of the kernel's own output by _assert_norm_of); the whole-tensor cosine >= 0.9999 is
+    held as well."""
+    o_ref = np.asarray(o_ref, dtype=np.float64)
+    want = oracle.gated_rmsnorm(o_ref, z, w, EPS)
+    yy = np.asarray(y.float().cpu().numpy(), dtype=np.float64)
+    op = np.asarray(o_plain.float().cpu().numpy(), dtype=np.float64)
+    zz = np.asarray(z.float().numpy(), dtype=np.float64)
+    ww = np.asarray(w.float().numpy(), dtype=np.float64)
+    delta = np.abs(op - o_ref).max(axis=-1, keepdims=True)
+    rr = np.sqrt((o_ref ** 2).mean(axis=-1, keepdims=True) + EPS)
+    silu = zz / (1.0 + np.exp(-zz))
+    lin = np.abs(ww * silu) * delta / np.maximum(rr - delta, 1e-300) * (1.0 + np.abs(o_ref) / rr)
+    u = np.abs(ww * o_ref / rr)
+    rel = (2.0 ** -8 if bf16_out else 0.0) + 1e-5
+    tol = lin + rel * np.abs(want) + 1e-6 * np.abs(want).max()
+    if bf16_out:
+        tol = tol + 2.0 * 0.5 * np.abs(zz) * 2.0 ** -11 * (u + lin)
+    err = np.abs(yy - want)
+    m = gdn_testutil.metrics(yy, want)
+    ok_tok = np.broadcast_to(delta < 0.5 * rr, err.shape)
+    ill = 1.0 - float((delta < 0.5 * rr).mean())
+    gdn_testutil.record(what, cos=m["cos"], maxrel=m["maxrel"],
+                        worst_err_over_bound=float((err / tol)[ok_tok].max()),
+                        ill_conditioned_tokens=ill)
     assert m["finite"], what
+    assert ill <= 0.01, f"{what}: {ill:.2%} of the tokens have a recurrence error >= rms / 2"
+    bad = (err > tol) & ok_tok
+    assert not bad.any(), f"{what}: {bad.sum()} elements off, worst {(err - tol)[bad].max():.3e}"
     assert m["cos"] >= 0.9999, f"{what}: {m}"
 
 
@@ -94,7 +130,6 @@ def test_prefill_tensor_core_path(gdn, out_dtype):
     inp = gi.make_inputs(sh, seed=6100, dtype="bf16", state="normal")
     z, w = _gate_inputs((2, 200, 6, 128), 1, "bf16")
     ref = oracle_full(inp)
-    want = oracle.gated_rmsnorm(ref.out, z, w, EPS)
     plain = to_device(inp)
     out_p = torch.empty(2, 200, 6, 128, dtype=torch.float32, device="cuda")
     _prefill(gdn, plain, out_p)
@@ -103,14 +138,16 @@ def test_prefill_tensor_core_path(gdn, out_dtype):
     _prefill(gdn, gated, out_g, gate=(z.cuda(), w.cuda()))
     assert gdn.gdn_get_device_error() == 0
     _assert_norm_of(out_g, out_p.cpu(), z, w, out_dtype == torch.bfloat16, "gated out")
-    _assert_end_to_end(out_g, want, "gated out vs oracle")
+    _assert_end_to_end(out_g, out_p, ref.out, z, w, out_dtype == torch.bfloat16,
+                       f"gated prefill B2 T200 ({out_dtype}) vs oracle")
     assert torch.equal(gated.state, plain.state)
     assert torch.equal(gated.conv_state, plain.conv_state)
 
 
 def test_prefill_27b_shape_skipped_row(gdn):
     """A 512-token call at the 27B shape (16/48 heads); batch row 1 is skipped by
-    state_slots and its outputs stay as they were.  Sampled heads against the oracle."""
+    state_slots and its outputs stay as they were.  Every head of rows 0 and 2 against the
+    oracle."""
     sh = gi.GDNShape(3, 512, 16, 48, conv_width=4)
     inp = gi.make_inputs(sh, seed=6200, dtype="bf16", state="normal")
     z, w = _gate_inputs((3, 512, 48, 128), 2, "bf16")
@@ -129,10 +166,9 @@ def test_prefill_27b_shape_skipped_row(gdn):
     o32, o = outs
     assert torch.all(o[1].float() == 7.0)
     _assert_norm_of(o[0::2], o32[0::2], z[0::2], w, True, "gated out")
-    for (b, h) in [(0, 0), (0, 47), (2, 17), (2, 30)]:
-        r = oracle.layer(**head_slice(inp, b, h))
-        want = oracle.gated_rmsnorm(r.out[0, :, 0], z[b, :, h], w, EPS)
-        _assert_end_to_end(o[b, :, h], want, f"gated out {b},{h} vs oracle")
+    ref = oracle_full(inp)
+    _assert_end_to_end(o[0::2], o32[0::2], ref.out[0::2], z[0::2], w, True,
+                       "gated prefill 27B-shape T512 (rows 0, 2) vs oracle")
 
 
 def test_prefill_fp32_mode(gdn):
@@ -185,12 +221,11 @@ def test_decode_27b_shape(gdn, B):
         inp.conv_state.shape).astype(np.float32))
     z, w = _gate_inputs((B, steps, 48, 128), 4 + B, "bf16")
     ref = oracle_full(inp)
-    want = oracle.gated_rmsnorm(ref.out, z, w, EPS)
     plain, gated = to_device(inp), to_device(inp)
-    _decode_run(gdn, plain, plain.x, plain.a, plain.b, steps)
+    out_p = _decode_run(gdn, plain, plain.x, plain.a, plain.b, steps, out_dtype=torch.float32)
     out = _decode_run(gdn, gated, gated.x, gated.a, gated.b, steps, z.cuda(), w.cuda())
     assert gdn.gdn_get_device_error() == 0
-    assert_bf16_parity(out.float().cpu(), want, what="gated decode out")
+    _assert_end_to_end(out, out_p, ref.out, z, w, True, f"gated decode 27B-shape B{B} vs oracle")
     assert torch.equal(gated.state, plain.state)
     assert torch.equal(gated.conv_state, plain.conv_state)
 

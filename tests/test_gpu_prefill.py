@@ -1,9 +1,9 @@
 """Parity of gdn_chunk_prefill (CUDA, through the C ABI) with the fp64 oracle.
 
 Workloads follow the Qwen3.5/3.6 gated-delta-net layer shapes (d = 128): the tiny fp32
-layer, the 0.8B-shape sweep over T (ragged tails included), the 4B-shape layer with conv
-and strongly decayed heads (small, then full size on sampled heads), and the 27B-shape
-131072-token prefill in 512-token buckets with checkpoints (sampled heads).
+layer, the 0.8B-shape sweep over T (ragged tails included), and the 4B-shape layer with conv
+and strongly decayed heads (small, then at full size with every unit checked, fp32 and bf16
+outputs).
 """
 import math
 
@@ -13,8 +13,9 @@ import torch
 
 import gdn_inputs as gi
 import oracle
-from gdn_testutil import (assert_bf16_parity, assert_f32_parity, assert_state_parity,
-                          head_slice, metrics, oracle_full, run_prefill, to_device)
+from gdn_testutil import (BF16_MAXREL, BF16_OUT_ROUNDING, BF16_STATE_RELF, assert_bf16_parity,
+                          assert_f32_parity, assert_state_parity, assert_units, oracle_full,
+                          run_prefill, to_device)
 
 pytestmark = pytest.mark.gpu
 
@@ -95,24 +96,39 @@ def test_4b_shape_conv_small(gdn):
     np.testing.assert_array_equal(dev.conv_state.float().cpu().numpy(), ref.conv_state)
 
 
-def test_4b_shape_full_size_sampled(gdn):
-    """The full 4B-shape workload (B=4, T=4096, conv, strong decay on heads 0..15):
-    sampled (batch, head) units against the oracle over all 4096 tokens."""
+@pytest.fixture(scope="module")
+def full_4b():
+    """The full 4B-shape workload (B=4, T=4096, 16/32 heads, conv, strong decay on value heads
+    0..15) and the oracle over all of it (128 units x 4096 tokens)."""
     sh = gi.GDNShape(4, 4096, 16, 32, conv_width=4)
     inp = gi.make_inputs(sh, seed=2000, dtype="bf16", strong_decay_half=True)
+    return inp, oracle_full(inp)
+
+
+@pytest.mark.parametrize("out_dtype", [torch.float32, torch.bfloat16])
+def test_4b_shape_full_size_every_unit(gdn, full_4b, out_dtype):
+    """Every (batch, value head) unit of the full 4B-shape call against the oracle, over all
+    4096 tokens: with fp32 outputs max|o - o_ref| / max|o_ref| <= 5e-3 per unit and cosine
+    >= 0.9999 (the stated bar, no allowance); with bf16 outputs the same plus the output's own
+    rounding.  The final state of every unit: cosine >= 0.9999, rel-F <= 5e-3."""
+    inp, ref = full_4b
+    sh = inp.shape
+    B, T, Hv, d = sh.batch, sh.seqlen, sh.num_v_heads, sh.head_dim
     dev = to_device(inp)
-    x_host = inp.x
-    out = run_prefill(gdn, dev)
+    out = run_prefill(gdn, dev, out_dtype=out_dtype)
     assert gdn.gdn_get_device_error() == 0
-    out_h = out.cpu()
-    S_h = dev.state.cpu()
-    for (b, h) in [(0, 0), (1, 9), (2, 17), (3, 31)]:
-        r = oracle.layer(**head_slice(inp, b, h))
-        assert_bf16_parity(out_h[b, :, h], r.out[0, :, 0], what=f"out[{b},:,{h}]")
-        assert_state_parity(S_h[b, h], r.state[0, 0], what=f"state[{b},{h}]")
+    tag = "f32" if out_dtype == torch.float32 else "bf16"
+    bound = BF16_MAXREL + (BF16_OUT_ROUNDING if out_dtype == torch.bfloat16 else 0.0)
+    units = lambda o: np.ascontiguousarray(np.asarray(o, dtype=np.float64)
+                                           .transpose(0, 2, 1, 3).reshape(B * Hv, T * d))
+    assert_units(units(out.double().cpu().numpy()), units(ref.out),
+                 f"qwen35_4b B4 T4096 out ({tag} out), per unit", maxrel=bound)
+    assert_units(dev.state.double().cpu().numpy().reshape(B * Hv, -1),
+                 ref.state.reshape(B * Hv, -1), f"qwen35_4b B4 T4096 final state ({tag} out)",
+                 relf=BF16_STATE_RELF)
     # conv state: the last 3 pre-conv inputs of every channel, bit for bit
     np.testing.assert_array_equal(dev.conv_state.cpu().float().numpy(),
-                                  x_host[:, -3:].float().numpy())
+                                  inp.x[:, -3:].float().numpy())
 
 
 def test_slots_skip_and_permutation(gdn):
