@@ -172,15 +172,75 @@ __device__ __forceinline__ void store_row_hilo(uint32_t tile_hi, uint32_t tile_l
   }
 }
 
-// T = (I + A)^{-1} for the strictly lower 64 x 64 matrix A (fp32, row stride LA), by blocked
-// forward substitution over 16 x 16 blocks, on the 256 threads of the local group (named
-// barrier 1).  Warps 0-3 invert one diagonal block each (lane = column; right-looking: once
-// t_s is final, every later row r subtracts A_rs t_s) while the other threads zero the
-// strictly upper blocks; then the off-diagonal blocks by distance from the diagonal,
-//   X_ij = sum_{k=j}^{i-1} A_ik T_kj,   T_ij = -T_ii X_ij,
-// 64 threads per block, each one row and four consecutive columns of it (so that every row
-// of A and every 4-wide row piece of T it loads feeds four multiply-adds).
-__device__ __forceinline__ void solve_unit_lower(const float* As, float* Ts, float* X, int lt) {
+// ---- warp-level tensor-core products for the solve (mma.sync m16n8k16, bf16 in, fp32 out).
+// A value x enters as the pair hi = rn(x), lo = rn(x - hi) and a product as hi*hi + hi*lo +
+// lo*hi (the lo*lo term is below 2^-16 of it), which keeps about 16 bits of each operand.
+// Fragment layouts (lane = 4 g + t): A (16 x 16, row-major) holds rows g and g + 8, columns
+// 2t, 2t + 1 and 8 + 2t, 9 + 2t; B (16 x 8, k x n) holds k = 2t, 2t + 1 and 8 + 2t, 9 + 2t at
+// n = g; the fp32 accumulator (16 x 8) holds rows g and g + 8 at columns 2t, 2t + 1.
+struct FragA { uint32_t h[4], l[4]; };
+struct FragB { uint32_t h[2], l[2]; };
+
+__device__ __forceinline__ void mma_m16n8k16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                             uint32_t b1) {
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, "
+      "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};\n"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+// d += a b with both operands as hi + lo pairs (small terms first)
+__device__ __forceinline__ void mma_hilo(float (&d)[4], const FragA& a, const FragB& b) {
+  mma_m16n8k16(d, a.l, b.h[0], b.h[1]);
+  mma_m16n8k16(d, a.h, b.l[0], b.l[1]);
+  mma_m16n8k16(d, a.h, b.h[0], b.h[1]);
+}
+// A fragment of the 16 x 16 block at (r0, c0) of a row-major fp32 matrix (row stride LA)
+__device__ __forceinline__ void load_a_hilo(const float* M, int r0, int c0, int lane, FragA& f) {
+  const int g = lane >> 2, t = lane & 3;
+  const float* p0 = M + (r0 + g) * LA + c0 + 2 * t;
+  const float* p1 = p0 + 8 * LA;
+  const float2 x0 = *reinterpret_cast<const float2*>(p0);
+  const float2 x1 = *reinterpret_cast<const float2*>(p1);
+  const float2 x2 = *reinterpret_cast<const float2*>(p0 + 8);
+  const float2 x3 = *reinterpret_cast<const float2*>(p1 + 8);
+  pack_hilo(x0.x, x0.y, f.h[0], f.l[0]);
+  pack_hilo(x1.x, x1.y, f.h[1], f.l[1]);
+  pack_hilo(x2.x, x2.y, f.h[2], f.l[2]);
+  pack_hilo(x3.x, x3.y, f.h[3], f.l[3]);
+}
+// B fragment of the 16 (k) x 8 (n) block at (k0, n0) of a row-major fp32 matrix [k][n]
+__device__ __forceinline__ void load_b_hilo(const float* M, int k0, int n0, int lane, FragB& f) {
+  const int g = lane >> 2, t = lane & 3;
+  const float* p = M + (k0 + 2 * t) * LA + n0 + g;
+  pack_hilo(p[0], p[LA], f.h[0], f.l[0]);
+  pack_hilo(p[8 * LA], p[9 * LA], f.h[1], f.l[1]);
+}
+// The accumulators of two adjacent 16 x 8 tiles (columns 0-7, 8-15 of a 16 x 16 block) as the
+// A fragment of that block: the accumulator and A layouts coincide.
+__device__ __forceinline__ void acc_to_a_hilo(const float (&d0)[4], const float (&d1)[4],
+                                              FragA& f) {
+  pack_hilo(d0[0], d0[1], f.h[0], f.l[0]);
+  pack_hilo(d0[2], d0[3], f.h[1], f.l[1]);
+  pack_hilo(d1[0], d1[1], f.h[2], f.l[2]);
+  pack_hilo(d1[2], d1[3], f.h[3], f.l[3]);
+}
+// -d into the 16 x 8 block at (r0, c0) of a row-major fp32 matrix
+__device__ __forceinline__ void store_neg(float* M, int r0, int c0, int lane, const float (&d)[4]) {
+  const int g = lane >> 2, t = lane & 3;
+  *reinterpret_cast<float2*>(M + (r0 + g) * LA + c0 + 2 * t) = make_float2(-d[0], -d[1]);
+  *reinterpret_cast<float2*>(M + (r0 + g + 8) * LA + c0 + 2 * t) = make_float2(-d[2], -d[3]);
+}
+
+// T = (I + A)^{-1} for the strictly lower 64 x 64 matrix A (fp32, row stride LA), by the
+// blocked form of forward substitution, on the 256 threads of a local group (named barrier
+// bar_id).  For a unit lower triangular L = [[L11, 0], [L21, L22]],
+//   L^{-1} = [[T11, 0], [-T22 L21 T11, T22]],   T11 = L11^{-1},  T22 = L22^{-1}.
+// Level 0: warps 0-3 invert one diagonal 16 x 16 block each in fp32 (lane = column;
+// right-looking: once t_s is final, every later row r subtracts A_rs t_s) while the other
+// threads zero the strictly upper blocks.  Level 1 (16 -> 32) and level 2 (32 -> 64) form
+// the off-diagonal blocks as (T22 A21) T11 on the tensor cores, four warps each.
+__device__ __forceinline__ void solve_unit_lower(const float* As, float* Ts, int lt,
+                                                 uint32_t bar_id) {
   const int w = lt >> 5, lane = lt & 31;
   if (w < 4 && lane < 16) {
     const int o = 16 * w, c = lane;
@@ -213,55 +273,60 @@ __device__ __forceinline__ void solve_unit_lower(const float* As, float* Ts, flo
       Ts[(16 * bi + (e >> 4)) * LA + 16 * bj + (e & 15)] = 0.f;
     }
   }
-  named_bar_sync(1, LGT);
-  const int q = lt >> 6, rr = (lt >> 2) & 15, c4 = 4 * (lt & 3);
+  named_bar_sync(bar_id, LGT);
+  // level 1: warp w forms columns 8 (w & 1) .. + 7 of block (i, j) = (1, 0) or (3, 2)
+  if (w < 4) {
+    const int i = 2 * (w >> 1) + 1, j = i - 1, nh = w & 1;
+    FragA tii;
+    load_a_hilo(Ts, 16 * i, 16 * i, lane, tii);
+    float z[2][4] = {};
 #pragma unroll
-  for (int dist = 1; dist <= 3; ++dist) {
-    const int i = dist + q, j = q;
-    const bool active = q < 4 - dist;
-    if (active) {
-      float acc[4] = {0.f, 0.f, 0.f, 0.f};
-      for (int k = j; k < i; ++k) {
-        float av[16];
-#pragma unroll
-        for (int m4 = 0; m4 < 4; ++m4) {
-          const float4 x = *reinterpret_cast<const float4*>(As + (16 * i + rr) * LA + 16 * k + 4 * m4);
-          av[4 * m4] = x.x; av[4 * m4 + 1] = x.y; av[4 * m4 + 2] = x.z; av[4 * m4 + 3] = x.w;
-        }
-#pragma unroll
-        for (int m = 0; m < 16; ++m) {
-          const float4 t = *reinterpret_cast<const float4*>(Ts + (16 * k + m) * LA + 16 * j + c4);
-          acc[0] = fmaf(av[m], t.x, acc[0]);
-          acc[1] = fmaf(av[m], t.y, acc[1]);
-          acc[2] = fmaf(av[m], t.z, acc[2]);
-          acc[3] = fmaf(av[m], t.w, acc[3]);
-        }
-      }
-      *reinterpret_cast<float4*>(X + q * 256 + rr * 16 + c4) =
-          make_float4(acc[0], acc[1], acc[2], acc[3]);
+    for (int nt = 0; nt < 2; ++nt) {
+      FragB aij;
+      load_b_hilo(As, 16 * i, 16 * j + 8 * nt, lane, aij);
+      mma_hilo(z[nt], tii, aij);
     }
-    named_bar_sync(1, LGT);
-    if (active) {
-      float tv[16];
-#pragma unroll
-      for (int m4 = 0; m4 < 4; ++m4) {
-        const float4 x = *reinterpret_cast<const float4*>(Ts + (16 * i + rr) * LA + 16 * i + 4 * m4);
-        tv[4 * m4] = x.x; tv[4 * m4 + 1] = x.y; tv[4 * m4 + 2] = x.z; tv[4 * m4 + 3] = x.w;
-      }
-      float acc[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-      for (int m = 0; m < 16; ++m) {
-        const float4 x = *reinterpret_cast<const float4*>(X + q * 256 + m * 16 + c4);
-        acc[0] = fmaf(tv[m], x.x, acc[0]);
-        acc[1] = fmaf(tv[m], x.y, acc[1]);
-        acc[2] = fmaf(tv[m], x.z, acc[2]);
-        acc[3] = fmaf(tv[m], x.w, acc[3]);
-      }
-      *reinterpret_cast<float4*>(Ts + (16 * i + rr) * LA + 16 * j + c4) =
-          make_float4(-acc[0], -acc[1], -acc[2], -acc[3]);
-    }
-    named_bar_sync(1, LGT);
+    FragA za;
+    acc_to_a_hilo(z[0], z[1], za);
+    FragB tjj;
+    load_b_hilo(Ts, 16 * j, 16 * j + 8 * nh, lane, tjj);
+    float r[4] = {};
+    mma_hilo(r, za, tjj);
+    store_neg(Ts, 16 * i, 16 * j + 8 * nh, lane, r);
   }
+  named_bar_sync(bar_id, LGT);
+  // level 2: the 32 x 32 block at rows 32.., columns 0..; warp w forms rows 32 + 16 (w >> 1)
+  // .. + 15, columns 16 (w & 1) .. + 15
+  if (w < 4) {
+    const int r0 = 32 + 16 * (w >> 1), nh = w & 1;
+    float z[4][4] = {};
+#pragma unroll
+    for (int kk = 0; kk < 2; ++kk) {
+      FragA tb;
+      load_a_hilo(Ts, r0, 32 + 16 * kk, lane, tb);
+#pragma unroll
+      for (int nt = 0; nt < 4; ++nt) {
+        FragB ab;
+        load_b_hilo(As, 32 + 16 * kk, 8 * nt, lane, ab);
+        mma_hilo(z[nt], tb, ab);
+      }
+    }
+    float r[2][4] = {};
+#pragma unroll
+    for (int kk = 0; kk < 2; ++kk) {
+      FragA za;
+      acc_to_a_hilo(z[2 * kk], z[2 * kk + 1], za);
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt) {
+        FragB ta;
+        load_b_hilo(Ts, 16 * kk, 16 * nh + 8 * nt, lane, ta);
+        mma_hilo(r[nt], za, ta);
+      }
+    }
+    store_neg(Ts, r0, 16 * nh, lane, r[0]);
+    store_neg(Ts, r0, 16 * nh + 8, lane, r[1]);
+  }
+  named_bar_sync(bar_id, LGT);
 }
 
 // Row scaling in place of the two 64-row blocks (kb = 0, 1; 16 KB apart) of a K or Q tile:
@@ -286,9 +351,10 @@ __device__ __forceinline__ void scale_rows_in_place(uint8_t* tile, const float* 
   }
 }
 
-// ======================================================================= local kernel
-// One CTA per (chunk j of the slice, value head h, sequence b), 256 threads, three CTAs per
-// SM.  Each tile for the chain is staged, in the swizzled layout the chain's MMAs read, in
+// ======================================================================= chunk-local unit
+// One unit = (chunk j of the slice, value head h, sequence b), processed by a group of 256
+// threads with its own named barrier, TMEM columns and mbarriers (here a whole CTA of the
+// chunk-local kernel).  Each tile for the chain is staged, in the swizzled layout the chain's MMAs read, in
 // shared memory that is free at that point (P in the T region before the solve, Q~ in place,
 // T'' beside T', K~ in place and -W^T over Q~ once K is read no more) and leaves with bulk
 // copies of whole rows.
@@ -298,40 +364,69 @@ constexpr uint32_t L_MISC = L_SOLVE + 2 * SOLVE_MAT;   // factors, solve scratch
 constexpr uint32_t L_SMEM = L_MISC + 6 * KB + KB;
 constexpr uint32_t L_TMEM = 128;        // G (128 columns); later W^T in its first 64
 
-template <typename Tin>
-__global__ void __launch_bounds__(LGT, 3)
-    gdn_chunk_local_kernel(const __grid_constant__ CUtensorMap tm_q,
-                           const __grid_constant__ CUtensorMap tm_k, const TcParams p) {
-  extern __shared__ uint8_t smem_raw[];
-  // 1024-byte aligned base, formed by offsetting the shared array itself so that every
-  // pointer derived from it stays in the shared state space
-  uint8_t* sm = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
-  const uint32_t sb = smem_addr(sm);
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int jc = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
-  const int kh = h / (p.Hv / p.Hk);
-  // a later slice of the call: the grid's last block alone waits for the previous slice's
-  // chain, at its end; that keeps the grid from completing before the chain has, and lets
-  // every other block finish and free its SM for the blocks behind it
-  const bool wait_late = p.late_wait && jc == (int)gridDim.x - 1 &&
-                         h == (int)gridDim.y - 1 && b == (int)gridDim.z - 1;
-  // this unit's tokens: chunk n0 + jc of sequence b, or of a packed batch, entry n0 + jc
-  int tok0 = (p.n0 + jc) * C, ntok = min(C, p.T - tok0), seq = b;
+// A group's resources: its 1024-byte aligned L_SMEM bytes (barriers and flags inside them),
+// its 128 TMEM columns, its named barrier, and the parities of its two mbarriers.
+struct LocalGroup {
+  uint8_t* sm;
+  uint32_t sb;
+  uint32_t tmem;
+  int lt;                  // thread index within the group, 0..255
+  uint32_t bar_id;         // named barrier of the group's 256 threads
+  uint32_t in_phase;       // parity of the next wait on bar_in
+  bool tmem_pending;       // the TMEM address is still to be read from tmem_slot() after the
+                           // unit's first group barrier (which publishes the allocation)
+  __device__ void sync() const { named_bar_sync(bar_id, LGT); }
+  __device__ bool sync_or(bool x) const { return named_bar_sync_or(bar_id, LGT, x); }
+  __device__ uint64_t* barmem() const { return reinterpret_cast<uint64_t*>(sm + L_MISC + 5120); }
+  __device__ uint32_t* tmem_slot() const {
+    return reinterpret_cast<uint32_t*>(sm + L_MISC + 5120 + 32);
+  }
+  __device__ volatile int* abort_flag() const {
+    return reinterpret_cast<volatile int*>(sm + L_MISC + 5120 + 36);
+  }
+};
+
+// Thread 0 of the group: its two mbarriers and its abort flag.
+__device__ __forceinline__ void local_group_init(const LocalGroup& g) {
+  if (g.lt == 0) {
+    mbar_init(smem_addr(&g.barmem()[0]), 1);
+    mbar_init(smem_addr(&g.barmem()[1]), 1);
+    *g.abort_flag() = 0;
+    fence_mbar_init();
+  }
+}
+
+// Tokens of unit jc of a slice: first token, count and sequence; false when the unit holds no
+// work (past the last chunk of a packed batch, or a skipped / out-of-range state slot, which
+// the chain reports).
+__device__ __forceinline__ bool local_unit_tokens(const TcParams& p, int jc, int b, int& tok0,
+                                                  int& ntok, int& seq) {
+  tok0 = (p.n0 + jc) * C;
+  ntok = min(C, p.T - tok0);
+  seq = b;
   if (p.cu) {
     const int4 e = p.ctab[p.n0 + jc];
     tok0 = e.x;
     ntok = e.y;
     seq = e.z;
-    if (ntok <= 0) {                             // past the last chunk
-      if (wait_late) pdl_wait();
-      return;
-    }
+    if (ntok <= 0) return false;
   }
   const int slot = p.slots ? p.slots[seq] : seq;
-  if (slot < 0 || slot >= p.num_slots) {        // the chain kernel reports bad slots
-    if (wait_late) pdl_wait();
-    return;
-  }
+  return slot >= 0 && slot < p.num_slots;
+}
+
+// Everything of one unit that does not depend on the state.  PDL_MID: the standalone local
+// kernel of a call's first slice waits for the kernel before it (and releases its
+// dependents) between the gates and the tile loads.  Returns false when a bounded wait gave
+// up (the group's abort flag is then set and the condition recorded).
+template <typename Tin, bool PDL_MID>
+__device__ __forceinline__ bool local_unit(LocalGroup& g, const CUtensorMap* tm_q,
+                                           const CUtensorMap* tm_k, const TcParams& p, int jc,
+                                           int h, int b, int tok0, int ntok) {
+  uint8_t* sm = g.sm;
+  const uint32_t sb = g.sb;
+  const int tid = g.lt, warp = tid >> 5, lane = tid & 31;
+  const int kh = h / (p.Hv / p.Hk);
   const size_t u = ((size_t)b * p.Hv + h) * p.ns + jc;
   uint8_t* unit = p.units + u * UNIT_BYTES;
 
@@ -342,22 +437,9 @@ __global__ void __launch_bounds__(LGT, 3)
   float* eG = gl2 + 256;                                 // e^{G_r}
   float* dK = gl2 + 320;                                 // e^{G_C - G_r}
   float* fT1 = gl2 + 384;                                // beta_s e^{G_s} / ||k_s||
-  float* sX = reinterpret_cast<float*>(sm + L_MISC + 2048);
-  uint64_t* barmem = reinterpret_cast<uint64_t*>(sm + L_MISC + 5120);
-  uint32_t* sTmem = reinterpret_cast<uint32_t*>(sm + L_MISC + 5120 + 32);
-  volatile int* sAbort = reinterpret_cast<volatile int*>(sm + L_MISC + 5120 + 36);
-  const uint32_t bar_in = smem_addr(&barmem[0]), bar_mma = smem_addr(&barmem[1]);
+  volatile int* sAbort = g.abort_flag();
+  const uint32_t bar_in = smem_addr(&g.barmem()[0]), bar_mma = smem_addr(&g.barmem()[1]);
 
-  if (tid == 0) {
-    mbar_init(bar_in, 1);
-    mbar_init(bar_mma, 1);
-    *sAbort = 0;
-    fence_mbar_init();
-  }
-  if (warp == 0) {
-    tmem_alloc(smem_addr(sTmem), L_TMEM);
-    tmem_relinquish();
-  }
   // gates: g, beta and G = inclusive prefix sum of g (warp 1, two tokens per lane)
   if (warp == 1) {
     const float A_log_h = p.gates_pre ? 0.f : p.A_log[h];
@@ -393,7 +475,7 @@ __global__ void __launch_bounds__(LGT, 3)
   // chain that last wrote it is then complete and visible.  A later slice of the call (its
   // own half of a double-buffered workspace; the conv output complete since the first slice)
   // skips this and waits at its end instead, running beside the previous slice's chain.
-  if (!p.late_wait) {
+  if (PDL_MID && !p.late_wait) {
     pdl_wait();
     pdl_trigger();
   }
@@ -401,15 +483,18 @@ __global__ void __launch_bounds__(LGT, 3)
     mbar_arrive_expect_tx(bar_in, 32 * KB);
 #pragma unroll
     for (int kb = 0; kb < 2; ++kb) {
-      tma_load_3d(sb + L_KQ + kb * 16 * KB, &tm_k, kh * D + 64 * kb, tok0, b, bar_in);
-      tma_load_3d(sb + L_KQ + kb * 16 * KB + 8 * KB, &tm_q, kh * D + 64 * kb, tok0, b, bar_in);
+      tma_load_3d(sb + L_KQ + kb * 16 * KB, tm_k, kh * D + 64 * kb, tok0, b, bar_in);
+      tma_load_3d(sb + L_KQ + kb * 16 * KB + 8 * KB, tm_q, kh * D + 64 * kb, tok0, b, bar_in);
     }
   }
   tc_fence_before();
-  __syncthreads();
+  g.sync();
   tc_fence_after();
-  const uint32_t tmem = *sTmem;
-  const uint32_t TM_G = tmem, TM_W = tmem;
+  if (g.tmem_pending) {
+    g.tmem = *g.tmem_slot();
+    g.tmem_pending = false;
+  }
+  const uint32_t TM_G = g.tmem, TM_W = g.tmem;
   const int gw = warp & 3, half = warp >> 2;
   const uint32_t lane_off = static_cast<uint32_t>(gw * 32) << 16;
   const int row = 32 * gw + lane;
@@ -417,8 +502,9 @@ __global__ void __launch_bounds__(LGT, 3)
   uint32_t mma_phase = 0;
 
   do {
-    if (!mbar_wait_or_abort(bar_in, 0, sAbort)) *sAbort = 1;
-    __syncthreads();
+    if (!mbar_wait_or_abort(bar_in, g.in_phase, sAbort)) *sAbort = 1;
+    g.in_phase ^= 1;
+    g.sync();
     if (*sAbort) break;
     // ---- MMA 1: G = [K; Q] [K; Q]^T  (M = N = 128: k_0..k_63, q_0..q_63; K = 128).  Its
     //      k.k and q.k blocks feed A and P, its diagonal gives the squared row norms.
@@ -441,7 +527,7 @@ __global__ void __launch_bounds__(LGT, 3)
     mma_phase ^= 1;
     pend_mma = false;
     tc_fence_after();
-    if (__syncthreads_or(*sAbort)) break;
+    if (g.sync_or(*sAbort)) break;
 
     // ---- E1: G -> A (fp32 [r][s], strictly lower) and P (bf16 hi/lo [r][s], K-major)
     {
@@ -463,7 +549,7 @@ __global__ void __launch_bounds__(LGT, 3)
         const float inv = p.l2norm ? 1.0f / sqrtf(d + p.eps) : 1.0f;
         if (isq) nq[r] = inv * p.scale; else nk[r] = inv;
       }
-      __syncthreads();
+      g.sync();
       if (tid < 64) fT1[tid] = beta[tid] * eG[tid] * nk[tid];
       const float Gr = gl2[r], sr = (isq ? 1.0f : beta[r]) * (isq ? nq[r] : nk[r]);
       float gs[32], ns[32];
@@ -495,7 +581,7 @@ __global__ void __launch_bounds__(LGT, 3)
     //      hit different banks).
     scale_rows_in_place(sm + L_KQ + 8 * KB, eG, nq, tid);
     fence_proxy_async_smem();
-    __syncthreads();
+    g.sync();
     if (tid == 0) {                  // (bulk-copy groups are per thread: thread 0 waits on them)
       bulk_store(unit + U_P, sb + L_SOLVE + SOLVE_MAT, 16 * KB);
       tma_store_commit();
@@ -504,13 +590,13 @@ __global__ void __launch_bounds__(LGT, 3)
       tma_store_commit();
       tma_store_wait_read_1();       // P has been read: the solve may write T over it
     }
-    __syncthreads();
+    g.sync();
 
     // ---- the direct solve T = (I + A)^{-1}, then T' and T'' as bf16 hi/lo B operands
     {
       float* As = reinterpret_cast<float*>(sm + L_SOLVE);
       float* Ts = reinterpret_cast<float*>(sm + L_SOLVE + SOLVE_MAT);
-      solve_unit_lower(As, Ts, sX, tid);
+      solve_unit_lower(As, Ts, tid, g.bar_id);
       // the T'/T'' tiles reuse the A/T region: read this thread's T entries first
       float tv[2][8];
 #pragma unroll
@@ -521,7 +607,7 @@ __global__ void __launch_bounds__(LGT, 3)
         tv[jj][0] = x0.x; tv[jj][1] = x0.y; tv[jj][2] = x0.z; tv[jj][3] = x0.w;
         tv[jj][4] = x1.x; tv[jj][5] = x1.y; tv[jj][6] = x1.z; tv[jj][7] = x1.w;
       }
-      __syncthreads();
+      g.sync();
 #pragma unroll
       for (int jj = 0; jj < 2; ++jj) {
         const int idx = tid + LGT * jj, r = idx >> 3, c = idx & 7;
@@ -541,7 +627,7 @@ __global__ void __launch_bounds__(LGT, 3)
       }
     }
     fence_proxy_async_smem();
-    __syncthreads();
+    g.sync();
     if (tid == 0) {
       bulk_store(unit + U_T2, sb + L_SOLVE + 16 * KB, 16 * KB);
       tma_store_commit();
@@ -562,7 +648,7 @@ __global__ void __launch_bounds__(LGT, 3)
     pend_mma = false;
     tc_fence_after();
     if (tid == 0) tma_store_wait_read_1();   // Q~ has been read out of the Q half
-    if (__syncthreads_or(*sAbort)) break;
+    if (g.sync_or(*sAbort)) break;
     // ---- K is read no more: K~ = diag(e^{G_C-G} / ||k||) K in place; E3: W^T -> -W^T bf16
     //      (MN-major: row = d_k index, 64 token columns) into the Q half
     scale_rows_in_place(sm + L_KQ, dK, nk, tid);
@@ -572,8 +658,9 @@ __global__ void __launch_bounds__(LGT, 3)
       tmem_wait_ld();
       store_row_bf16(sb + L_KQ + (row < 64 ? 8 * KB : 24 * KB), row & 63, 4 * half, v, -1.0f);
     }
+    tc_fence_before();               // (the next unit's MMAs write these TMEM columns)
     fence_proxy_async_smem();
-    __syncthreads();
+    g.sync();
     if (tid == 0) {
       bulk_store(unit + U_KT, sb + L_KQ, 8 * KB);
       bulk_store(unit + U_KT + 8 * KB, sb + L_KQ + 16 * KB, 8 * KB);
@@ -583,18 +670,54 @@ __global__ void __launch_bounds__(LGT, 3)
     }
   } while (0);
 
-  // ---- teardown: the bulk copies out have read shared memory, (abort path only) pending
-  //      MMAs are done, then TMEM is freed
+  // ---- the unit's end: the bulk copies out have read shared memory (the next unit's loads
+  //      may overwrite it), (abort path only) pending MMAs are done
+  const bool aborted = *sAbort != 0;
   if (tid == 0) {
     tma_store_wait_read();
     if (pend_mma) mbar_wait_bounded(bar_mma, mma_phase, 1u << 16);
-    if (*sAbort) atomicOr(&g_err_tc, kErrTimeout);
+    if (aborted) atomicOr(&g_err_tc, kErrTimeout);
   }
+  return !aborted;
+}
+
+// Standalone chunk-local kernel: one CTA (one group) per (chunk j of the slice, value head h,
+// sequence b), 256 threads, three CTAs per SM.
+template <typename Tin>
+__global__ void __launch_bounds__(LGT, 3)
+    gdn_chunk_local_kernel(const __grid_constant__ CUtensorMap tm_q,
+                           const __grid_constant__ CUtensorMap tm_k, const TcParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  // 1024-byte aligned base, formed by offsetting the shared array itself so that every
+  // pointer derived from it stays in the shared state space
+  uint8_t* sm = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
+  const int tid = threadIdx.x, warp = tid >> 5;
+  const int jc = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+  // a later slice of the call: the grid's last block alone waits for the previous slice's
+  // chain, at its end; that keeps the grid from completing before the chain has, and lets
+  // every other block finish and free its SM for the blocks behind it
+  const bool wait_late = p.late_wait && jc == (int)gridDim.x - 1 &&
+                         h == (int)gridDim.y - 1 && b == (int)gridDim.z - 1;
+  int tok0, ntok, seq;
+  if (!local_unit_tokens(p, jc, b, tok0, ntok, seq)) {
+    if (wait_late) pdl_wait();
+    return;
+  }
+  LocalGroup g{sm, smem_addr(sm), 0u, tid, 1u, 0u, true};
+  local_group_init(g);
+  if (warp == 0) {
+    tmem_alloc(smem_addr(g.tmem_slot()), L_TMEM);
+    tmem_relinquish();
+  }
+  // (local_unit publishes the barrier initialisation and the TMEM address with its first
+  // group barrier, after the gates, before either is used)
+  local_unit<Tin, true>(g, &tm_q, &tm_k, p, jc, h, b, tok0, ntok);
+  // ---- teardown: TMEM is freed once every thread's last TMEM access is done
   tc_fence_before();
   __syncthreads();
   if (warp == 0) {
     tc_fence_after();
-    tmem_dealloc(tmem, L_TMEM);
+    tmem_dealloc(g.tmem, L_TMEM);
   }
   // a later slice: this grid completes only after the previous slice's chain has, so that the
   // next chain (started by this grid's completion) reads the state that chain left
@@ -657,8 +780,8 @@ __device__ __forceinline__ void store_tile_passes(const CUtensorMap* tm, Tout* s
 // local kernel plus V, double-buffered.
 //
 // The chain S -> S0 -> U -> S is the critical path; per chunk it runs
-//   C0 (S0 = bf16(S), S *= e^{G_C})  ->  U^T += S0 (-W)^T  ->  C2 (U^T -> bf16 hi / lo)
-//   ->  S += U^T K~
+//   C0 (S0 = bf16(S); S *= e^{G_C} after signalling S0)  ->  U^T += S0 (-W)^T  ->  C2 (U^T ->
+//   bf16 hi / lo)  ->  S += U^T K~
 // with one commit barrier after each of its two MMA groups.  The output MMAs (O^T = S0 Q~^T,
 // O^T += U^T P^T) and the state-independent U'^T = V^T T''^T of the next chunk are issued
 // behind them and run while the epilogue warps work on the next step.  The finished output
@@ -965,16 +1088,19 @@ __global__ void __launch_bounds__(CH_THREADS, 1)
             pk[jj] = pack_bf16(v[32 * g + 2 * jj], v[32 * g + 2 * jj + 1]);
           tmem_st16(tmem + lane_off + TM_S0 + 32 * hc + 16 * g, pk);
         }
+        tmem_wait_st();
+        if (snap_here && lane == 0) tma_store_wait_read();
+        // S0 is what the next MMAs read: signal it now, and rescale S (which only the S
+        // update, issued after C2, accumulates into) while U^T += S0 (-W)^T runs
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar_c0);
 #pragma unroll
         for (int jj = 0; jj < 64; ++jj) v[jj] *= egc;
         tmem_st32(ta, *reinterpret_cast<float(*)[32]>(&v[0]));
         tmem_st32(ta + 32, *reinterpret_cast<float(*)[32]>(&v[32]));
         tmem_wait_st();
-        if (snap_here && lane == 0) tma_store_wait_read();
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar_c0);
       // ---- C2: U^T (fp32) -> bf16 hi / lo, packed into TMEM as A operands
       if (!__all_sync(0xffffffffu, mbar_wait_or_abort(bar_u, nl & 1, sAbort))) {
         ok = false;

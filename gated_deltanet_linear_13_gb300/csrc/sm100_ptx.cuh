@@ -80,6 +80,20 @@ __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t count) {
   asm volatile("bar.sync %0, %1;\n" ::"r"(id), "r"(count) : "memory");
 }
 
+// Named barrier that also ORs a predicate over its `count` threads.
+__device__ __forceinline__ bool named_bar_sync_or(uint32_t id, uint32_t count, bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.or.pred q, %2, %3, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}\n"
+      : "=r"(r)
+      : "r"(pred ? 1u : 0u), "r"(id), "r"(count)
+      : "memory");
+  return r != 0;
+}
+
 // 2^x on the MUFU unit (approximate, about 22 correct bits).
 __device__ __forceinline__ float ex2_approx(float x) {
   float y;
@@ -92,6 +106,7 @@ __device__ __forceinline__ float ex2_approx(float x) {
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
 }
+
 
 // ---------------------------------------------------------------- TMA
 
