@@ -155,6 +155,9 @@ struct GdnLayerArgs {
   const int32_t* ccs;
   const void* ctab;
   int n_chunks;
+  // the conv of the value channels [2 Hk d, C_conv) is still to be launched (tensor-core
+  // prefill): the prefill launches it after its first chunk-local kernel, beside which it runs
+  int vconv_pending;
 };
 
 // Workspace bytes the tensor-core prefill needs for B sequences of T tokens, Hv value heads.
@@ -176,10 +179,15 @@ bool gdn_make_map(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int 
                   int width, int T, int B, long long tok_stride, int box0, int box1,
                   bool swizzle128);
 
+// Channels [c_lo, c_hi) only (c_lo a multiple of the 512-byte channel tile; c_hi < 0: to C).
+// pdl: launched with programmatic dependent launch; late_wait: the grid's last block waits at
+// its end for the kernel before it, so that the grid completes only after that kernel (a
+// launch that runs beside a kernel it does not depend on).
 cudaError_t gdn_launch_conv(int B, int T, int C, int W, int bf16, const void* x,
                             long long x_tok_stride, const void* w, const void* bias,
                             void* conv_state, int num_slots, const int32_t* slots, int silu,
-                            void* y, long long y_tok_stride, cudaStream_t stream);
+                            void* y, long long y_tok_stride, cudaStream_t stream, int c_lo = 0,
+                            int c_hi = -1, bool pdl = false, bool late_wait = false);
 // Conv-state snapshots of an in-call snapshot prefill: snapshot j of row b is the W-1
 // pre-conv rows of x ending at token (j + 1) * every, copied to bank row slots[b * n_snap + j]
 // (nothing for a row whose row_slots entry is negative; row_slots may be NULL).

@@ -57,25 +57,66 @@ __device__ __forceinline__ void st_word(float* p, const float (&v)[2]) {
   *reinterpret_cast<float2*>(p) = make_float2(v[0], v[1]);
 }
 
-// x * sigmoid(x) = x / (1 + 2^(-x log2 e)) with the hardware 2^x and reciprocal (a few ulp;
-// 2^(-x log2 e) overflows to +inf for very negative x, whose reciprocal is 0: silu -> 0)
-__device__ __forceinline__ float silu_fast(float x) {
-  float r;
-  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(1.0f + ex2_approx(-1.4426950408889634f * x)));
-  return x * r;
+
+// One token of a thread's CPT channels: y = bias + sum_j w[j] win[j] (then SiLU), on channel
+// pairs with the packed fp32x2 multiply-add (each lane the same fp32 FMA as fmaf, in the same
+// order), and the SiLU x / (1 + 2^(-x log2 e)) with the hardware 2^x and reciprocal per lane.
+template <int W, int CPT>
+__device__ __forceinline__ void conv_token(const float (&wt)[W][CPT], const float (&bi)[CPT],
+                                           const float (&win)[W][CPT], int silu,
+                                           float (&out)[CPT]) {
+#pragma unroll
+  for (int e = 0; e < CPT; e += 2) {
+    float2 acc = make_float2(bi[e], bi[e + 1]);
+#pragma unroll
+    for (int j = 0; j < W; ++j)
+      acc = __ffma2_rn(make_float2(wt[j][e], wt[j][e + 1]), make_float2(win[j][e], win[j][e + 1]),
+                       acc);
+    if (silu) {
+      const float2 m = __fmul2_rn(acc, make_float2(-1.4426950408889634f, -1.4426950408889634f));
+      const float2 d = __fadd2_rn(make_float2(1.0f, 1.0f),
+                                  make_float2(ex2_approx(m.x), ex2_approx(m.y)));
+      float r0, r1;
+      asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r0) : "f"(d.x));
+      asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r1) : "f"(d.y));
+      acc = __fmul2_rn(acc, make_float2(r0, r1));
+    }
+    out[e] = acc.x;
+    out[e + 1] = acc.y;
+  }
 }
+
+template <typename T, int W>
+__device__ __forceinline__ void conv_tile(const CUtensorMap& tm_x, int B, int T_, int C,
+                                          const T* x, long long xs, const T* w, const T* bias,
+                                          T* cs, int num_slots, const int32_t* slots, int silu,
+                                          T* y, long long ys, int c_base);
 
 template <typename T, int W>
 __global__ void __launch_bounds__(CONV_THREADS, 3) gdn_conv_kernel(
     const __grid_constant__ CUtensorMap tm_x, int B, int T_, int C, const T* x, long long xs,
     const T* w, const T* bias, T* cs, int num_slots, const int32_t* slots, int silu, T* y,
-    long long ys) {
+    long long ys, int c_base, int late_wait) {
+  conv_tile<T, W>(tm_x, B, T_, C, x, xs, w, bias, cs, num_slots, slots, silu, y, ys, c_base);
+  // a launch that runs beside the kernel before it (which it does not depend on) completes
+  // only after that kernel has: its last block waits for it, so that the kernel after this
+  // one, which waits for this grid, may rely on both
+  if (late_wait && blockIdx.x == gridDim.x - 1 && blockIdx.y == gridDim.y - 1 &&
+      blockIdx.z == gridDim.z - 1)
+    pdl_wait();
+}
+
+template <typename T, int W>
+__device__ __forceinline__ void conv_tile(const CUtensorMap& tm_x, int B, int T_, int C,
+                                          const T* x, long long xs, const T* w, const T* bias,
+                                          T* cs, int num_slots, const int32_t* slots, int silu,
+                                          T* y, long long ys, int c_base) {
   constexpr int CC = TILE_BYTES / (int)sizeof(T);       // channels per tile
   constexpr int CPT = 8 / (int)sizeof(T);               // channels per thread (4 or 2)
   constexpr int H = W - 1;                              // halo rows
   __shared__ __align__(128) uint8_t tile[TILE_ROWS * TILE_BYTES];
   __shared__ uint64_t bar;
-  const int t0 = blockIdx.x * TT, cb = blockIdx.y * CC, b = blockIdx.z;
+  const int t0 = blockIdx.x * TT, cb = c_base + blockIdx.y * CC, b = blockIdx.z;
   const int tid = threadIdx.x;
   pdl_trigger();              // the kernel that consumes y may start its set-up
   const int slot = slots ? slots[b] : b;
@@ -155,13 +196,7 @@ __global__ void __launch_bounds__(CONV_THREADS, 3) gdn_conv_kernel(
       if (t < n) {
         ld_word(col + (tb + t + H) * CC, win[H]);
         float out[CPT];
-#pragma unroll
-        for (int e = 0; e < CPT; ++e) {
-          float acc = bi[e];
-#pragma unroll
-          for (int j = 0; j < W; ++j) acc = fmaf(wt[j][e], win[j][e], acc);
-          out[e] = silu ? silu_fast(acc) : acc;
-        }
+        conv_token<W, CPT>(wt, bi, win, silu, out);
         st_word(yp, out);
         yp += ys;
 #pragma unroll
@@ -177,47 +212,55 @@ __global__ void __launch_bounds__(CONV_THREADS, 3) gdn_conv_kernel(
   }
 }
 
+template <typename T, int W>
+cudaError_t launch_conv_w(dim3 grid, cudaStream_t stream, const CUtensorMap& m, int B, int Tn,
+                          int C, const T* x, long long xs, const T* w, const T* bias, T* cs,
+                          int ns, const int32_t* slots, int silu, T* y, long long ys, int c_base,
+                          bool pdl, bool late_wait) {
+  static unsigned done = 0u;       // room for several tiles per SM
+  cudaError_t e = set_carveout_once(gdn_conv_kernel<T, W>, 100, &done);
+  if (e != cudaSuccess) return e;
+  return launch_pdl(pdl, gdn_conv_kernel<T, W>, grid, dim3(CONV_THREADS), 0, stream, m, B, Tn, C,
+                    x, xs, w, bias, cs, ns, slots, silu, y, ys, c_base, late_wait ? 1 : 0);
+}
+
 template <typename T>
-void launch_conv_t(dim3 grid, cudaStream_t stream, const CUtensorMap& m, int B, int Tn, int C,
-                   int W, const T* x, long long xs, const T* w, const T* bias, T* cs, int ns,
-                   const int32_t* slots, int silu, T* y, long long ys) {
-  static unsigned done[5] = {0u, 0u, 0u, 0u, 0u};   // room for several tiles per SM
+cudaError_t launch_conv_t(dim3 grid, cudaStream_t stream, const CUtensorMap& m, int B, int Tn,
+                          int C, int W, const T* x, long long xs, const T* w, const T* bias,
+                          T* cs, int ns, const int32_t* slots, int silu, T* y, long long ys,
+                          int c_base, bool pdl, bool late_wait) {
   switch (W) {
-    case 1: set_carveout_once(gdn_conv_kernel<T, 1>, 100, &done[1]); break;
-    case 2: set_carveout_once(gdn_conv_kernel<T, 2>, 100, &done[2]); break;
-    case 3: set_carveout_once(gdn_conv_kernel<T, 3>, 100, &done[3]); break;
-    default: set_carveout_once(gdn_conv_kernel<T, 4>, 100, &done[4]); break;
-  }
-  switch (W) {
-    case 1: gdn_conv_kernel<T, 1><<<grid, CONV_THREADS, 0, stream>>>(m, B, Tn, C, x, xs, w, bias, cs, ns, slots, silu, y, ys); break;
-    case 2: gdn_conv_kernel<T, 2><<<grid, CONV_THREADS, 0, stream>>>(m, B, Tn, C, x, xs, w, bias, cs, ns, slots, silu, y, ys); break;
-    case 3: gdn_conv_kernel<T, 3><<<grid, CONV_THREADS, 0, stream>>>(m, B, Tn, C, x, xs, w, bias, cs, ns, slots, silu, y, ys); break;
-    default: gdn_conv_kernel<T, 4><<<grid, CONV_THREADS, 0, stream>>>(m, B, Tn, C, x, xs, w, bias, cs, ns, slots, silu, y, ys); break;
+    case 1: return launch_conv_w<T, 1>(grid, stream, m, B, Tn, C, x, xs, w, bias, cs, ns, slots, silu, y, ys, c_base, pdl, late_wait);
+    case 2: return launch_conv_w<T, 2>(grid, stream, m, B, Tn, C, x, xs, w, bias, cs, ns, slots, silu, y, ys, c_base, pdl, late_wait);
+    case 3: return launch_conv_w<T, 3>(grid, stream, m, B, Tn, C, x, xs, w, bias, cs, ns, slots, silu, y, ys, c_base, pdl, late_wait);
+    default: return launch_conv_w<T, 4>(grid, stream, m, B, Tn, C, x, xs, w, bias, cs, ns, slots, silu, y, ys, c_base, pdl, late_wait);
   }
 }
 
 cudaError_t gdn_launch_conv(int B, int T, int C, int W, int bf16, const void* x,
                             long long x_tok_stride, const void* w, const void* bias,
                             void* conv_state, int num_slots, const int32_t* slots, int silu,
-                            void* y, long long y_tok_stride, cudaStream_t stream) {
+                            void* y, long long y_tok_stride, cudaStream_t stream, int c_lo,
+                            int c_hi, bool pdl, bool late_wait) {
   if (B == 0 || T == 0) return cudaSuccess;
   if (W < 1 || W > 4) return cudaErrorInvalidValue;
   const int eb = bf16 ? 2 : 4, cc = TILE_BYTES / eb;
+  if (c_hi < 0) c_hi = C;
+  if (c_lo < 0 || c_lo % cc != 0 || c_hi > C || c_lo >= c_hi) return cudaErrorInvalidValue;
   CUtensorMap m;
   if (!gdn_make_map(&m, x, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
                     eb, C, T, B, x_tok_stride, cc, TT + W - 1, false))
     return cudaErrorInvalidValue;
-  dim3 grid((unsigned)((T + TT - 1) / TT), (unsigned)((C + cc - 1) / cc), (unsigned)B);
+  dim3 grid((unsigned)((T + TT - 1) / TT), (unsigned)((c_hi - c_lo + cc - 1) / cc), (unsigned)B);
   if (bf16)
-    launch_conv_t<__nv_bfloat16>(grid, stream, m, B, T, C, W, (const __nv_bfloat16*)x,
-                                 x_tok_stride, (const __nv_bfloat16*)w,
-                                 (const __nv_bfloat16*)bias, (__nv_bfloat16*)conv_state,
-                                 num_slots, slots, silu, (__nv_bfloat16*)y, y_tok_stride);
-  else
-    launch_conv_t<float>(grid, stream, m, B, T, C, W, (const float*)x, x_tok_stride,
-                         (const float*)w, (const float*)bias, (float*)conv_state, num_slots,
-                         slots, silu, (float*)y, y_tok_stride);
-  return cudaGetLastError();
+    return launch_conv_t<__nv_bfloat16>(grid, stream, m, B, T, C, W, (const __nv_bfloat16*)x,
+                                        x_tok_stride, (const __nv_bfloat16*)w,
+                                        (const __nv_bfloat16*)bias, (__nv_bfloat16*)conv_state,
+                                        num_slots, slots, silu, (__nv_bfloat16*)y, y_tok_stride,
+                                        c_lo, pdl, late_wait);
+  return launch_conv_t<float>(grid, stream, m, B, T, C, W, (const float*)x, x_tok_stride,
+                              (const float*)w, (const float*)bias, (float*)conv_state, num_slots,
+                              slots, silu, (float*)y, y_tok_stride, c_lo, pdl, late_wait);
 }
 
 // ======================================================================= packed sequences
@@ -314,13 +357,7 @@ __global__ void __launch_bounds__(CONV_THREADS, 3) gdn_conv_varlen_kernel(
       }
       ld_word(col + (tb + t + H) * CC, win[H]);
       float out[CPT];
-#pragma unroll
-      for (int e = 0; e < CPT; ++e) {
-        float acc = bi[e];
-#pragma unroll
-        for (int j = 0; j < W; ++j) acc = fmaf(wt[j][e], win[j][e], acc);
-        out[e] = silu ? silu_fast(acc) : acc;
-      }
+      conv_token<W, CPT>(wt, bi, win, silu, out);
       st_word(yp, out);
       yp += ys;
 #pragma unroll

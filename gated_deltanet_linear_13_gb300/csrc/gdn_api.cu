@@ -215,10 +215,14 @@ static gdn_status prefill_impl(const gdn_dims* dims, const gdn_opts* opts, const
   L.scratch = need > conv_bytes ? static_cast<char*>(workspace) + conv_bytes : nullptr;
   L.scratch_bytes = need - conv_bytes;
   if (c.W > 0) {
-    // conv (+SiLU) of all channels into the workspace, conv state updated in place
+    // conv (+SiLU) into the workspace, conv state updated in place.  The tensor-core prefill
+    // needs only the q / k channels before its chunk-local kernel: the value channels are
+    // convolved by a second launch that runs beside that kernel (see vconv_pending).
+    const int c_hi = L.in_bf16 ? 2 * c.Hk * gdn::kHeadDim : c.Cc;
+    L.vconv_pending = c_hi < c.Cc;
     cudaError_t e = gdn_launch_conv(c.B, c.T, c.Cc, c.W, L.in_bf16, q, c.Cc, conv_weight,
                                     conv_bias, conv_state, c.num_slots, state_slots,
-                                    L.silu, workspace, c.Cc, s);
+                                    L.silu, workspace, c.Cc, s, 0, c_hi);
     if (e != cudaSuccess) return GDN_ERR_CUDA;
     const char* y = static_cast<const char*>(workspace);
     L.q = y;

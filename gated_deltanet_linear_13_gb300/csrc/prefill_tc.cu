@@ -84,6 +84,12 @@ constexpr uint32_t ID_KT = idesc_bf16(128, 64, true, false);   // K^T T'^T, V^T 
 constexpr uint32_t ID_SW = idesc_bf16(128, 64, false, true);   // S0 (-W)^T
 constexpr uint32_t ID_SQ = idesc_bf16(128, 64, false, false);  // S0 Q~^T, U^T P^T
 constexpr uint32_t ID_UK = idesc_bf16(128, 128, false, true);  // U^T K~
+// Products whose right factor is lower triangular in (output token r, summed token s) --
+// X T'^T, X T''^T, X P^T with T', T'' zero for s > r and P zero for s > r: the 16-token K-block
+// kb only reaches outputs r >= 16 kb, so it runs with N = 64 - 16 kb on columns 16 kb..63 (and
+// B's rows from 16 kb on), 62.5% of the full work.
+__host__ __device__ constexpr uint32_t id_tri_kt(int kb) { return idesc_bf16(128, 64 - 16 * kb, true, false); }
+__host__ __device__ constexpr uint32_t id_tri_sq(int kb) { return idesc_bf16(128, 64 - 16 * kb, false, false); }
 
 constexpr float LOG2E = 1.4426950408889634f;
 
@@ -636,10 +642,12 @@ __device__ __forceinline__ bool local_unit(LocalGroup& g, const CUtensorMap* tm_
     if (warp == 0 && elect_one()) {
       tc_fence_after();
 #pragma unroll
-      for (int k = 0; k < 8; ++k)
-        mma_bf16(TM_W, sdesc_sw128(sb + L_KQ + (k & 3) * 2048, 16 * KB, 1024),
-                 sdesc_sw128(sb + L_SOLVE + (k < 4 ? 0 : 8 * KB) + (k & 3) * 32, 16, 1024),
-                 ID_KT, k > 0);
+      for (int k = 0; k < 8; ++k) {
+        const int kb = k & 3;          // (T' is lower triangular: see id_tri_kt)
+        mma_bf16(TM_W + 16 * kb, sdesc_sw128(sb + L_KQ + kb * 2048, 16 * KB, 1024),
+                 sdesc_sw128(sb + L_SOLVE + (k < 4 ? 0 : 8 * KB) + kb * (2048 + 32), 16, 1024),
+                 id_tri_kt(kb), k > 0);
+      }
       mma_commit(bar_mma);
     }
     pend_mma = true;
@@ -942,10 +950,12 @@ __global__ void __launch_bounds__(CH_THREADS, 1)
       tc_fence_after();
       if (leader) {
 #pragma unroll
-        for (int k = 0; k < 8; ++k)
-          mma_bf16(tmem + TM_U, sdesc_sw128(buf + CH_V + (k & 3) * 2048, 8 * KB, 1024),
-                   sdesc_sw128(buf + U_T2 + (k < 4 ? 0 : 8 * KB) + (k & 3) * 32, 16, 1024),
-                   ID_KT, k > 0);
+        for (int k = 0; k < 8; ++k) {
+          const int kb = k & 3;        // (T'' is lower triangular: see id_tri_kt)
+          mma_bf16(tmem + TM_U + 16 * kb, sdesc_sw128(buf + CH_V + kb * 2048, 8 * KB, 1024),
+                   sdesc_sw128(buf + U_T2 + (k < 4 ? 0 : 8 * KB) + kb * (2048 + 32), 16, 1024),
+                   id_tri_kt(kb), k > 0);
+        }
       }
       __syncwarp();
       // C1 once C0 is done: U^T += S0 (-W)^T (critical), then O^T = S0 Q~^T
@@ -1009,8 +1019,10 @@ __global__ void __launch_bounds__(CH_THREADS, 1)
         for (int k = 0; k < 12; ++k) {
           const uint32_t ua = (k < 4 || k >= 8) ? TM_UH : TM_UL;
           const uint32_t pb = (k < 8) ? 0u : 8 * KB;
-          mma_bf16_ta(tmO, tmem + ua + 8 * (k & 3),
-                      sdesc_sw128(buf + U_P + pb + (k & 3) * 32, 16, 1024), ID_SQ, true);
+          const int kb = k & 3;        // (P is lower triangular: see id_tri_sq)
+          mma_bf16_ta(tmO + 16 * kb, tmem + ua + 8 * kb,
+                      sdesc_sw128(buf + U_P + pb + kb * (2048 + 32), 16, 1024), id_tri_sq(kb),
+                      true);
         }
         mma_commit((nl & 1) ? bar_o1 : bar_o0);
         if (refill_p) load_p(nl + 1);
@@ -1428,6 +1440,16 @@ cudaError_t launch_tc_t(const GdnLayerArgs& L, cudaStream_t stream) {
                    dim3((unsigned)p.ns, (unsigned)L.Hv, (unsigned)MB), dim3(LGT), L_SMEM, stream,
                    mq, mk, p);
     if (e != cudaSuccess) return e;
+    if (si == 0 && L.vconv_pending) {
+      // the value channels' conv, beside the first chunk-local kernel (which releases it right
+      // after its own grid wait and reads no value channel); its last block waits for that
+      // kernel, so the chain after it may rely on both.  It writes V into the conv output
+      // (whose base L.q is) and the value channels' conv state.
+      e = gdn_launch_conv(L.B, L.T, L.C_conv, L.W, 1, L.x, L.C_conv, L.conv_w, L.conv_b,
+                          L.conv_state, L.num_slots, L.slots, L.silu, const_cast<void*>(L.q),
+                          L.C_conv, stream, 2 * L.Hk * D, -1, true, true);
+      if (e != cudaSuccess) return e;
+    }
     e = launch_pdl(true, gdn_chunk_chain_kernel<Tout>, dim3((unsigned)(L.B * L.Hv)), dim3(CH_THREADS),
                    CH_SMEM, stream, mv, mo, ms, msn, mz, p);
     if (e != cudaSuccess) return e;
