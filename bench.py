@@ -12,8 +12,9 @@ reported as HBM GB/s under "decode".
 
 Under torchrun (N > 1) every rank runs the same workload on its own GPU (independent
 sequences: no data-path collective); the control plane (barrier, max of the times) uses
-gloo.  `--impl reference` times the fp64 CPU oracle on a bounded sample of the same
-workload instead (rank 0 only).
+gloo.  `cpu_baseline`: the fp64 CPU oracle over each GPU workload in full, on the same
+inputs, on this host's cores (rank 0, after the GPU timings).  `--impl reference` times the
+fp64 CPU oracle on a bounded sample of the same workload instead (rank 0 only).
 """
 from __future__ import annotations
 
@@ -286,14 +287,113 @@ def oracle_sample(tokens: int, heads: int = HV, seed: int = 4000, reps: int = 1)
     return time.perf_counter() - t, nthreads
 
 
+# Arm CPU part numbers (/proc/cpuinfo "CPU part") of the cores these hosts use
+_ARM_PARTS = {"0xd4f": "Neoverse-V2", "0xd40": "Neoverse-V1", "0xd0c": "Neoverse-N1",
+              "0xd49": "Neoverse-N2", "0xd8e": "Neoverse-N3", "0xd84": "Neoverse-V3"}
+
+
 def cpu_model():
+    """The host CPU's model name and the number of cores this process may run on."""
+    name = None
     try:
-        for line in open("/proc/cpuinfo"):
-            if line.lower().startswith(("model name", "cpu part")):
-                return line.split(":", 1)[1].strip()
-    except OSError:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.strip().lower().startswith("model name"):
+                name = line.split(":", 1)[1].strip()
+                break
+    except (OSError, subprocess.SubprocessError):
         pass
-    return "unknown"
+    if not name or name == "-":
+        try:
+            for line in open("/proc/cpuinfo"):
+                key = line.split(":", 1)[0].strip().lower()
+                if key == "model name":
+                    name = line.split(":", 1)[1].strip()
+                    break
+                if key == "cpu part":
+                    part = line.split(":", 1)[1].strip().lower()
+                    name = _ARM_PARTS.get(part, "Arm part " + part)
+                    break
+        except OSError:
+            pass
+    return f"{name or 'unknown'}, {len(os.sched_getaffinity(0))} cores"
+
+
+def _kh_layer(inp, kh, x=None, a=None, b=None, state=None, conv_state=None):
+    """Keyword arguments of oracle.layer for key head kh with its r value heads, as a layer of
+    one key head (exact: the conv is depthwise and value head h reads key head h / r); the
+    device tensors (or the given ones) are sliced and copied to the host."""
+    sh = inp.shape
+    r = sh.num_v_heads // sh.num_k_heads
+    h0 = kh * r
+    idx = torch.cat([torch.arange(kh * D, (kh + 1) * D),
+                     torch.arange(sh.num_k_heads * D + kh * D, sh.num_k_heads * D + (kh + 1) * D),
+                     torch.arange(2 * sh.num_k_heads * D + h0 * D,
+                                  2 * sh.num_k_heads * D + (h0 + r) * D)]).to(inp.x.device)
+    x = inp.x if x is None else x
+    a = inp.a if a is None else a
+    b = inp.b if b is None else b
+    B = x.shape[0]
+    return dict(num_k_heads=1, num_v_heads=r, head_dim=D, nthreads=r,
+                x=x.index_select(2, idx).cpu(), a=a[:, :, h0:h0 + r].cpu(),
+                b=b[:, :, h0:h0 + r].cpu(), A_log=inp.A_log[h0:h0 + r].cpu(),
+                dt_bias=inp.dt_bias[h0:h0 + r].cpu(),
+                conv_weight=inp.conv_weight.index_select(0, idx).cpu(),
+                state=(torch.zeros(B, r, D, D) if state is None else state[:, h0:h0 + r].cpu()),
+                conv_state=(torch.zeros(B, W - 1, (2 + r) * D) if conv_state is None
+                            else conv_state.index_select(2, idx).cpu()))
+
+
+def _oracle_jobs(jobs, cores):
+    """oracle.layer over a list of keyword sets, as many at a time as the cores allow (the C
+    oracle runs outside the interpreter lock); returns the wall seconds."""
+    import concurrent.futures as cf
+    import oracle
+    workers = max(1, cores // max(1, jobs[0]["nthreads"]))
+    t = time.perf_counter()
+    with cf.ThreadPoolExecutor(max_workers=workers) as ex:
+        list(ex.map(lambda kw: oracle.layer(**kw), jobs))
+    return time.perf_counter() - t
+
+
+def cpu_full_baselines(device, prefill_inp, dwl):
+    """The fp64 oracle on the host cores over each GPU workload IN FULL, on the same inputs:
+    the 27B-shape prefill (131072 tokens x 48 value heads), the 27B-shape decode (256 steps at
+    B = 128), the 4B-shape prefill (B = 4, T = 4096).  Copying the inputs to the host is not
+    timed; the oracle calls are."""
+    cores = len(os.sched_getaffinity(0))
+    out = {}
+    jobs = [_kh_layer(prefill_inp, kh) for kh in range(HK)]
+    secs = _oracle_jobs(jobs, cores)
+    out["prefill"] = {"value": T_TOTAL / secs, "unit": "tokens/s", "seconds": secs,
+                      "sample": f"the whole workload: {T_TOTAL} tokens x {HV} value heads in one "
+                                f"pass (conv + norm + gates + recurrence, fp64)"}
+    del jobs
+    # decode: 256 consecutive tokens per row are 256 decode steps (the same recurrence)
+    dec = dwl["dec"]
+    xs = dec["x"].transpose(0, 1)                         # [B, steps, C]
+    a_, b_ = dec["a"].transpose(0, 1), dec["b"].transpose(0, 1)
+    dinp = gi.GDNInputs(gi.GDNShape(DECODE_B, DECODE_STEPS, HK, HV, conv_width=W), "bf16",
+                        None, None, None, xs, a_, b_, dwl["A_log"], dwl["dt_bias"], dwl["cw"],
+                        dwl["state"], dwl["conv_state"])
+    jobs = [_kh_layer(dinp, kh, state=dwl["state"], conv_state=dwl["conv_state"])
+            for kh in range(HK)]
+    for kw in jobs:
+        kw["nthreads"] = cores
+    secs = _oracle_jobs(jobs, cores)
+    out["decode"] = {"value": DECODE_STEPS / secs, "unit": "steps/s", "seconds": secs,
+                     "sample": f"{DECODE_STEPS} decode steps at B = {DECODE_B} ({DECODE_B * HV} "
+                               f"units), the whole decode workload"}
+    del jobs
+    sh4 = gi.GDNShape(4, 4096, 16, 32, conv_width=W)
+    in4 = gi.make_inputs_device(sh4, seed=4400, device=device, strong_decay_half=True)
+    jobs = [_kh_layer(in4, kh) for kh in range(16)]
+    for kw in jobs:
+        kw["nthreads"] = max(1, cores // 4)
+    secs = _oracle_jobs(jobs, cores)
+    out["prefill_4b"] = {"value": 4 * 4096 / secs, "unit": "tokens/s", "seconds": secs,
+                         "sample": "the whole workload: B = 4 x 4096 tokens x 32 value heads"}
+    return out
 
 
 def run_reference(args):
@@ -386,8 +486,6 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="gdn", choices=["gdn", "reference"])
     ap.add_argument("--ref-tokens", type=int, default=2048)
-    ap.add_argument("--cpu-tokens", type=int, default=8192)
-    ap.add_argument("--cpu-reps", type=int, default=12)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-decode-sweep", action="store_true")
     ap.add_argument("--no-prefill-4b", action="store_true")
@@ -515,7 +613,7 @@ def main():
         tf4 = tok4 * 32 * (6 * D * D + 10 * 64 * D) / 1e12
         other_prefill.append({"workload": "qwen35_4b_gdn_prefill_B4_T4096", "tokens_per_s": tok4,
                               "ms_per_call": ms4, "tflops": tf4,
-                              "frac_of_bf16_sustained": tf4 / peaks["bf16_sustained"]})
+                              "frac_of_bf16_burst": tf4 / peaks["bf16"]})
         del g4, in4, out4
 
     # ---------------- the same 27B-shape long-context workload as ONE call that records the
@@ -555,7 +653,7 @@ def main():
         tf1 = tok1 * FLOP_PER_TOKEN / 1e12
         other_prefill.append({"workload": "qwen36_27b_prefill_T131072_one_call_snapshot_every512",
                               "tokens_per_s": tok1, "ms_per_call": ms1, "tflops": tf1,
-                              "frac_of_bf16_sustained": tf1 / peaks["bf16_sustained"]})
+                              "frac_of_bf16_burst": tf1 / peaks["bf16"]})
         del g1, ws1
 
     # ---------------- a packed variable-length batch of the 27B shape: 16 sequences of seeded
@@ -595,7 +693,7 @@ def main():
         tfv = tokv * FLOP_PER_TOKEN / 1e12
         other_prefill.append({"workload": f"qwen36_27b_prefill_varlen_16seq_T{Tv}",
                               "tokens_per_s": tokv, "ms_per_call": msv, "tflops": tfv,
-                              "frac_of_bf16_sustained": tfv / peaks["bf16_sustained"],
+                              "frac_of_bf16_burst": tfv / peaks["bf16"],
                               "lengths": [int(x) for x in lens]})
         del gv, inv, stv, csv, outv, wsv
 
@@ -724,7 +822,7 @@ def main():
                  "decode_gbs": gd_bytes / (gd_ms / 1e3) / 1e9,
                  "decode_frac_of_hbm": gd_bytes / (gd_ms / 1e3) / 1e9 / peaks["hbm_gbs"]}
         del g_gd, g_gp, gz, gzp
-    del g_dec, dwl
+    del g_dec              # (the decode inputs stay for the CPU baseline)
     # multi-token steps (gdn_decode_multi) at B = 128: T = 4 and 16 new tokens per sequence in
     # one step, against T single-token steps; bytes are those of one step plus the extra
     # tokens' inputs and outputs
@@ -884,15 +982,15 @@ def main():
                "pipeline": f"a, b up once; x up and out down per {grp} buckets "
                            f"({args.e2e_streams} upload streams), compute per 512-token bucket"}
 
-    # ---------------- CPU oracle baseline (rank 0, bounded sample)
+    # ---------------- CPU oracle baseline (rank 0): every GPU workload in full, same inputs
     cpu = None
     if rank == 0 and not args.no_cpu:
-        secs, nthreads = oracle_sample(args.cpu_tokens, reps=args.cpu_reps)
-        cpu = {"value": args.cpu_tokens * args.cpu_reps / secs, "unit": "tokens/s",
-               "cores": nthreads, "kind": "oracle", "cpu": cpu_model(), "seconds": secs,
-               "sample": f"{args.cpu_reps} consecutive passes (state carried) over the first "
-                         f"{args.cpu_tokens} tokens x {HV} value heads of the 27B-shape "
-                         f"workload (conv + norm + gates + recurrence, fp64)"}
+        full = cpu_full_baselines(device, wl["inp"], dwl)
+        cpu = dict(full["prefill"], cores=len(os.sched_getaffinity(0)), kind="oracle",
+                   cpu=cpu_model(),
+                   other_workloads=[dict(full["decode"], workload=f"qwen36_27b_decode_B{DECODE_B}"),
+                                    dict(full["prefill_4b"],
+                                         workload="qwen35_4b_gdn_prefill_B4_T4096")])
 
     if rank == 0:
         # per bucket: conv, then (chunk-local kernel + state-chain kernel) per slice of
@@ -912,12 +1010,14 @@ def main():
                        "checkpoint_every": BUCKET, "l2": "inputs larger than L2 (2.7 GB x)",
                        "parallelism": f"replicas x{world}"},
             "roofline": {"bound": "tensor", "achieved": achieved_tflops,
-                         "peak": peaks["bf16_sustained"], "unit": "TFLOP/s",
-                         "frac": achieved_tflops / peaks["bf16_sustained"],
+                         "peak": peaks["bf16"], "unit": "TFLOP/s",
+                         "frac": achieved_tflops / peaks["bf16"],
                          "traffic": measured_traffic("prefill_call", f"qwen36_27b_prefill_bucket{BUCKET}"),
                          "kernel": "gdn_chunk_prefill (conv + chunked recurrence), 512 tokens",
                          "flop_per_launch": FLOP_PER_TOKEN * BUCKET,
-                         "launch_ms": call_ms, "peak_source": peaks["source"] + " sustained"},
+                         "launch_ms": call_ms,
+                         "peak_source": peaks["source"] + " burst (the call is timed in a "
+                                        "sub-second region)"},
             "other_prefill": other_prefill,
             "latency": latency,
             "decode": {"metric": "decode state-update HBM GB/s", "value": dec_gbs,
