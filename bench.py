@@ -993,12 +993,13 @@ def main():
                                          workload="qwen35_4b_gdn_prefill_B4_T4096")])
 
     if rank == 0:
-        # per bucket: conv, then (chunk-local kernel + state-chain kernel) per slice of
-        # chunks whose tiles fit the 48 MB slice budget (80 KB per chunk and value head),
-        # then the checkpoint
+        # per bucket: the q/k conv, then (chunk-local kernel + state-chain kernel) per slice
+        # of chunks whose tiles fit the 48 MB slice budget (80 KB per chunk and value head),
+        # the value-channel conv launched once beside the first slice (bf16 input), then
+        # the checkpoint
         nch = BUCKET // 64
         per_slice = max(1, min(512, nch, (48 << 20) // (HV * 80 * 1024)))
-        launches_per_step = nbk * (1 + 2 * (-(-nch // per_slice)) + 1)
+        launches_per_step = nbk * (1 + 2 * (-(-nch // per_slice)) + 1 + 1)
         line = {
             "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,

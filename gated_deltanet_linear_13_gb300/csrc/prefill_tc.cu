@@ -80,7 +80,6 @@ constexpr uint32_t UNIT_BYTES = 80 * KB;
 constexpr size_t SLICE_BUDGET = (size_t)96 << 20;   // workspace bytes for one slice of units
 
 constexpr uint32_t ID_G = idesc_bf16(128, 128, false, false);  // [K;Q] [K;Q]^T
-constexpr uint32_t ID_KT = idesc_bf16(128, 64, true, false);   // K^T T'^T, V^T T''^T
 constexpr uint32_t ID_SW = idesc_bf16(128, 64, false, true);   // S0 (-W)^T
 constexpr uint32_t ID_SQ = idesc_bf16(128, 64, false, false);  // S0 Q~^T, U^T P^T
 constexpr uint32_t ID_UK = idesc_bf16(128, 128, false, true);  // U^T K~
