@@ -190,45 +190,59 @@ def make_prefill_workload(device):
     cbank = torch.empty(nbk, W - 1, C_CONV, dtype=torch.bfloat16, device=device)
     out = torch.empty(1, T_TOTAL, HV, D, dtype=torch.bfloat16, device=device)
     import gated_deltanet_linear_13_gb300 as gdn
-    ws = torch.empty(gdn.gdn_prefill_workspace_size(1, BUCKET, HK, HV, W), dtype=torch.uint8,
-                     device=device)
+    # two workspaces, used by alternate buckets: each call continues the one before it
+    ws = [torch.empty(gdn.gdn_prefill_workspace_size(1, BUCKET, HK, HV, W), dtype=torch.uint8,
+                      device=device) for _ in range(2)]
     rows = torch.zeros(1, dtype=torch.int32, device=device)
     slot_ids = torch.arange(nbk, dtype=torch.int32, device=device)
     return dict(inp=inp, bank=bank, cbank=cbank, out=out, ws=ws, rows=rows, slots=slot_ids)
 
 
+def bucket_call(gdn, wl, i, checkpoint=True, gate=None):
+    """Bucket i of the sequence through the public API: a call that continues bucket i - 1
+    (its kernels start while that call's state chain finishes); with `checkpoint`, the state
+    and conv state after the bucket go to checkpoint-bank slot i (an in-call snapshot at the
+    call's end: the same bank rows as a gdn_state_checkpoint SAVE after the call)."""
+    inp = wl["inp"]
+    sl = slice(i * BUCKET, (i + 1) * BUCKET)
+    kw = dict(num_k_heads=HK, conv_weight=inp.conv_weight, conv_state=inp.conv_state,
+              workspace=wl["ws"][i & 1], prev_workspace=wl["ws"][(i - 1) & 1] if i else None)
+    if checkpoint:
+        kw.update(snap_every=BUCKET, snap_state=wl["bank"], snap_conv_state=wl["cbank"],
+                  snap_slots=wl["slots"][i:i + 1].view(1, 1))
+    if gate is not None:
+        kw.update(gate_z=gate[0][:, sl], gate_weight=gate[1])
+    gdn.gdn_chunk_prefill_ex(inp.x[:, sl], None, None, inp.a[:, sl], inp.b[:, sl], inp.A_log,
+                             inp.dt_bias, inp.state, wl["out"][:, sl], **kw)
+
+
 def prefill_step(gdn, wl):
-    """A fresh sequence: 256 bucket calls of 512 tokens, a checkpoint SAVE after each."""
+    """A fresh sequence: 256 bucket calls of 512 tokens, a checkpoint of the state and conv
+    state after each."""
     inp = wl["inp"]
     inp.state.zero_()
     inp.conv_state.zero_()
     for i in range(T_TOTAL // BUCKET):
-        t0 = i * BUCKET
-        gdn.gdn_chunk_prefill(inp.x[:, t0:t0 + BUCKET], None, None, inp.a[:, t0:t0 + BUCKET],
-                              inp.b[:, t0:t0 + BUCKET], inp.A_log, inp.dt_bias, inp.state,
-                              wl["out"][:, t0:t0 + BUCKET], num_k_heads=HK,
-                              conv_weight=inp.conv_weight, conv_state=inp.conv_state,
-                              workspace=wl["ws"])
+        bucket_call(gdn, wl, i)
+
+
+def prefill_step_separate_saves(gdn, wl):
+    """The step with a gdn_state_checkpoint SAVE after each bucket call instead of the
+    in-call snapshot (each save ends the overlap of consecutive calls)."""
+    inp = wl["inp"]
+    inp.state.zero_()
+    inp.conv_state.zero_()
+    for i in range(T_TOTAL // BUCKET):
+        bucket_call(gdn, wl, i, checkpoint=False)
         gdn.gdn_state_checkpoint("save", inp.state, inp.conv_state, wl["bank"], wl["cbank"],
                                  wl["rows"], wl["slots"][i:i + 1], num_k_heads=HK)
 
 
 def prefill_calls_only(gdn, wl, gate=None):
     """The 256 bucket prefill calls of a step without the checkpoints (kernel timing); with
-    `gate` = (z [1, T, Hv, d], weight [d]) the gated-norm entry point instead."""
-    inp = wl["inp"]
+    `gate` = (z [1, T, Hv, d], weight [d]) the gated output norm too."""
     for i in range(T_TOTAL // BUCKET):
-        t0 = i * BUCKET
-        args = (inp.x[:, t0:t0 + BUCKET], None, None, inp.a[:, t0:t0 + BUCKET],
-                inp.b[:, t0:t0 + BUCKET], inp.A_log, inp.dt_bias, inp.state,
-                wl["out"][:, t0:t0 + BUCKET])
-        kw = dict(num_k_heads=HK, conv_weight=inp.conv_weight, conv_state=inp.conv_state,
-                  workspace=wl["ws"])
-        if gate is None:
-            gdn.gdn_chunk_prefill(*args, **kw)
-        else:
-            gdn.gdn_chunk_prefill_gated(*args, gate_z=gate[0][:, t0:t0 + BUCKET],
-                                        gate_weight=gate[1], **kw)
+        bucket_call(gdn, wl, i, checkpoint=False, gate=gate)
 
 
 def make_decode_workload(device):
@@ -548,6 +562,9 @@ def main():
     g_calls = torch.cuda.CUDAGraph()          # the prefill calls alone, for the kernel timing
     with torch.cuda.graph(g_calls):
         prefill_calls_only(gdn, wl)
+    g_saves = torch.cuda.CUDAGraph()          # the step with separate checkpoint saves
+    with torch.cuda.graph(g_saves):
+        prefill_step_separate_saves(gdn, wl)
     for _ in range(args.warmup):
         g_step.replay()
     t_start = torch.cuda.Event(enable_timing=True)
@@ -571,6 +588,15 @@ def main():
         barrier()
     prefill_ms = t_start.elapsed_time(t_end)
     call_ms = c0.elapsed_time(c1) / (reps * nbk)
+    g_saves.replay()
+    s0 = torch.cuda.Event(enable_timing=True)
+    s1 = torch.cuda.Event(enable_timing=True)
+    s0.record()
+    g_saves.replay()
+    s1.record()
+    torch.cuda.synchronize()
+    separate_saves_ms = s0.elapsed_time(s1)
+    del g_saves
     clocks = clk.summary()
     st = gdn.gdn_get_device_error()
     if st != 0:
@@ -936,14 +962,7 @@ def main():
                     ev_in[gi_].record(s_up)
                 comp.wait_event(ev_in[gi_])
                 for i in range(gi_ * grp, min(nbk, (gi_ + 1) * grp)):
-                    sl = slice(i * BUCKET, (i + 1) * BUCKET)
-                    gdn.gdn_chunk_prefill(inp.x[:, sl], None, None, inp.a[:, sl], inp.b[:, sl],
-                                          inp.A_log, inp.dt_bias, inp.state, wl["out"][:, sl],
-                                          num_k_heads=HK, conv_weight=inp.conv_weight,
-                                          conv_state=inp.conv_state, workspace=wl["ws"])
-                    gdn.gdn_state_checkpoint("save", inp.state, inp.conv_state, wl["bank"],
-                                             wl["cbank"], wl["rows"], wl["slots"][i:i + 1],
-                                             num_k_heads=HK)
+                    bucket_call(gdn, wl, i)
                 ev_out[gi_].record(comp)
                 with torch.cuda.stream(s_down):
                     s_down.wait_event(ev_out[gi_])
@@ -993,13 +1012,12 @@ def main():
                                          workload="qwen35_4b_gdn_prefill_B4_T4096")])
 
     if rank == 0:
-        # per bucket: the q/k conv, then (chunk-local kernel + state-chain kernel) per slice
-        # of chunks whose tiles fit the 48 MB slice budget (80 KB per chunk and value head),
-        # the value-channel conv launched once beside the first slice (bf16 input), then
-        # the checkpoint
+        # per bucket: (chunk-local kernel with the conv + state-chain kernel) per slice of
+        # chunks whose tiles fit the 96 MB slice budget (96 KB per chunk and value head), then
+        # the conv-state snapshot (the state snapshot is stored by the chain itself)
         nch = BUCKET // 64
-        per_slice = max(1, min(512, nch, (48 << 20) // (HV * 80 * 1024)))
-        launches_per_step = nbk * (1 + 2 * (-(-nch // per_slice)) + 1 + 1)
+        per_slice = max(1, min(512, nch, (96 << 20) // (HV * 96 * 1024)))
+        launches_per_step = nbk * (2 * (-(-nch // per_slice)) + 1)
         line = {
             "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
@@ -1008,7 +1026,12 @@ def main():
             "config": {"workload": "qwen36_27b_gdn_prefill_T131072_bucket512",
                        "batch": 1, "seq_len": T_TOTAL, "bucket": BUCKET, "num_k_heads": HK,
                        "num_v_heads": HV, "head_dim": D, "conv_width": W, "chunk": 64,
-                       "checkpoint_every": BUCKET, "l2": "inputs larger than L2 (2.7 GB x)",
+                       "checkpoint_every": BUCKET,
+                       "checkpoint": "state and conv state into bank slot i at the end of "
+                                     "bucket call i (in-call snapshot); each call continues "
+                                     "the previous one",
+                       "step_ms_with_separate_checkpoint_saves": separate_saves_ms,
+                       "l2": "inputs larger than L2 (2.7 GB x)",
                        "parallelism": f"replicas x{world}"},
             "roofline": {"bound": "tensor", "achieved": achieved_tflops,
                          "peak": peaks["bf16"], "unit": "TFLOP/s",

@@ -30,7 +30,7 @@ EXPORTED = ("gdn_prefill_workspace_size", "gdn_chunk_prefill", "gdn_decode_step"
             "gdn_chunk_prefill_snapshots", "gdn_chunk_prefill_gated", "gdn_decode_step_gated",
             "gdn_prefill_varlen_workspace_size", "gdn_chunk_prefill_varlen", "gdn_decode_multi",
             "gdn_get_device_error", "gdn_status_string", "gdn_version",
-            "gdn_selftest_device_timeout")
+            "gdn_selftest_device_timeout", "gdn_chunk_prefill_ex")
 NOALLOC_SCRATCH_BYTES = 64 << 20   # GDN_NOALLOC_SCRATCH_BYTES in include/gdn.h
 
 
@@ -58,6 +58,13 @@ class GdnOutGate(ctypes.Structure):
     _fields_ = [("z", ctypes.c_void_p), ("weight", ctypes.c_void_p), ("eps", ctypes.c_float)]
 
 
+class GdnPrefillExt(ctypes.Structure):
+    _fields_ = [("gate", ctypes.c_void_p), ("snap_every", ctypes.c_int32),
+                ("snap_state", ctypes.c_void_p), ("snap_conv_state", ctypes.c_void_p),
+                ("num_snap_slots", ctypes.c_int32), ("snap_slots", ctypes.c_void_p),
+                ("prev_workspace", ctypes.c_void_p)]
+
+
 _vp = ctypes.c_void_p
 _lib = None
 
@@ -83,6 +90,9 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     gp = ctypes.POINTER(GdnOutGate)
     L.gdn_chunk_prefill_gated.restype = ctypes.c_int
     L.gdn_chunk_prefill_gated.argtypes = [dp, op] + [_vp] * 13 + [gp, _vp, ctypes.c_size_t, _vp]
+    L.gdn_chunk_prefill_ex.restype = ctypes.c_int
+    L.gdn_chunk_prefill_ex.argtypes = ([dp, op] + [_vp] * 13 +
+                                       [ctypes.POINTER(GdnPrefillExt), _vp, ctypes.c_size_t, _vp])
     L.gdn_decode_step_gated.restype = ctypes.c_int
     L.gdn_decode_step_gated.argtypes = [dp, op] + [_vp] * 13 + [gp, _vp]
     L.gdn_prefill_varlen_workspace_size.restype = ctypes.c_size_t
@@ -292,8 +302,7 @@ def gdn_chunk_prefill_noalloc(q, k, v, a, b, A_log, dt_bias, state, out, *, num_
                               qk_l2norm: bool = True, conv_silu: bool = True,
                               gates_precomputed: bool = False, stream=None) -> torch.Tensor:
     """gdn_chunk_prefill without a workspace, for callers that cannot allocate: the library's
-    fixed device scratch array (NOALLOC_SCRATCH_BYTES per GPU) holds the post-conv
-    activations.  Raises GDNError(GDN_ERR_WORKSPACE) when the call needs more than that.
+    fixed device scratch array (NOALLOC_SCRATCH_BYTES per GPU) holds the call's workspace.  Raises GDNError(GDN_ERR_WORKSPACE) when the call needs more than that.
     Calls that overlap on the GPU share that array and must be serialised."""
     L = load_library()
     B, T, Hk, Hv, W, num_slots = _layer_dims(q, k, v, a, num_k_heads, conv_weight, conv_state,
@@ -370,6 +379,60 @@ def gdn_chunk_prefill_gated(q, k, v, a, b, A_log, dt_bias, state, out, *, gate_z
                                    ctypes.byref(gate), _ptr(workspace), ws_bytes,
                                    _stream(stream))
     _check(st, "gdn_chunk_prefill_gated")
+    return out
+
+
+def gdn_chunk_prefill_ex(q, k, v, a, b, A_log, dt_bias, state, out, *, num_k_heads=None,
+                         conv_weight=None, conv_bias=None, conv_state=None, state_slots=None,
+                         scale: float = 1.0, eps: float = 1e-6, qk_l2norm: bool = True,
+                         conv_silu: bool = True, gates_precomputed: bool = False,
+                         gate_z=None, gate_weight=None, gate_eps: float = 1e-6,
+                         snap_every: int = 0, snap_state=None, snap_slots=None,
+                         snap_conv_state=None, prev_workspace: Optional[torch.Tensor] = None,
+                         workspace: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """gdn_chunk_prefill with any of its optional parts (see gdn_chunk_prefill_ex in
+    include/gdn.h): the gated output norm (``gate_z``, ``gate_weight``), in-call snapshots
+    (``snap_every`` > 0, as gdn_chunk_prefill_snapshots), and ``prev_workspace``: the
+    workspace of the previous prefill call of the same sequences on this stream, which this
+    call continues (its kernels may then start while that call finishes; pass the two
+    workspaces alternately).  Returns ``out``."""
+    L = load_library()
+    B, T, Hk, Hv, W, num_slots = _layer_dims(q, k, v, a, num_k_heads, conv_weight, conv_state,
+                                             state, state_slots, None)
+    _check_layer(q, k, v, a, b, A_log, dt_bias, conv_weight, conv_bias, state, conv_state,
+                 state_slots, out, B, T, Hk, Hv, W, num_slots, gates_precomputed)
+    dev = q.device
+    ext = GdnPrefillExt()
+    gate = None
+    if gate_z is not None or gate_weight is not None:
+        gate = _out_gate(gate_z, gate_weight, gate_eps, out, q.dtype)
+        ext.gate = ctypes.cast(ctypes.pointer(gate), ctypes.c_void_p)
+    if snap_every:
+        n_snap = T // snap_every if snap_every > 0 else 0
+        nb = snap_state.shape[0]
+        _need(snap_state, "snap_state", (nb, Hv, HEAD_DIM, HEAD_DIM), torch.float32, dev)
+        _need(snap_slots, "snap_slots", (B, n_snap), torch.int32, dev)
+        if W > 1:
+            _need(snap_conv_state, "snap_conv_state", (nb, W - 1, (2 * Hk + Hv) * HEAD_DIM),
+                  q.dtype, dev)
+        ext.snap_every = int(snap_every)
+        ext.snap_state = _ptr(snap_state)
+        ext.snap_conv_state = _ptr(snap_conv_state)
+        ext.num_snap_slots = nb
+        ext.snap_slots = _ptr(snap_slots)
+    ext.prev_workspace = _ptr(prev_workspace)
+    dims = GdnDims(B, T, Hk, Hv, HEAD_DIM, 64, W, num_slots)
+    opts = _opts(_dt(q), _dt(out), qk_l2norm, eps, scale, conv_silu, gates_precomputed)
+    need = int(L.gdn_prefill_workspace_size(ctypes.byref(dims), ctypes.byref(opts)))
+    if need and workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    st = L.gdn_chunk_prefill_ex(ctypes.byref(dims), ctypes.byref(opts), _ptr(q), _ptr(k),
+                                _ptr(v), _ptr(a), _ptr(b), _ptr(A_log), _ptr(dt_bias),
+                                _ptr(conv_weight), _ptr(conv_bias), _ptr(state),
+                                _ptr(conv_state), _ptr(state_slots), _ptr(out),
+                                ctypes.byref(ext), _ptr(workspace), ws_bytes, _stream(stream))
+    _check(st, "gdn_chunk_prefill_ex")
     return out
 
 

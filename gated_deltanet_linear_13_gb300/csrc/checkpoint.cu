@@ -77,13 +77,17 @@ cudaError_t gdn_launch_checkpoint(int op, int Hv, int d, int conv_elems, int con
 // state after token t is the W-1 pre-conv inputs t-W+2 .. t, which are rows of the call's own
 // input x (every >= 64 > W-1), so each snapshot is a copy of `rows` rows of x.  One CTA per
 // (sequence, snapshot); 16-byte elements.
+constexpr int SN_ILP = 8;
+
 __global__ void __launch_bounds__(256) gdn_conv_snapshot_kernel(
     const uint8_t* x, long long x_tok_bytes, long long x_seq_bytes, int row_v4, int rows,
     int every, int n_snap, uint4* bank, int num_bank, const int32_t* slots,
     const int32_t* row_slots) {
   // launched behind the prefill's kernels with programmatic dependent launch (x is an input
   // of the call and nothing else in the call touches the bank, so the wait only keeps the
-  // copy in the call's order)
+  // copy in the call's order).  The kernel after it (a call continuing the sequence) reads
+  // nothing this one writes: it may start at once
+  pdl_trigger();
   pdl_wait();
   const long long i = blockIdx.x;                // b * n_snap + j
   const long long bb = i / n_snap, j = i % n_snap;
@@ -96,10 +100,20 @@ __global__ void __launch_bounds__(256) gdn_conv_snapshot_kernel(
   const long long t0 = (j + 1) * every - rows;   // first copied token
   const uint8_t* src = x + bb * x_seq_bytes + t0 * x_tok_bytes;
   uint4* dst = bank + (size_t)slot * rows * row_v4;
+  // SN_ILP elements per thread and pass, every load before the stores
   const int total = rows * row_v4;
-  for (int e = threadIdx.x; e < total; e += blockDim.x) {
-    const int r = e / row_v4, c = e % row_v4;
-    dst[e] = reinterpret_cast<const uint4*>(src + r * x_tok_bytes)[c];
+  for (int e0 = threadIdx.x; e0 < total; e0 += SN_ILP * blockDim.x) {
+    uint4 v[SN_ILP];
+#pragma unroll
+    for (int k = 0; k < SN_ILP; ++k) {
+      const int e = e0 + k * blockDim.x;
+      if (e < total) v[k] = reinterpret_cast<const uint4*>(src + (e / row_v4) * x_tok_bytes)[e % row_v4];
+    }
+#pragma unroll
+    for (int k = 0; k < SN_ILP; ++k) {
+      const int e = e0 + k * blockDim.x;
+      if (e < total) dst[e] = v[k];
+    }
   }
 }
 

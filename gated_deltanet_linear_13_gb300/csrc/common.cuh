@@ -158,6 +158,17 @@ struct GdnLayerArgs {
   // the conv of the value channels [2 Hk d, C_conv) is still to be launched (tensor-core
   // prefill): the prefill launches it after its first chunk-local kernel, beside which it runs
   int vconv_pending;
+  // the tensor-core prefill with conv width 4 (bf16, not a packed batch): the conv of the q
+  // and k channels fused into the chunk-local kernel, that of the v channels (into `v`) the
+  // call's first launch; the call's conv tail (its last W-1 inputs, [B][W-1][C_conv]) goes to
+  // `tail` and from there, by the last state-chain kernel, into conv_state
+  int fuse;
+  void* tail;
+  // the call continues the sequences of the call before it on the stream: the inputs before
+  // its first token come from that call's conv tail `prev_tail` (not from conv_state), and its
+  // first kernel may start while that call's last kernels still run
+  int chained;
+  const void* prev_tail;
 };
 
 // Workspace bytes the tensor-core prefill needs for B sequences of T tokens, Hv value heads.
@@ -182,12 +193,17 @@ bool gdn_make_map(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int 
 // Channels [c_lo, c_hi) only (c_lo a multiple of the 512-byte channel tile; c_hi < 0: to C).
 // pdl: launched with programmatic dependent launch; late_wait: the grid's last block waits at
 // its end for the kernel before it, so that the grid completes only after that kernel (a
-// launch that runs beside a kernel it does not depend on).
+// launch that runs beside a kernel it does not depend on).  halo: the W-1 inputs before the
+// first token come from rows [slot (halo_by_slot) or b][W-1][C] of halo instead of the conv
+// state, and the new state goes to rows [b][W-1][C] of tail instead (the conv state is left
+// alone).  Channel c is stored at column c - y_cbase of y.
 cudaError_t gdn_launch_conv(int B, int T, int C, int W, int bf16, const void* x,
                             long long x_tok_stride, const void* w, const void* bias,
                             void* conv_state, int num_slots, const int32_t* slots, int silu,
                             void* y, long long y_tok_stride, cudaStream_t stream, int c_lo = 0,
-                            int c_hi = -1, bool pdl = false, bool late_wait = false);
+                            int c_hi = -1, bool pdl = false, bool late_wait = false,
+                            const void* halo = nullptr, int halo_by_slot = 1,
+                            void* tail = nullptr, int y_cbase = 0);
 // Conv-state snapshots of an in-call snapshot prefill: snapshot j of row b is the W-1
 // pre-conv rows of x ending at token (j + 1) * every, copied to bank row slots[b * n_snap + j]
 // (nothing for a row whose row_slots entry is negative; row_slots may be NULL).

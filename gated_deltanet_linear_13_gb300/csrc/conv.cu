@@ -14,6 +14,7 @@
 // the only one that reads the old state of its channels, and it also writes the new state
 // (taken from x, which nobody modifies), so no two threads race on it.
 #include "common.cuh"
+#include "conv_math.cuh"
 #include "sm100_ptx.cuh"
 
 using namespace gdn;
@@ -58,46 +59,31 @@ __device__ __forceinline__ void st_word(float* p, const float (&v)[2]) {
 }
 
 
-// One token of a thread's CPT channels: y = bias + sum_j w[j] win[j] (then SiLU), on channel
-// pairs with the packed fp32x2 multiply-add (each lane the same fp32 FMA as fmaf, in the same
-// order), and the SiLU x / (1 + 2^(-x log2 e)) with the hardware 2^x and reciprocal per lane.
-template <int W, int CPT>
-__device__ __forceinline__ void conv_token(const float (&wt)[W][CPT], const float (&bi)[CPT],
-                                           const float (&win)[W][CPT], int silu,
-                                           float (&out)[CPT]) {
-#pragma unroll
-  for (int e = 0; e < CPT; e += 2) {
-    float2 acc = make_float2(bi[e], bi[e + 1]);
-#pragma unroll
-    for (int j = 0; j < W; ++j)
-      acc = __ffma2_rn(make_float2(wt[j][e], wt[j][e + 1]), make_float2(win[j][e], win[j][e + 1]),
-                       acc);
-    if (silu) {
-      const float2 m = __fmul2_rn(acc, make_float2(-1.4426950408889634f, -1.4426950408889634f));
-      const float2 d = __fadd2_rn(make_float2(1.0f, 1.0f),
-                                  make_float2(ex2_approx(m.x), ex2_approx(m.y)));
-      float r0, r1;
-      asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r0) : "f"(d.x));
-      asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r1) : "f"(d.y));
-      acc = __fmul2_rn(acc, make_float2(r0, r1));
-    }
-    out[e] = acc.x;
-    out[e + 1] = acc.y;
-  }
-}
+// Where the inputs before the call's first token come from, and where the new conv state
+// goes: halo == nullptr: the conv state rows of slot slots[b] (read, then overwritten);
+// else rows [b or slot][W-1][C] of `halo` (halo_by_slot picks the index), and the new state
+// goes to rows [b][W-1][C] of `tail` (the conv state is not touched).
+template <typename T>
+struct ConvEnds {
+  const T* halo;
+  int halo_by_slot;
+  T* tail;
+};
 
 template <typename T, int W>
 __device__ __forceinline__ void conv_tile(const CUtensorMap& tm_x, int B, int T_, int C,
                                           const T* x, long long xs, const T* w, const T* bias,
                                           T* cs, int num_slots, const int32_t* slots, int silu,
-                                          T* y, long long ys, int c_base);
+                                          T* y, long long ys, int c_base, int y_cbase,
+                                          const ConvEnds<T>& ends);
 
 template <typename T, int W>
 __global__ void __launch_bounds__(CONV_THREADS, 3) gdn_conv_kernel(
     const __grid_constant__ CUtensorMap tm_x, int B, int T_, int C, const T* x, long long xs,
     const T* w, const T* bias, T* cs, int num_slots, const int32_t* slots, int silu, T* y,
-    long long ys, int c_base, int late_wait) {
-  conv_tile<T, W>(tm_x, B, T_, C, x, xs, w, bias, cs, num_slots, slots, silu, y, ys, c_base);
+    long long ys, int c_base, int late_wait, int y_cbase, const ConvEnds<T> ends) {
+  conv_tile<T, W>(tm_x, B, T_, C, x, xs, w, bias, cs, num_slots, slots, silu, y, ys, c_base,
+                  y_cbase, ends);
   // a launch that runs beside the kernel before it (which it does not depend on) completes
   // only after that kernel has: its last block waits for it, so that the kernel after this
   // one, which waits for this grid, may rely on both
@@ -110,7 +96,8 @@ template <typename T, int W>
 __device__ __forceinline__ void conv_tile(const CUtensorMap& tm_x, int B, int T_, int C,
                                           const T* x, long long xs, const T* w, const T* bias,
                                           T* cs, int num_slots, const int32_t* slots, int silu,
-                                          T* y, long long ys, int c_base) {
+                                          T* y, long long ys, int c_base, int y_cbase,
+                                          const ConvEnds<T>& ends) {
   constexpr int CC = TILE_BYTES / (int)sizeof(T);       // channels per tile
   constexpr int CPT = 8 / (int)sizeof(T);               // channels per thread (4 or 2)
   constexpr int H = W - 1;                              // halo rows
@@ -127,6 +114,8 @@ __device__ __forceinline__ void conv_tile(const CUtensorMap& tm_x, int B, int T_
   }
   const T* xb = x + (size_t)b * T_ * xs;
   T* csb = cs + (size_t)slot * H * C;
+  const T* oldb = ends.halo ? ends.halo + (size_t)(ends.halo_by_slot ? slot : b) * H * C : csb;
+  T* newb = ends.tail ? ends.tail + (size_t)b * H * C : csb;
   const int nt = min(TT, T_ - t0);
   // ---- tile row r = the input of token t0 - H + r (the copy fills rows outside the
   //      sequence with zeros; rows before its start are replaced by the conv state below)
@@ -149,7 +138,7 @@ __device__ __forceinline__ void conv_tile(const CUtensorMap& tm_x, int B, int T_
 #pragma unroll
     for (int i = 0; i < H; ++i) {
       const int tau = T_ - H + i;
-      ld_word(csb + (size_t)i * C + c0, old[i]);
+      ld_word(oldb + (size_t)i * C + c0, old[i]);
       if (tau >= 0) ld_word(xb + (size_t)tau * xs + c0, nst[i]);
     }
     // a sequence shorter than W-1 keeps part of the old state (position H + tau)
@@ -189,7 +178,7 @@ __device__ __forceinline__ void conv_tile(const CUtensorMap& tm_x, int B, int T_
     float win[W][CPT];
 #pragma unroll
     for (int i = 0; i < H; ++i) ld_word(col + (tb + i) * CC, win[i]);
-    T* yp = y + ((size_t)b * T_ + t0 + tb) * ys + c0;
+    T* yp = y + ((size_t)b * T_ + t0 + tb) * ys + (c0 - y_cbase);
     const int n = min(TG, nt - tb);
 #pragma unroll
     for (int t = 0; t < TG; ++t) {
@@ -208,7 +197,7 @@ __device__ __forceinline__ void conv_tile(const CUtensorMap& tm_x, int B, int T_
   }
   if (owner) {
 #pragma unroll
-    for (int i = 0; i < H; ++i) st_word(csb + (size_t)i * C + c0, nst[i]);
+    for (int i = 0; i < H; ++i) st_word(newb + (size_t)i * C + c0, nst[i]);
   }
 }
 
@@ -216,24 +205,26 @@ template <typename T, int W>
 cudaError_t launch_conv_w(dim3 grid, cudaStream_t stream, const CUtensorMap& m, int B, int Tn,
                           int C, const T* x, long long xs, const T* w, const T* bias, T* cs,
                           int ns, const int32_t* slots, int silu, T* y, long long ys, int c_base,
-                          bool pdl, bool late_wait) {
+                          bool pdl, bool late_wait, int y_cbase, const ConvEnds<T>& ends) {
   static unsigned done = 0u;       // room for several tiles per SM
   cudaError_t e = set_carveout_once(gdn_conv_kernel<T, W>, 100, &done);
   if (e != cudaSuccess) return e;
   return launch_pdl(pdl, gdn_conv_kernel<T, W>, grid, dim3(CONV_THREADS), 0, stream, m, B, Tn, C,
-                    x, xs, w, bias, cs, ns, slots, silu, y, ys, c_base, late_wait ? 1 : 0);
+                    x, xs, w, bias, cs, ns, slots, silu, y, ys, c_base, late_wait ? 1 : 0,
+                    y_cbase, ends);
 }
 
 template <typename T>
 cudaError_t launch_conv_t(dim3 grid, cudaStream_t stream, const CUtensorMap& m, int B, int Tn,
                           int C, int W, const T* x, long long xs, const T* w, const T* bias,
                           T* cs, int ns, const int32_t* slots, int silu, T* y, long long ys,
-                          int c_base, bool pdl, bool late_wait) {
+                          int c_base, bool pdl, bool late_wait, int y_cbase,
+                          const ConvEnds<T>& ends) {
   switch (W) {
-    case 1: return launch_conv_w<T, 1>(grid, stream, m, B, Tn, C, x, xs, w, bias, cs, ns, slots, silu, y, ys, c_base, pdl, late_wait);
-    case 2: return launch_conv_w<T, 2>(grid, stream, m, B, Tn, C, x, xs, w, bias, cs, ns, slots, silu, y, ys, c_base, pdl, late_wait);
-    case 3: return launch_conv_w<T, 3>(grid, stream, m, B, Tn, C, x, xs, w, bias, cs, ns, slots, silu, y, ys, c_base, pdl, late_wait);
-    default: return launch_conv_w<T, 4>(grid, stream, m, B, Tn, C, x, xs, w, bias, cs, ns, slots, silu, y, ys, c_base, pdl, late_wait);
+    case 1: return launch_conv_w<T, 1>(grid, stream, m, B, Tn, C, x, xs, w, bias, cs, ns, slots, silu, y, ys, c_base, pdl, late_wait, y_cbase, ends);
+    case 2: return launch_conv_w<T, 2>(grid, stream, m, B, Tn, C, x, xs, w, bias, cs, ns, slots, silu, y, ys, c_base, pdl, late_wait, y_cbase, ends);
+    case 3: return launch_conv_w<T, 3>(grid, stream, m, B, Tn, C, x, xs, w, bias, cs, ns, slots, silu, y, ys, c_base, pdl, late_wait, y_cbase, ends);
+    default: return launch_conv_w<T, 4>(grid, stream, m, B, Tn, C, x, xs, w, bias, cs, ns, slots, silu, y, ys, c_base, pdl, late_wait, y_cbase, ends);
   }
 }
 
@@ -241,7 +232,8 @@ cudaError_t gdn_launch_conv(int B, int T, int C, int W, int bf16, const void* x,
                             long long x_tok_stride, const void* w, const void* bias,
                             void* conv_state, int num_slots, const int32_t* slots, int silu,
                             void* y, long long y_tok_stride, cudaStream_t stream, int c_lo,
-                            int c_hi, bool pdl, bool late_wait) {
+                            int c_hi, bool pdl, bool late_wait, const void* halo,
+                            int halo_by_slot, void* tail, int y_cbase) {
   if (B == 0 || T == 0) return cudaSuccess;
   if (W < 1 || W > 4) return cudaErrorInvalidValue;
   const int eb = bf16 ? 2 : 4, cc = TILE_BYTES / eb;
@@ -253,14 +245,16 @@ cudaError_t gdn_launch_conv(int B, int T, int C, int W, int bf16, const void* x,
     return cudaErrorInvalidValue;
   dim3 grid((unsigned)((T + TT - 1) / TT), (unsigned)((c_hi - c_lo + cc - 1) / cc), (unsigned)B);
   if (bf16)
-    return launch_conv_t<__nv_bfloat16>(grid, stream, m, B, T, C, W, (const __nv_bfloat16*)x,
-                                        x_tok_stride, (const __nv_bfloat16*)w,
-                                        (const __nv_bfloat16*)bias, (__nv_bfloat16*)conv_state,
-                                        num_slots, slots, silu, (__nv_bfloat16*)y, y_tok_stride,
-                                        c_lo, pdl, late_wait);
+    return launch_conv_t<__nv_bfloat16>(
+        grid, stream, m, B, T, C, W, (const __nv_bfloat16*)x, x_tok_stride,
+        (const __nv_bfloat16*)w, (const __nv_bfloat16*)bias, (__nv_bfloat16*)conv_state,
+        num_slots, slots, silu, (__nv_bfloat16*)y, y_tok_stride, c_lo, pdl, late_wait, y_cbase,
+        ConvEnds<__nv_bfloat16>{(const __nv_bfloat16*)halo, halo_by_slot,
+                                (__nv_bfloat16*)tail});
   return launch_conv_t<float>(grid, stream, m, B, T, C, W, (const float*)x, x_tok_stride,
                               (const float*)w, (const float*)bias, (float*)conv_state, num_slots,
-                              slots, silu, (float*)y, y_tok_stride, c_lo, pdl, late_wait);
+                              slots, silu, (float*)y, y_tok_stride, c_lo, pdl, late_wait, y_cbase,
+                              ConvEnds<float>{(const float*)halo, halo_by_slot, (float*)tail});
 }
 
 // ======================================================================= packed sequences

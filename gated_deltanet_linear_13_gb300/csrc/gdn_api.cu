@@ -96,15 +96,30 @@ gdn_status check_layer_ptrs(const Checked& c, const gdn_opts* o, const void* q, 
   return GDN_OK;
 }
 
-// Workspace: [post-conv activations, when conv_width > 0][tensor-core prefill tiles, bf16].
-size_t conv_bytes_for(const Checked& c) {
+// The tensor-core prefill with conv width 4 runs the conv of the q and k channels inside its
+// chunk-local kernel (and that of the v channels as its first launch).
+bool conv_fused(const Checked& c, const gdn_opts* o) { return o->in_dtype == GDN_BF16 && c.W == 4; }
+
+size_t round_kb(size_t n) { return (n + 1023) & ~(size_t)1023; }
+// the call's conv tail [B][W-1][C_conv], at offset 0 of a fused call's workspace, where a
+// call that continues this one reads it
+size_t tail_bytes_for(const Checked& c) {
+  return round_kb((size_t)c.B * (size_t)(c.W - 1) * (size_t)c.Cc * c.in_elem);
+}
+
+// Workspace: [conv_width > 0, fused: the conv tail, then the post-conv v channels
+// [B][T][Hv d] | conv_width > 0, not fused: the post-conv activations [B][T][C_conv]]
+// [tensor-core prefill tiles, bf16].
+size_t conv_bytes_for(const Checked& c, const gdn_opts* o) {
   if (c.W == 0) return 0;
-  const size_t n = (size_t)c.B * (size_t)c.T * (size_t)c.Cc * c.in_elem;
-  return (n + 1023) & ~(size_t)1023;
+  if (conv_fused(c, o))
+    return tail_bytes_for(c) +
+           round_kb((size_t)c.B * (size_t)c.T * (size_t)c.Hv * gdn::kHeadDim * c.in_elem);
+  return round_kb((size_t)c.B * (size_t)c.T * (size_t)c.Cc * c.in_elem);
 }
 
 size_t workspace_bytes_for(const Checked& c, const gdn_opts* o) {
-  size_t n = conv_bytes_for(c);
+  size_t n = conv_bytes_for(c, o);
   if (o->in_dtype == GDN_BF16) n += gdn_prefill_tc_scratch_bytes(c.B, c.T, c.Hv);
   return n;
 }
@@ -180,8 +195,8 @@ static gdn_status prefill_impl(const gdn_dims* dims, const gdn_opts* opts, const
                                void* conv_state, const int32_t* state_slots, void* out,
                                int32_t snap_every, float* snap_state, void* snap_conv_state,
                                int32_t num_snap_slots, const int32_t* snap_slots,
-                               const gdn_out_gate* gate, bool gated, void* workspace,
-                               size_t workspace_bytes, void* stream) {
+                               const gdn_out_gate* gate, bool gated, const void* prev_ws,
+                               void* workspace, size_t workspace_bytes, void* stream) {
   Checked c;
   gdn_status st = check_dims(dims, opts, false, &c);
   if (st != GDN_OK) return st;
@@ -210,11 +225,31 @@ static gdn_status prefill_impl(const gdn_dims* dims, const gdn_opts* opts, const
   const size_t need = workspace_bytes_for(c, opts);
   if (need > 0 && (!workspace || workspace_bytes < need || !aligned16(workspace)))
     return GDN_ERR_WORKSPACE;
+  const bool fuse = conv_fused(c, opts);
+  if (fuse && (!aligned16(conv_weight) || (conv_bias && !aligned16(conv_bias))))
+    return GDN_ERR_INVALID_ARGUMENT;
+  // a continuing call (the tensor-core path with the conv fused, or without a conv): the
+  // previous call's workspace must not overlap this one's
+  const bool chain = prev_ws && L.in_bf16 && (fuse || c.W == 0);
+  if (chain) {
+    const char* pw = static_cast<const char*>(prev_ws);
+    const char* w0 = static_cast<const char*>(workspace);
+    const size_t prev_bytes = fuse ? tail_bytes_for(c) : 1;
+    if (!aligned16(prev_ws) || !(pw + prev_bytes <= w0 || pw >= w0 + need))
+      return GDN_ERR_INVALID_ARGUMENT;
+  }
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  const size_t conv_bytes = conv_bytes_for(c);
+  const size_t conv_bytes = conv_bytes_for(c, opts);
   L.scratch = need > conv_bytes ? static_cast<char*>(workspace) + conv_bytes : nullptr;
   L.scratch_bytes = need - conv_bytes;
-  if (c.W > 0) {
+  L.chained = chain;
+  if (fuse) {
+    L.fuse = 1;
+    L.tail = workspace;
+    L.prev_tail = chain ? prev_ws : nullptr;
+    L.v = static_cast<char*>(workspace) + tail_bytes_for(c);
+    L.v_tok_stride = (long long)c.Hv * gdn::kHeadDim;
+  } else if (c.W > 0) {
     // conv (+SiLU) into the workspace, conv state updated in place.  The tensor-core prefill
     // needs only the q / k channels before its chunk-local kernel: the value channels are
     // convolved by a second launch that runs beside that kernel (see vconv_pending).
@@ -257,7 +292,7 @@ gdn_status gdn_chunk_prefill(const gdn_dims* dims, const gdn_opts* opts, const v
                              size_t workspace_bytes, void* stream) {
   return prefill_impl(dims, opts, q, k, v, a, b, A_log, dt_bias, conv_weight, conv_bias, state,
                       conv_state, state_slots, out, 0, nullptr, nullptr, 0, nullptr, nullptr,
-                      false, workspace, workspace_bytes, stream);
+                      false, nullptr, workspace, workspace_bytes, stream);
 }
 
 gdn_status gdn_chunk_prefill_gated(const gdn_dims* dims, const gdn_opts* opts, const void* q,
@@ -269,7 +304,22 @@ gdn_status gdn_chunk_prefill_gated(const gdn_dims* dims, const gdn_opts* opts, c
                                    size_t workspace_bytes, void* stream) {
   return prefill_impl(dims, opts, q, k, v, a, b, A_log, dt_bias, conv_weight, conv_bias, state,
                       conv_state, state_slots, out, 0, nullptr, nullptr, 0, nullptr, gate, true,
-                      workspace, workspace_bytes, stream);
+                      nullptr, workspace, workspace_bytes, stream);
+}
+
+gdn_status gdn_chunk_prefill_ex(const gdn_dims* dims, const gdn_opts* opts, const void* q,
+                                const void* k, const void* v, const void* a, const void* b,
+                                const float* A_log, const float* dt_bias,
+                                const void* conv_weight, const void* conv_bias, float* state,
+                                void* conv_state, const int32_t* state_slots, void* out,
+                                const gdn_prefill_ext* ext, void* workspace,
+                                size_t workspace_bytes, void* stream) {
+  static const gdn_prefill_ext none = {};
+  const gdn_prefill_ext& e = ext ? *ext : none;
+  return prefill_impl(dims, opts, q, k, v, a, b, A_log, dt_bias, conv_weight, conv_bias, state,
+                      conv_state, state_slots, out, e.snap_every, e.snap_state,
+                      e.snap_conv_state, e.num_snap_slots, e.snap_slots, e.gate, false,
+                      e.prev_workspace, workspace, workspace_bytes, stream);
 }
 
 gdn_status gdn_chunk_prefill_snapshots(const gdn_dims* dims, const gdn_opts* opts, const void* q,
@@ -285,8 +335,8 @@ gdn_status gdn_chunk_prefill_snapshots(const gdn_dims* dims, const gdn_opts* opt
   if (snap_every <= 0) return GDN_ERR_INVALID_ARGUMENT;
   return prefill_impl(dims, opts, q, k, v, a, b, A_log, dt_bias, conv_weight, conv_bias, state,
                       conv_state, state_slots, out, snap_every, snap_state, snap_conv_state,
-                      num_snap_slots, snap_slots, nullptr, false, workspace, workspace_bytes,
-                      stream);
+                      num_snap_slots, snap_slots, nullptr, false, nullptr, workspace,
+                      workspace_bytes, stream);
 }
 
 size_t gdn_prefill_varlen_workspace_size(const gdn_dims* dims, const gdn_opts* opts) {

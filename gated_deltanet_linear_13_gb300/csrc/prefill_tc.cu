@@ -46,6 +46,7 @@
 // GDN_ERR_DEVICE_TIMEOUT, waits (bounded) for its own copies and MMAs, frees TMEM and
 // returns.
 #include "common.cuh"
+#include "conv_math.cuh"
 #include "sm100_ptx.cuh"
 
 using namespace gdn;
@@ -119,10 +120,28 @@ struct TcParams {
   const int32_t* ccs;
   const int4* ctab;
   void* out;              // for the ragged last chunk of a packed sequence (plain stores)
-  // slices after the first of a call: the local kernel waits for the kernel before it (the
-  // previous slice's chain) only at the end of its last block; every slice but the last: the
-  // chain lets the next slice's local kernel start as soon as its own grid wait has returned
+  // slices after the first of a call (and the first slice of a call that continues the one
+  // before it): the local kernel waits for the kernel before it (the previous chain) only at
+  // the end of its last block; the chain lets the kernel after it (the next slice's or call's
+  // local kernel) start as soon as its own grid wait has returned
   int late_wait, early_trigger;
+  // a late-waiting local kernel that releases its chain at its start (the first slice of an
+  // ordinary call with the conv fused)
+  int trigger_first;
+  // the conv of the q and k channels fused into the local kernel (tm_q and tm_k then map the
+  // pre-conv input x, [B][T][Cc]): the unit convolves its key head's q and k channels
+  // (positions before the call's first token from `halo`: the conv state rows of slot
+  // slots[b] when halo_by_slot, else rows [b][W-1][Cc] of the previous call's conv tail); the
+  // units of the call's last chunk leave the q / k part of the call's conv tail in `tail`
+  // [B][W-1][Cc] (the conv kernel before them leaves the v part); the last slice's chain
+  // copies the tail into conv_state (cs_out, null before the last slice)
+  int fuse, Cc, silu, halo_by_slot;
+  const __nv_bfloat16* x;
+  const __nv_bfloat16* cw;
+  const __nv_bfloat16* cb;
+  const __nv_bfloat16* halo;
+  __nv_bfloat16* tail;
+  __nv_bfloat16* cs_out;
 };
 
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
@@ -369,6 +388,124 @@ constexpr uint32_t L_MISC = L_SOLVE + 2 * SOLVE_MAT;   // factors, solve scratch
 constexpr uint32_t L_SMEM = L_MISC + 6 * KB + KB;
 constexpr uint32_t L_TMEM = 128;        // G (128 columns); later W^T in its first 64
 
+// ======================================================================= fused conv
+// The causal depthwise conv of width 4 (model card, "How It Works": the short conv in front of
+// the recurrence) of the unit's q and k channels, computed inside the chunk-local unit in
+// place on its K and Q tiles, which arrive by TMA as the pre-conv input x in the layout the
+// MMAs read.  Thread lt owns one channel pair of one 64-channel tile block and 32 tokens, and
+// slides up its column from the last token, so that each input is read before its row is
+// overwritten; the three inputs below its first token are read before any thread writes (the
+// rows of the thread below it, or, for the chunk's first rows, the tokens before the chunk:
+// x, or at the call's start the halo rows).  The per-token arithmetic is the conv kernels'
+// (conv_token), so the results are the same bits.  (The v channels are convolved by the conv
+// kernel launched before the chunk-local kernel.)
+constexpr int FC_W = 4, FC_H = FC_W - 1;
+
+__device__ __forceinline__ float2 bf2_to_f2(uint32_t u) {
+  return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u));
+}
+__device__ __forceinline__ uint32_t lds32(uint32_t addr) {
+  uint32_t v;
+  asm volatile("ld.shared.b32 %0, [%1];\n" : "=r"(v) : "r"(addr));
+  return v;
+}
+__device__ __forceinline__ void sts32(uint32_t addr, uint32_t v) {
+  asm volatile("st.shared.b32 [%0], %1;\n" ::"r"(addr), "r"(v) : "memory");
+}
+
+// The pre-conv input pair at x channel ch of token t of the call (t >= -3; t < 0: halo row
+// t + 3 -- the conv state rows of slot `slot`, or the previous call's conv tail of sequence b).
+__device__ __forceinline__ uint32_t input_pair(const TcParams& p, int slot, int b, int t, int ch) {
+  if (t < 0) {
+    const size_t row = (size_t)(p.halo_by_slot ? slot : b) * FC_H + (t + FC_H);
+    return __ldcg(reinterpret_cast<const unsigned int*>(p.halo + row * p.Cc + ch));
+  }
+  return __ldg(reinterpret_cast<const unsigned int*>(p.x + ((size_t)b * p.T + t) * p.Cc + ch));
+}
+
+// One thread's share of the fused conv (see above).  Its first part (taps, biases and the three
+// inputs below its rows) must complete in every thread before any thread runs its second part.
+struct FusedConvQK {
+  uint32_t tile, cofs;
+  int q, th;
+  float w[FC_W][2], bias[2];
+  uint32_t below[FC_H];
+
+  __device__ __forceinline__ uint32_t addr(int r) const {
+    return tile + (uint32_t)r * 128u + ((uint32_t)(((q >> 2) ^ (r & 7)) << 4)) + cofs;
+  }
+
+  __device__ __forceinline__ void prepare(const TcParams& p, uint32_t sb, int lt, int kh, int b,
+                                          int slot, int tok0) {
+    const int pp = lt & 127, blk = pp >> 5, kb = blk & 1, isk = blk >> 1;
+    q = pp & 31;
+    th = lt >> 7;
+    const int ch = (isk ? p.Hk * D : 0) + kh * D + 64 * kb + 2 * q;
+    tile = sb + L_KQ + kb * 16 * KB + (isk ? 0u : 8 * KB);
+    cofs = (uint32_t)((q & 3) * 4);
+    // taps: conv_weight rows ch, ch + 1 (4 bf16 each); biases ch, ch + 1
+    const uint4 wv = __ldg(reinterpret_cast<const uint4*>(p.cw + (size_t)ch * FC_W));
+    const float2 a01 = bf2_to_f2(wv.x), a23 = bf2_to_f2(wv.y);
+    const float2 b01 = bf2_to_f2(wv.z), b23 = bf2_to_f2(wv.w);
+    w[0][0] = a01.x; w[1][0] = a01.y; w[2][0] = a23.x; w[3][0] = a23.y;
+    w[0][1] = b01.x; w[1][1] = b01.y; w[2][1] = b23.x; w[3][1] = b23.y;
+    const float2 bb = p.cb ? bf2_to_f2(__ldg(reinterpret_cast<const unsigned int*>(p.cb + ch)))
+                           : make_float2(0.f, 0.f);
+    bias[0] = bb.x;
+    bias[1] = bb.y;
+#pragma unroll
+    for (int j = 0; j < FC_H; ++j) {
+      const int r = 32 * th - FC_H + j;
+      below[j] = th ? lds32(addr(r)) : input_pair(p, slot, b, tok0 + r, ch);
+    }
+  }
+
+  // rows 32 th + 31 .. 32 th, bottom up; rows at or past ntok are zero
+  __device__ __forceinline__ void run(int ntok, int silu) {
+    const int r0 = 32 * th;
+    uint32_t win[FC_W];
+#pragma unroll
+    for (int j = 0; j < FC_W; ++j) win[j] = lds32(addr(r0 + 31 - FC_H + j));
+#pragma unroll
+    for (int t = 31; t >= 0; --t) {
+      const int r = r0 + t;
+      float x2[FC_W][2], y2[2];
+#pragma unroll
+      for (int j = 0; j < FC_W; ++j) {
+        const float2 f = bf2_to_f2(win[j]);
+        x2[j][0] = f.x;
+        x2[j][1] = f.y;
+      }
+      conv_token<FC_W, 2>(w, bias, x2, silu, y2);
+      sts32(addr(r), r < ntok ? pack_bf16(y2[0], y2[1]) : 0u);
+      if (t > 0) {
+#pragma unroll
+        for (int j = FC_W - 1; j > 0; --j) win[j] = win[j - 1];
+        win[0] = t >= FC_W ? lds32(addr(r0 + t - FC_W)) : below[(t >= 1 && t <= FC_H) ? t - 1 : 0];
+      }
+    }
+  }
+};
+
+// The call's conv tail of the q and k channels of key head kh (its last 3 inputs, from x or,
+// for a call of fewer than 3 tokens, partly from the halo) -> tail rows [b][0..2].  Threads
+// 0..95, one 16-byte word each.
+__device__ __forceinline__ void fused_conv_tail_qk(const TcParams& p, int tid, int kh, int b,
+                                                   int slot) {
+  if (tid >= 96) return;
+  const int j = tid >> 5, cc = tid & 31;
+  const int ch = ((cc >> 4) ? p.Hk * D : 0) + kh * D + 8 * (cc & 15);
+  const int t = p.T - FC_H + j;
+  uint4 v;
+  if (t < 0) {
+    const size_t row = (size_t)(p.halo_by_slot ? slot : b) * FC_H + (t + FC_H);
+    v = __ldcg(reinterpret_cast<const uint4*>(p.halo + row * p.Cc + ch));
+  } else {
+    v = __ldg(reinterpret_cast<const uint4*>(p.x + ((size_t)b * p.T + t) * p.Cc + ch));
+  }
+  *reinterpret_cast<uint4*>(p.tail + ((size_t)b * FC_H + j) * p.Cc + ch) = v;
+}
+
 // A group's resources: its 1024-byte aligned L_SMEM bytes (barriers and flags inside them),
 // its 128 TMEM columns, its named barrier, and the parities of its two mbarriers.
 struct LocalGroup {
@@ -434,6 +571,7 @@ __device__ __forceinline__ bool local_unit(LocalGroup& g, const CUtensorMap* tm_
   const int kh = h / (p.Hv / p.Hk);
   const size_t u = ((size_t)b * p.Hv + h) * p.ns + jc;
   uint8_t* unit = p.units + u * UNIT_BYTES;
+  const int slot = p.slots ? p.slots[b] : b;
 
   float* gl2 = reinterpret_cast<float*>(sm + L_MISC);   // G_r * log2(e)
   float* beta = gl2 + 64;
@@ -485,13 +623,20 @@ __device__ __forceinline__ bool local_unit(LocalGroup& g, const CUtensorMap* tm_
     pdl_trigger();
   }
   if (tid == 0) {
+    // the K and Q tiles (with the conv fused: the pre-conv q and k channels of x, which the
+    // conv below then replaces in place)
+    const int k0 = p.fuse ? p.Hk * D : 0;
     mbar_arrive_expect_tx(bar_in, 32 * KB);
 #pragma unroll
     for (int kb = 0; kb < 2; ++kb) {
-      tma_load_3d(sb + L_KQ + kb * 16 * KB, tm_k, kh * D + 64 * kb, tok0, b, bar_in);
+      tma_load_3d(sb + L_KQ + kb * 16 * KB, tm_k, k0 + kh * D + 64 * kb, tok0, b, bar_in);
       tma_load_3d(sb + L_KQ + kb * 16 * KB + 8 * KB, tm_q, kh * D + 64 * kb, tok0, b, bar_in);
     }
   }
+  // the call's last chunk: the conv tail of the q / k channels (the first value head of a key
+  // head writes it)
+  if (p.fuse && p.tail && tok0 + C >= p.T && h % (p.Hv / p.Hk) == 0)
+    fused_conv_tail_qk(p, tid, kh, b, slot);
   tc_fence_before();
   g.sync();
   tc_fence_after();
@@ -511,6 +656,14 @@ __device__ __forceinline__ bool local_unit(LocalGroup& g, const CUtensorMap* tm_
     g.in_phase ^= 1;
     g.sync();
     if (*sAbort) break;
+    if (p.fuse) {
+      FusedConvQK fc;
+      fc.prepare(p, sb, tid, kh, b, slot, tok0);
+      g.sync();
+      fc.run(ntok, p.silu);
+      fence_proxy_async_smem();        // (the tensor cores read the K and Q tiles next)
+      g.sync();
+    }
     // ---- MMA 1: G = [K; Q] [K; Q]^T  (M = N = 128: k_0..k_63, q_0..q_63; K = 128).  Its
     //      k.k and q.k blocks feed A and P, its diagonal gives the squared row norms.
     if (warp == 0 && elect_one()) {
@@ -705,6 +858,7 @@ __global__ void __launch_bounds__(LGT, 3)
   // every other block finish and free its SM for the blocks behind it
   const bool wait_late = p.late_wait && jc == (int)gridDim.x - 1 &&
                          h == (int)gridDim.y - 1 && b == (int)gridDim.z - 1;
+  if (p.trigger_first) pdl_trigger();
   int tok0, ntok, seq;
   if (!local_unit_tokens(p, jc, b, tok0, ntok, seq)) {
     if (wait_late) pdl_wait();
@@ -1207,6 +1361,26 @@ __global__ void __launch_bounds__(CH_THREADS, 1)
       z_chunk = nl;
     };
     if (p.gate && ns > 0) load_z(0);
+    // the last slice of a call whose conv ran in the local kernels: the call's conv tail (left
+    // by them, complete since the grid wait) into the conv state -- this CTA's v channels and,
+    // for the first value head of a key head, that key head's q and k channels
+    if (p.cs_out) {
+      const int kh = h / (p.Hv / p.Hk);
+      for (int k = tid - CH_STORE * 32; k < 48 + 96; k += 128) {
+        int j, ch;
+        if (k < 48) {
+          j = k >> 4;
+          ch = 2 * p.Hk * D + h * D + 8 * (k & 15);
+        } else {
+          if (h % (p.Hv / p.Hk) != 0) break;
+          const int cc = (k - 48) & 31;
+          j = (k - 48) >> 5;
+          ch = ((cc >> 4) ? p.Hk * D : 0) + kh * D + 8 * (cc & 15);
+        }
+        *reinterpret_cast<uint4*>(p.cs_out + ((size_t)slot * FC_H + j) * p.Cc + ch) =
+            __ldcg(reinterpret_cast<const uint4*>(p.tail + ((size_t)b * FC_H + j) * p.Cc + ch));
+      }
+    }
     bool ok = true;
     for (int nl = 0; nl < ns; ++nl) {
       if (!__all_sync(0xffffffffu, mbar_wait_or_abort((nl & 1) ? bar_o1 : bar_o0,
@@ -1363,13 +1537,21 @@ cudaError_t launch_tc_t(const GdnLayerArgs& L, cudaStream_t stream) {
   const int out_rows = (int)((L.gate ? 2 : 4) * KB / (32 * sizeof(Tout)));
   // a packed batch has all its tokens on one axis: batch extent 1 in the tensor maps
   const int MB = L.cu ? 1 : L.B;
+  // the q / k conv fused into the local kernel: the K and Q maps are one map over the pre-conv
+  // input x (the k channels at offset Hk d), the V map one over the conv kernel's output
+  const bool fuse = L.fuse != 0;
+  const bool maps_in =
+      (fuse ? gdn_make_map(&mq, L.x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, L.C_conv, L.T, MB,
+                           L.C_conv, 64, 64, true)
+            : (gdn_make_map(&mq, L.q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, L.Hk * D, L.T, MB,
+                            L.q_tok_stride, 64, 64, true) &&
+               gdn_make_map(&mk, L.k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, L.Hk * D, L.T, MB,
+                            L.k_tok_stride, 64, 64, true))) &&
+      gdn_make_map(&mv, L.v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, L.Hv * D, L.T, MB,
+                   L.v_tok_stride, 64, 64, true);
+  if (fuse) mk = mq;
   const bool ok =
-      gdn_make_map(&mq, L.q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, L.Hk * D, L.T, MB, L.q_tok_stride,
-               64, 64, true) &&
-      gdn_make_map(&mk, L.k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, L.Hk * D, L.T, MB, L.k_tok_stride,
-               64, 64, true) &&
-      gdn_make_map(&mv, L.v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, L.Hv * D, L.T, MB, L.v_tok_stride,
-               64, 64, true) &&
+      maps_in &&
       gdn_make_map(&mo, L.out,
                sizeof(Tout) == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
                (int)sizeof(Tout), L.Hv * D, L.T, MB, (long long)L.Hv * D, 32, out_rows, false) &&
@@ -1405,6 +1587,8 @@ cudaError_t launch_tc_t(const GdnLayerArgs& L, cudaStream_t stream) {
   const size_t units = (size_t)ns_max * MB * L.Hv;
   if (!L.scratch || L.scratch_bytes < gdn_prefill_tc_scratch_bytes(MB, nch * C, L.Hv))
     return cudaErrorInvalidValue;
+  if (fuse && (!L.tail || (L.chained && !L.prev_tail) || (!L.chained && !L.conv_state)))
+    return cudaErrorInvalidValue;
   const int nslices = (nch + ns_max - 1) / ns_max;
   const size_t half_bytes = scratch_half_bytes(units);
   TcParams p;
@@ -1422,6 +1606,31 @@ cudaError_t launch_tc_t(const GdnLayerArgs& L, cudaStream_t stream) {
   p.ccs = L.ccs;
   p.ctab = static_cast<const int4*>(L.ctab);
   p.out = L.out;
+  p.fuse = fuse;
+  p.Cc = L.C_conv;
+  p.silu = L.silu;
+  p.x = static_cast<const __nv_bfloat16*>(L.x);
+  p.cw = static_cast<const __nv_bfloat16*>(L.conv_w);
+  p.cb = static_cast<const __nv_bfloat16*>(L.conv_b);
+  p.halo_by_slot = !L.chained;
+  p.halo = static_cast<const __nv_bfloat16*>(L.chained ? L.prev_tail : L.conv_state);
+  p.tail = static_cast<__nv_bfloat16*>(L.tail);
+  // a call that continues the one before it on the stream: its first local kernel starts
+  // beside that call's last chain (which released it right after its own grid wait), reads
+  // only this call's inputs and the previous conv tail before its grid wait, and waits for
+  // that chain at its end like a later slice's local kernel
+  const bool chained = L.chained != 0 && (fuse || L.W == 0);
+  if (fuse) {
+    // the v channels' conv first: it reads only this call's input and the halo, writes V (into
+    // the workspace) and the v part of the conv tail, and lets the local kernel start at once;
+    // its last block waits for the kernel before it, so that the call's kernels complete in
+    // stream order behind it
+    e = gdn_launch_conv(L.B, L.T, L.C_conv, L.W, 1, L.x, L.C_conv, L.conv_w, L.conv_b,
+                        L.conv_state, L.num_slots, L.slots, L.silu, const_cast<void*>(L.v),
+                        (long long)L.Hv * D, stream, 2 * L.Hk * D, -1, chained, true, p.halo,
+                        p.halo_by_slot, L.tail, 2 * L.Hk * D);
+    if (e != cudaSuccess) return e;
+  }
   for (int si = 0; si < nslices; ++si) {
     const int n0 = si * ns_max;
     p.n0 = n0;
@@ -1430,12 +1639,20 @@ cudaError_t launch_tc_t(const GdnLayerArgs& L, cudaStream_t stream) {
     p.units = static_cast<uint8_t*>(L.scratch) +
               (nslices > 1 ? (size_t)(si & 1) * half_bytes : 0);
     p.egc = reinterpret_cast<float*>(p.units + units * UNIT_BYTES);
-    p.late_wait = si > 0;
-    p.early_trigger = si + 1 < nslices;
+    // (with the conv fused, every local kernel runs behind a kernel it does not depend on --
+    // the v conv or the previous chain -- and waits for it at its end only; the first one of
+    // an ordinary call releases its chain at once, whose set-up then reads the state early:
+    // everything before this call had completed when the v conv started)
+    p.late_wait = si > 0 || chained || fuse;
+    p.trigger_first = fuse && si == 0 && !chained;
+    // (every chain releases the kernel after it early: the next slice's local kernel, or the
+    // next call's first kernel, each of which waits for the chain before reading what it wrote)
+    p.early_trigger = 1;
+    p.cs_out = (fuse && si + 1 == nslices) ? static_cast<__nv_bfloat16*>(L.conv_state) : nullptr;
     // (the first slice's local kernel reads the caller's gate inputs, and a packed batch's
     // chunk table, before its grid wait: it may start early only behind this call's own conv
-    // kernels, which began after everything earlier had completed)
-    e = launch_pdl(n0 > 0 || L.W > 0, gdn_chunk_local_kernel<__nv_bfloat16>,
+    // kernels, which began after everything earlier had completed, or as a continuing call)
+    e = launch_pdl(n0 > 0 || chained || L.W > 0, gdn_chunk_local_kernel<__nv_bfloat16>,
                    dim3((unsigned)p.ns, (unsigned)L.Hv, (unsigned)MB), dim3(LGT), L_SMEM, stream,
                    mq, mk, p);
     if (e != cudaSuccess) return e;

@@ -92,12 +92,14 @@ typedef struct {
  */
 
 /*
- * Bytes of device workspace gdn_chunk_prefill needs for these dims/opts (0 when none): the
- * post-conv activations when conv_width > 0, plus, for bf16 inputs, the per-chunk operand
- * tiles the tensor-core prefill passes from its chunk-local kernel to its state-chain kernel
- * (80 KB per chunk and value head for a slice of at most ~96 MB; twice that when the call
- * spans several slices, so that one slice's tiles are written while the previous slice's are
- * read).  Returns 0 for invalid dims.
+ * Bytes of device workspace gdn_chunk_prefill needs for these dims/opts (0 when none): for
+ * bf16 inputs with conv_width 4, the call's conv tail (its last W-1 pre-conv inputs,
+ * [B][W-1][C_conv], at offset 0), else the post-conv activations when conv_width > 0; plus,
+ * for bf16 inputs, the per-chunk operand tiles the tensor-core prefill passes from its
+ * chunk-local kernel to its state-chain kernel (80 KB per chunk and value head, 96 KB when
+ * the conv runs in the chunk-local kernel, for a slice of at most ~96 MB; twice that when the
+ * call spans several slices, so that one slice's tiles are written while the previous
+ * slice's are read).  Returns 0 for invalid dims.
  */
 size_t gdn_prefill_workspace_size(const gdn_dims* dims, const gdn_opts* opts);
 
@@ -117,8 +119,10 @@ size_t gdn_prefill_workspace_size(const gdn_dims* dims, const gdn_opts* opts);
  *                gates_precomputed.
  *   A_log        [Hv] fp32 (ignored when gates_precomputed).
  *   dt_bias      [Hv] fp32 or NULL (= 0).
- *   conv_weight  [C_conv, W] in in_dtype (required when conv_width > 0, else ignored).
- *   conv_bias    [C_conv] in in_dtype or NULL (= 0).
+ *   conv_weight  [C_conv, W] in in_dtype (required when conv_width > 0, else ignored);
+ *                16-byte aligned when in_dtype is bf16 and W = 4 (the conv then runs inside
+ *                the chunk-local kernel, 16 bytes of taps at a time), else 4-byte aligned.
+ *   conv_bias    [C_conv] in in_dtype or NULL (= 0); aligned as conv_weight.
  *   state        [num_slots, Hv, d, d] fp32, S[v][k]; read and written in place.
  *   conv_state   [num_slots, W-1, C_conv] in in_dtype: the last W-1 pre-conv inputs, oldest
  *                first; read and written in place (ignored when conv_width == 0).
@@ -225,6 +229,51 @@ gdn_status gdn_decode_step_gated(const gdn_dims* dims, const gdn_opts* opts, con
                                  const void* conv_weight, const void* conv_bias, float* state,
                                  void* conv_state, const int32_t* state_slots, void* out,
                                  const gdn_out_gate* gate, void* stream);
+
+/*
+ * gdn_chunk_prefill_ex -- gdn_chunk_prefill with any of its optional parts, and the one call
+ * form that can continue the previous call.  `ext` NULL (or zero-initialised) is the plain
+ * call; each field adds one part:
+ *   gate            non-NULL: the gated output norm, as gdn_chunk_prefill_gated.
+ *   snap_every ...  snap_every > 0: in-call snapshots, as gdn_chunk_prefill_snapshots (same
+ *                   fields, same errors); 0: none.
+ *   prev_workspace  non-NULL: this call continues the sequences of the previous prefill call
+ *                   enqueued on the same stream -- the next bucket of a long context prefilled
+ *                   in fixed-size calls (the chunked form carries the state across calls
+ *                   exactly; PR #164 "Fused DeltaNet Direct-Solve Follow-Up").  It is the
+ *                   workspace that call used, whose first (W-1) * C_conv * B elements hold that
+ *                   call's last W-1 pre-conv inputs per sequence (every call of the tensor-core
+ *                   path with conv_width 4 leaves them there): the inputs before this call's
+ *                   first token, read instead of conv_state.  16-byte aligned and not
+ *                   overlapping `workspace` (else GDN_ERR_INVALID_ARGUMENT): alternate two
+ *                   workspaces.  This call's first kernels may then start while the previous
+ *                   call's state chain is still running (until it has finished they read only
+ *                   this call's inputs and that conv tail); the results are those of the plain
+ *                   call.  The caller guarantees that the previous call was a prefill of the
+ *                   same sequences (same dims, state, conv_state and state_slots), that nothing
+ *                   but gdn_state_checkpoint saves was enqueued on `stream` after it, and that
+ *                   it wrote no input of this call.  The overlap applies to the tensor-core
+ *                   path (in_dtype bf16) with conv_width 4 or 0; other calls ignore
+ *                   prev_workspace and run as ordinary calls.
+ * Errors: those of gdn_chunk_prefill and of the parts used.
+ */
+typedef struct {
+  const gdn_out_gate* gate;
+  int32_t snap_every;
+  float* snap_state;
+  void* snap_conv_state;
+  int32_t num_snap_slots;
+  const int32_t* snap_slots;
+  const void* prev_workspace;
+} gdn_prefill_ext;
+
+gdn_status gdn_chunk_prefill_ex(const gdn_dims* dims, const gdn_opts* opts, const void* q,
+                                const void* k, const void* v, const void* a, const void* b,
+                                const float* A_log, const float* dt_bias,
+                                const void* conv_weight, const void* conv_bias, float* state,
+                                void* conv_state, const int32_t* state_slots, void* out,
+                                const gdn_prefill_ext* ext, void* workspace,
+                                size_t workspace_bytes, void* stream);
 
 /*
  * gdn_chunk_prefill_varlen -- gdn_chunk_prefill for a packed variable-length batch: N

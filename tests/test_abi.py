@@ -111,6 +111,39 @@ def test_gated_entries_reject_bad_gate(L):
     assert L.gdn_chunk_prefill_gated(*bad_dims, ctypes.byref(g), None, 0, None) == 2
 
 
+def test_prefill_ex_rejects_bad_arguments(L):
+    """gdn_chunk_prefill_ex: NULL ext is the plain call; each part is checked as in its own
+    entry point; a continued call's previous workspace must be aligned and must not overlap
+    this call's; with conv width 4 (bf16) the conv taps and biases must be 16-byte aligned."""
+    dc = _dims(conv_width=4)
+    o = _opts()
+    need = L.gdn_prefill_workspace_size(ctypes.byref(dc), ctypes.byref(o))
+    ws = 0x100000
+
+    def call(ext, conv_w=A, ws_=ws, d=dc):
+        return L.gdn_chunk_prefill_ex(ctypes.byref(d), ctypes.byref(o), A, None, None, A, A, A,
+                                      None, conv_w, None, A, A, None, A,
+                                      None if ext is None else ctypes.byref(ext), ws_, need, None)
+
+    ext = gdn.GdnPrefillExt()
+    ext.prev_workspace = ws + 64                      # inside this call's workspace
+    assert call(ext) == 1
+    ext.prev_workspace = ws - 16                      # its conv tail runs into this workspace
+    assert call(ext) == 1
+    ext.prev_workspace = ws + need + 8                # misaligned
+    assert call(ext) == 1
+    assert call(None, conv_w=A + 4) == 1              # taps not 16-byte aligned (fused conv)
+    bad = gdn.GdnPrefillExt()
+    bad.snap_every = 100                              # not a whole number of chunks
+    assert call(bad) == 1
+    g = gdn.GdnOutGate(A + 4, A, 1e-6)                # misaligned gate
+    bg = gdn.GdnPrefillExt()
+    bg.gate = ctypes.cast(ctypes.pointer(g), ctypes.c_void_p)
+    assert call(bg) == 1
+    assert call(None, d=_dims(conv_width=4, head_dim=64)) == 2
+    assert call(None, d=_dims(batch=0, conv_width=4)) == 0
+
+
 def test_decode_multi_rejects_bad_arguments(L):
     def call(d, snap_state=None, snap_conv=None, nb=0, snap_slots=None):
         return L.gdn_decode_multi(ctypes.byref(d), ctypes.byref(_opts()), A, A, A, A, A, A, None,
@@ -196,12 +229,34 @@ def test_prefill_workspace_two_halves_past_one_slice(L):
     assert L.gdn_prefill_workspace_size(ctypes.byref(long_), ctypes.byref(o)) == 2 * half
 
 
+def test_prefill_workspace_fused_conv(L):
+    """With conv width 4 (bf16) the chunk-local kernel convolves the q and k channels itself:
+    the workspace holds the call's conv tail [B][3][C_conv] (bf16, 1 KiB rounded) at offset 0,
+    then the post-conv v channels [B][T][Hv d], then the tiles (25 chunks per slice at 48
+    value heads, as without the conv)."""
+    o = _opts()
+    cc = (2 * 16 + 48) * 128
+    tail = ((3 * cc * 2 + 1023) // 1024) * 1024
+    half = 25 * 48 * 80 * 1024 + ((25 * 48 * 4 + 255) // 256) * 256
+    for T, halves in ((25 * 64, 1), (26 * 64, 2), (2048 * 64, 2)):
+        d = _dims(seqlen=T, num_k_heads=16, num_v_heads=48, conv_width=4)
+        v = ((T * 48 * 128 * 2 + 1023) // 1024) * 1024
+        assert L.gdn_prefill_workspace_size(ctypes.byref(d), ctypes.byref(o)) == (
+            tail + v + halves * half), T
+
+
 def test_prefill_workspace_checked(L):
     dc, o = _dims(conv_width=4), _opts()
     need = L.gdn_prefill_workspace_size(ctypes.byref(dc), ctypes.byref(o))
-    # bf16: one chunk x 16 value heads of 80 KB tiles + their e^{G_C} (256-byte rounded)
+    # bf16, conv width 4: the conv tail (3 rows of the 6144 channels) + the post-conv v
+    # channels (16 tokens x 16 heads x 128) + one chunk x 16 value heads of 80 KB tiles + their
+    # e^{G_C} (256-byte rounded)
+    assert need == 3 * (2 * 16 + 16) * 128 * 2 + 16 * 16 * 128 * 2 + 1 * 16 * 80 * 1024 + 256
+    # bf16, another conv width: the post-conv activations + 80 KB tiles
     tiles = 1 * 16 * 80 * 1024 + 256
-    assert need == 1 * 16 * (2 * 16 + 16) * 128 * 2 + tiles
+    d2 = _dims(conv_width=2)
+    assert (L.gdn_prefill_workspace_size(ctypes.byref(d2), ctypes.byref(o)) ==
+            1 * 16 * (2 * 16 + 16) * 128 * 2 + tiles)
     assert L.gdn_prefill_workspace_size(ctypes.byref(_dims()), ctypes.byref(o)) == tiles
     # the all-fp32 path needs only the conv activations
     of = _opts(in_dtype=gdn.GDN_F32, out_dtype=gdn.GDN_F32)
