@@ -143,6 +143,8 @@ struct GdnLayerArgs {
   int snap_every, n_snap, num_snap_slots;
   float* snap_state;
   const int32_t* snap_slots;
+  void* snap_conv_state;      // the conv-state bank (the tensor-core prefill with conv width 4
+                              // writes it from its chains; other paths launch a copy kernel)
   // gated RMS norm of the output (gate != 0): out = w * o / sqrt(mean(o^2) + eps) * silu(z)
   int gate;
   const void* gate_z;         // [B, T, Hv, d] in the input type

@@ -221,6 +221,7 @@ static gdn_status prefill_impl(const gdn_dims* dims, const gdn_opts* opts, const
     L.num_snap_slots = num_snap_slots;
     L.snap_state = snap_state;
     L.snap_slots = snap_slots;
+    L.snap_conv_state = snap_conv_state;
   }
   const size_t need = workspace_bytes_for(c, opts);
   if (need > 0 && (!workspace || workspace_bytes < need || !aligned16(workspace)))
@@ -274,8 +275,9 @@ static gdn_status prefill_impl(const gdn_dims* dims, const gdn_opts* opts, const
                                   c.num_slots, s);
     if (e != cudaSuccess) return GDN_ERR_CUDA;
   }
-  if (n_snap > 0 && c.W > 1) {
-    // the conv state at each boundary: W-1 rows of the call's pre-conv input
+  if (n_snap > 0 && c.W > 1 && !L.fuse) {
+    // the conv state at each boundary: W-1 rows of the call's pre-conv input (with the conv
+    // fused, the state-chain kernels copy them)
     e = gdn_launch_conv_snapshots(c.B, c.T, c.Cc * c.in_elem, (long long)c.Cc * c.in_elem,
                                   c.W - 1, q, snap_every, n_snap, snap_conv_state,
                                   num_snap_slots, snap_slots, state_slots, s);

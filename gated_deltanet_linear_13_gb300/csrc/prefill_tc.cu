@@ -126,8 +126,9 @@ struct TcParams {
   // local kernel) start as soon as its own grid wait has returned
   int late_wait, early_trigger;
   // a late-waiting local kernel that releases its chain at its start (the first slice of an
-  // ordinary call with the conv fused)
-  int trigger_first;
+  // ordinary call with the conv fused), or (trigger_end) once each block's unit is done, the
+  // chain then reading the state only after its grid wait (state_late)
+  int trigger_first, trigger_end, state_late;
   // the conv of the q and k channels fused into the local kernel (tm_q and tm_k then map the
   // pre-conv input x, [B][T][Cc]): the unit convolves its key head's q and k channels
   // (positions before the call's first token from `halo`: the conv state rows of slot
@@ -142,6 +143,9 @@ struct TcParams {
   const __nv_bfloat16* halo;
   __nv_bfloat16* tail;
   __nv_bfloat16* cs_out;
+  // with the conv fused and in-call snapshots: the conv-state bank [n_snap_slots][W-1][Cc]
+  // (written by the chains), else null
+  __nv_bfloat16* cbank;
 };
 
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
@@ -880,8 +884,10 @@ __global__ void __launch_bounds__(LGT, 3)
     tc_fence_after();
     tmem_dealloc(g.tmem, L_TMEM);
   }
+  // the chain after this grid may be launched (and set up) once every block's unit is done
+  if (p.trigger_end) pdl_trigger();
   // a later slice: this grid completes only after the previous slice's chain has, so that the
-  // next chain (started by this grid's completion) reads the state that chain left
+  // next chain (released by this grid's completion) reads the state that chain left
   if (wait_late) pdl_wait();
 }
 
@@ -1056,18 +1062,21 @@ __global__ void __launch_bounds__(CH_THREADS, 1)
   const uint32_t lane_off = static_cast<uint32_t>(gw * 32) << 16;
   const int row = 32 * gw + lane;                       // state row / d_v index of this thread
   float* Sg = p.state + ((size_t)slot * p.Hv + h) * D * D + (size_t)row * D + 64 * hc;
-  // the entering state (fp32, row i -> TMEM lane i; this thread: 64 columns), loaded while
-  // TMEM is being allocated
-  // (the state was last written by the chain of the previous slice or call, whose completion
-  // the local kernel before this one waited for before letting this one start)
+  // the entering state (fp32, row i -> TMEM lane i; this thread: 64 columns).  It was last
+  // written by the chain of the previous slice or call, which completed before the local
+  // kernel before this one did; this kernel is launched either then (the state is read while
+  // TMEM is being allocated) or earlier (state_late: it is read after the grid wait)
   float sv[64];
-  if (tid < CH_EPI) {
+  auto load_state = [&]() {
+    if (tid < CH_EPI) {
 #pragma unroll
-    for (int q = 0; q < 16; ++q) {
-      const float4 f = reinterpret_cast<const float4*>(Sg)[q];
-      sv[4 * q] = f.x; sv[4 * q + 1] = f.y; sv[4 * q + 2] = f.z; sv[4 * q + 3] = f.w;
+      for (int q = 0; q < 16; ++q) {
+        const float4 f = reinterpret_cast<const float4*>(Sg)[q];
+        sv[4 * q] = f.x; sv[4 * q + 1] = f.y; sv[4 * q + 2] = f.z; sv[4 * q + 3] = f.w;
+      }
     }
-  }
+  };
+  if (!p.state_late) load_state();
   // the local kernel's tiles and e^{G_C} (and the conv output V) from here on
   pdl_wait();
   // another slice follows: its local kernel may run beside this chain now (it writes the
@@ -1078,6 +1087,7 @@ __global__ void __launch_bounds__(CH_THREADS, 1)
       load_main(i);
       load_p(i);
     }
+  if (p.state_late) load_state();
   for (int i = tid; i < ns; i += CH_THREADS) sEgc[i] = p.egc[u0 + i];
   tc_fence_before();
   __syncthreads();
@@ -1361,24 +1371,45 @@ __global__ void __launch_bounds__(CH_THREADS, 1)
       z_chunk = nl;
     };
     if (p.gate && ns > 0) load_z(0);
-    // the last slice of a call whose conv ran in the local kernels: the call's conv tail (left
-    // by them, complete since the grid wait) into the conv state -- this CTA's v channels and,
-    // for the first value head of a key head, that key head's q and k channels
+    // Conv-state rows of this CTA's channels (the conv fused into the local kernels): its v
+    // channels and, for the first value head of a key head, that key head's q and k channels;
+    // word k of the 3 rows x those channels -> (row j, channel ch)
+    const int n_words = (h % (p.Hv / p.Hk) == 0) ? 48 + 96 : 48;
+    auto conv_word = [&](int k, int& j, int& ch) {
+      if (k < 48) {
+        j = k >> 4;
+        ch = 2 * p.Hk * D + h * D + 8 * (k & 15);
+      } else {
+        const int cc = (k - 48) & 31;
+        j = (k - 48) >> 5;
+        ch = ((cc >> 4) ? p.Hk * D : 0) + (h / (p.Hv / p.Hk)) * D + 8 * (cc & 15);
+      }
+    };
+    // the last slice: the call's conv tail (left by the conv and local kernels, complete since
+    // the grid wait) into the conv state
     if (p.cs_out) {
-      const int kh = h / (p.Hv / p.Hk);
-      for (int k = tid - CH_STORE * 32; k < 48 + 96; k += 128) {
+      for (int k = tid - CH_STORE * 32; k < n_words; k += 128) {
         int j, ch;
-        if (k < 48) {
-          j = k >> 4;
-          ch = 2 * p.Hk * D + h * D + 8 * (k & 15);
-        } else {
-          if (h % (p.Hv / p.Hk) != 0) break;
-          const int cc = (k - 48) & 31;
-          j = (k - 48) >> 5;
-          ch = ((cc >> 4) ? p.Hk * D : 0) + kh * D + 8 * (cc & 15);
-        }
+        conv_word(k, j, ch);
         *reinterpret_cast<uint4*>(p.cs_out + ((size_t)slot * FC_H + j) * p.Cc + ch) =
             __ldcg(reinterpret_cast<const uint4*>(p.tail + ((size_t)b * FC_H + j) * p.Cc + ch));
+      }
+    }
+    // in-call snapshots of the conv state at the boundaries this slice ends a chunk on: the
+    // W-1 inputs before the boundary token (rows of x) into conv bank row snap_slots[b][j]
+    // (an out-of-range bank row is skipped; the state snapshot reports it)
+    if (p.cbank) {
+      for (int nb = (p.n0 / p.se_c + 1) * p.se_c; nb <= p.n0 + ns && nb * C <= p.T;
+           nb += p.se_c) {
+        const int bs = p.snap_slots[(size_t)b * p.n_snap + nb / p.se_c - 1];
+        if (bs < 0 || bs >= p.n_snap_slots) continue;
+        for (int k = tid - CH_STORE * 32; k < n_words; k += 128) {
+          int j, ch;
+          conv_word(k, j, ch);
+          const size_t t = (size_t)b * p.T + (size_t)nb * C - FC_H + j;
+          *reinterpret_cast<uint4*>(p.cbank + ((size_t)bs * FC_H + j) * p.Cc + ch) =
+              __ldg(reinterpret_cast<const uint4*>(p.x + t * p.Cc + ch));
+        }
       }
     }
     bool ok = true;
@@ -1599,6 +1630,7 @@ cudaError_t launch_tc_t(const GdnLayerArgs& L, cudaStream_t stream) {
   p.n_snap = snaps ? L.n_snap : 0;
   p.n_snap_slots = snaps ? L.num_snap_slots : 0;
   p.snap_slots = snaps ? L.snap_slots : nullptr;
+  p.cbank = (snaps && L.fuse) ? static_cast<__nv_bfloat16*>(L.snap_conv_state) : nullptr;
   p.gate = L.gate;
   p.gw = L.gate_w;
   p.geps = L.gate_eps;
@@ -1645,6 +1677,8 @@ cudaError_t launch_tc_t(const GdnLayerArgs& L, cudaStream_t stream) {
     // everything before this call had completed when the v conv started)
     p.late_wait = si > 0 || chained || fuse;
     p.trigger_first = fuse && si == 0 && !chained;
+    p.trigger_end = p.late_wait && !p.trigger_first;
+    p.state_late = p.trigger_end;
     // (every chain releases the kernel after it early: the next slice's local kernel, or the
     // next call's first kernel, each of which waits for the chain before reading what it wrote)
     p.early_trigger = 1;
