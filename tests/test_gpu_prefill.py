@@ -235,3 +235,24 @@ def test_split_call_matches_whole(gdn):
             assert_bf16_parity(o_split.cpu(), o_whole.cpu())
             assert_state_parity(part.state.cpu(), whole.state.cpu())
         assert torch.equal(part.conv_state, whole.conv_state)
+
+
+@pytest.mark.parametrize("Hk,Hv", [(2, 2), (2, 8), (1, 8)])
+def test_conv_fused_group_sizes(gdn, Hk, Hv):
+    """With conv width 4 the chunk-local kernel convolves the q / k channels itself, shared by
+    the value heads of a key head as a cluster when there are 2 to 4 of them: one value head
+    per key head (no sharing), four (a cluster of four) and eight (each CTA alone), against the
+    oracle, over a ragged chunk and a non-zero conv state."""
+    sh = gi.GDNShape(2, 150, Hk, Hv, conv_width=4)
+    inp = gi.make_inputs(sh, seed=4300 + Hv, dtype="bf16", state="normal")
+    g = torch.Generator().manual_seed(4301 + Hv)
+    inp.conv_state = (torch.randn(inp.conv_state.shape, generator=g) * 0.5).to(torch.bfloat16)
+    ref = oracle_full(inp)
+    dev = to_device(inp)
+    out = torch.empty(2, 150, Hv, 128, dtype=torch.bfloat16, device="cuda")
+    gdn.gdn_chunk_prefill(dev.x, None, None, dev.a, dev.b, dev.A_log, dev.dt_bias, dev.state, out,
+                          num_k_heads=Hk, conv_weight=dev.conv_weight, conv_state=dev.conv_state)
+    assert gdn.gdn_get_device_error() == 0
+    assert_bf16_parity(out.cpu(), ref.out)
+    assert_state_parity(dev.state.cpu(), ref.state)
+    np.testing.assert_array_equal(dev.conv_state.cpu().float().numpy(), ref.conv_state)
