@@ -1012,12 +1012,12 @@ def main():
                                          workload="qwen35_4b_gdn_prefill_B4_T4096")])
 
     if rank == 0:
-        # per bucket: (chunk-local kernel with the conv + state-chain kernel) per slice of
-        # chunks whose tiles fit the 96 MB slice budget (96 KB per chunk and value head), then
-        # the conv-state snapshot (the state snapshot is stored by the chain itself)
+        # per bucket: the conv of the value channels, then (chunk-local kernel with the q / k
+        # conv + state-chain kernel) per slice of chunks whose tiles fit the 96 MB slice budget
+        # (80 KB per chunk and value head); the chains store the checkpoint rows themselves
         nch = BUCKET // 64
-        per_slice = max(1, min(512, nch, (96 << 20) // (HV * 96 * 1024)))
-        launches_per_step = nbk * (2 * (-(-nch // per_slice)) + 1)
+        per_slice = max(1, min(512, nch, (96 << 20) // (HV * 80 * 1024)))
+        launches_per_step = nbk * (1 + 2 * (-(-nch // per_slice)))
         line = {
             "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,

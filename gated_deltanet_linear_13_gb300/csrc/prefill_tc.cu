@@ -146,6 +146,8 @@ struct TcParams {
   // with the conv fused and in-call snapshots: the conv-state bank [n_snap_slots][W-1][Cc]
   // (written by the chains), else null
   __nv_bfloat16* cbank;
+  // with the conv fused: the post-conv v channels in the workspace [B][T][Hv d], else null
+  const __nv_bfloat16* vbuf;
 };
 
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
@@ -1192,6 +1194,19 @@ __global__ void __launch_bounds__(CH_THREADS, 1)
       }
       __syncwarp();
       if (refill_p) lp_chunk[(nl + 1) & 1] = nl + 1;
+      // chunk nl's tiles in the workspace (and, with the conv fused, its V rows there) have
+      // been copied in and are read no more: their L2 lines are dropped, not written back
+      {
+        const uint8_t* unit = p.units + (u0 + nl) * UNIT_BYTES;
+        for (uint32_t off = (uint32_t)lane * 128u; off < UNIT_BYTES; off += 32u * 128u)
+          l2_discard_line(unit + off);
+        if (p.vbuf) {
+          const int rows = min(C, p.T - (tbase + nl * C));   // (vbuf: not a packed batch)
+          for (int i = lane; i < 2 * rows; i += 32)
+            l2_discard_line(p.vbuf + ((size_t)bt * p.T + tbase + nl * C + (i >> 1)) * p.Hv * D +
+                            h * D + 64 * (i & 1));
+        }
+      }
     }
   } else if (tid < CH_EPI) {
     // ======================= epilogue warps
@@ -1631,6 +1646,7 @@ cudaError_t launch_tc_t(const GdnLayerArgs& L, cudaStream_t stream) {
   p.n_snap_slots = snaps ? L.num_snap_slots : 0;
   p.snap_slots = snaps ? L.snap_slots : nullptr;
   p.cbank = (snaps && L.fuse) ? static_cast<__nv_bfloat16*>(L.snap_conv_state) : nullptr;
+  p.vbuf = L.fuse ? static_cast<const __nv_bfloat16*>(L.v) : nullptr;
   p.gate = L.gate;
   p.gw = L.gate_w;
   p.geps = L.gate_eps;

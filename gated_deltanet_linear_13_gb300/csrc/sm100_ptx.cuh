@@ -101,6 +101,14 @@ __device__ __forceinline__ float ex2_approx(float x) {
   return y;
 }
 
+// ---------------------------------------------------------------- L2
+
+// Drops the 128-byte L2 line at global address p without writing it back (its contents are
+// undefined afterwards): for data that has been consumed and will only be overwritten.
+__device__ __forceinline__ void l2_discard_line(const void* p) {
+  asm volatile("discard.global.L2 [%0], 128;\n" ::"l"(p) : "memory");
+}
+
 // ---------------------------------------------------------------- fences
 
 __device__ __forceinline__ void fence_proxy_async_smem() {
