@@ -18,6 +18,18 @@ constexpr int kChunk = 64;
 // Bits of a translation unit's device error word.
 enum : unsigned { kErrIndex = 1u, kErrTimeout = 2u };
 
+// Index checks of the -DGDN_BOUNDS_CHECK build: in_bounds(word, ok) records kErrIndex in the
+// translation unit's error word and returns false when a computed global index is out of its
+// array (the caller then skips the access); in the normal build it is true and costs nothing.
+#ifdef GDN_BOUNDS_CHECK
+__device__ __forceinline__ bool in_bounds(unsigned int* word, bool ok) {
+  if (!ok) atomicOr(word, kErrIndex);
+  return ok;
+}
+#else
+__device__ __forceinline__ constexpr bool in_bounds(unsigned int*, bool) { return true; }
+#endif
+
 // ----------------------------------------------------------------- element access
 
 __device__ __forceinline__ float ld_elem(const float* p) { return *p; }

@@ -114,6 +114,7 @@ __device__ __forceinline__ void conv_tile(const CUtensorMap& tm_x, int B, int T_
   }
   const T* xb = x + (size_t)b * T_ * xs;
   T* csb = cs + (size_t)slot * H * C;
+  if (!in_bounds(&g_err_conv, b < B && t0 < T_)) return;
   const T* oldb = ends.halo ? ends.halo + (size_t)(ends.halo_by_slot ? slot : b) * H * C : csb;
   T* newb = ends.tail ? ends.tail + (size_t)b * H * C : csb;
   const int nt = min(TT, T_ - t0);
@@ -179,6 +180,8 @@ __device__ __forceinline__ void conv_tile(const CUtensorMap& tm_x, int B, int T_
 #pragma unroll
     for (int i = 0; i < H; ++i) ld_word(col + (tb + i) * CC, win[i]);
     T* yp = y + ((size_t)b * T_ + t0 + tb) * ys + (c0 - y_cbase);
+    if (!in_bounds(&g_err_conv, b < B && t0 + tb + min(TG, nt - tb) <= T_ && c0 >= y_cbase))
+      return;
     const int n = min(TG, nt - tb);
 #pragma unroll
     for (int t = 0; t < TG; ++t) {

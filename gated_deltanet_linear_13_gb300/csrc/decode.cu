@@ -148,6 +148,10 @@ __global__ void __launch_bounds__(DEC_THREADS, DEC_CPS) gdn_decode_stream_kernel
     const int b = c.item / p.Hk, kh = c.item % p.Hk;
     const int slot = p.slots ? p.slots[b] : b;
     const int h = kh * r + c.blk / DEC_BPH;
+    // (the -DGDN_BOUNDS_CHECK build: a row out of the state array is recorded and replaced by
+    // row 0, so that the copy pipeline keeps its shape)
+    if (!in_bounds(&g_err_decode, slot >= 0 && slot < p.num_slots && h < p.Hv && b < p.B))
+      return p.state;
     return p.state + (((size_t)slot * p.Hv + h) * D + (size_t)(c.blk % DEC_BPH) * DEC_RB) * D;
   };
   // ---- producer state (thread 0): loads run DEC_NS - 1 blocks ahead of the consumers

@@ -104,6 +104,8 @@ struct TcParams {
   float* state;
   const int32_t* slots;
   uint8_t* units;         // workspace: ns * B * Hv units of UNIT_BYTES
+  size_t n_units;         // units in one half of the workspace (bounds checks)
+  int Bm;                 // batch extent of the token arrays (1 for a packed batch)
   float* egc;             // workspace: e^{G_C} per unit
   // in-call snapshots: the state entering chunk n (n > 0, n a multiple of se_c, n C <= T) goes
   // to bank row snap_slots[b * n_snap + n / se_c - 1]; se_c == 0: none
@@ -424,8 +426,12 @@ __device__ __forceinline__ void sts32(uint32_t addr, uint32_t v) {
 __device__ __forceinline__ uint32_t input_pair(const TcParams& p, int slot, int b, int t, int ch) {
   if (t < 0) {
     const size_t row = (size_t)(p.halo_by_slot ? slot : b) * FC_H + (t + FC_H);
+    if (!in_bounds(&g_err_tc, row < (size_t)(p.halo_by_slot ? p.num_slots : p.Bm) * FC_H &&
+                                  t >= -FC_H && ch < p.Cc))
+      return 0u;
     return __ldcg(reinterpret_cast<const unsigned int*>(p.halo + row * p.Cc + ch));
   }
+  if (!in_bounds(&g_err_tc, b < p.Bm && t < p.T && ch < p.Cc)) return 0u;
   return __ldg(reinterpret_cast<const unsigned int*>(p.x + ((size_t)b * p.T + t) * p.Cc + ch));
 }
 
@@ -502,6 +508,9 @@ __device__ __forceinline__ void fused_conv_tail_qk(const TcParams& p, int tid, i
   const int j = tid >> 5, cc = tid & 31;
   const int ch = ((cc >> 4) ? p.Hk * D : 0) + kh * D + 8 * (cc & 15);
   const int t = p.T - FC_H + j;
+  if (!in_bounds(&g_err_tc, b < p.Bm && ch + 8 <= p.Cc &&
+                                (t >= 0 || (p.halo_by_slot ? slot < p.num_slots : true))))
+    return;
   uint4 v;
   if (t < 0) {
     const size_t row = (size_t)(p.halo_by_slot ? slot : b) * FC_H + (t + FC_H);
@@ -599,6 +608,7 @@ __device__ __forceinline__ bool local_unit(LocalGroup& g, const CUtensorMap* tm_
       const int r = 2 * lane + e;
       if (r < ntok) {
         const size_t gi = ((size_t)b * p.T + tok0 + r) * p.Hv + h;
+        if (!in_bounds(&g_err_tc, gi < (size_t)p.Bm * p.T * p.Hv)) continue;
         if (p.gates_pre) {
           g2[e] = reinterpret_cast<const float*>(p.a)[gi];
           b2[e] = reinterpret_cast<const float*>(p.b)[gi];
@@ -866,7 +876,11 @@ __global__ void __launch_bounds__(LGT, 3)
                          h == (int)gridDim.y - 1 && b == (int)gridDim.z - 1;
   if (p.trigger_first) pdl_trigger();
   int tok0, ntok, seq;
-  if (!local_unit_tokens(p, jc, b, tok0, ntok, seq)) {
+  // (the -DGDN_BOUNDS_CHECK build also drops a unit whose workspace unit or token rows would
+  // fall outside their arrays)
+  if (!local_unit_tokens(p, jc, b, tok0, ntok, seq) ||
+      !in_bounds(&g_err_tc, ((size_t)b * p.Hv + h) * p.ns + jc < p.n_units && b < p.Bm &&
+                                tok0 >= 0 && tok0 + ntok <= p.T)) {
     if (wait_late) pdl_wait();
     return;
   }
@@ -1009,6 +1023,10 @@ __global__ void __launch_bounds__(CH_THREADS, 1)
     if (tid == 0 && (p.cu || p.n0 == 0)) atomicOr(&g_err_tc, kErrIndex);
     return;
   }
+  // (the -DGDN_BOUNDS_CHECK build: this CTA's units, token rows and state rows)
+  if (!in_bounds(&g_err_tc, u0 + ns <= p.n_units && bt < p.Bm && tbase >= 0 &&
+                                (p.cu || tbase + (ns - 1) * C < p.T) && h < p.Hv))
+    return;
   float* sEgc = reinterpret_cast<float*>(sm + CH_MISC);
   uint64_t* barmem = reinterpret_cast<uint64_t*>(sm + CH_MISC + 2048);
   uint32_t* sTmem = reinterpret_cast<uint32_t*>(sm + CH_MISC + 2048 + 256);
@@ -1406,6 +1424,7 @@ __global__ void __launch_bounds__(CH_THREADS, 1)
       for (int k = tid - CH_STORE * 32; k < n_words; k += 128) {
         int j, ch;
         conv_word(k, j, ch);
+        if (!in_bounds(&g_err_tc, b < p.Bm && ch + 8 <= p.Cc && j < FC_H)) continue;
         *reinterpret_cast<uint4*>(p.cs_out + ((size_t)slot * FC_H + j) * p.Cc + ch) =
             __ldcg(reinterpret_cast<const uint4*>(p.tail + ((size_t)b * FC_H + j) * p.Cc + ch));
       }
@@ -1422,6 +1441,7 @@ __global__ void __launch_bounds__(CH_THREADS, 1)
           int j, ch;
           conv_word(k, j, ch);
           const size_t t = (size_t)b * p.T + (size_t)nb * C - FC_H + j;
+          if (!in_bounds(&g_err_tc, b < p.Bm && nb * C <= p.T && ch + 8 <= p.Cc)) continue;
           *reinterpret_cast<uint4*>(p.cbank + ((size_t)bs * FC_H + j) * p.Cc + ch) =
               __ldg(reinterpret_cast<const uint4*>(p.x + t * p.Cc + ch));
         }
@@ -1655,6 +1675,7 @@ cudaError_t launch_tc_t(const GdnLayerArgs& L, cudaStream_t stream) {
   p.ctab = static_cast<const int4*>(L.ctab);
   p.out = L.out;
   p.fuse = fuse;
+  p.Bm = MB;
   p.Cc = L.C_conv;
   p.silu = L.silu;
   p.x = static_cast<const __nv_bfloat16*>(L.x);
@@ -1687,6 +1708,7 @@ cudaError_t launch_tc_t(const GdnLayerArgs& L, cudaStream_t stream) {
     p.units = static_cast<uint8_t*>(L.scratch) +
               (nslices > 1 ? (size_t)(si & 1) * half_bytes : 0);
     p.egc = reinterpret_cast<float*>(p.units + units * UNIT_BYTES);
+    p.n_units = units;
     // (with the conv fused, every local kernel runs behind a kernel it does not depend on --
     // the v conv or the previous chain -- and waits for it at its end only; the first one of
     // an ordinary call releases its chain at once, whose set-up then reads the state early:
