@@ -176,6 +176,10 @@ __device__ __forceinline__ void tma_store_wait_read() {
 __device__ __forceinline__ void tma_store_wait_read_1() {
   asm volatile("cp.async.bulk.wait_group.read 1;\n" ::: "memory");
 }
+// Every committed bulk-store group has completed (its writes performed).
+__device__ __forceinline__ void tma_store_wait_all() {
+  asm volatile("cp.async.bulk.wait_group 0;\n" ::: "memory");
+}
 
 // ---------------------------------------------------------------- tcgen05: TMEM
 
