@@ -1106,7 +1106,8 @@ __global__ void __launch_bounds__(WS_THREADS, 1)
     pending = 0;
     if (warp >= WS_RW) graw = load_gate_raw<Tin>(p, item0 / p.Hk, T, item0 % p.Hk, r, pt);
   }
-  // the row warps' copies start now (two passes ahead, and further ahead into L2)
+  // the row warps' copies start once the staging copies are issued (two passes ahead, and
+  // further ahead into L2)
   const int NQ = r * (D / (4 * RowGeo<TM>::RL));       // passes per item (>= 16 > WS_RW)
   float4* buf = reinterpret_cast<float4*>(wsm + lay.rows) + (warp < WS_RW ? warp : 0) * nb * SBUF;
   int cs = slot0, ci = item0, cq = warp;               // copy cursor (row warps)
@@ -1127,6 +1128,8 @@ __global__ void __launch_bounds__(WS_THREADS, 1)
       advance(li, ls, lq);
     }
   };
+  // (the staged inputs go first: the rows' copies queue behind them)
+  __syncthreads();
   if (warp < WS_RW) {
     for (int j = 0; j < WS_L2AHEAD; ++j) {
       if (li < nitems && lane == 0)
