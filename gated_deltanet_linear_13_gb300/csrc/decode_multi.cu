@@ -30,7 +30,7 @@
 // rows, 512 contiguous bytes per eight lanes, coalesced: asynchronous copies put a warp's
 // coming passes' rows into its shared buffers ahead of use, and stores write the new rows.
 // Two kernels run it:
-//  - large batches: a persistent, warp-specialised CTA per SM.  Twelve row warps stream state
+//  - large batches of up to four tokens: a persistent, warp-specialised CTA per SM.  Twelve row warps stream state
 //    rows without a break (three buffers per warp, the copies running two passes ahead across
 //    item boundaries), while four prologue warps prepare the next item into the other half of
 //    a double-buffered prologue area: its inputs (x rows, conv state, conv weights and bias,
@@ -42,8 +42,8 @@
 //    per-thread global stores into the row stream.  mbarriers hand each prologue buffer to the
 //    row warps ("ready") and back ("free"); the first item's prologue is computed by all
 //    warps together.
-//  - small batches: one CTA per item, or a thread-block cluster of nsplit CTAs that split the
-//    rows of each value head.  All CTAs of a cluster read the old q/k conv state; a cluster
+//  - small batches, and more than four tokens: one CTA per item, or a thread-block cluster of
+//    nsplit CTAs that split the rows of each value head.  All CTAs of a cluster read the old q/k conv state; a cluster
 //    barrier orders those reads before the one CTA (rank 0) that writes the new one.
 #include "common.cuh"
 #include "sm100_ptx.cuh"
@@ -1299,23 +1299,27 @@ cudaError_t launch_multi_tm(const GdnLayerArgs& p, int T, float* snap_state, int
   if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
     return e;
   const int nitems = p.B * p.Hk;
-  // large batches: the warp-specialised kernel, with as many row buffers per warp as fit (up
-  // to five), when the inputs can be staged
-  if (nitems > sms && T * r <= WS_PT && stageable(p) && aligned16(p.out)) {
-    auto kern = gdn_decode_multi_ws_kernel<Tin, Tout, TM>;
-    const bool hb = p.conv_b != nullptr;
-    int nb = WS_MAXNB;
-    size_t smem = WsLayout(T, TM, r, p.W, hb, (int)sizeof(Tin), nb).total;
-    while (nb > 2 && smem > (size_t)kMaxDynSmem)
-      smem = WsLayout(T, TM, r, p.W, hb, (int)sizeof(Tin), --nb).total;
-    static int have[32] = {};
-    if (smem <= (size_t)kMaxDynSmem &&
-        ensure_smem(kern, (int)smem, kMaxDynSmem, &have[dev & 31]) == cudaSuccess) {
-      const int grid = nitems < sms ? nitems : sms;
-      return launch_pdl(false, kern, dim3(grid), dim3(WS_THREADS), smem, stream, p, T, nb,
-                        snap_state, num_snap, snap_slots, static_cast<Tin*>(snap_conv));
+  // large batches of up to four tokens: the warp-specialised kernel, with as many row buffers
+  // per warp as fit (up to five), when the inputs can be staged (at eight tokens and more the
+  // per-item kernel below measured faster: 317.5 against 324 us at 16/48 heads, B = 128,
+  // T = 8)
+  if constexpr (TM == 4) {
+    if (nitems > sms && T * r <= WS_PT && stageable(p) && aligned16(p.out)) {
+      auto kern = gdn_decode_multi_ws_kernel<Tin, Tout, TM>;
+      const bool hb = p.conv_b != nullptr;
+      int nb = WS_MAXNB;
+      size_t smem = WsLayout(T, TM, r, p.W, hb, (int)sizeof(Tin), nb).total;
+      while (nb > 2 && smem > (size_t)kMaxDynSmem)
+        smem = WsLayout(T, TM, r, p.W, hb, (int)sizeof(Tin), --nb).total;
+      static int have[32] = {};
+      if (smem <= (size_t)kMaxDynSmem &&
+          ensure_smem(kern, (int)smem, kMaxDynSmem, &have[dev & 31]) == cudaSuccess) {
+        const int grid = nitems < sms ? nitems : sms;
+        return launch_pdl(false, kern, dim3(grid), dim3(WS_THREADS), smem, stream, p, T, nb,
+                          snap_state, num_snap, snap_slots, static_cast<Tin*>(snap_conv));
+      }
+      (void)cudaGetLastError();        // (a refused size: the per-item kernel below)
     }
-    (void)cudaGetLastError();          // (a refused size: the per-item kernel below)
   }
   // rows of each value head split over a cluster of nsplit CTAs when the (sequence, key head)
   // items alone would leave most SMs idle

@@ -147,10 +147,12 @@ def test_per_token_snapshots(gdn):
             assert bool((bank[row] == 12345.0).all())
 
 
-# ---------------------------------------------------------------- the persistent kernel
-# Batches with more (sequence, key head) items than SMs take the persistent kernel (two CTAs a
-# SM, each working through items in turn, the next item's inputs staged by bulk copies while
-# the current item's rows stream).  The batches below give each CTA two or more items.
+# ---------------------------------------------------------------- large batches
+# Batches with more (sequence, key head) items than SMs take, for up to four tokens, the
+# persistent warp-specialised kernel (a CTA per SM working through items in turn: row warps
+# stream state rows while prologue warps prepare the next item from inputs staged by bulk
+# copies); with more tokens, the per-item kernel.  The batches below give each persistent CTA
+# two or more items.
 
 def _persistent_batch(Hk, items_per_cta=2.5):
     sms = torch.cuda.get_device_properties(0).multi_processor_count
@@ -174,11 +176,13 @@ def _run_ref(gdn, inp, sh, out_dtype, conv_bias=None, **kw):
 
 
 @pytest.mark.parametrize("dtype,W,Hk,Hv,T,bias", [
-    ("bf16", 4, 2, 6, 4, False),     # GQA 1:3, four tokens
-    ("bf16", 4, 4, 8, 7, True),      # seven tokens in the eight-token unroll, a conv bias
-    ("bf16", 2, 2, 6, 5, False),     # conv width 2
-    ("f32", 4, 2, 4, 3, True),       # fp32 inputs and outputs
-    ("bf16", 0, 2, 4, 16, False),    # no conv, sixteen tokens
+    ("bf16", 4, 2, 6, 4, False),     # persistent: GQA 1:3, four tokens
+    ("bf16", 4, 4, 8, 3, True),      # persistent: a conv bias
+    ("bf16", 2, 2, 6, 4, False),     # persistent: conv width 2
+    ("f32", 4, 2, 4, 3, True),       # persistent: fp32 inputs and outputs
+    ("bf16", 0, 2, 4, 2, False),     # persistent: no conv
+    ("bf16", 4, 4, 8, 7, True),      # per-item: seven tokens in the eight-token unroll
+    ("bf16", 0, 2, 4, 16, False),    # per-item: no conv, sixteen tokens
 ])
 def test_persistent_kernel_every_unit(gdn, dtype, W, Hk, Hv, T, bias):
     B = _persistent_batch(Hk)
