@@ -125,30 +125,36 @@ __device__ __forceinline__ void transpose_reduce8(float (&x)[V], int lane) {
 // state-row geometry: RL rows a lane, a warp pass of 4 RL rows of one value head
 template <int TM>
 struct RowGeo {
-  static constexpr int RL = TM <= 8 ? 2 : 1;          // state rows per lane
+  static constexpr int RL = TM <= 8 ? 2 : 1;          // state rows per lane (TM <= 8: two)
   static constexpr int V = RL * 2 * TM, VPL = V / 8;  // reduced values; values per lane
   static constexpr int SBUF = 4 * RL * D / 4;         // float4s per pass buffer
 };
 __host__ __device__ constexpr int rows_per_lane(int TM) { return TM <= 8 ? 2 : 1; }
 
-// The per-item prologue results in shared memory (floats) for T tokens, TM >= T the unrolled
-// capacity, r value heads: q^_t, k^_t, v_t of the item's rows, KK, QK, per value head
+// The T tokens of a step are taken in chunks of TM (the unrolled capacity; one chunk when
+// T <= TM), the state carried from chunk to chunk: the chunked form of the recurrence again,
+// with chunks of TM tokens.
+__host__ __device__ inline int token_chunks(int T, int TM) { return (T + TM - 1) / TM; }
+
+// The per-item prologue results in shared memory (floats) for T tokens in NC chunks of TM,
+// r value heads: q^_t, k^_t, v_t of the item's rows, KK, QK, per value head and chunk
 // Mt [TM][2 TM] (column s of (I + A)^{-1}, then of P (I + A)^{-1}), P [TM][TM], e^{G_t},
-// beta_t, e^{G_{T-1} - G_t}, e^{g_t}; the gates g_t, beta_t per value head and token; the
-// snapshot rows of the T tokens (ints).
+// beta_t, e^{G_last - G_t}, e^{g_t} (G from the chunk's start); the gates g_t, beta_t per
+// value head and token (NC TM of them); the snapshot rows of the tokens (ints).
 struct ProOffsets {
   int qh, kh, vv, kk, qk, mats, gb, ssl, total;      // total: a multiple of 4
   static __host__ __device__ int head_block(int TM) { return 3 * TM * TM + 4 * TM; }
   __host__ __device__ ProOffsets(int T, int TM, int r, int R) {
+    const int NC = token_chunks(T, TM), TS = NC * TM;
     qh = 0;
     kh = qh + T * D;
     vv = kh + T * D;
     kk = vv + T * r * R;
     qk = kk + T * T;
     mats = (qk + T * T + 3) & ~3;
-    gb = mats + r * head_block(TM);
-    ssl = gb + 2 * TM * r;
-    total = (ssl + TM + 3) & ~3;
+    gb = mats + r * NC * head_block(TM);
+    ssl = gb + 2 * TS * r;
+    total = (ssl + TS + 3) & ~3;
   }
 };
 
@@ -215,14 +221,14 @@ __device__ __forceinline__ GateRaw load_gate_raw(const GdnLayerArgs& p, int b, i
   return g;
 }
 
-// g_t and beta_t into gb[(hh TM + t) 2 + {0, 1}]
+// g_t and beta_t into gb[(hh TS + t) 2 + {0, 1}], TS = the tokens rounded up to whole chunks
 template <int TM>
 __device__ __forceinline__ void store_gate(const GdnLayerArgs& p, const GateRaw& g, float* gb,
                                            int T, int r, int i) {
   if (i < T * r) {
-    const int t = i / r, hh = i - t * r;
-    gb[(hh * TM + t) * 2] = p.gates_pre ? g.a : gate_g(g.a, g.A_log, g.dt_bias);
-    gb[(hh * TM + t) * 2 + 1] = p.gates_pre ? g.b : sigmoid_f(g.b);
+    const int t = i / r, hh = i - t * r, ts = token_chunks(T, TM) * TM;
+    gb[(hh * ts + t) * 2] = p.gates_pre ? g.a : gate_g(g.a, g.A_log, g.dt_bias);
+    gb[(hh * ts + t) * 2 + 1] = p.gates_pre ? g.b : sigmoid_f(g.b);
   }
 }
 
@@ -239,14 +245,16 @@ __device__ __forceinline__ void mt_norms(const GdnLayerArgs& p, const ProView& v
   }
 }
 
-// ---- 3. KK_ts = k_t . k_s and QK_ts = q_t . k_s: eight lanes a pair (16 elements each, a
-//      group's 128-bit loads covering all banks once), reduced over the group
-__device__ __forceinline__ void mt_dots(const ProView& v, int T, int w0, int nw, int lane) {
+// ---- 3. KK_ts = k_t . k_s and QK_ts = q_t . k_s for t, s in the same chunk of TM tokens:
+//      eight lanes a pair (16 elements each, a group's 128-bit loads covering all banks
+//      once), reduced over the group
+__device__ __forceinline__ void mt_dots(const ProView& v, int T, int TM, int w0, int nw,
+                                        int lane) {
   const int gl = lane & 7, np = 2 * T * T;
   for (int base = w0 * 4; base < np; base += nw * 4) {
     const int pr = base + (lane >> 3);
-    const bool on = pr < np;
     const int which = pr / (T * T), t = (pr / T) % T, s2 = pr % T;
+    const bool on = pr < np && t / TM == s2 / TM;
     float d = 0.f;
     if (on) {
       const float4* a4 = reinterpret_cast<const float4*>((which ? v.qh : v.kh) + t * D);
@@ -261,14 +269,18 @@ __device__ __forceinline__ void mt_dots(const ProView& v, int T, int w0, int nw,
   }
 }
 
-// ---- 4. per value head: G, (I + A)^{-1}, P and P (I + A)^{-1} (warp w0 + j nw takes value
-//      head hh = j, lanes = tokens); entries of tokens T .. TM-1 are zero
+// ---- 4. per value head and chunk: G, (I + A)^{-1}, P and P (I + A)^{-1} (warp w0 + j nw
+//      takes job j = (chunk c, value head hh), lanes = the chunk's tokens); entries of tokens
+//      past the chunk's end are zero
 template <int TM>
 __device__ __forceinline__ void mt_mats(const ProView& v, int T, int r, int w0, int nw,
                                         int lane) {
   constexpr int HB = 3 * TM * TM + 4 * TM;
-  for (int hh = w0; hh < r; hh += nw) {
-    float* Mt = v.mats + hh * HB;
+  const int NC = token_chunks(T, TM), TS = NC * TM, Tall = T;
+  for (int job = w0; job < r * NC; job += nw) {
+    const int c = job / r, hh = job - c * r, t0 = c * TM;
+    const int T = min(TM, Tall - t0);                  // tokens of this chunk
+    float* Mt = v.mats + (c * r + hh) * HB;
     float* P = Mt + 2 * TM * TM;
     float* eG = P + TM * TM;        // e^{G_t}
     float* bt = eG + TM;            // beta_t
@@ -276,8 +288,8 @@ __device__ __forceinline__ void mt_mats(const ProView& v, int T, int r, int w0, 
     float* eg = dk + TM;            // e^{g_t}
     float g = 0.f, beta = 0.f;
     if (lane < T) {
-      g = v.gb[(hh * TM + lane) * 2];
-      beta = v.gb[(hh * TM + lane) * 2 + 1];
+      g = v.gb[(hh * TS + t0 + lane) * 2];
+      beta = v.gb[(hh * TS + t0 + lane) * 2 + 1];
     }
     float G = g;                    // inclusive prefix over tokens
 #pragma unroll
@@ -301,8 +313,8 @@ __device__ __forceinline__ void mt_mats(const ProView& v, int T, int r, int w0, 
       float a = 0.f, pp = 0.f;
       if (lane < T && s2 < T && s2 <= lane) {
         const float e = expf(G - Gs);
-        if (s2 < lane) a = beta * e * v.kk[lane * T + s2];
-        pp = e * v.qk[lane * T + s2];
+        if (s2 < lane) a = beta * e * v.kk[(t0 + lane) * Tall + t0 + s2];
+        pp = e * v.qk[(t0 + lane) * Tall + t0 + s2];
       }
       if (lane < TM) {
         Mt[lane * TM + s2] = a;
@@ -401,10 +413,10 @@ __device__ __forceinline__ void read_pass(const float4* buf, float4 (&st)[RowGeo
 // ---- 5. one warp pass of an item's state rows (pass q: value head q / QO), whose rows
 //      (st) this lane has read: eight lanes a row (elements 4 (gl + 8 m) .. + 3, m < 4) and
 //      RL rows a lane (rows i0 + 4 rho + grp), so that each k / q slice read from shared
-//      memory serves RL rows.  Writes the outputs into ost [T][r][R'] (R' = the rows of a
+//      memory serves RL rows; the tokens chunk by chunk.  Writes the outputs into ost [T][r][R'] (R' = the rows of a
 //      value head the CTA holds; fp32, or the output type) and the new rows (and per-token
 //      snapshots) to HBM.
-template <int TM, typename OT>
+template <int TM, int NCMAX, typename OT>
 __device__ __forceinline__ void mt_pass(const GdnLayerArgs& p, const ProView& v, OT* ost,
                                         const RowItem& it, int T, int r, int q,
                                         float* snap_state, int num_snap,
@@ -420,125 +432,135 @@ __device__ __forceinline__ void mt_pass(const GdnLayerArgs& p, const ProView& v,
   const int tk0 = role_a ? tr0 : tr0 - TM;             // token of value slot 0
   const int h = it.kh * r + hh, irow = i0 + 4 * rho;   // the row of the reduced values
   const int lrow = irow - it.r_lo;                     // ... among the CTA's rows of the head
-  const float4* q4 = reinterpret_cast<const float4*>(v.qh);
-  const float4* k4 = reinterpret_cast<const float4*>(v.kh);
-  const float* Mt = v.mats + hh * HB;
-  const float* eG = Mt + 3 * TM * TM;
-  const float* bt = eG + TM;
-  const float* dk = bt + TM;
-  const float* eg = dk + TM;
-  // 2T partial dot products per row over this lane's 16 elements, reduced over the row's
-  // eight lanes
-  float x[V];
+  const int Rv = it.R;                                 // v / output rows held per head
+  // the chunks of TM tokens in turn (at most NCMAX), the rows' state carried in registers
+  // from one to the next
 #pragma unroll
-  for (int t = 0; t < TM; ++t) {
-    float a[RL], c[RL];
+  for (int c = 0; c < NCMAX; ++c) {
+    const int t0 = c * TM, Tc = NCMAX == 1 ? T : min(TM, T - t0);
+    if (NCMAX > 1 && Tc <= 0) break;
+    const float4* q4 = reinterpret_cast<const float4*>(v.qh + t0 * D);
+    const float4* k4 = reinterpret_cast<const float4*>(v.kh + t0 * D);
+    const float* Mt = v.mats + (c * r + hh) * HB;
+    const float* eG = Mt + 3 * TM * TM;
+    const float* bt = eG + TM;
+    const float* dk = bt + TM;
+    const float* eg = dk + TM;
+    // 2 Tc partial dot products per row over this lane's 16 elements, reduced over the row's
+    // eight lanes
+    float x[V];
 #pragma unroll
-    for (int rr = 0; rr < RL; ++rr) a[rr] = c[rr] = 0.f;
-    if (t < T) {
+    for (int t = 0; t < TM; ++t) {
+      float a[RL], cq[RL];
 #pragma unroll
-      for (int m = 0; m < 4; ++m) {
-        const float4 kv = k4[t * (D / 4) + gl + 8 * m];
-        const float4 qv = q4[t * (D / 4) + gl + 8 * m];
+      for (int rr = 0; rr < RL; ++rr) a[rr] = cq[rr] = 0.f;
+      if (t < Tc) {
 #pragma unroll
-        for (int rr = 0; rr < RL; ++rr) {
-          a[rr] = fma4(st[rr][m], kv, a[rr]);
-          c[rr] = fma4(st[rr][m], qv, c[rr]);
+        for (int m = 0; m < 4; ++m) {
+          const float4 kv = k4[t * (D / 4) + gl + 8 * m];
+          const float4 qv = q4[t * (D / 4) + gl + 8 * m];
+#pragma unroll
+          for (int rr = 0; rr < RL; ++rr) {
+            a[rr] = fma4(st[rr][m], kv, a[rr]);
+            cq[rr] = fma4(st[rr][m], qv, cq[rr]);
+          }
         }
       }
+#pragma unroll
+      for (int rr = 0; rr < RL; ++rr) {
+        x[rr * 2 * TM + t] = a[rr];
+        x[rr * 2 * TM + TM + t] = cq[rr];
+      }
     }
-#pragma unroll
-    for (int rr = 0; rr < RL; ++rr) {
-      x[rr * 2 * TM + t] = a[rr];
-      x[rr * 2 * TM + TM + t] = c[rr];
-    }
-  }
-  transpose_reduce8<V>(x, lane);
-  // x[k]: k_t . s0 (role_a) or q_t . s0 of row irow, t = tk0 + k
-  const int Rv = it.R;                                 // v / output rows held per head
-  float rhs[VPL], acc[VPL];
-#pragma unroll
-  for (int k = 0; k < VPL; ++k) {
-    const int t = tk0 + k;
-    rhs[k] = (role_a && t < T) ? bt[t] * (v.vv[(t * r + hh) * Rv + lrow] - eG[t] * x[k]) : 0.f;
-    acc[k] = 0.f;
-  }
-  // role_a lanes: u = (I + A)^{-1} rhs; the others: P (I + A)^{-1} rhs
-#pragma unroll
-  for (int s2 = 0; s2 < TM; ++s2) {
-    if (s2 < T) {
-      const float rs = __shfl_sync(0xffffffffu, rhs[s2 % VPL], (rho * 2 * TM + s2) / VPL, 8);
-      const float* mrow = Mt + s2 * 2 * TM + tr0;
-#pragma unroll
-      for (int k = 0; k < VPL; ++k) acc[k] = fmaf(mrow[k], rs, acc[k]);
-    }
-  }
-  if (!role_a) {
+    transpose_reduce8<V>(x, lane);
+    // x[k]: k_t . s (role_a) or q_t . s of row irow, t = t0 + tk0 + k, s the state at the
+    // chunk's start
+    float rhs[VPL], acc[VPL];
 #pragma unroll
     for (int k = 0; k < VPL; ++k) {
       const int t = tk0 + k;
-      if (t < T) ost[(t * r + hh) * Rv + lrow] = from_float<OT>(fmaf(eG[t], x[k], acc[k]));
+      rhs[k] = (role_a && t < Tc)
+                   ? bt[t] * (v.vv[((t0 + t) * r + hh) * Rv + lrow] - eG[t] * x[k]) : 0.f;
+      acc[k] = 0.f;
     }
-  }
-  // the state: token by token with snapshots, else relative to the last token; u_s of row
-  // rr sits in lane (rr 2 TM + s) / VPL, slot s % VPL
-  if (snap_state) {
+    // role_a lanes: u = (I + A)^{-1} rhs; the others: P (I + A)^{-1} rhs
 #pragma unroll
     for (int s2 = 0; s2 < TM; ++s2) {
-      if (s2 < T) {
-        float us[RL];
+      if (s2 < Tc) {
+        const float rs = __shfl_sync(0xffffffffu, rhs[s2 % VPL], (rho * 2 * TM + s2) / VPL, 8);
+        const float* mrow = Mt + s2 * 2 * TM + tr0;
 #pragma unroll
-        for (int rr = 0; rr < RL; ++rr)
-          us[rr] = __shfl_sync(0xffffffffu, acc[s2 % VPL], (rr * 2 * TM + s2) / VPL, 8);
-        const float e = eg[s2];
-        const int sl = v.ssl[s2];
+        for (int k = 0; k < VPL; ++k) acc[k] = fmaf(mrow[k], rs, acc[k]);
+      }
+    }
+    if (!role_a) {
 #pragma unroll
-        for (int m = 0; m < 4; ++m) {
-          const float4 kv = k4[s2 * (D / 4) + gl + 8 * m];
+      for (int k = 0; k < VPL; ++k) {
+        const int t = tk0 + k;
+        if (t < Tc)
+          ost[((t0 + t) * r + hh) * Rv + lrow] = from_float<OT>(fmaf(eG[t], x[k], acc[k]));
+      }
+    }
+    // the state: token by token with snapshots, else relative to the chunk's last token;
+    // u_s of row rr sits in lane (rr 2 TM + s) / VPL, slot s % VPL
+    if (snap_state) {
 #pragma unroll
-          for (int rr = 0; rr < RL; ++rr) {
-            st[rr][m].x = fmaf(e, st[rr][m].x, us[rr] * kv.x);
-            st[rr][m].y = fmaf(e, st[rr][m].y, us[rr] * kv.y);
-            st[rr][m].z = fmaf(e, st[rr][m].z, us[rr] * kv.z);
-            st[rr][m].w = fmaf(e, st[rr][m].w, us[rr] * kv.w);
+      for (int s2 = 0; s2 < TM; ++s2) {
+        if (s2 < Tc) {
+          float us[RL];
+#pragma unroll
+          for (int rr = 0; rr < RL; ++rr)
+            us[rr] = __shfl_sync(0xffffffffu, acc[s2 % VPL], (rr * 2 * TM + s2) / VPL, 8);
+          const float e = eg[s2];
+          const int sl = v.ssl[t0 + s2];
+#pragma unroll
+          for (int m = 0; m < 4; ++m) {
+            const float4 kv = k4[s2 * (D / 4) + gl + 8 * m];
+#pragma unroll
+            for (int rr = 0; rr < RL; ++rr) {
+              st[rr][m].x = fmaf(e, st[rr][m].x, us[rr] * kv.x);
+              st[rr][m].y = fmaf(e, st[rr][m].y, us[rr] * kv.y);
+              st[rr][m].z = fmaf(e, st[rr][m].z, us[rr] * kv.z);
+              st[rr][m].w = fmaf(e, st[rr][m].w, us[rr] * kv.w);
+            }
           }
-        }
-        if (sl >= 0 && sl < num_snap) {
+          if (sl >= 0 && sl < num_snap) {
 #pragma unroll
-          for (int rr = 0; rr < RL; ++rr) {
-            float4* dst = reinterpret_cast<float4*>(
-                snap_state + (((size_t)sl * p.Hv + h) * D + i0 + 4 * rr) * D);
+            for (int rr = 0; rr < RL; ++rr) {
+              float4* dst = reinterpret_cast<float4*>(
+                  snap_state + (((size_t)sl * p.Hv + h) * D + i0 + 4 * rr) * D);
 #pragma unroll
-            for (int m = 0; m < 4; ++m) dst[gl + 8 * m] = st[rr][m];
+              for (int m = 0; m < 4; ++m) dst[gl + 8 * m] = st[rr][m];
+            }
           }
         }
       }
-    }
-  } else {
-    const float eT = eG[T - 1];
+    } else {
+      const float eT = eG[Tc - 1];
 #pragma unroll
-    for (int rr = 0; rr < RL; ++rr)
-#pragma unroll
-      for (int m = 0; m < 4; ++m) {
-        st[rr][m].x *= eT; st[rr][m].y *= eT; st[rr][m].z *= eT; st[rr][m].w *= eT;
-      }
-#pragma unroll
-    for (int s2 = 0; s2 < TM; ++s2) {
-      if (s2 < T) {
-        float us[RL];
-#pragma unroll
-        for (int rr = 0; rr < RL; ++rr)
-          us[rr] = __shfl_sync(0xffffffffu, acc[s2 % VPL], (rr * 2 * TM + s2) / VPL, 8) *
-                   dk[s2];
+      for (int rr = 0; rr < RL; ++rr)
 #pragma unroll
         for (int m = 0; m < 4; ++m) {
-          const float4 kv = k4[s2 * (D / 4) + gl + 8 * m];
+          st[rr][m].x *= eT; st[rr][m].y *= eT; st[rr][m].z *= eT; st[rr][m].w *= eT;
+        }
 #pragma unroll
-          for (int rr = 0; rr < RL; ++rr) {
-            st[rr][m].x = fmaf(us[rr], kv.x, st[rr][m].x);
-            st[rr][m].y = fmaf(us[rr], kv.y, st[rr][m].y);
-            st[rr][m].z = fmaf(us[rr], kv.z, st[rr][m].z);
-            st[rr][m].w = fmaf(us[rr], kv.w, st[rr][m].w);
+      for (int s2 = 0; s2 < TM; ++s2) {
+        if (s2 < Tc) {
+          float us[RL];
+#pragma unroll
+          for (int rr = 0; rr < RL; ++rr)
+            us[rr] = __shfl_sync(0xffffffffu, acc[s2 % VPL], (rr * 2 * TM + s2) / VPL, 8) *
+                     dk[s2];
+#pragma unroll
+          for (int m = 0; m < 4; ++m) {
+            const float4 kv = k4[s2 * (D / 4) + gl + 8 * m];
+#pragma unroll
+            for (int rr = 0; rr < RL; ++rr) {
+              st[rr][m].x = fmaf(us[rr], kv.x, st[rr][m].x);
+              st[rr][m].y = fmaf(us[rr], kv.y, st[rr][m].y);
+              st[rr][m].z = fmaf(us[rr], kv.z, st[rr][m].z);
+              st[rr][m].w = fmaf(us[rr], kv.w, st[rr][m].w);
+            }
           }
         }
       }
@@ -588,8 +610,9 @@ struct MtLayout {
   }
 };
 
-// TM: the token capacity the loops are unrolled for (T <= TM)
-template <typename Tin, typename Tout, int TM>
+// TM: the chunk of tokens the row loops are unrolled for; TT >= T: the tokens the conv window
+// is unrolled for
+template <typename Tin, typename Tout, int TM, int TT>
 __global__ void __launch_bounds__(MT_THREADS, 2) gdn_decode_multi_kernel(GdnLayerArgs p, int T,
                                                                       float* snap_state,
                                                                       int num_snap,
@@ -625,7 +648,7 @@ __global__ void __launch_bounds__(MT_THREADS, 2) gdn_decode_multi_kernel(GdnLaye
   // ---- 1. conv (+SiLU) of this CTA's channels over the T tokens, or plain loads; the new
   //      conv state, and the conv state after every token for the snapshots (for the q/k
   //      channels, which every CTA of a cluster reads, once the cluster's reads are done)
-  float qkwin[3 + TM];                                  // this thread's q/k channel (tid < 256)
+  float qkwin[3 + TT];                                  // this thread's q/k channel (tid < 256)
   int qkch = -1;
   for (int cl = tid; cl < ch_all; cl += MT_THREADS) {
     // local channel cl: q (0..127), k (128..255), then v of value head vh, row r_lo + vi
@@ -637,29 +660,29 @@ __global__ void __launch_bounds__(MT_THREADS, 2) gdn_decode_multi_kernel(GdnLaye
     const int dstride = cl < ch_qk ? D : r * R;
     if (W > 0) {
       const Tin* cs = (const Tin*)p.conv_state + (size_t)slot * H * C + ch;
-      float win[3 + TM], w4[4];
+      float win[3 + TT], w4[4];
 #pragma unroll
       for (int j = 0; j < 3; ++j) win[j] = j >= 3 - H ? ld_elem(cs + (size_t)(j - 3 + H) * C) : 0.f;
 #pragma unroll
-      for (int t = 0; t < TM; ++t)
+      for (int t = 0; t < TT; ++t)
         win[3 + t] = t < T ? ld_elem((const Tin*)p.x + ((size_t)b * T + t) * C + ch) : 0.f;
       const float bias = p.conv_b ? ld_elem((const Tin*)p.conv_b + ch) : 0.f;
       const Tin* w = (const Tin*)p.conv_w + (size_t)ch * W;
 #pragma unroll
       for (int j = 0; j < 4; ++j) w4[j] = j >= 4 - W ? ld_elem(w + j - 4 + W) : 0.f;
-      conv_tokens<TM>(win, w4, bias, p.silu, T, dst, dstride);
+      conv_tokens<TT>(win, w4, bias, p.silu, T, dst, dstride);
       // new conv state: window entries T + 3 - H ..; after token t: t + 4 - H ..
       if (cl < ch_qk) {
         qkch = ch;
 #pragma unroll
-        for (int i = 0; i < 3 + TM; ++i) qkwin[i] = win[i];
+        for (int i = 0; i < 3 + TT; ++i) qkwin[i] = win[i];
       } else {
-        store_window<TM>(win, (Tin*)p.conv_state + (size_t)slot * H * C + ch, T + 3 - H, H, C);
+        store_window<TT>(win, (Tin*)p.conv_state + (size_t)slot * H * C + ch, T + 3 - H, H, C);
         if (snap_conv && snap_slots)
           for (int t = 0; t < T; ++t) {
             const int sl = snap_slots[b * T + t];
             if (sl >= 0 && sl < num_snap)
-              store_window<TM>(win, snap_conv + (size_t)sl * H * C + ch, t + 4 - H, H, C);
+              store_window<TT>(win, snap_conv + (size_t)sl * H * C + ch, t + 4 - H, H, C);
           }
       }
     } else {
@@ -676,11 +699,12 @@ __global__ void __launch_bounds__(MT_THREADS, 2) gdn_decode_multi_kernel(GdnLaye
   // every CTA of the cluster has read the old q/k conv state (the values are consumed)
   if (nsplit > 1) cluster_arrive_relaxed_mt();
   const bool per_token = snap_state && snap_slots;
-  if (tid < TM) v.ssl[tid] = (per_token && tid < T) ? snap_slots[b * T + tid] : -1;
+  if (tid < token_chunks(T, TM) * TM)
+    v.ssl[tid] = (per_token && tid < T) ? snap_slots[b * T + tid] : -1;
   __syncthreads();
   mt_norms(p, v, T, warp, MT_WARPS, lane);
   __syncthreads();
-  mt_dots(v, T, warp, MT_WARPS, lane);
+  mt_dots(v, T, TM, warp, MT_WARPS, lane);
   __syncthreads();
   mt_mats<TM>(v, T, r, warp, MT_WARPS, lane);
   __syncthreads();
@@ -691,7 +715,8 @@ __global__ void __launch_bounds__(MT_THREADS, 2) gdn_decode_multi_kernel(GdnLaye
     cp_async_wait_all();                               // this pass's rows (buffer pk)
     read_pass<TM>(stg + pk * SBUF, st, lane);
     if (q + MT_WARPS < NQ) prefetch_pass<TM>(p, it, r, q + MT_WARPS, stg + (pk ^ 1) * SBUF, lane);
-    mt_pass<TM>(p, v, ost, it, T, r, q, per_token ? snap_state : nullptr, num_snap, st, lane);
+    mt_pass<TM, TT / TM>(p, v, ost, it, T, r, q, per_token ? snap_state : nullptr, num_snap, st,
+                         lane);
   }
   __syncthreads();
   mt_outputs<Tout>(p, ost, it, T, r, tid, MT_THREADS);
@@ -699,12 +724,12 @@ __global__ void __launch_bounds__(MT_THREADS, 2) gdn_decode_multi_kernel(GdnLaye
   // reads of the old one
   if (nsplit > 1) cluster_wait_mt();
   if (sp == 0 && W > 0 && qkch >= 0) {
-    store_window<TM>(qkwin, (Tin*)p.conv_state + (size_t)slot * H * C + qkch, T + 3 - H, H, C);
+    store_window<TT>(qkwin, (Tin*)p.conv_state + (size_t)slot * H * C + qkch, T + 3 - H, H, C);
     if (snap_conv && snap_slots)
       for (int t = 0; t < T; ++t) {
         const int sl = snap_slots[b * T + t];
         if (sl >= 0 && sl < num_snap)
-          store_window<TM>(qkwin, snap_conv + (size_t)sl * H * C + qkch, t + 4 - H, H, C);
+          store_window<TT>(qkwin, snap_conv + (size_t)sl * H * C + qkch, t + 4 - H, H, C);
       }
   }
   if (tid == 0 && sp == 0 && snap_slots && kh == 0) check_snap_rows(snap_slots, num_snap, b, T);
@@ -1186,8 +1211,8 @@ __global__ void __launch_bounds__(WS_THREADS, 1)
         read_pass<TM>(buf + pk * SBUF, st, lane);
         issue(pk == 0 ? nb - 1 : pk - 1);              // the buffer read a pass ago
         pk = pk + 1 == nb ? 0 : pk + 1;
-        mt_pass<TM>(p, v, ost, it, T, r, q, per_token ? snap_state : nullptr, num_snap, st,
-                    lane);
+        mt_pass<TM, 1>(p, v, ost, it, T, r, q, per_token ? snap_state : nullptr, num_snap, st,
+                       lane);
       }
       // this warp's share of the item is done; the last row warp to finish it sends the
       // outputs (a bulk store per token row of the item's heads) and, once they have read
@@ -1289,7 +1314,7 @@ cudaError_t ensure_smem(K kernel, int bytes, int initial, int* have) {
   return e;
 }
 
-template <typename Tin, typename Tout, int TM>
+template <typename Tin, typename Tout, int TM, int TT>
 cudaError_t launch_multi_tm(const GdnLayerArgs& p, int T, float* snap_state, int num_snap,
                             const int32_t* snap_slots, void* snap_conv, cudaStream_t stream) {
   const int r = p.Hv / p.Hk;
@@ -1326,9 +1351,9 @@ cudaError_t launch_multi_tm(const GdnLayerArgs& p, int T, float* snap_state, int
   int nsplit = 1;
   while (nsplit < 8 && nitems * nsplit * 2 <= 2 * sms) nsplit *= 2;
   const size_t smem = sizeof(float) * MtLayout(T, TM, r, D / nsplit).total;
-  const int top = (int)(sizeof(float) * MtLayout(TM, TM, 8, D).total);
+  const int top = (int)(sizeof(float) * MtLayout(TT, TM, 8, D).total);
   static int have_c[32] = {};
-  if ((e = ensure_smem(gdn_decode_multi_kernel<Tin, Tout, TM>, (int)smem,
+  if ((e = ensure_smem(gdn_decode_multi_kernel<Tin, Tout, TM, TT>, (int)smem,
                        top < kMaxDynSmem ? top : kMaxDynSmem, &have_c[dev & 31])) !=
       cudaSuccess)
     return e;
@@ -1344,21 +1369,22 @@ cudaError_t launch_multi_tm(const GdnLayerArgs& p, int T, float* snap_state, int
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = nsplit > 1 ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, gdn_decode_multi_kernel<Tin, Tout, TM>, p, T, snap_state,
+  return cudaLaunchKernelEx(&cfg, gdn_decode_multi_kernel<Tin, Tout, TM, TT>, p, T, snap_state,
                             num_snap, snap_slots, static_cast<Tin*>(snap_conv), nsplit);
 }
 
 template <typename Tin, typename Tout>
 cudaError_t launch_multi_t(const GdnLayerArgs& p, int T, float* snap_state, int num_snap,
                            const int32_t* snap_slots, void* snap_conv, cudaStream_t stream) {
+  // up to 4 tokens: one chunk of 4; up to 8: one chunk of 8; up to 16: chunks of 8
   if (T <= 4)
-    return launch_multi_tm<Tin, Tout, 4>(p, T, snap_state, num_snap, snap_slots, snap_conv,
-                                         stream);
+    return launch_multi_tm<Tin, Tout, 4, 4>(p, T, snap_state, num_snap, snap_slots, snap_conv,
+                                            stream);
   if (T <= 8)
-    return launch_multi_tm<Tin, Tout, 8>(p, T, snap_state, num_snap, snap_slots, snap_conv,
-                                         stream);
-  return launch_multi_tm<Tin, Tout, 16>(p, T, snap_state, num_snap, snap_slots, snap_conv,
-                                        stream);
+    return launch_multi_tm<Tin, Tout, 8, 8>(p, T, snap_state, num_snap, snap_slots, snap_conv,
+                                            stream);
+  return launch_multi_tm<Tin, Tout, 8, 16>(p, T, snap_state, num_snap, snap_slots, snap_conv,
+                                           stream);
 }
 
 }  // namespace

@@ -49,7 +49,7 @@ def _run(gdn, dev, sh, out_dtype, state_slots=None, **snap):
     return out
 
 
-@pytest.mark.parametrize("T", [1, 2, 5, 16])
+@pytest.mark.parametrize("T", [1, 2, 5, 9, 16])
 def test_bf16_conv_matches_oracle(gdn, T):
     sh, inp = _inputs(3, T, 2, 6, 4, "bf16", 8000 + T)
     ref = oracle_full(inp)
@@ -113,11 +113,13 @@ def test_skipped_row(gdn):
     assert_state_parity(dev.state[2].cpu(), ref.state[0])
 
 
-def test_per_token_snapshots(gdn):
+@pytest.mark.parametrize("T", [5, 12])
+def test_per_token_snapshots(gdn, T):
     """The state and conv state after every token of every row, into permuted bank rows with
-    one pair masked: each equals the oracle after that many tokens."""
-    B, T = 2, 5
-    sh, inp = _inputs(B, T, 2, 6, 4, "bf16", 8400)
+    one pair masked: each equals the oracle after that many tokens (T = 12: two chunks of
+    tokens, the second ragged)."""
+    B = 2
+    sh, inp = _inputs(B, T, 2, 6, 4, "bf16", 8400 + T)
     nb = B * T + 2
     perm = np.random.default_rng(1).permutation(nb)[:B * T].reshape(B, T)
     perm[1, 2] = -1
