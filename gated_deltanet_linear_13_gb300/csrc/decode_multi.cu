@@ -761,17 +761,18 @@ struct MpStage {
 };
 
 // shared memory of the warp-specialised kernel (bytes): two prologue buffers, two output
-// buffers [T][r][D], the staging area, nb row buffers per row warp, the mbarriers
+// buffers [T][r][D] (output type), the staging area, nb row buffers per row warp, the mbarriers
 // (staged, ready[2], free[2]), the abort flag and the row warps' per-buffer done counts
 struct WsLayout {
   ProOffsets pro;
   MpStage stg;
   int nb, pb, ost, stage, rows, bars, total;
-  __host__ __device__ WsLayout(int T, int TM, int r, int W, bool has_bias, int esz, int nb_)
+  __host__ __device__ WsLayout(int T, int TM, int r, int W, bool has_bias, int esz, int osz,
+                               int nb_)
       : pro(T, TM, r, D), stg(T, r, W, has_bias, esz), nb(nb_) {
     pb = 0;
     ost = pb + 2 * pro.total * 4;
-    stage = ost + 2 * T * r * D * 4;
+    stage = ost + ((2 * T * r * D * osz + 15) & ~15);
     rows = stage + stg.bytes;
     bars = rows + WS_RW * nb * 4 * rows_per_lane(TM) * D * 4;
     total = bars + 7 * 8;
@@ -1095,7 +1096,8 @@ __global__ void __launch_bounds__(WS_THREADS, 1)
   constexpr int SBUF = RowGeo<TM>::SBUF;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int r = p.Hv / p.Hk, nitems = p.B * p.Hk;
-  const WsLayout lay(T, TM, r, p.W, p.conv_b != nullptr, (int)sizeof(Tin), nb);
+  const WsLayout lay(T, TM, r, p.W, p.conv_b != nullptr, (int)sizeof(Tin), (int)sizeof(Tout),
+                     nb);
   const uint32_t bars = ptx::smem_addr(wsm + lay.bars);
   const uint32_t staged = bars, ready0 = bars + 8, free0 = bars + 24;
   volatile int* abort = reinterpret_cast<volatile int*>(wsm + lay.bars + 40);
@@ -1333,9 +1335,10 @@ cudaError_t launch_multi_tm(const GdnLayerArgs& p, int T, float* snap_state, int
       auto kern = gdn_decode_multi_ws_kernel<Tin, Tout, TM>;
       const bool hb = p.conv_b != nullptr;
       int nb = WS_MAXNB;
-      size_t smem = WsLayout(T, TM, r, p.W, hb, (int)sizeof(Tin), nb).total;
+      const int isz = (int)sizeof(Tin), osz = (int)sizeof(Tout);
+      size_t smem = WsLayout(T, TM, r, p.W, hb, isz, osz, nb).total;
       while (nb > 2 && smem > (size_t)kMaxDynSmem)
-        smem = WsLayout(T, TM, r, p.W, hb, (int)sizeof(Tin), --nb).total;
+        smem = WsLayout(T, TM, r, p.W, hb, isz, osz, --nb).total;
       static int have[32] = {};
       if (smem <= (size_t)kMaxDynSmem &&
           ensure_smem(kern, (int)smem, kMaxDynSmem, &have[dev & 31]) == cudaSuccess) {
