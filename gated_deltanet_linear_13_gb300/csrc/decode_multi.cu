@@ -375,28 +375,21 @@ __device__ __forceinline__ void prefetch_pass(const GdnLayerArgs& p, const RowIt
     const int gl = lane & 7, grp = lane >> 3;
     const int QO = it.R / (4 * RL), hh = q / QO;
     const int i0 = it.r_lo + (q - hh * QO) * 4 * RL + grp;
+    // (the -DGDN_BOUNDS_CHECK build: rows out of the state array are recorded and replaced by
+    // row 0, so that the copy groups keep their shape)
+    const bool ok = in_bounds(&g_err_multi, it.slot >= 0 && it.slot < p.num_slots &&
+                                                it.kh * r + hh < p.Hv && i0 + 4 * (RL - 1) < D);
 #pragma unroll
     for (int rr = 0; rr < RL; ++rr) {
       const float4* src = reinterpret_cast<const float4*>(
-          p.state + (((size_t)it.slot * p.Hv + it.kh * r + hh) * D + i0 + 4 * rr) * D);
+          ok ? p.state + (((size_t)it.slot * p.Hv + it.kh * r + hh) * D + i0 + 4 * rr) * D
+             : p.state);
 #pragma unroll
       for (int m = 0; m < 4; ++m)
         cp_async16(dst + (rr * 4 + grp) * (D / 4) + gl + 8 * m, src + gl + 8 * m);
     }
   }
   cp_async_commit();
-}
-
-// L2 prefetch of a pass's rows (8 or 4 consecutive rows of 512 bytes; one lane)
-template <int TM>
-__device__ __forceinline__ void l2_prefetch_pass(const GdnLayerArgs& p, const RowItem& it, int r,
-                                                 int q) {
-  constexpr int RL = RowGeo<TM>::RL;
-  const int QO = it.R / (4 * RL), hh = q / QO;
-  const int i0 = it.r_lo + (q - hh * QO) * 4 * RL;
-  const float* src = p.state + (((size_t)it.slot * p.Hv + it.kh * r + hh) * D + i0) * D;
-  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;\n" ::"l"(src), "r"(4 * RL * D * 4)
-               : "memory");
 }
 
 // this lane's pieces of a pass's rows, from its shared buffer
@@ -566,6 +559,9 @@ __device__ __forceinline__ void mt_pass(const GdnLayerArgs& p, const ProView& v,
       }
     }
   }
+  if (!in_bounds(&g_err_multi, it.slot >= 0 && it.slot < p.num_slots && h < p.Hv &&
+                                  i0 + 4 * (RL - 1) < D))
+    return;
 #pragma unroll
   for (int rr = 0; rr < RL; ++rr) {
     float4* Sr = reinterpret_cast<float4*>(
@@ -739,7 +735,6 @@ __global__ void __launch_bounds__(MT_THREADS, 2) gdn_decode_multi_kernel(GdnLaye
 constexpr int WS_RW = 12;                    // row warps
 constexpr int WS_PW = 4;                     // prologue warps
 constexpr int WS_MAXNB = 5;                  // row buffers per row warp (at most)
-constexpr int WS_L2AHEAD = 0;                // passes prefetched into L2 beyond the copies
 constexpr int WS_THREADS = (WS_RW + WS_PW) * 32;
 constexpr int WS_RT = WS_RW * 32, WS_PT = WS_PW * 32;
 constexpr uint32_t WS_BAR_PRO = 2;           // named barrier of the prologue warps
@@ -789,6 +784,11 @@ __device__ __forceinline__ void stage_item(const GdnLayerArgs& p, int T, int r, 
                                            uint32_t bar, int lane) {
   constexpr int E = sizeof(Tin);
   const int W = p.W, H = W > 0 ? W - 1 : 0, C = p.C_conv, ch = (2 + r) * D;
+  // (the -DGDN_BOUNDS_CHECK build: an item outside the batch or the slot range is recorded and
+  // replaced by item 0 of slot 0, so that the staged byte count stays what the barrier expects)
+  if (!in_bounds(&g_err_multi, b >= 0 && b < p.B && kh >= 0 && kh < p.Hk && slot >= 0 &&
+                                   slot < p.num_slots))
+    b = kh = slot = 0;
   const int nx = 3 * T, ncs = nx + 3 * H, nw = ncs + (W > 0 ? 3 : 0);
   const int n = nw + (W > 0 && p.conv_b ? 3 : 0);
   if (lane == 0) ptx::mbar_arrive_expect_tx(bar, (uint32_t)sl.bytes);
@@ -1133,38 +1133,22 @@ __global__ void __launch_bounds__(WS_THREADS, 1)
     pending = 0;
     if (warp >= WS_RW) graw = load_gate_raw<Tin>(p, item0 / p.Hk, T, item0 % p.Hk, r, pt);
   }
-  // the row warps' copies start once the staging copies are issued (two passes ahead, and
-  // further ahead into L2)
+  // the row warps' copies start once the staging copies are issued (two passes ahead)
   const int NQ = r * (D / (4 * RowGeo<TM>::RL));       // passes per item (>= 16 > WS_RW)
   float4* buf = reinterpret_cast<float4*>(wsm + lay.rows) + (warp < WS_RW ? warp : 0) * nb * SBUF;
   int cs = slot0, ci = item0, cq = warp;               // copy cursor (row warps)
-  int ls = slot0, li = item0, lq = warp;               // L2-prefetch cursor, WS_L2AHEAD further
-  auto advance = [&](int& c, int& s, int& q) {
-    if (c < nitems && (q += WS_RW) >= NQ) {
-      q = warp;
-      c = next_item(p, c + gridDim.x, nitems, s);
-    }
-  };
   auto issue = [&](int into) {
     prefetch_pass<TM>(p, RowItem{ci / p.Hk, ci % p.Hk, cs, 0, D}, r, cq, buf + into * SBUF,
                       lane, ci < nitems);
-    advance(ci, cs, cq);
-    if (WS_L2AHEAD > 0) {
-      if (li < nitems && lane == 0)
-        l2_prefetch_pass<TM>(p, RowItem{li / p.Hk, li % p.Hk, ls, 0, D}, r, lq);
-      advance(li, ls, lq);
+    if (ci < nitems && (cq += WS_RW) >= NQ) {
+      cq = warp;
+      ci = next_item(p, ci + gridDim.x, nitems, cs);
     }
   };
   // (the staged inputs go first: the rows' copies queue behind them)
   __syncthreads();
-  if (warp < WS_RW) {
-    for (int j = 0; j < WS_L2AHEAD; ++j) {
-      if (li < nitems && lane == 0)
-        l2_prefetch_pass<TM>(p, RowItem{li / p.Hk, li % p.Hk, ls, 0, D}, r, lq);
-      advance(li, ls, lq);
-    }
+  if (warp < WS_RW)
     for (int j = 0; j < nb - 1; ++j) issue(j);
-  }
   bool ok0 = true;
   if (item0 < nitems) {
     const RowItem it{item0 / p.Hk, item0 % p.Hk, slot0, 0, D};

@@ -2,8 +2,8 @@
 
 Its kernels check their computed global indices (workspace units, token rows, state and
 conv-state rows, halo and tail rows) and record GDN_ERR_DEVICE_INDEX instead of faulting.
-Small cases of every prefill form, the decode step and a checkpoint round trip run through
-it in a process of their own: each must match the oracle, report no index error, and give the
+Small cases of every prefill form, the decode step, the multi-token step (both of its
+kernels) and a checkpoint round trip run through it in a process of their own: each must match the oracle, report no index error, and give the
 same bits on a second run (determinism).
 """
 import os
@@ -95,6 +95,26 @@ gdn.gdn_chunk_prefill_varlen(dev.x, None, None, dev.a, dev.b, dev.A_log, dev.dt_
                              out, num_k_heads=2, conv_weight=dev.conv_weight,
                              conv_state=dev.conv_state, cu_seqlens=cu)
 clean("packed batch")
+
+# multi-token steps: a small batch (per-item kernel, clusters), a batch of more items than
+# SMs at T = 4 (the persistent kernel: staged inputs, bulk stores) and at T = 12 (chunks of 8)
+sms = torch.cuda.get_device_properties(0).multi_processor_count
+for (B, T, seed) in ((3, 4, 18), (sms // 2 + 7, 4, 19), (sms // 2 + 7, 12, 20)):
+    sh = gi.GDNShape(B, T, 2, 6, conv_width=4)
+    inp = gi.make_inputs(sh, seed=seed, dtype="bf16", state="normal")
+    ref = oracle_full(inp)
+    outs = []
+    for rep in range(2):
+        dev = to_device(inp)
+        out = torch.empty(B, T, 6, 128, dtype=torch.bfloat16, device="cuda")
+        gdn.gdn_decode_multi(dev.x, None, None, dev.a, dev.b, dev.A_log, dev.dt_bias, dev.state,
+                             out, num_k_heads=2, conv_weight=dev.conv_weight,
+                             conv_state=dev.conv_state)
+        clean(f"multi-token B={B} T={T}")
+        outs.append((out, dev.state.clone(), dev.conv_state.clone()))
+    assert all(torch.equal(a, b) for a, b in zip(outs[0], outs[1]))
+    assert_bf16_parity(outs[0][0].cpu(), ref.out, f"checked multi-token B={B} T={T}")
+    assert_state_parity(outs[0][1].cpu(), ref.state, what=f"checked multi-token state B={B}")
 
 # a decode step, then a checkpoint round trip
 sh = gi.GDNShape(3, 1, 16, 48, conv_width=4)
