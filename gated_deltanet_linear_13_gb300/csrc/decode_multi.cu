@@ -29,22 +29,24 @@
 // the norms, the gates and, per value head, M in shared memory.  Then warps stream the state
 // rows, 512 contiguous bytes per eight lanes, coalesced: asynchronous copies put a warp's
 // coming passes' rows into its shared buffers ahead of use, and stores write the new rows.
-// Two kernels run it:
-//  - large batches of up to four tokens: a persistent, warp-specialised CTA per SM.  Twelve row warps stream state
-//    rows without a break (three buffers per warp, the copies running two passes ahead across
-//    item boundaries), while four prologue warps prepare the next item into the other half of
-//    a double-buffered prologue area: its inputs (x rows, conv state, conv weights and bias,
-//    a few contiguous runs each) bulk-copied into a staging area while the item before is
-//    prepared, its gates loaded into registers ahead of use; the conv four channels a thread
-//    with the q/k norms as warp reductions, the dot products four lanes a pair, M one thread
-//    per (value head, column).  The new conv state leaves by bulk stores straight from the
-//    staged rows, the outputs by bulk stores from shared memory, so that neither role issues
-//    per-thread global stores into the row stream.  mbarriers hand each prologue buffer to the
-//    row warps ("ready") and back ("free"); the first item's prologue is computed by all
-//    warps together.
-//  - small batches, and more than four tokens: one CTA per item, or a thread-block cluster of
-//    nsplit CTAs that split the rows of each value head.  All CTAs of a cluster read the old q/k conv state; a cluster
-//    barrier orders those reads before the one CTA (rank 0) that writes the new one.
+// More than eight tokens are taken in chunks of eight, the rows' state carried in registers
+// from one chunk to the next.  Two kernels run it:
+//  - large batches of up to four tokens: a persistent, warp-specialised CTA per SM.  Twelve
+//    row warps stream state rows without a break (three buffers per warp, the copies running
+//    two passes ahead across item boundaries), while four prologue warps prepare the next
+//    item into the other half of a double-buffered prologue area: its inputs (x rows, conv
+//    state, conv weights and bias, a few contiguous runs each) bulk-copied into a staging
+//    area while the item before is prepared, its gates loaded into registers ahead of use;
+//    the conv four channels a thread with the q/k norms as warp reductions, the dot products
+//    four lanes a pair, M one thread per (value head, column).  The new conv state leaves by
+//    bulk stores straight from the staged rows, the outputs by bulk stores from shared
+//    memory, so that neither role issues per-thread global stores into the row stream.
+//    mbarriers hand each prologue buffer to the row warps ("ready") and back ("free"); the
+//    first item's prologue is computed by all warps together.
+//  - small batches, and more than four tokens: one CTA per item, or a thread-block cluster
+//    of nsplit CTAs that split the rows of each value head.  All CTAs of a cluster read the
+//    old q/k conv state; a cluster barrier orders those reads before the one CTA (rank 0)
+//    that writes the new one.
 #include "common.cuh"
 #include "sm100_ptx.cuh"
 
@@ -406,9 +408,9 @@ __device__ __forceinline__ void read_pass(const float4* buf, float4 (&st)[RowGeo
 // ---- 5. one warp pass of an item's state rows (pass q: value head q / QO), whose rows
 //      (st) this lane has read: eight lanes a row (elements 4 (gl + 8 m) .. + 3, m < 4) and
 //      RL rows a lane (rows i0 + 4 rho + grp), so that each k / q slice read from shared
-//      memory serves RL rows; the tokens chunk by chunk.  Writes the outputs into ost [T][r][R'] (R' = the rows of a
-//      value head the CTA holds; fp32, or the output type) and the new rows (and per-token
-//      snapshots) to HBM.
+//      memory serves RL rows; the tokens chunk by chunk.  Writes the outputs into
+//      ost [T][r][R'] (R' = the rows of a value head the CTA holds; fp32, or the output type)
+//      and the new rows (and per-token snapshots) to HBM.
 template <int TM, int NCMAX, typename OT>
 __device__ __forceinline__ void mt_pass(const GdnLayerArgs& p, const ProView& v, OT* ost,
                                         const RowItem& it, int T, int r, int q,
@@ -870,7 +872,9 @@ __device__ __forceinline__ void store_conv_rows(const GdnLayerArgs& p, int T, in
       shift = job + 3 - H;                              // token t = job - 1: t + 4 - H
     }
     const int pos = shift + row, lch = run * D, len = run == 2 ? r * D : D;
-    const int gch = run == 0 ? it.kh * D : run == 1 ? (p.Hk + it.kh) * D : (2 * p.Hk + it.kh * r) * D;
+    const int gch = run == 0   ? it.kh * D
+                    : run == 1 ? (p.Hk + it.kh) * D
+                               : (2 * p.Hk + it.kh * r) * D;
     const uint8_t* src = pos < 3 ? stage + sl.cs + ((pos - (3 - H)) * ch + lch) * E
                                  : stage + sl.x + ((pos - 3) * ch + lch) * E;
     ptx::bulk_store(base + (size_t)row * C + gch, ptx::smem_addr(src), (uint32_t)(len * E));
@@ -956,7 +960,8 @@ __device__ __forceinline__ void pro_conv_norm(const GdnLayerArgs& p, const ProVi
 #pragma unroll
       for (int t = 0; t < TM; ++t) {
         if (t < T) {
-          const float inv = (p.l2norm ? 1.0f / sqrtf(ss[t] + p.eps) : 1.0f) * (isq ? p.scale : 1.0f);
+          const float inv =
+              (p.l2norm ? 1.0f / sqrtf(ss[t] + p.eps) : 1.0f) * (isq ? p.scale : 1.0f);
 #pragma unroll
           for (int c = 0; c < 4; ++c) w[t][c] *= inv;
         }
@@ -1038,7 +1043,8 @@ __device__ __forceinline__ void pro_mats(const ProView& v, int T, int r, int pt)
       float a = 0.f;
 #pragma unroll
       for (int s2 = 0; s2 < TM; ++s2)
-        if (s2 >= j && s2 < t) a = fmaf(beta[t] * expf(G[t] - G[s2]) * v.kk[t * T + s2], col[s2], a);
+        if (s2 >= j && s2 < t)
+          a = fmaf(beta[t] * expf(G[t] - G[s2]) * v.kk[t * T + s2], col[s2], a);
       col[t] = -a;
     }
   }
