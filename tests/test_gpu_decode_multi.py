@@ -306,3 +306,28 @@ def test_27b_shape_full_size_every_unit(gdn):
             assert_bf16_parity(o[b, :, h], ref.out[b, :, h], what=f"out {b},{h}")
             assert_state_parity(s[b, h], ref.state[b, h], what=f"state {b},{h}")
     np.testing.assert_array_equal(dev.conv_state.float().cpu().numpy(), ref.conv_state)
+
+
+@pytest.mark.parametrize("large", [False, True])
+def test_options_both_kernels(gdn, large):
+    """Precomputed gates (fp32 g and beta), a q scale, no q/k L2 norm and no SiLU, through the
+    per-item kernel (B = 3) and the persistent kernel (a batch of more items than SMs), T = 3.
+    x is scaled by 0.1 so that the unnormalised keys keep the delta rule stable."""
+    Hk, Hv, T = 2, 6, 3
+    B = _persistent_batch(Hk) if large else 3
+    sh, inp = _inputs(B, T, Hk, Hv, 4, "bf16", 8800 + int(large))
+    inp.x = (inp.x.float() * 0.1).to(torch.bfloat16)
+    rng = np.random.default_rng(88)
+    inp.a = torch.from_numpy(-rng.uniform(0, 4, (B, T, Hv)).astype(np.float32))
+    inp.b = torch.from_numpy(rng.uniform(0, 1, (B, T, Hv)).astype(np.float32))
+    opts = dict(scale=0.5, qk_l2norm=False, conv_silu=False, gates_precomputed=True)
+    ref = oracle_full(inp, **opts)
+    dev = to_device(inp)
+    out = torch.full((B, T, Hv, 128), 7.0, dtype=torch.bfloat16, device="cuda")
+    gdn.gdn_decode_multi(dev.x, None, None, dev.a, dev.b, None, None, dev.state, out,
+                         num_k_heads=Hk, conv_weight=dev.conv_weight, conv_state=dev.conv_state,
+                         **opts)
+    assert gdn.gdn_get_device_error() == 0
+    assert_bf16_parity(out.cpu(), ref.out, f"options B={B}")
+    assert_state_parity(dev.state.cpu(), ref.state, what=f"options state B={B}")
+    np.testing.assert_array_equal(dev.conv_state.float().cpu().numpy(), ref.conv_state)
