@@ -183,6 +183,9 @@ def _run_ref(gdn, inp, sh, out_dtype, conv_bias=None, **kw):
     ("bf16", 2, 2, 6, 4, False),     # persistent: conv width 2
     ("f32", 4, 2, 4, 3, True),       # persistent: fp32 inputs and outputs
     ("bf16", 0, 2, 4, 2, False),     # persistent: no conv
+    ("bf16", 1, 2, 6, 4, False),     # persistent: conv width 1 (no conv state)
+    ("bf16", 3, 4, 4, 2, True),      # persistent: conv width 3, GQA 1:1
+    ("f32", 0, 2, 4, 4, False),      # persistent: fp32 without a conv
     ("bf16", 4, 4, 8, 7, True),      # per-item: seven tokens in the eight-token unroll
     ("bf16", 0, 2, 4, 16, False),    # per-item: no conv, sixteen tokens
 ])
